@@ -1,0 +1,248 @@
+/*
+ * k3moe.h - C ABI of the latent routed-expert MoE layer over MXFP4 weights
+ * (Kimi-K3 style), hand-written CUDA for sm_103a (GB300).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [PR26185]  llama.cpp PR #26185 "model: add Kimi-K3 text model"
+ *     - opening post (pwilkin): latent MoE (routed experts run at the latent
+ *       width) and the "situ" activation replacing SwiGLU;
+ *     - review by GrEarl, section "Dry run: prepare_tensors() completes, all
+ *       93 layers mapped, file type = 38": 896 experts, 16 used, sigmoid
+ *       expert-score gating, exp_probs_b, ffn_routed_{down,up,norm};
+ *     - review by GrEarl, section "repack_mxfp4_blocks is bit-exact - 0
+ *       mismatches over 11,010,048 values": the MXFP4 source format, the ggml
+ *       17-byte block and the repack.
+ *   [PR573]   Lucebox PR #573 "feat(kimi-k3): add DSpark Q8 artifact and shared
+ *       speculative runtime", section "DSpark acceptance-contract
+ *       correction": RMS epsilon 1e-5.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is DEVICE memory owned by the caller unless the
+ *     entry point says "host".  The library allocates nothing in these calls
+ *     (scratch lives in the caller's workspace) and keeps no pointer after
+ *     the call returns.
+ *   - Tensors are dense and row-major.  bf16 tensors are passed as uint16_t
+ *     bit patterns, fp32 as float.  Every base pointer must be 16-byte
+ *     aligned (K3MOE_ERR_ALIGN otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises the
+ *     host except k3moe_get_status and k3moe_forward_host.
+ *   - Host-detectable errors (null pointer, bad shape, misalignment, small
+ *     workspace) return before anything is launched.  Errors found on the
+ *     device (a non-finite router logit, an expired bounded wait) are
+ *     recorded in the workspace status word; read them with
+ *     k3moe_get_status.  Outputs are unspecified after an error, but every
+ *     kernel terminates.
+ *   - Results are deterministic: the same inputs give bitwise identical
+ *     outputs, run to run.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MOE_ABI_VERSION 1
+
+typedef enum k3moe_status {
+    K3MOE_OK = 0,
+    K3MOE_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size */
+    K3MOE_ERR_SHAPE = 2,        /* unsupported shape (cols % 32, k > E, k > 32, ...) */
+    K3MOE_ERR_ALIGN = 3,        /* a base pointer is not 16-byte aligned */
+    K3MOE_ERR_WORKSPACE = 4,    /* workspace smaller than required */
+    K3MOE_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, copy, ...) */
+    K3MOE_ERR_NONFINITE = 6,    /* device: a router logit was NaN or inf */
+    K3MOE_ERR_TIMEOUT = 7,      /* device: a bounded wait inside a kernel expired */
+    K3MOE_ERR_UNSUPPORTED = 8   /* activation or path not available for the shape */
+} k3moe_status;
+
+/* Gated expert activation.  The pages name a "situ" activation that replaces
+ * SwiGLU ([PR26185], opening post) but do not define it; it is a pluggable
+ * epilogue, exercised as silu(g) * u with g = W1 x (gate) and u = W3 x (up). */
+typedef enum k3moe_act {
+    K3MOE_ACT_SILU_GATED = 0
+} k3moe_act;
+
+/* Expert-path selector.  AUTO picks DECODE for T <= 8 and GROUPED otherwise.
+ *   DECODE : streaming GEMV over the selected experts' bytes (CUDA cores).
+ *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
+ *            dequantisation, TMA-fed, TMEM accumulators. */
+typedef enum k3moe_path {
+    K3MOE_PATH_AUTO = 0,
+    K3MOE_PATH_DECODE = 1,
+    K3MOE_PATH_GROUPED = 2
+} k3moe_path;
+
+/* One MoE layer.  All pointers are device memory owned by the caller and must
+ * stay valid while work that uses them is in flight.
+ *
+ * Expert weights ([PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact"):
+ * compressed-tensors MXFP4, logical [out, in] per expert; `*_q` holds two
+ * E2M1 codes per byte (element 2i in the low nibble, sign in bit 3,
+ * magnitudes [0,.5,1,1.5,2,3,4,6]); `*_s` holds one E8M0 byte e per 32
+ * consecutive inputs, value 2^(e-127) (e = 255 is not allowed).
+ *   w1_q [E, f, d/2]  w1_s [E, f, d/32]   gate projection
+ *   w3_q [E, f, d/2]  w3_s [E, f, d/32]   up projection
+ *   w2_q [E, d, f/2]  w2_s [E, d, f/32]   down projection
+ * Router ([PR26185], GrEarl, "Dry run"): logits l = x_r W_r^T, scores
+ * s = sigmoid(l); the k experts with the largest s + b are selected (ties to
+ * the lower index, slots listed in that order); combine weights are
+ * s / sum(s) over the selected k (the bias only steers selection).
+ * Block mode (D > 0): the input is h [T, D]; hn = RMSNorm(h) * gamma (eps),
+ * the router reads hn (d_router = D), the experts read z = hn W_down^T
+ * [T, d], and the output is W_up applied to the combined latent rows. */
+typedef struct k3moe_layer_desc {
+    int32_t E;          /* routed experts (896) */
+    int32_t k;          /* experts per token (16), 1 <= k <= min(E, 32) */
+    int32_t d;          /* latent width (3584), multiple of 64 (of 128 in block mode) */
+    int32_t f;          /* expert hidden width (3072), multiple of 64 */
+    int32_t d_router;   /* router input width: d (latent mode) or D (block mode) */
+    int32_t act;        /* k3moe_act */
+    int32_t path;       /* k3moe_path */
+    int32_t D;          /* block mode: model width (7168), multiple of 128; 0 = latent mode */
+    float eps;          /* block mode: RMSNorm epsilon (1e-5 per [PR573]) */
+    int32_t reserved;   /* must be 0 */
+    const uint8_t* w1_q;
+    const uint8_t* w1_s;
+    const uint8_t* w3_q;
+    const uint8_t* w3_s;
+    const uint8_t* w2_q;
+    const uint8_t* w2_s;
+    const uint16_t* router_w;    /* [E, d_router] bf16 */
+    const float* router_b;       /* [E] fp32 selection bias (exp_probs_b) */
+    const uint16_t* norm_gamma;  /* block mode: [D] bf16 (ffn_routed_norm) */
+    const uint16_t* w_down;      /* block mode: [d, D] bf16 (ffn_routed_down) */
+    const uint16_t* w_up;        /* block mode: [D, d] bf16 (ffn_routed_up) */
+} k3moe_layer_desc;
+
+/* Library ABI version (K3MOE_ABI_VERSION of the build). */
+int k3moe_abi_version(void);
+
+/* Static description of a status code (never NULL). */
+const char* k3moe_status_string(int status);
+
+/* MXFP4 repack: compressed-tensors (packed, scale) -> ggml 17-byte blocks.
+ * [PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact": block b of a row is
+ * byte 0 = e (stored unchanged; ggml decodes it as 2^(e-128) with doubled
+ * kvalues, so the value is unchanged), bytes 1..16 = qs with element j in the
+ * low nibble and element j+16 in the high nibble of qs[j].
+ *   packed     [rows, cols/2] uint8 (device)
+ *   scale      [rows, cols/32] uint8 (device)
+ *   blocks_out [rows, cols/32, 17] uint8 (device; no alignment needed)
+ * Errors: INVALID_ARG (null, rows or cols <= 0), SHAPE (cols % 32 != 0),
+ * ALIGN (packed not 16-byte aligned), CUDA. Bit-exact integer work. */
+k3moe_status k3moe_repack_mxfp4(const uint8_t* packed, const uint8_t* scale, int64_t rows,
+                                int64_t cols, uint8_t* blocks_out, void* stream);
+
+/* Inverse of k3moe_repack_mxfp4 (ggml blocks -> packed nibbles + E8M0).
+ *   blocks [rows, cols/32, 17] uint8; packed_out [rows, cols/2] (16-byte
+ *   aligned); scale_out [rows, cols/32].  Errors as for the repack. */
+k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t cols,
+                                uint8_t* packed_out, uint8_t* scale_out, void* stream);
+
+/* Workspace bytes that k3moe_route needs for T tokens and E experts. */
+size_t k3moe_route_workspace_size(int32_t T, int32_t E);
+
+/* Router: logits, sigmoid scores, biased top-k selection, renormalised
+ * weights ([PR26185], GrEarl, "Dry run": sigmoid gating, exp_probs_b, top-16
+ * of 896).
+ *   x        [T, d_r] bf16       router input
+ *   router_w [E, d_r] bf16
+ *   bias     [E] fp32
+ *   idx_out  [T, k] int32        selected experts, slot order = (s+b) desc, index asc
+ *   w_out    [T, k] fp32         s / sum(s) over the selected experts
+ *   logits_out [T, E] fp32 or NULL  the fp32 logits the selection used
+ *   ws, ws_bytes                 scratch >= k3moe_route_workspace_size(T, E)
+ * Logits accumulate bf16 products in fp32; s = 1 / (1 + expf(-l)) and
+ * s + b are fp32.  Errors: INVALID_ARG, SHAPE (k > 32, k > E, d_r % 8), ALIGN,
+ * WORKSPACE, CUDA; device: NONFINITE (a logit was not finite). */
+k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16_t* router_w,
+                         const float* bias, int32_t E, int32_t k, int32_t* idx_out,
+                         float* w_out, float* logits_out, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Expert histogram, exclusive scan and token permutation of a selection.
+ * Pairs are numbered p = t*k + j.
+ *   idx      [T, k] int32 in [0, E)
+ *   counts   [E] int32; offsets [E+1] int32 (exclusive scan, offsets[E] = T*k)
+ *   perm     [T*k] int32: row r of the permuted order holds pair perm[r];
+ *            rows of expert e are offsets[e]..offsets[e+1]-1, tokens ascending
+ *   inv      [T*k] int32: inv[p] = row of pair p
+ * Scratch: ws of k3moe_route_workspace_size(T, E) bytes.  Integer work,
+ * deterministic.  Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, CUDA. */
+k3moe_status k3moe_permute(const int32_t* idx, int32_t T, int32_t k, int32_t E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* RMSNorm over rows ([PR26185] ffn_routed_norm; eps 1e-5 per [PR573]):
+ * out = bf16(h / sqrt(mean(h^2) + eps) * gamma), fp32 arithmetic.
+ *   h [T, D] bf16, gamma [D] bf16, out [T, D] bf16.  D % 8 == 0. */
+k3moe_status k3moe_rmsnorm(const uint16_t* h, int32_t T, int32_t D, const uint16_t* gamma,
+                           float eps, uint16_t* out, void* stream);
+
+/* Dense bf16 GEMM on tcgen05 (the latent projections ffn_routed_down/up and
+ * the router logits at large T): out[t, n] = sum_c x[t, c] * w[n, c].
+ *   x [T, K] bf16, w [N, K] bf16, out [T, N] bf16 (out_fp32 = 0) or fp32 (1).
+ *   N % 128 == 0, K % 64 == 0, T >= 1.  fp32 accumulation in tensor memory. */
+k3moe_status k3moe_gemm_bf16(const uint16_t* x, const uint16_t* w, int32_t T, int32_t N,
+                             int32_t K, void* out, int32_t out_fp32, void* stream);
+
+/* Workspace bytes that k3moe_forward needs for up to T_max tokens.  A new
+ * workspace must be zero-filled once before its first use (cudaMemset); the
+ * library keeps its 256-byte header consistent from then on.  The same holds
+ * for the workspaces of k3moe_route and k3moe_permute. */
+size_t k3moe_workspace_size(const k3moe_layer_desc* desc, int32_t T_max);
+
+/* The MoE layer (latent mode) or the full latent block (block mode).
+ *   hidden [T, d] bf16 (latent mode) or [T, D] bf16 (block mode)
+ *   out    same shape as hidden, bf16
+ *   ws     scratch of at least k3moe_workspace_size(desc, T) bytes
+ * out[t] = sum_j w[t,j] * W2_e (act(W1_e x_t, W3_e x_t)), e = idx[t,j].
+ * Both paths stage each (token, expert) result in fp32 and sum a token's
+ * k terms in slot order, so the result does not depend on scheduling.
+ * Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, UNSUPPORTED, CUDA; device
+ * errors via k3moe_get_status. */
+k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* k3moe_forward on HOST buffers: copies hidden (host) to the device on
+ * `stream`, runs the layer, copies out back to host memory and waits for the
+ * stream.  Pinned host memory gives asynchronous copies; pageable memory
+ * works too.  The workspace must hold k3moe_workspace_size(desc, T) plus
+ * k3moe_host_staging_size(desc, T) bytes. */
+size_t k3moe_host_staging_size(const k3moe_layer_desc* desc, int32_t T);
+k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hidden_host,
+                                int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Copy the routing of the last k3moe_forward that used `ws` (device to
+ * device, on `stream`): idx_out [T, k] int32, w_out [T, k] fp32, logits_out
+ * [T, E] fp32 or NULL. */
+k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws, int32_t T,
+                                   int32_t* idx_out, float* w_out, float* logits_out,
+                                   void* stream);
+
+/* Read and clear the device status word of a workspace.  Synchronises
+ * `stream`; *device_status receives K3MOE_OK or the first device error code.
+ * Returns CUDA if the stream reported an error. */
+k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status);
+
+/* Kernel tracing.  While enabled (enable != 0), k3moe_forward records a CUDA
+ * event on its stream after each kernel it launches.  k3moe_trace_read waits
+ * for the last recorded event and fills up to `max` entries with the kernel
+ * names (static strings) and the milliseconds between consecutive events of
+ * the most recent forward; it returns the number of entries.  Tracing is
+ * process-wide and meant for one host thread; it is off by default.  Returns
+ * of k3moe_trace: the previous setting. */
+int k3moe_trace(int enable);
+int k3moe_trace_read(int max, const char** names, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

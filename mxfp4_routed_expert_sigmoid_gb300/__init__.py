@@ -1,0 +1,342 @@
+"""Python binding of libk3moe: the latent routed-expert MoE layer over MXFP4
+weights (Kimi-K3 style) for GB300 (sm_103a).
+
+This module only marshals arguments: every step of the layer runs in the CUDA
+kernels of ``lib/libk3moe.so`` (built in-tree by ``_build.py``).  PyTorch
+provides device memory and streams.  The functions carry the C ABI's names
+(``include/k3moe.h``); tensors go in and out.  If the library is missing the
+import of a function fails loudly: there is no other implementation.
+
+bf16 tensors are ``torch.bfloat16`` (int16/uint16 tensors holding bf16 bits
+are accepted and viewed).  All device tensors must be contiguous and 16-byte
+aligned.  Workspaces are uint8 device tensors; a fresh workspace must be
+zero-filled (the helpers here allocate with ``torch.zeros``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libk3moe.so")
+
+ACT_SILU_GATED = 0
+PATH_AUTO, PATH_DECODE, PATH_GROUPED = 0, 1, 2
+
+STATUS = {
+    0: "K3MOE_OK", 1: "K3MOE_ERR_INVALID_ARG", 2: "K3MOE_ERR_SHAPE", 3: "K3MOE_ERR_ALIGN",
+    4: "K3MOE_ERR_WORKSPACE", 5: "K3MOE_ERR_CUDA", 6: "K3MOE_ERR_NONFINITE",
+    7: "K3MOE_ERR_TIMEOUT", 8: "K3MOE_ERR_UNSUPPORTED",
+}
+
+#: every symbol the C header declares (checked by the CPU test suite)
+EXPORTS = (
+    "k3moe_abi_version", "k3moe_status_string", "k3moe_repack_mxfp4", "k3moe_unpack_mxfp4",
+    "k3moe_route_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_rmsnorm",
+    "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
+    "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
+    "k3moe_trace_read",
+)
+
+
+class K3MoEError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {what}")
+
+
+class LayerDesc(ctypes.Structure):
+    """Mirror of ``k3moe_layer_desc``."""
+    _fields_ = [
+        ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("f", ctypes.c_int32), ("d_router", ctypes.c_int32), ("act", ctypes.c_int32),
+        ("path", ctypes.c_int32), ("D", ctypes.c_int32), ("eps", ctypes.c_float),
+        ("reserved", ctypes.c_int32),
+        ("w1_q", ctypes.c_void_p), ("w1_s", ctypes.c_void_p), ("w3_q", ctypes.c_void_p),
+        ("w3_s", ctypes.c_void_p), ("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
+        ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
+        ("norm_gamma", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libk3moe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    f32 = ctypes.c_float
+    sigs = {
+        "k3moe_abi_version": ([], ctypes.c_int),
+        "k3moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "k3moe_repack_mxfp4": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "k3moe_unpack_mxfp4": ([vp, i64, i64, vp, vp, vp], ctypes.c_int),
+        "k3moe_route_workspace_size": ([i32, i32], sz),
+        "k3moe_route": ([vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_permute": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_rmsnorm": ([vp, i32, i32, vp, f32, vp, vp], ctypes.c_int),
+        "k3moe_gemm_bf16": ([vp, vp, i32, i32, i32, vp, i32, vp], ctypes.c_int),
+        "k3moe_workspace_size": ([ctypes.POINTER(LayerDesc), i32], sz),
+        "k3moe_forward": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_host_staging_size": ([ctypes.POINTER(LayerDesc), i32], sz),
+        "k3moe_forward_host": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_forward_routing": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, vp],
+                                  ctypes.c_int),
+        "k3moe_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "k3moe_trace": ([ctypes.c_int], ctypes.c_int),
+        "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                              ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def _check(st: int):
+    if st != 0:
+        raise K3MoEError(st, lib().k3moe_status_string(st).decode())
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _bf16(t: torch.Tensor, name: str):
+    _dev(t, name)
+    if t.dtype in (torch.int16, torch.uint16):
+        t = t.view(torch.bfloat16)
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bf16")
+    return t
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled uint8 device workspace of nbytes."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def k3moe_abi_version() -> int:
+    return lib().k3moe_abi_version()
+
+
+def k3moe_repack_mxfp4(packed: torch.Tensor, scale: torch.Tensor, out=None, stream=None):
+    """compressed-tensors (packed [rows, cols/2], scale [rows, cols/32]) -> ggml blocks [rows, cols/32, 17]."""
+    _dev(packed, "packed"), _dev(scale, "scale")
+    rows, cols = packed.shape[0], packed.shape[-1] * 2
+    if out is None:
+        out = torch.empty((rows, cols // 32, 17), dtype=torch.uint8, device=packed.device)
+    _check(lib().k3moe_repack_mxfp4(_p(packed), _p(scale), rows, cols, _p(_dev(out, "out")),
+                                    _stream(stream)))
+    return out
+
+
+def k3moe_unpack_mxfp4(blocks: torch.Tensor, packed_out=None, scale_out=None, stream=None):
+    """ggml blocks [rows, cols/32, 17] -> (packed [rows, cols/2], scale [rows, cols/32])."""
+    _dev(blocks, "blocks")
+    rows, nb = blocks.shape[0], blocks.shape[1]
+    cols = nb * 32
+    if packed_out is None:
+        packed_out = torch.empty((rows, cols // 2), dtype=torch.uint8, device=blocks.device)
+    if scale_out is None:
+        scale_out = torch.empty((rows, nb), dtype=torch.uint8, device=blocks.device)
+    _check(lib().k3moe_unpack_mxfp4(_p(blocks), rows, cols, _p(packed_out), _p(scale_out),
+                                    _stream(stream)))
+    return packed_out, scale_out
+
+
+def k3moe_route_workspace_size(T: int, E: int) -> int:
+    return lib().k3moe_route_workspace_size(T, E)
+
+
+def k3moe_route(x, router_w, bias, k: int, with_logits: bool = True, ws=None, stream=None):
+    """Router: returns (idx [T,k] int32, w [T,k] fp32, logits [T,E] fp32 or None)."""
+    x, router_w = _bf16(x, "x"), _bf16(router_w, "router_w")
+    _dev(bias, "bias")
+    T, d_r = x.shape
+    E = router_w.shape[0]
+    dev = x.device
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if with_logits else None
+    if ws is None:
+        ws = workspace(k3moe_route_workspace_size(T, E), dev)
+    _check(lib().k3moe_route(_p(x), T, d_r, _p(router_w), _p(bias), E, k, _p(idx), _p(w),
+                             _p(logits), _p(ws), ws.numel(), _stream(stream)))
+    return idx, w, logits
+
+
+def k3moe_permute(idx, E: int, ws=None, stream=None):
+    """Histogram, scan and permutation: dict counts, offsets, perm, inv (int32)."""
+    _dev(idx, "idx")
+    T, k = idx.shape
+    dev = idx.device
+    out = {
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "perm": torch.empty(T * k, dtype=torch.int32, device=dev),
+        "inv": torch.empty(T * k, dtype=torch.int32, device=dev),
+    }
+    if ws is None:
+        ws = workspace(k3moe_route_workspace_size(T, E), dev)
+    _check(lib().k3moe_permute(_p(idx), T, k, E, _p(out["counts"]), _p(out["offsets"]),
+                               _p(out["perm"]), _p(out["inv"]), _p(ws), ws.numel(),
+                               _stream(stream)))
+    return out
+
+
+def k3moe_rmsnorm(h, gamma, eps: float, out=None, stream=None):
+    h, gamma = _bf16(h, "h"), _bf16(gamma, "gamma")
+    T, D = h.shape
+    if out is None:
+        out = torch.empty_like(h)
+    _check(lib().k3moe_rmsnorm(_p(h), T, D, _p(gamma), float(eps), _p(out), _stream(stream)))
+    return out
+
+
+def k3moe_gemm_bf16(x, w, out_fp32: bool = False, out=None, stream=None):
+    """out[t, n] = sum_c x[t, c] w[n, c] on tcgen05 (bf16 in, fp32 accumulate)."""
+    x, w = _bf16(x, "x"), _bf16(w, "w")
+    T, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=x.device)
+    _check(lib().k3moe_gemm_bf16(_p(x), _p(w), T, N, K, _p(out), 1 if out_fp32 else 0,
+                                 _stream(stream)))
+    return out
+
+
+class MoELayer:
+    """Device tensors of one layer plus the ``k3moe_layer_desc`` that points at them."""
+
+    def __init__(self, *, w1_q, w1_s, w3_q, w3_s, w2_q, w2_s, router_w, router_b, k: int,
+                 norm_gamma=None, w_down=None, w_up=None, eps: float = 1e-5,
+                 path: int = PATH_AUTO, act: int = ACT_SILU_GATED):
+        self.tensors = dict(w1_q=w1_q, w1_s=w1_s, w3_q=w3_q, w3_s=w3_s, w2_q=w2_q, w2_s=w2_s,
+                            router_w=_bf16(router_w, "router_w"), router_b=router_b)
+        E, f, half_d = w1_q.shape
+        d = 2 * half_d
+        block = w_down is not None
+        if block:
+            self.tensors.update(norm_gamma=_bf16(norm_gamma, "norm_gamma"),
+                                w_down=_bf16(w_down, "w_down"), w_up=_bf16(w_up, "w_up"))
+        D = w_down.shape[1] if block else 0
+        desc = LayerDesc()
+        desc.E, desc.k, desc.d, desc.f = E, k, d, f
+        desc.d_router = D if block else d
+        desc.act, desc.path, desc.D, desc.eps, desc.reserved = act, path, D, eps, 0
+        for name, t in self.tensors.items():
+            setattr(desc, name, t.data_ptr())
+        self.desc = desc
+        self.E, self.k, self.d, self.f, self.D = E, k, d, f, D
+
+    def with_path(self, path: int) -> "MoELayer":
+        other = object.__new__(MoELayer)
+        other.__dict__.update(self.__dict__)
+        desc = LayerDesc.from_buffer_copy(self.desc)
+        desc.path = path
+        other.desc = desc
+        return other
+
+    @property
+    def width(self) -> int:
+        return self.D if self.D else self.d
+
+
+def k3moe_workspace_size(layer: MoELayer, T: int) -> int:
+    return lib().k3moe_workspace_size(ctypes.byref(layer.desc), T)
+
+
+def k3moe_host_staging_size(layer: MoELayer, T: int) -> int:
+    return lib().k3moe_host_staging_size(ctypes.byref(layer.desc), T)
+
+
+def k3moe_forward(layer: MoELayer, hidden, out=None, ws=None, stream=None):
+    """The layer (or block) on device tensors: hidden [T, width] bf16 -> out [T, width] bf16."""
+    hidden = _bf16(hidden, "hidden")
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = workspace(k3moe_workspace_size(layer, T), hidden.device)
+    _check(lib().k3moe_forward(ctypes.byref(layer.desc), _p(hidden), T, _p(out), _p(ws),
+                               ws.numel(), _stream(stream)))
+    return out
+
+
+def k3moe_forward_host(layer: MoELayer, hidden_host: torch.Tensor, out_host=None, ws=None,
+                       stream=None):
+    """The layer on HOST tensors (bf16, ideally pinned); copies happen inside the call."""
+    if hidden_host.is_cuda or not hidden_host.is_contiguous():
+        raise ValueError("hidden_host must be a contiguous host tensor")
+    if hidden_host.dtype in (torch.int16, torch.uint16):
+        hidden_host = hidden_host.view(torch.bfloat16)
+    T = hidden_host.shape[0]
+    if out_host is None:
+        out_host = torch.empty_like(hidden_host, pin_memory=hidden_host.is_pinned())
+    if ws is None:
+        ws = workspace(k3moe_workspace_size(layer, T) + k3moe_host_staging_size(layer, T))
+    _check(lib().k3moe_forward_host(ctypes.byref(layer.desc), _p(hidden_host), T, _p(out_host),
+                                    _p(ws), ws.numel(), _stream(stream)))
+    return out_host
+
+
+def k3moe_forward_routing(layer: MoELayer, ws, T: int, with_logits: bool = True, stream=None):
+    dev = ws.device
+    idx = torch.empty((T, layer.k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, layer.k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, layer.E), dtype=torch.float32, device=dev) if with_logits else None
+    _check(lib().k3moe_forward_routing(ctypes.byref(layer.desc), _p(ws), T, _p(idx), _p(w),
+                                       _p(logits), _stream(stream)))
+    return idx, w, logits
+
+
+def k3moe_get_status(ws, stream=None) -> int:
+    """Synchronise and return (and clear) the workspace's device status word."""
+    st = ctypes.c_int32(0)
+    _check(lib().k3moe_get_status(_p(ws), _stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+def k3moe_trace(enable: bool) -> bool:
+    """Turn per-kernel event tracing of k3moe_forward on or off; returns the old setting."""
+    return bool(lib().k3moe_trace(1 if enable else 0))
+
+
+def k3moe_trace_read(max_entries: int = 32):
+    """[(kernel name, ms)] of the most recent traced forward (waits for its events)."""
+    names = (ctypes.c_char_p * max_entries)()
+    ms = (ctypes.c_float * max_entries)()
+    n = lib().k3moe_trace_read(max_entries, names, ms)
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]

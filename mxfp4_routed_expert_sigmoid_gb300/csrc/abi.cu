@@ -1,0 +1,477 @@
+// Host side of the k3moe C ABI: argument checks, workspace layout, dispatch.
+// Every step of the layer runs in the kernels of this library; nothing here
+// computes on the host.
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+using namespace k3;
+
+namespace {
+
+constexpr int kDecodeMaxT = 8;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+k3moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// workspace layouts
+// ---------------------------------------------------------------------------
+struct Carve {
+    size_t off = sizeof(WsHeader);
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    }
+};
+
+struct RoutePlan {
+    size_t logits, chunk, active, total;
+};
+
+RoutePlan route_plan(int T, int E) {
+    Carve c;
+    RoutePlan p;
+    p.logits = c.take(static_cast<size_t>(T) * E * 4);
+    p.chunk = c.take(permute_scratch_bytes(T, E));
+    p.active = c.take(static_cast<size_t>(E + 1) * 4);
+    p.total = c.off;
+    return p;
+}
+
+struct FwdPlan {
+    size_t logits, idx, wts, counts, offsets, active, perm, inv, chunk;
+    size_t dec, y;                                  // decode scratch, shared y (fp32)
+    size_t xp, xp_exp, hb, h_amax, hp, hp_exp, tiles;  // grouped
+    size_t hn, z, m;                                // block mode
+    size_t total;
+    int tiles_cap;
+};
+
+FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
+    Carve c;
+    FwdPlan p{};
+    const size_t P = static_cast<size_t>(T) * d->k;
+    p.logits = c.take(static_cast<size_t>(T) * d->E * 4);
+    p.idx = c.take(P * 4);
+    p.wts = c.take(P * 4);
+    p.counts = c.take(static_cast<size_t>(d->E) * 4);
+    p.offsets = c.take(static_cast<size_t>(d->E + 1) * 4);
+    p.active = c.take(static_cast<size_t>(d->E + 1) * 4);
+    p.perm = c.take(P * 4);
+    p.inv = c.take(P * 4);
+    p.chunk = c.take(permute_scratch_bytes(T, d->E));
+    const int Td = std::min(T, kDecodeMaxT);
+    const size_t Pd = static_cast<size_t>(Td) * d->k;
+    p.dec = c.take(decode_scratch_bytes(Td, d->k, d->d, d->f));
+    p.y = c.take(std::max(P, 2 * Pd) * d->d * 4);  // grouped: 1 slot; decode: 2 slots
+    p.xp = c.take(P * d->d * 2);
+    p.xp_exp = c.take(P * 4);
+    p.hb = c.take(P * d->f * 2);
+    p.h_amax = c.take(P * 4);
+    p.hp = c.take(P * d->f * 2);
+    p.hp_exp = c.take(P * 4);
+    p.tiles_cap = static_cast<int>(grouped_tile_cap(T, d->E, d->k));
+    p.tiles = c.take(static_cast<size_t>(p.tiles_cap) * 4 * 4);
+    if (d->D > 0) {
+        p.hn = c.take(static_cast<size_t>(T) * d->D * 2);
+        p.z = c.take(static_cast<size_t>(T) * d->d * 2);
+        p.m = c.take(static_cast<size_t>(T) * d->d * 2);
+    }
+    p.total = c.off;
+    return p;
+}
+
+k3moe_status check_desc(const k3moe_layer_desc* d) {
+    if (!d) return K3MOE_ERR_INVALID_ARG;
+    if (d->E < 1 || d->k < 1 || d->d < 1 || d->f < 1 || d->d_router < 1) return K3MOE_ERR_INVALID_ARG;
+    if (d->reserved != 0) return K3MOE_ERR_INVALID_ARG;
+    if (d->k > d->E || d->k > 32 || d->E > 1024) return K3MOE_ERR_SHAPE;
+    if (d->d % 64 || d->f % 64) return K3MOE_ERR_SHAPE;
+    if (d->D < 0) return K3MOE_ERR_SHAPE;
+    if (d->D > 0) {
+        if (d->D % 128 || d->d % 128 || d->d_router != d->D) return K3MOE_ERR_SHAPE;
+        if (!(d->eps >= 0.0f)) return K3MOE_ERR_INVALID_ARG;
+        if (!d->norm_gamma || !d->w_down || !d->w_up) return K3MOE_ERR_INVALID_ARG;
+        if (!aligned16(d->norm_gamma) || !aligned16(d->w_down) || !aligned16(d->w_up))
+            return K3MOE_ERR_ALIGN;
+    } else if (d->d_router != d->d) {
+        return K3MOE_ERR_SHAPE;
+    }
+    if (d->act != K3MOE_ACT_SILU_GATED) return K3MOE_ERR_UNSUPPORTED;
+    if (d->path < K3MOE_PATH_AUTO || d->path > K3MOE_PATH_GROUPED) return K3MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {d->w1_q, d->w1_s, d->w3_q, d->w3_s, d->w2_q, d->w2_s, d->router_w, d->router_b};
+    for (const void* p : ptrs) {
+        if (!p) return K3MOE_ERR_INVALID_ARG;
+        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+    }
+    return K3MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tracing: events between the kernel launches of one forward
+// ---------------------------------------------------------------------------
+struct Trace {
+    std::mutex mu;
+    bool on = false;
+    int n = 0;
+    cudaEvent_t ev[33] = {};
+    const char* names[32] = {};
+    int n_last = 0;
+    float ms_last[32] = {};
+    const char* names_last[32] = {};
+};
+Trace g_trace;
+
+void trace_begin(cudaStream_t s) {
+    if (!g_trace.on) return;
+    g_trace.n = 0;
+    if (!g_trace.ev[0])
+        for (auto& e : g_trace.ev) cudaEventCreate(&e);
+    cudaEventRecord(g_trace.ev[0], s);
+}
+
+void trace_end() {
+    if (!g_trace.on) return;
+    g_trace.n_last = 0;
+    if (g_trace.n == 0) return;
+    // read lazily in k3moe_trace_read; remember names now
+    for (int i = 0; i < g_trace.n; ++i) g_trace.names_last[i] = g_trace.names[i];
+    g_trace.n_last = -g_trace.n;  // negative: events pending
+}
+
+}  // namespace
+
+namespace k3 {
+void trace_mark(const char* name, cudaStream_t s) {
+    if (!g_trace.on || g_trace.n >= 32) return;
+    g_trace.names[g_trace.n] = name;
+    cudaEventRecord(g_trace.ev[g_trace.n + 1], s);
+    ++g_trace.n;
+}
+}  // namespace k3
+
+extern "C" {
+
+int k3moe_trace(int enable) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    const int prev = g_trace.on ? 1 : 0;
+    g_trace.on = enable != 0;
+    return prev;
+}
+
+int k3moe_trace_read(int max, const char** names, float* ms) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    if (g_trace.n_last < 0) {
+        const int n = -g_trace.n_last;
+        cudaEventSynchronize(g_trace.ev[n]);
+        for (int i = 0; i < n; ++i) {
+            float t = 0.0f;
+            cudaEventElapsedTime(&t, g_trace.ev[i], g_trace.ev[i + 1]);
+            g_trace.ms_last[i] = t;
+        }
+        g_trace.n_last = n;
+    }
+    const int n = g_trace.n_last < max ? g_trace.n_last : max;
+    for (int i = 0; i < n; ++i) {
+        if (names) names[i] = g_trace.names_last[i];
+        if (ms) ms[i] = g_trace.ms_last[i];
+    }
+    return n;
+}
+
+int k3moe_abi_version(void) { return K3MOE_ABI_VERSION; }
+
+const char* k3moe_status_string(int status) {
+    switch (status) {
+        case K3MOE_OK: return "ok";
+        case K3MOE_ERR_INVALID_ARG: return "invalid argument";
+        case K3MOE_ERR_SHAPE: return "unsupported shape";
+        case K3MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case K3MOE_ERR_WORKSPACE: return "workspace too small";
+        case K3MOE_ERR_CUDA: return "CUDA error";
+        case K3MOE_ERR_NONFINITE: return "non-finite router logit";
+        case K3MOE_ERR_TIMEOUT: return "bounded wait expired on the device";
+        case K3MOE_ERR_UNSUPPORTED: return "unsupported activation or path";
+        default: return "unknown status";
+    }
+}
+
+k3moe_status k3moe_repack_mxfp4(const uint8_t* packed, const uint8_t* scale, int64_t rows,
+                                int64_t cols, uint8_t* blocks_out, void* stream) {
+    if (!packed || !scale || !blocks_out || rows <= 0 || cols <= 0) return K3MOE_ERR_INVALID_ARG;
+    if (cols % 32) return K3MOE_ERR_SHAPE;
+    if (!aligned16(packed)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_repack(packed, scale, rows * (cols / 32), blocks_out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t cols,
+                                uint8_t* packed_out, uint8_t* scale_out, void* stream) {
+    if (!blocks || !packed_out || !scale_out || rows <= 0 || cols <= 0) return K3MOE_ERR_INVALID_ARG;
+    if (cols % 32) return K3MOE_ERR_SHAPE;
+    if (!aligned16(packed_out)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_unpack(blocks, rows * (cols / 32), packed_out, scale_out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t k3moe_route_workspace_size(int32_t T, int32_t E) {
+    if (T < 1 || E < 1) return 0;
+    return route_plan(T, E).total;
+}
+
+k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16_t* router_w,
+                         const float* bias, int32_t E, int32_t k, int32_t* idx_out,
+                         float* w_out, float* logits_out, void* ws, size_t ws_bytes,
+                         void* stream) {
+    if (!x || !router_w || !bias || !idx_out || !w_out || !ws) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || d_r < 1 || E < 1 || k < 1) return K3MOE_ERR_INVALID_ARG;
+    if (k > E || k > 32 || E > 1024 || d_r % 64) return K3MOE_ERR_SHAPE;
+    const void* ptrs[] = {x, router_w, bias, idx_out, w_out, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+    if (logits_out && !aligned16(logits_out)) return K3MOE_ERR_ALIGN;
+    const RoutePlan p = route_plan(T, E);
+    if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RouteArgs a{};
+    a.x = x; a.T = T; a.d_r = d_r; a.w = router_w; a.bias = bias; a.E = E; a.k = k;
+    a.idx = idx_out; a.wts = w_out;
+    a.logits = logits_out ? logits_out : reinterpret_cast<float*>(base + p.logits);
+    a.hdr = reinterpret_cast<WsHeader*>(base);
+    if (T <= kDecodeMaxT) return cuda_status(launch_route_small(a, s));
+    cudaError_t e = cudaSuccess;
+    if (T >= 64 && E % 128 == 0) {
+        e = launch_gemm_bf16(x, router_w, T, E, d_r, a.logits, 1, a.hdr, device_sms(), s);
+        if (e == cudaErrorNotSupported) e = launch_logits_simt(a, s);
+    } else {
+        e = launch_logits_simt(a, s);
+    }
+    if (e != cudaSuccess) return K3MOE_ERR_CUDA;
+    return cuda_status(launch_topk(a, s));
+}
+
+k3moe_status k3moe_permute(const int32_t* idx, int32_t T, int32_t k, int32_t E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
+                           size_t ws_bytes, void* stream) {
+    if (!idx || !counts || !offsets || !perm || !inv || !ws) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || E < 1) return K3MOE_ERR_INVALID_ARG;
+    if (k > E || k > 32) return K3MOE_ERR_SHAPE;
+    const void* ptrs[] = {idx, counts, offsets, perm, inv, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+    const RoutePlan p = route_plan(T, E);
+    if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    return cuda_status(launch_permute(idx, T, k, E, counts, offsets, perm, inv,
+                                      reinterpret_cast<int32_t*>(base + p.active),
+                                      base + p.chunk, reinterpret_cast<WsHeader*>(base),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_rmsnorm(const uint16_t* h, int32_t T, int32_t D, const uint16_t* gamma,
+                           float eps, uint16_t* out, void* stream) {
+    if (!h || !gamma || !out || T < 1 || D < 1) return K3MOE_ERR_INVALID_ARG;
+    if (D % 8) return K3MOE_ERR_SHAPE;
+    if (!aligned16(h) || !aligned16(gamma) || !aligned16(out)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_rmsnorm(h, T, D, gamma, eps, out, static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_gemm_bf16(const uint16_t* x, const uint16_t* w, int32_t T, int32_t N,
+                             int32_t K, void* out, int32_t out_fp32, void* stream) {
+    if (!x || !w || !out || T < 1 || N < 1 || K < 1) return K3MOE_ERR_INVALID_ARG;
+    if (N % 128 || K % 64) return K3MOE_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return K3MOE_ERR_ALIGN;
+    const cudaError_t e = launch_gemm_bf16(x, w, T, N, K, out, out_fp32 ? 1 : 0, nullptr,
+                                           device_sms(), static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+size_t k3moe_workspace_size(const k3moe_layer_desc* desc, int32_t T_max) {
+    if (!desc || T_max < 1 || desc->E < 1 || desc->k < 1) return 0;
+    return fwd_plan(desc, T_max).total;
+}
+
+size_t k3moe_host_staging_size(const k3moe_layer_desc* desc, int32_t T) {
+    if (!desc || T < 1) return 0;
+    const size_t width = desc->D > 0 ? desc->D : desc->d;
+    return 2 * align_up(static_cast<size_t>(T) * width * 2);
+}
+
+k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    k3moe_status st = check_desc(desc);
+    if (st != K3MOE_OK) return st;
+    if (!hidden || !out || !ws || T < 1) return K3MOE_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(out) || !aligned16(ws)) return K3MOE_ERR_ALIGN;
+    const FwdPlan p = fwd_plan(desc, T);
+    if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
+    int path = desc->path;
+    if (path == K3MOE_PATH_AUTO) path = T <= kDecodeMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
+    if (path == K3MOE_PATH_DECODE && T > kDecodeMaxT) return K3MOE_ERR_UNSUPPORTED;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(base);
+    const int sms = device_sms();
+    std::lock_guard<std::mutex> trace_lock(g_trace.mu);
+    trace_begin(s);
+    struct TraceEnd { ~TraceEnd() { trace_end(); } } trace_end_guard;
+    auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+    cudaError_t e = cudaSuccess;
+
+    const uint16_t* x_router = hidden;
+    const uint16_t* x_expert = hidden;
+    uint16_t* latent_out = out;
+    if (desc->D > 0) {
+        uint16_t* hn = static_cast<uint16_t*>(at(p.hn));
+        uint16_t* z = static_cast<uint16_t*>(at(p.z));
+        if ((e = launch_rmsnorm(hidden, T, desc->D, desc->norm_gamma, desc->eps, hn, s))) return K3MOE_ERR_CUDA;
+        e = launch_gemm_bf16(hn, desc->w_down, T, desc->d, desc->D, z, 0, hdr, sms, s);
+        if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+        if (e) return K3MOE_ERR_CUDA;
+        x_router = hn;
+        x_expert = z;
+        latent_out = static_cast<uint16_t*>(at(p.m));
+    }
+
+    RouteArgs r{};
+    r.x = x_router; r.T = T; r.d_r = desc->d_router; r.w = desc->router_w; r.bias = desc->router_b;
+    r.E = desc->E; r.k = desc->k;
+    r.idx = static_cast<int32_t*>(at(p.idx));
+    r.wts = static_cast<float*>(at(p.wts));
+    r.logits = static_cast<float*>(at(p.logits));
+    r.hdr = hdr;
+    int32_t* counts = static_cast<int32_t*>(at(p.counts));
+    int32_t* offsets = static_cast<int32_t*>(at(p.offsets));
+    int32_t* perm = static_cast<int32_t*>(at(p.perm));
+    int32_t* inv = static_cast<int32_t*>(at(p.inv));
+    int32_t* active = static_cast<int32_t*>(at(p.active));
+    if (T <= kDecodeMaxT) {
+        r.counts = counts; r.offsets = offsets; r.perm = perm; r.inv = inv; r.active = active;
+        if ((e = launch_route_small(r, s))) return K3MOE_ERR_CUDA;
+    } else {
+        if (T >= 64 && desc->E % 128 == 0) {
+            e = launch_gemm_bf16(x_router, desc->router_w, T, desc->E, desc->d_router, r.logits, 1,
+                                 hdr, sms, s);
+            if (e == cudaErrorNotSupported) e = launch_logits_simt(r, s);
+        } else {
+            e = launch_logits_simt(r, s);
+        }
+        if (e) return K3MOE_ERR_CUDA;
+        if ((e = launch_topk(r, s))) return K3MOE_ERR_CUDA;
+        if ((e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active,
+                                at(p.chunk), hdr, s)))
+            return K3MOE_ERR_CUDA;
+    }
+
+    if (path == K3MOE_PATH_DECODE) {
+        DecodeArgs a{};
+        a.w1_q = desc->w1_q; a.w1_s = desc->w1_s; a.w3_q = desc->w3_q; a.w3_s = desc->w3_s;
+        a.w2_q = desc->w2_q; a.w2_s = desc->w2_s;
+        a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
+        a.offsets = offsets; a.perm = perm; a.active = active; a.wts = r.wts; a.inv = inv;
+        a.scratch = at(p.dec);
+        a.y = static_cast<float*>(at(p.y));
+        a.out = latent_out; a.hdr = hdr; a.num_sms = sms;
+        if ((e = launch_decode(a, s))) return K3MOE_ERR_CUDA;
+    } else {
+        GroupedArgs g{};
+        g.w1_q = desc->w1_q; g.w1_s = desc->w1_s; g.w3_q = desc->w3_q; g.w3_s = desc->w3_s;
+        g.w2_q = desc->w2_q; g.w2_s = desc->w2_s;
+        g.x = x_expert; g.T = T; g.E = desc->E; g.k = desc->k; g.d = desc->d; g.f = desc->f;
+        g.counts = counts; g.offsets = offsets; g.perm = perm; g.inv = inv; g.wts = r.wts;
+        g.xp = static_cast<uint16_t*>(at(p.xp));
+        g.xp_exp = static_cast<int32_t*>(at(p.xp_exp));
+        g.hb = static_cast<uint16_t*>(at(p.hb));
+        g.h_amax = static_cast<uint32_t*>(at(p.h_amax));
+        g.hp = static_cast<uint16_t*>(at(p.hp));
+        g.hp_exp = static_cast<int32_t*>(at(p.hp_exp));
+        g.y = static_cast<float*>(at(p.y));
+        g.tiles = static_cast<int32_t*>(at(p.tiles));
+        g.tiles_cap = p.tiles_cap;
+        g.out = latent_out; g.hdr = hdr; g.num_sms = sms;
+        e = launch_grouped(g, s);
+        if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+        if (e) return K3MOE_ERR_CUDA;
+    }
+
+    if (desc->D > 0) {
+        e = launch_gemm_bf16(latent_out, desc->w_up, T, desc->D, desc->d, out, 0, hdr, sms, s);
+        if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+        if (e) return K3MOE_ERR_CUDA;
+    }
+    return K3MOE_OK;
+}
+
+k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hidden_host,
+                                int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,
+                                void* stream) {
+    k3moe_status st = check_desc(desc);
+    if (st != K3MOE_OK) return st;
+    if (!hidden_host || !out_host || !ws || T < 1) return K3MOE_ERR_INVALID_ARG;
+    const size_t need = k3moe_workspace_size(desc, T);
+    const size_t stage = k3moe_host_staging_size(desc, T);
+    if (ws_bytes < need + stage) return K3MOE_ERR_WORKSPACE;
+    const size_t width = desc->D > 0 ? desc->D : desc->d;
+    const size_t bytes = static_cast<size_t>(T) * width * 2;
+    char* base = static_cast<char*>(ws);
+    uint16_t* in_dev = reinterpret_cast<uint16_t*>(base + need);
+    uint16_t* out_dev = reinterpret_cast<uint16_t*>(base + need + stage / 2);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(in_dev, hidden_host, bytes, cudaMemcpyHostToDevice, s)) return K3MOE_ERR_CUDA;
+    st = k3moe_forward(desc, in_dev, T, out_dev, ws, need, stream);
+    if (st != K3MOE_OK) return st;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s)) return K3MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws, int32_t T,
+                                   int32_t* idx_out, float* w_out, float* logits_out,
+                                   void* stream) {
+    if (!desc || !ws || !idx_out || !w_out || T < 1 || desc->E < 1 || desc->k < 1)
+        return K3MOE_ERR_INVALID_ARG;
+    const FwdPlan p = fwd_plan(desc, T);
+    const char* base = static_cast<const char*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t P = static_cast<size_t>(T) * desc->k;
+    if (cudaMemcpyAsync(idx_out, base + p.idx, P * 4, cudaMemcpyDeviceToDevice, s)) return K3MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(w_out, base + p.wts, P * 4, cudaMemcpyDeviceToDevice, s)) return K3MOE_ERR_CUDA;
+    if (logits_out &&
+        cudaMemcpyAsync(logits_out, base + p.logits, static_cast<size_t>(T) * desc->E * 4,
+                        cudaMemcpyDeviceToDevice, s))
+        return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status) {
+    if (!ws || !device_status) return K3MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return K3MOE_ERR_CUDA;
+    int32_t st = 0;
+    if (cudaMemcpy(&st, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_ERR_CUDA;
+    *device_status = st;
+    if (st != 0 && cudaMemset(ws, 0, 8) != cudaSuccess) return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,425 @@
+// Router and token -> expert permutation.
+//
+// Router (llama.cpp PR #26185 "model: add Kimi-K3 text model", review by
+// GrEarl, section "Dry run": 896 experts, 16 used, sigmoid expert-score
+// gating, exp_probs_b selection bias):
+//   l = <x, W_r[e]> (bf16 products, fp32 accumulation), s = 1 / (1 + expf(-l)),
+//   selection key s + b (fp32), top-k with ties to the lower index, slots in
+//   key order, w = s / sum(s) over the selected experts (sum in slot order).
+//
+// Top-k: each warp owns one token; every lane holds the keys of experts
+// lane, lane+32, ... as 64-bit integers (order-preserving fp32 bits of s + b
+// in the high word, ~expert in the low word, so the larger key wins and equal
+// scores fall to the lower index); k rounds of a warp-wide max extract the
+// selection in slot order.  Keys are unique, so the result is deterministic.
+//
+// Permutation: histogram of the selection, exclusive scan, and a stable
+// scatter that lists each expert's pairs in ascending token order, plus the
+// inverse map and the ascending list of experts that received any token.
+#include "common.cuh"
+
+namespace k3 {
+namespace {
+
+constexpr int kMaxE = 1024;   // experts handled by the in-register top-k
+constexpr int kKeysPerLane = kMaxE / 32;
+
+__device__ __forceinline__ uint32_t order_bits(float v) {
+    uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+// top-k of one token by one warp; logits row in global memory.  Writes idx/w
+// (global) and optionally the selection into shared memory.
+__device__ void topk_token(const float* lrow, const float* __restrict__ bias, int E,
+                           int k, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                           int32_t* sel_smem, WsHeader* hdr) {
+    const int lane = threadIdx.x & 31;
+    uint64_t key[kKeysPerLane];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kKeysPerLane; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = 0;
+        if (e < E) {
+            const float l = lrow[e];
+            bad |= !isfinite(l);
+            const float beta = sigmoid_f32(l) + bias[e];
+            key[i] = (static_cast<uint64_t>(order_bits(beta)) << 32) |
+                     static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(hdr, K3MOE_ERR_NONFINITE, 1);
+    float s_mine = 0.0f;  // lane j keeps the score of slot j
+    int e_mine = 0;
+    for (int j = 0; j < k; ++j) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int i = 0; i < kKeysPerLane; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+        // the owner lane removes the winner
+        if ((e & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < kKeysPerLane; ++i)
+                if (key[i] == best) key[i] = 0;
+        }
+        if (lane == j) {
+            e_mine = e;
+            s_mine = sigmoid_f32(lrow[e]);
+        }
+    }
+    // renormalise over the selection, summing in slot order
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, s_mine, j);
+    if (lane < k) {
+        idx_out[lane] = e_mine;
+        w_out[lane] = s_mine / sum;
+        if (sel_smem) sel_smem[lane] = e_mine;
+    }
+}
+
+// exclusive scan of n <= 4 * blockDim ints in shared memory (in place);
+// returns the total.  Requires blockDim.x == 256.
+__device__ int block_exclusive_scan(int* data, int n) {
+    __shared__ int warp_tot[8];
+    __shared__ int total_s;
+    const int tid = threadIdx.x;
+    int v[4];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int p = tid * 4 + i;
+        v[i] = p < n ? data[p] : 0;
+        local += v[i];
+    }
+    // inclusive warp scan of the per-thread totals
+    int incl = local;
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            int t = warp_tot[w];
+            warp_tot[w] = run;
+            run += t;
+        }
+        total_s = run;
+    }
+    __syncthreads();
+    int run = warp_tot[wid] + incl - local;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int p = tid * 4 + i;
+        if (p < n) data[p] = run;
+        run += v[i];
+    }
+    __syncthreads();
+    return total_s;
+}
+
+// permutation of a small selection held in shared memory (T*k <= 256, E <= 1024)
+__device__ void permute_small(const int32_t* sel, int T, int k, int E, int32_t* counts,
+                              int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active) {
+    __shared__ int cnt[kMaxE];
+    __shared__ int off[kMaxE];
+    const int tid = threadIdx.x;
+    const int P = T * k;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cnt[sel[p]], 1);
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) off[e] = cnt[e];
+    __syncthreads();
+    block_exclusive_scan(off, E);
+    for (int e = tid; e < E; e += blockDim.x) {
+        counts[e] = cnt[e];
+        offsets[e] = off[e];
+    }
+    if (tid == 0) offsets[E] = P;
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = sel[p];
+        int rank = 0;
+        for (int q = 0; q < p; ++q) rank += (sel[q] == e);
+        const int row = off[e] + rank;
+        perm[row] = p;
+        inv[p] = row;
+    }
+    __syncthreads();
+    // ascending list of experts that received a token
+    for (int e = tid; e < E; e += blockDim.x) off[e] = cnt[e] > 0 ? 1 : 0;
+    __syncthreads();
+    const int n_active = block_exclusive_scan(off, E);
+    for (int e = tid; e < E; e += blockDim.x)
+        if (cnt[e] > 0) active[off[e]] = e;
+    if (tid == 0) active[E] = n_active;
+}
+
+// Logits by GEMV (one warp per expert, all T tokens), then the last CTA to
+// finish runs top-k for every token and, if requested, the permutation.
+__global__ void __launch_bounds__(256)
+route_small_kernel(RouteArgs a) {
+    __shared__ int32_t sel[256];
+    __shared__ uint32_t ticket_s;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int e = blockIdx.x * 8 + wid;
+    if (e < a.E) {
+        float acc[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
+        const uint16_t* wrow = a.w + static_cast<size_t>(e) * a.d_r;
+        for (int c0 = 0; c0 < a.d_r; c0 += 256 * 4) {
+            uint4 wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 256 + lane * 8;
+                wv[u] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 256 + lane * 8;
+                if (c >= a.d_r) continue;
+                const uint32_t wq[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    if (t >= a.T) break;
+                    const uint4 xv = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.d_r + c);
+                    const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+                    float s = acc[t];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        s = fmaf(__uint_as_float(wq[i] << 16), __uint_as_float(xq[i] << 16), s);
+                        s = fmaf(__uint_as_float(wq[i] & 0xFFFF0000u),
+                                 __uint_as_float(xq[i] & 0xFFFF0000u), s);
+                    }
+                    acc[t] = s;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t >= a.T) break;
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) a.logits[static_cast<size_t>(t) * a.E + e] = v;
+        }
+    }
+    // last CTA to finish does the selection
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ticket_s = atomicAdd(&a.hdr->counters[CTR_ROUTE], 1u);
+    __syncthreads();
+    if (ticket_s != gridDim.x - 1) return;
+    if (threadIdx.x == 0) a.hdr->counters[CTR_ROUTE] = 0;
+    __threadfence();
+    for (int t = wid; t < a.T; t += 8)
+        topk_token(a.logits + static_cast<size_t>(t) * a.E, a.bias, a.E, a.k,
+                   a.idx + static_cast<size_t>(t) * a.k, a.wts + static_cast<size_t>(t) * a.k,
+                   sel + t * a.k, a.hdr);
+    __syncthreads();
+    if (a.counts)
+        permute_small(sel, a.T, a.k, a.E, a.counts, a.offsets, a.perm, a.inv, a.active);
+}
+
+__global__ void __launch_bounds__(256)
+topk_kernel(RouteArgs a) {
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    topk_token(a.logits + static_cast<size_t>(t) * a.E, a.bias, a.E, a.k,
+               a.idx + static_cast<size_t>(t) * a.k, a.wts + static_cast<size_t>(t) * a.k,
+               nullptr, a.hdr);
+}
+
+// Plain tiled SIMT logits for moderate T: 64 tokens x 64 experts per CTA.
+__global__ void __launch_bounds__(256)
+logits_simt_kernel(RouteArgs a) {
+    __shared__ float xs[64][33];
+    __shared__ float ws[64][33];
+    const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads, 4x4 each
+    float acc[4][4] = {};
+    for (int c0 = 0; c0 < a.d_r; c0 += 32) {
+        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+            const int r = i >> 5, c = i & 31;
+            const int t = t0 + r, e = e0 + r;
+            xs[r][c] = (t < a.T) ? bf16_to_f32(a.x[static_cast<size_t>(t) * a.d_r + c0 + c]) : 0.0f;
+            ws[r][c] = (e < a.E) ? bf16_to_f32(a.w[static_cast<size_t>(e) * a.d_r + c0 + c]) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c) {
+            float xv[4], wv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xv[i] = xs[ty * 4 + i][c];
+                wv[i] = ws[tx * 4 + i][c];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
+            if (t < a.T && e < a.E) a.logits[static_cast<size_t>(t) * a.E + e] = acc[i][j];
+        }
+}
+
+// ---- chunked permutation for any T ----------------------------------------
+constexpr int kChunk = 64;  // tokens per chunk
+
+__global__ void __launch_bounds__(256)
+perm_count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* chunk_cnt,
+                  WsHeader* hdr) {
+    extern __shared__ int hist[];
+    const int c = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int t0 = c * kChunk, t1 = min(T, t0 + kChunk);
+    for (int p = t0 * k + threadIdx.x; p < t1 * k; p += blockDim.x) {
+        const int e = idx[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[e], 1);
+        else
+            set_error(hdr, K3MOE_ERR_INVALID_ARG, 2);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_cnt[static_cast<size_t>(c) * E + e] = hist[e];
+}
+
+// one CTA: per-expert running sums over chunks, exclusive scan over experts,
+// active list
+__global__ void __launch_bounds__(256)
+perm_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int P, int32_t* counts,
+                 int32_t* offsets, int32_t* active) {
+    extern __shared__ int sm[];  // [2 * E]
+    int* tot = sm;
+    int* flag = sm + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            int* p = chunk_cnt + static_cast<size_t>(c) * E + e;
+            const int v = *p;
+            *p = run;  // exclusive within the expert
+            run += v;
+        }
+        tot[e] = run;
+        counts[e] = run;
+        flag[e] = run > 0 ? 1 : 0;
+    }
+    __syncthreads();
+    // scan in chunks of 1024 (block_exclusive_scan handles up to 1024 entries)
+    int base = 0, abase = 0;
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        const int n = min(1024, E - e0);
+        const int t = block_exclusive_scan(tot + e0, n);
+        const int ta = block_exclusive_scan(flag + e0, n);
+        for (int e = threadIdx.x; e < n; e += blockDim.x) {
+            offsets[e0 + e] = base + tot[e0 + e];
+            if (counts[e0 + e] > 0) active[abase + flag[e0 + e]] = e0 + e;
+        }
+        base += t;
+        abase += ta;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = P;
+        active[E] = abase;
+    }
+}
+
+// one warp per chunk: tokens in order, slots in parallel (distinct experts)
+__global__ void __launch_bounds__(32)
+perm_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                    int32_t* perm, int32_t* inv) {
+    extern __shared__ int running[];
+    const int c = blockIdx.x, lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32)
+        running[e] = offsets[e] + chunk_base[static_cast<size_t>(c) * E + e];
+    __syncwarp();
+    const int t0 = c * kChunk, t1 = min(T, t0 + kChunk);
+    for (int t = t0; t < t1; ++t) {
+        if (lane < k) {
+            const int p = t * k + lane;
+            const int e = idx[p];
+            if (e >= 0 && e < E) {
+                const int row = running[e];
+                running[e] = row + 1;
+                perm[row] = p;
+                inv[p] = row;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
+    const int grid = (a.E + 7) / 8;
+    route_small_kernel<<<grid, 256, 0, s>>>(a);
+    trace_mark("route_small", s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s) {
+    topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a);
+    trace_mark("topk", s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logits_simt(const RouteArgs& a, cudaStream_t s) {
+    dim3 grid((a.E + 63) / 64, (a.T + 63) / 64);
+    logits_simt_kernel<<<grid, 256, 0, s>>>(a);
+    trace_mark("logits_simt", s);
+    return cudaGetLastError();
+}
+
+size_t permute_scratch_bytes(int T, int E) {
+    const size_t nchunks = (static_cast<size_t>(T) + kChunk - 1) / kChunk;
+    return align_up(nchunks * E * sizeof(int32_t));
+}
+
+cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                           void* scratch, WsHeader* hdr, cudaStream_t s) {
+    const int nchunks = (T + kChunk - 1) / kChunk;
+    int32_t* chunk = static_cast<int32_t*>(scratch);
+    const size_t smem = static_cast<size_t>(E) * sizeof(int);
+    if (smem > 48 * 1024) {
+        cudaFuncSetAttribute(perm_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+        cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    }
+    if (2 * smem > 48 * 1024)
+        cudaFuncSetAttribute(perm_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(2 * smem));
+    perm_count_kernel<<<nchunks, 256, smem, s>>>(idx, T, k, E, chunk, hdr);
+    trace_mark("perm_count", s);
+    perm_scan_kernel<<<1, 256, 2 * smem, s>>>(chunk, nchunks, E, T * k, counts, offsets, active);
+    trace_mark("perm_scan", s);
+    perm_scatter_kernel<<<nchunks, 32, smem, s>>>(idx, T, k, E, chunk, offsets, perm, inv);
+    trace_mark("perm_scatter", s);
+    return cudaGetLastError();
+}
+
+}  // namespace k3

@@ -1,0 +1,129 @@
+"""GPU parity of the tcgen05 kernels: the dense bf16 GEMM (latent projections,
+router logits at large T) and the grouped expert path of k3moe_forward.
+
+Dense GEMM: fp32 accumulation of exact bf16 products; compared with the
+float64 product within 1e-5 of the sum of |products| (plus bf16 output
+rounding when the output is bf16).  Layer outputs: max |err| per token <=
+1e-2 x RMS of the oracle row (spec tolerance of the dequantising path).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import bf16_tensor_to_np, make_layer, oracle_forward, rel_err_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def k3():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mxfp4_routed_expert_sigmoid_gb300 as k3mod
+
+    return k3mod
+
+
+@pytest.mark.parametrize("T,N,K,fp32", [(1, 128, 64, True), (300, 256, 320, False),
+                                        (1000, 896, 3584, True), (512, 3584, 1024, False),
+                                        (257, 384, 7168, False)])
+def test_gemm_bf16(k3, T, N, K, fp32):
+    import torch
+
+    rng = np.random.default_rng(T + N + K)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
+    w = synth.f32_to_bf16_bits((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    out = k3.k3moe_gemm_bf16(to_dev(x, "cuda"), to_dev(w, "cuda"), out_fp32=fp32)
+    got = out.float().cpu().numpy().astype(np.float64)
+    xf, wf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(w)
+    ref = xf @ wf.T
+    bound = np.abs(xf) @ np.abs(wf).T
+    tol = 1e-5 * bound + (0 if fp32 else 2.0 ** -8 * np.abs(ref))
+    assert np.all(np.abs(got - ref) <= tol + 1e-30), np.max(np.abs(got - ref) - tol)
+
+
+def compare_forward(k3, cfg, path, tokens=None, bundle=None, tol=TOL):
+    layer, dense, expert, _ = bundle or make_layer(cfg, path=path)
+    x = to_dev(dense["hidden"], "cuda")
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))
+    out = k3.k3moe_forward(layer, x, ws=ws)
+    idx_gpu, _, _ = k3.k3moe_forward_routing(layer, ws, cfg.T)
+    assert k3.k3moe_get_status(ws) == 0
+    got = bf16_tensor_to_np(out)
+    idx_gpu = idx_gpu.cpu().numpy().astype(np.int64)
+    tokens = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+    ref = oracle_forward(cfg, dense, expert, tokens=tokens)
+    thr = 1e-3 if cfg.block else 1e-5
+    near = ref["margin"] < thr
+    same = np.all(ref["idx"] == idx_gpu[tokens], axis=1)
+    assert np.all(same | near), "selection differs outside near ties"
+    if np.any(~same):
+        ref = oracle_forward(cfg, dense, expert, tokens=tokens, idx=idx_gpu[tokens])
+    err = rel_err_rows(got[tokens], ref["out"])
+    assert np.all(err <= tol), f"max err/rms {err.max():.3e} at token {tokens[np.argmax(err)]}"
+    return out, ws, err
+
+
+@pytest.mark.parametrize("T", [4, 9, 33])
+def test_tiny_grouped(k3, T):
+    compare_forward(k3, synth.custom("tiny", T=T), 2)
+
+
+@pytest.mark.parametrize("T", [8, 40, 300])
+def test_mid_grouped(k3, T):
+    # several m-tiles, K stages and units; ragged expert segments
+    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1152, seed_index=21)
+    compare_forward(k3, cfg, 2)
+
+
+def test_paths_agree(k3):
+    """Decode and grouped paths on the same 8 tokens: both within tolerance of
+    the oracle and of each other."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=8, E=64, k=8, d=768, f=1152, seed_index=22)
+    bundle = make_layer(cfg, path=1)
+    out_d, _, _ = compare_forward(k3, cfg, 1, bundle=bundle)
+    layer_g = bundle[0].with_path(2)
+    out_g, _, _ = compare_forward(k3, cfg, 2, bundle=(layer_g,) + tuple(bundle[1:]))
+    a, b = bf16_tensor_to_np(out_d), bf16_tensor_to_np(out_g)
+    assert np.all(rel_err_rows(a, b) <= 2 * TOL)
+
+
+def test_grouped_deterministic_and_power_of_two(k3):
+    import torch
+
+    cfg = synth.custom("decode_t1", T=64, E=32, k=4, d=512, f=384, seed_index=23)
+    layer, dense, expert, ex = make_layer(cfg, path=2)
+    x = to_dev(dense["hidden"], "cuda")
+    out1 = k3.k3moe_forward(layer, x)
+    out2 = k3.k3moe_forward(layer, x)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    ex2 = dict(ex)
+    ex2["w2_s"] = ex["w2_s"] + 1
+    layer2 = k3.MoELayer(router_w=layer.tensors["router_w"], router_b=layer.tensors["router_b"],
+                         k=cfg.k, path=2, **ex2)
+    out3 = k3.k3moe_forward(layer2, x)
+    assert torch.equal(out3.float(), 2 * out1.float())
+
+
+@pytest.mark.parametrize("T,path", [(4, 1), (4, 2), (300, 2)])
+def test_block_small(k3, T, path):
+    """Full latent block (RMSNorm, projections, router at the model width)."""
+    cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=256, f=384, D=512, seed_index=24)
+    compare_forward(k3, cfg, path)
+
+
+def test_chunk_t512_full_sampled(k3):
+    cfg = synth.CONFIGS["chunk_t512"]
+    rng = np.random.default_rng(5)
+    toks = np.sort(rng.choice(cfg.T, 4, replace=False))
+    compare_forward(k3, cfg, 0, tokens=toks)
