@@ -48,7 +48,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 decode, 2 grouped")
+    ap.add_argument("--E", type=int, default=0,
+                    help="fewer resident experts (small profiling captures only; not a bench line)")
     return ap.parse_args()
+
+
+def bench_config(args):
+    cfg = synth.CONFIGS[args.config]
+    if args.E:
+        cfg = synth.custom(cfg.name, E=args.E)
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -203,7 +212,7 @@ def reference_arm(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    cfg = synth.CONFIGS[args.config]
+    cfg = bench_config(args)
     dense = synth.dense_inputs(cfg)
     pool = token_pool(cfg, max(args.steps + args.warmup, 1))
     nt, times = time_oracle(cfg, pool, args.steps, args.warmup, dense)
@@ -240,7 +249,7 @@ def ours_arm(args):
     __graft_entry__.build()
     import mxfp4_routed_expert_sigmoid_gb300 as k3
 
-    cfg = synth.CONFIGS[args.config]
+    cfg = bench_config(args)
     dense = synth.dense_inputs(cfg)
     ex = synth.experts_torch(cfg, dev)
 
@@ -263,8 +272,10 @@ def ours_arm(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    ws_f = ws[:ws_fwd]
+
     def step(i):
-        k3.k3moe_forward(layer, pool[i % args.pool], out=out, ws=ws[:ws_fwd])
+        k3.k3moe_forward(layer, pool[i % args.pool], out=out, ws=ws_f)
 
     # routing of every pool entry: experts touched per step (algorithmic bytes)
     uniq = []
@@ -275,8 +286,25 @@ def ours_arm(args):
     if k3.k3moe_get_status(ws) != 0:
         raise RuntimeError("device status error during setup")
 
-    for i in range(args.warmup):
-        step(i)
+    # one CUDA graph per token batch: the forward's launches replay back to
+    # back on the device, without host launch overhead between them
+    def capture(traced):
+        k3.k3moe_trace(traced)
+        step(0)  # outside capture: creates the trace events on first use
+        torch.cuda.synchronize()
+        graphs = []
+        cap = torch.cuda.Stream()
+        for i in range(args.pool):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                step(i)
+            graphs.append(gr)
+        k3.k3moe_trace(False)
+        return graphs
+
+    graphs = capture(False)
+    for i in range(max(args.warmup, 3)):
+        graphs[i % args.pool].replay()
     torch.cuda.synchronize()
 
     # ---- timed region: K steps, per-step events on the launching stream ----
@@ -289,7 +317,7 @@ def ours_arm(args):
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)
-            step(args.warmup + i)
+            graphs[(args.warmup + i) % args.pool].replay()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -304,18 +332,18 @@ def ours_arm(args):
     value = tokens / (total_ms / 1e3)
 
     # ---- per-kernel durations (traced pass over the same steps) ----
-    k3.k3moe_trace(True)
+    tgraphs = capture(True)
     per_kernel = {}
     launches_per_step = 0
     for i in range(args.steps):
         flush.zero_()
-        step(args.warmup + i)
+        tgraphs[(args.warmup + i) % args.pool].replay()
         tr = k3.k3moe_trace_read()
         launches_per_step = len(tr)
         for name, ms in tr:
             per_kernel.setdefault(name, []).append(ms)
-    k3.k3moe_trace(False)
     kern_mean = {n: sum(v) / len(v) for n, v in per_kernel.items()}
+    del graphs, tgraphs
 
     # ---- end to end through the host-buffer entry point ----
     width = layer.width

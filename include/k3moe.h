@@ -232,12 +232,13 @@ k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws,
 k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status);
 
 /* Kernel tracing.  While enabled (enable != 0), k3moe_forward records a CUDA
- * event on its stream after each kernel it launches.  k3moe_trace_read waits
- * for the last recorded event and fills up to `max` entries with the kernel
- * names (static strings) and the milliseconds between consecutive events of
- * the most recent forward; it returns the number of entries.  Tracing is
- * process-wide and meant for one host thread; it is off by default.  Returns
- * of k3moe_trace: the previous setting. */
+ * event on its stream after each kernel it launches (a forward captured into
+ * a CUDA graph captures the event records too, and each replay re-records
+ * them).  k3moe_trace_read waits for the last event and fills up to `max`
+ * entries with the kernel names (static strings) and the milliseconds between
+ * consecutive events of the most recently traced forward; it returns the
+ * number of entries.  Tracing is process-wide and meant for one host thread;
+ * it is off by default.  k3moe_trace returns the previous setting. */
 int k3moe_trace(int enable);
 int k3moe_trace_read(int max, const char** names, float* ms);
 

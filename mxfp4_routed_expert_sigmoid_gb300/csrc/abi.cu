@@ -150,11 +150,10 @@ void trace_begin(cudaStream_t s) {
 
 void trace_end() {
     if (!g_trace.on) return;
-    g_trace.n_last = 0;
-    if (g_trace.n == 0) return;
-    // read lazily in k3moe_trace_read; remember names now
+    // the events are read in k3moe_trace_read (they may also be replayed by a
+    // CUDA graph that captured this forward); remember the names now
     for (int i = 0; i < g_trace.n; ++i) g_trace.names_last[i] = g_trace.names[i];
-    g_trace.n_last = -g_trace.n;  // negative: events pending
+    g_trace.n_last = g_trace.n;
 }
 
 }  // namespace
@@ -179,15 +178,14 @@ int k3moe_trace(int enable) {
 
 int k3moe_trace_read(int max, const char** names, float* ms) {
     std::lock_guard<std::mutex> lock(g_trace.mu);
-    if (g_trace.n_last < 0) {
-        const int n = -g_trace.n_last;
+    if (g_trace.n_last > 0) {
+        const int n = g_trace.n_last;
         cudaEventSynchronize(g_trace.ev[n]);
         for (int i = 0; i < n; ++i) {
             float t = 0.0f;
             cudaEventElapsedTime(&t, g_trace.ev[i], g_trace.ev[i + 1]);
             g_trace.ms_last[i] = t;
         }
-        g_trace.n_last = n;
     }
     const int n = g_trace.n_last < max ? g_trace.n_last : max;
     for (int i = 0; i < n; ++i) {

@@ -37,6 +37,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -662,10 +663,18 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& a3, const CUtenso
                       const TcParams& p, int grid, cudaStream_t s, const char* name) {
     constexpr size_t smem = smem_bytes<MODE>();
     static_assert(smem <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    // the attribute is per device; set it once per device (not inside graph captures)
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        done.fetch_or(bit);
+    }
     tc_gemm_kernel<MODE><<<grid, Cfg<MODE>::THREADS, smem, s>>>(a, a3, b, p);
     trace_mark(name, s);
     return cudaGetLastError();

@@ -4,7 +4,8 @@ router logits at large T) and the grouped expert path of k3moe_forward.
 Dense GEMM: fp32 accumulation of exact bf16 products; compared with the
 float64 product within 1e-5 of the sum of |products| (plus bf16 output
 rounding when the output is bf16).  Layer outputs: max |err| per token <=
-1e-2 x RMS of the oracle row (spec tolerance of the dequantising path).
+1e-2 x RMS of the oracle row (the stated tolerance of the dequantising path),
+plus half a bf16 ulp for the conversion to the bf16 output.
 """
 import numpy as np
 import pytest
@@ -95,7 +96,7 @@ def test_paths_agree(k3):
     layer_g = bundle[0].with_path(2)
     out_g, _, _ = compare_forward(k3, cfg, 2, bundle=(layer_g,) + tuple(bundle[1:]))
     a, b = bf16_tensor_to_np(out_d), bf16_tensor_to_np(out_g)
-    assert np.all(rel_err_rows(a, b) <= 2 * TOL)
+    assert np.all(rel_err_rows(a, b) <= 2 * TOL + 2.0 ** -8)
 
 
 def test_grouped_deterministic_and_power_of_two(k3):
