@@ -289,22 +289,16 @@ def ours_arm(args):
     # one CUDA graph per token batch: the forward's launches replay back to
     # back on the device, without host launch overhead between them
     def capture(traced):
+        # one library-made CUDA graph of k3moe_forward per token batch
         k3.k3moe_trace(traced)
-        step(0)  # outside capture: creates the trace events on first use
+        graphs = [k3.ForwardGraph(layer, pool[i], out, ws_f) for i in range(args.pool)]
         torch.cuda.synchronize()
-        graphs = []
-        cap = torch.cuda.Stream()
-        for i in range(args.pool):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=cap):
-                step(i)
-            graphs.append(gr)
         k3.k3moe_trace(False)
         return graphs
 
     graphs = capture(False)
     for i in range(max(args.warmup, 3)):
-        graphs[i % args.pool].replay()
+        graphs[i % args.pool].launch(stream)
     torch.cuda.synchronize()
 
     # ---- timed region: K steps, per-step events on the launching stream ----
@@ -317,7 +311,7 @@ def ours_arm(args):
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)
-            graphs[(args.warmup + i) % args.pool].replay()
+            graphs[(args.warmup + i) % args.pool].launch(stream)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -337,7 +331,7 @@ def ours_arm(args):
     launches_per_step = 0
     for i in range(args.steps):
         flush.zero_()
-        tgraphs[(args.warmup + i) % args.pool].replay()
+        tgraphs[(args.warmup + i) % args.pool].launch(stream)
         tr = k3.k3moe_trace_read()
         launches_per_step = len(tr)
         for name, ms in tr:

@@ -219,6 +219,21 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
                                 int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/* CUDA graph of one k3moe_forward with fixed buffers, for callers that run
+ * the same layer call repeatedly (a decode loop): the graph replays every
+ * kernel of the forward back to back on the device, without per-kernel host
+ * launch overhead.  k3moe_graph_create runs the forward once on a private
+ * stream (one-time set-up), then captures it (thread-local capture mode) and
+ * instantiates the executable graph; it allocates the graph objects (host and
+ * driver), which k3moe_graph_destroy frees.  The buffers named here must stay
+ * valid while the graph exists; new inputs are written into `hidden` in place.
+ * k3moe_graph_launch enqueues one replay on `stream` and allocates nothing.
+ * Errors: those of k3moe_forward, CUDA if capture or instantiation fails. */
+k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                                uint16_t* out, void* ws, size_t ws_bytes, void** graph_out);
+k3moe_status k3moe_graph_launch(void* graph, void* stream);
+k3moe_status k3moe_graph_destroy(void* graph);
+
 /* Copy the routing of the last k3moe_forward that used `ws` (device to
  * device, on `stream`): idx_out [T, k] int32, w_out [T, k] fp32, logits_out
  * [T, E] fp32 or NULL. */

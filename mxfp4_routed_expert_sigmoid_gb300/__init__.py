@@ -37,6 +37,7 @@ EXPORTS = (
     "k3moe_route_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_rmsnorm",
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
+    "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
     "k3moe_trace_read",
 )
 
@@ -93,6 +94,10 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int),
         "k3moe_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "k3moe_trace": ([ctypes.c_int], ctypes.c_int),
+        "k3moe_graph_create": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz,
+                                ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+        "k3moe_graph_launch": ([vp, vp], ctypes.c_int),
+        "k3moe_graph_destroy": ([vp], ctypes.c_int),
         "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                               ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
     }
@@ -340,3 +345,41 @@ def k3moe_trace_read(max_entries: int = 32):
     ms = (ctypes.c_float * max_entries)()
     n = lib().k3moe_trace_read(max_entries, names, ms)
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+class ForwardGraph:
+    """A CUDA graph of one k3moe_forward with fixed buffers (k3moe_graph_create)."""
+
+    def __init__(self, layer: MoELayer, hidden, out, ws):
+        hidden = _bf16(hidden, "hidden")
+        self._keep = (layer, hidden, out, ws)
+        h = ctypes.c_void_p(None)
+        _check(lib().k3moe_graph_create(ctypes.byref(layer.desc), _p(hidden), hidden.shape[0],
+                                        _p(out), _p(ws), ws.numel(), ctypes.byref(h)))
+        self.handle = h
+
+    def launch(self, stream=None):
+        _check(lib().k3moe_graph_launch(self.handle, _stream(stream)))
+
+    def close(self):
+        if self.handle:
+            lib().k3moe_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def k3moe_graph_create(layer: MoELayer, hidden, out, ws) -> ForwardGraph:
+    return ForwardGraph(layer, hidden, out, ws)
+
+
+def k3moe_graph_launch(graph: ForwardGraph, stream=None):
+    graph.launch(stream)
+
+
+def k3moe_graph_destroy(graph: ForwardGraph):
+    graph.close()

@@ -1,6 +1,7 @@
 // Host side of the k3moe C ABI: argument checks, workspace layout, dispatch.
 // Every step of the layer runs in the kernels of this library; nothing here
 // computes on the host.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -29,6 +30,15 @@ int device_sms() {
 }
 
 k3moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA; }
+
+// PDL is on unless K3MOE_NO_PDL is set in the environment (read once)
+bool pdl_on() {
+    static const bool on = [] {
+        const char* v = getenv("K3MOE_NO_PDL");
+        return !(v && v[0] && v[0] != '0');
+    }();
+    return on;
+}
 
 // ---------------------------------------------------------------------------
 // workspace layouts
@@ -84,7 +94,7 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     p.y = c.take(std::max(P, 2 * Pd) * d->d * 4);  // grouped: 1 slot; decode: 2 slots
     p.xp = c.take(P * d->d * 2);
     p.xp_exp = c.take(P * 4);
-    p.hb = c.take(P * d->f * 2);
+    p.hb = c.take(P * d->f * 4);
     p.h_amax = c.take(P * 4);
     p.hp = c.take(P * d->f * 2);
     p.hp_exp = c.take(P * 4);
@@ -159,6 +169,8 @@ void trace_end() {
 }  // namespace
 
 namespace k3 {
+bool pdl_enabled() { return pdl_on(); }
+
 void trace_mark(const char* name, cudaStream_t s) {
     if (!g_trace.on || g_trace.n >= 32) return;
     g_trace.names[g_trace.n] = name;
@@ -364,8 +376,10 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     int32_t* perm = static_cast<int32_t*>(at(p.perm));
     int32_t* inv = static_cast<int32_t*>(at(p.inv));
     int32_t* active = static_cast<int32_t*>(at(p.active));
+    const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_DECODE && desc->D == 0;
     if (T <= kDecodeMaxT) {
         r.counts = counts; r.offsets = offsets; r.perm = perm; r.inv = inv; r.active = active;
+        if (fuse_prep) decode_x16_slots(at(p.dec), T, desc->d, &r.x16, &r.xexp);
         if ((e = launch_route_small(r, s))) return K3MOE_ERR_CUDA;
     } else {
         if (T >= 64 && desc->E % 128 == 0) {
@@ -387,6 +401,7 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
         a.w1_q = desc->w1_q; a.w1_s = desc->w1_s; a.w3_q = desc->w3_q; a.w3_s = desc->w3_s;
         a.w2_q = desc->w2_q; a.w2_s = desc->w2_s;
         a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
+        a.x16_ready = fuse_prep ? 1 : 0;
         a.offsets = offsets; a.perm = perm; a.active = active; a.wts = r.wts; a.inv = inv;
         a.scratch = at(p.dec);
         a.y = static_cast<float*>(at(p.y));
@@ -400,7 +415,7 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
         g.counts = counts; g.offsets = offsets; g.perm = perm; g.inv = inv; g.wts = r.wts;
         g.xp = static_cast<uint16_t*>(at(p.xp));
         g.xp_exp = static_cast<int32_t*>(at(p.xp_exp));
-        g.hb = static_cast<uint16_t*>(at(p.hb));
+        g.hf = static_cast<float*>(at(p.hb));
         g.h_amax = static_cast<uint32_t*>(at(p.h_amax));
         g.hp = static_cast<uint16_t*>(at(p.hp));
         g.hp_exp = static_cast<int32_t*>(at(p.hp_exp));
@@ -441,6 +456,64 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
     if (st != K3MOE_OK) return st;
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s)) return K3MOE_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
+}
+
+namespace {
+struct ForwardGraph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+}  // namespace
+
+k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                                uint16_t* out, void* ws, size_t ws_bytes, void** graph_out) {
+    if (!graph_out) return K3MOE_ERR_INVALID_ARG;
+    *graph_out = nullptr;
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return K3MOE_ERR_CUDA;
+    // one uncaptured forward: argument checks and one-time set-up
+    k3moe_status st = k3moe_forward(desc, hidden, T, out, ws, ws_bytes, cs);
+    if (st == K3MOE_OK && cudaStreamSynchronize(cs) != cudaSuccess) st = K3MOE_ERR_CUDA;
+    ForwardGraph* fg = nullptr;
+    if (st == K3MOE_OK) {
+        fg = new ForwardGraph();
+        if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+            st = K3MOE_ERR_CUDA;
+        } else {
+            st = k3moe_forward(desc, hidden, T, out, ws, ws_bytes, cs);
+            const cudaError_t e = cudaStreamEndCapture(cs, &fg->graph);
+            if (st == K3MOE_OK && e != cudaSuccess) st = K3MOE_ERR_CUDA;
+        }
+        if (st == K3MOE_OK && cudaGraphInstantiate(&fg->exec, fg->graph, 0) != cudaSuccess)
+            st = K3MOE_ERR_CUDA;
+    }
+    cudaStreamDestroy(cs);
+    if (st != K3MOE_OK) {
+        if (fg) {
+            if (fg->exec) cudaGraphExecDestroy(fg->exec);
+            if (fg->graph) cudaGraphDestroy(fg->graph);
+            delete fg;
+        }
+        cudaGetLastError();  // leave no pending error behind
+        return st;
+    }
+    *graph_out = fg;
+    return K3MOE_OK;
+}
+
+k3moe_status k3moe_graph_launch(void* graph, void* stream) {
+    if (!graph) return K3MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaGraphLaunch(static_cast<ForwardGraph*>(graph)->exec,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_graph_destroy(void* graph) {
+    if (!graph) return K3MOE_ERR_INVALID_ARG;
+    ForwardGraph* fg = static_cast<ForwardGraph*>(graph);
+    cudaError_t e1 = cudaGraphExecDestroy(fg->exec);
+    cudaError_t e2 = cudaGraphDestroy(fg->graph);
+    delete fg;
+    return (e1 == cudaSuccess && e2 == cudaSuccess) ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
 
 k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws, int32_t T,

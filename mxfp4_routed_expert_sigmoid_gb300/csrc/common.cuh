@@ -135,6 +135,15 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl() may
+// start while its predecessor on the stream is still running: it must call
+// pdl_wait() before it touches anything the predecessor writes or reads.
+// pdl_trigger() lets the next kernel begin launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -153,6 +162,24 @@ namespace k3 {
 // Tracing hook: records an event after a launch when tracing is on (abi.cu).
 void trace_mark(const char* name, cudaStream_t s);
 
+// Kernel launch with programmatic stream serialisation (see pdl_wait).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 struct RouteArgs {
     const uint16_t* x;
     int T, d_r;
@@ -169,7 +196,39 @@ struct RouteArgs {
     int32_t* perm;     // [T*k]
     int32_t* inv;      // [T*k]
     int32_t* active;   // [E] ascending experts with count > 0; active[E] = n_active (at index E)
+    // optional (decode, latent mode): the router input as f16 rows with one
+    // power-of-two exponent per row, written by the last CTA
+    uint16_t* x16;     // [T, d_r]
+    int32_t* xexp;     // [T]
 };
+
+// one warp: row (K bf16) -> f16 * 2^-e with e = floor(log2(max |row|)); returns e
+__device__ __forceinline__ int row_to_f16(const uint16_t* src, int K, uint16_t* dst) {
+    const int lane = threadIdx.x & 31;
+    float amax = 0.0f;
+    for (int c = lane * 8; c < K; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
+    amax = warp_max(amax);
+    const int ex = ilog2f(amax);
+    const float sc = exp2i(-ex);
+    for (int c = lane * 8; c < K; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint4 o;
+        o.x = f32x2_to_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
+        o.y = f32x2_to_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
+        o.z = f32x2_to_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
+        o.w = f32x2_to_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
+        *reinterpret_cast<uint4*>(dst + c) = o;
+    }
+    return ex;
+}
 
 cudaError_t launch_repack(const uint8_t* packed, const uint8_t* scale, int64_t nblocks,
                           uint8_t* out, cudaStream_t s);
@@ -199,6 +258,7 @@ cudaError_t launch_combine(const float* y, int nslots, const float* wts, const i
 struct DecodeArgs {
     const uint8_t *w1_q, *w1_s, *w3_q, *w3_s, *w2_q, *w2_s;
     const uint16_t* x;     // [T, d] bf16 expert input
+    int x16_ready;         // 1: the router already wrote the f16 rows into the scratch
     int T, E, k, d, f;
     const int32_t* offsets;  // [E+1]
     const int32_t* perm;     // [T*k]
@@ -212,6 +272,8 @@ struct DecodeArgs {
     int num_sms;
 };
 size_t decode_scratch_bytes(int T, int k, int d, int f);
+// where the decode scratch keeps the f16 token rows and their exponents
+void decode_x16_slots(void* scratch, int T, int d, uint16_t** x16, int32_t** xexp);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // grouped (tcgen05) path
@@ -226,7 +288,7 @@ struct GroupedArgs {
     const float* wts;        // [T, k]
     uint16_t* xp;            // [T*k, d] f16 prescaled rows (permuted order)
     int32_t* xp_exp;         // [T*k]
-    uint16_t* hb;            // [T*k, f] bf16 (up epilogue output)
+    float* hf;               // [T*k, f] fp32 (up epilogue output)
     uint32_t* h_amax;        // [T*k] fp32 bits of max |h| per row
     uint16_t* hp;            // [T*k, f] f16 prescaled h
     int32_t* hp_exp;         // [T*k]

@@ -155,6 +155,8 @@ __device__ __forceinline__ void compute_stage(const Stage& st, int t, float (&to
 template <int NMAT>
 __global__ void __launch_bounds__(kThreads)
 decode_phase_kernel(DecodeArgs a, Phase ph) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -228,34 +230,12 @@ decode_phase_kernel(DecodeArgs a, Phase ph) {
 __global__ void __launch_bounds__(256)
 prep_rows_kernel(const uint16_t* __restrict__ x, int T, int K, uint16_t* __restrict__ x16,
                  int32_t* __restrict__ xexp) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
     if (r >= T) return;
-    const uint16_t* src = x + static_cast<size_t>(r) * K;
-    float amax = 0.0f;
-    for (int c = lane * 8; c < K; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
-                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
-    }
-    amax = warp_max(amax);
-    const int ex = ilog2f(amax);
-    const float sc = exp2i(-ex);
-    uint16_t* dst = x16 + static_cast<size_t>(r) * K;
-    for (int c = lane * 8; c < K; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint4 o;
-        o.x = f32x2_to_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
-        o.y = f32x2_to_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
-        o.z = f32x2_to_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
-        o.w = f32x2_to_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
-        *reinterpret_cast<uint4*>(dst + c) = o;
-    }
-    if (lane == 0) xexp[r] = ex;
+    const int ex = row_to_f16(x + static_cast<size_t>(r) * K, K, x16 + static_cast<size_t>(r) * K);
+    if ((threadIdx.x & 31) == 0) xexp[r] = ex;
 }
 
 // h = silu(g) * u from the two partial slots (slot 0 + slot 1), then f16 with a
@@ -263,6 +243,8 @@ prep_rows_kernel(const uint16_t* __restrict__ x, int T, int K, uint16_t* __restr
 __global__ void __launch_bounds__(256)
 finish_up_kernel(const float* __restrict__ part, int P, int f, uint16_t* __restrict__ h16,
                  int32_t* __restrict__ hexp) {
+    pdl_wait();
+    pdl_trigger();
     const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (p >= P) return;
@@ -302,9 +284,9 @@ cudaError_t launch_phase(const DecodeArgs& a, const Phase& ph, cudaStream_t s, c
     // four CTAs of four warps per SM; the kernel trims the warp count so that
     // every warp owns at least one whole tile of K chunks
     const int grid = 4 * a.num_sms;
-    decode_phase_kernel<NMAT><<<grid, kThreads, 0, s>>>(a, ph);
+    const cudaError_t e = launch_pdl(decode_phase_kernel<NMAT>, dim3(grid), dim3(kThreads), 0, s, a, ph);
     trace_mark(name, s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
@@ -320,6 +302,12 @@ size_t decode_scratch_bytes(int T, int k, int d, int f) {
     return b;
 }
 
+void decode_x16_slots(void* scratch, int T, int d, uint16_t** x16, int32_t** xexp) {
+    char* base = static_cast<char*>(scratch);
+    *x16 = reinterpret_cast<uint16_t*>(base);
+    *xexp = reinterpret_cast<int32_t*>(base + align_up(static_cast<size_t>(T) * d * 2));
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     const int P = a.T * a.k;
     char* base = reinterpret_cast<char*>(a.scratch);
@@ -333,8 +321,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     base += align_up(static_cast<size_t>(P) * a.f * 2);
     int32_t* hexp = reinterpret_cast<int32_t*>(base);
 
-    prep_rows_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.x, a.T, a.d, x16, xexp);
-    trace_mark("decode_prep", s);
+    if (!a.x16_ready) {
+        cudaError_t e0 = launch_pdl(prep_rows_kernel, dim3((a.T + 7) / 8), dim3(256), 0, s, a.x,
+                                    a.T, a.d, x16, xexp);
+        trace_mark("decode_prep", s);
+        if (e0 != cudaSuccess) return e0;
+    }
 
     Phase up{};
     up.q[0] = a.w1_q; up.q[1] = a.w3_q; up.s[0] = a.w1_s; up.s[1] = a.w3_s;
@@ -343,8 +335,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     cudaError_t e = launch_phase<2>(a, up, s, "decode_up");
     if (e != cudaSuccess) return e;
 
-    finish_up_kernel<<<(P + 7) / 8, 256, 0, s>>>(upart, P, a.f, h16, hexp);
+    e = launch_pdl(finish_up_kernel, dim3((P + 7) / 8), dim3(256), 0, s,
+                   static_cast<const float*>(upart), P, a.f, h16, hexp);
     trace_mark("decode_finish_up", s);
+    if (e != cudaSuccess) return e;
 
     Phase dn{};
     dn.q[0] = a.w2_q; dn.q[1] = a.w2_q; dn.s[0] = a.w2_s; dn.s[1] = a.w2_s;

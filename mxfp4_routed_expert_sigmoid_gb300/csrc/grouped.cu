@@ -26,7 +26,7 @@
 // MoE; w1/w3 logical [f, d], w2 [d, f], MXFP4 blocks of 32 along the input):
 //   UP   : A = W1 and W3 rows of expert e, B = the expert's gathered token
 //          rows (f16, one power-of-two exponent per row); epilogue h =
-//          silu(g) * u, stored bf16 with a per-row |h| maximum;
+//          silu(g) * u, stored fp32 with a per-row |h| maximum;
 //   DOWN : A = W2 rows, B = the f16 h rows; epilogue y in fp32.
 // Work units (expert, first row, row count <= BN) are built on the device
 // from the permutation, so no token count ever returns to the host.
@@ -192,7 +192,7 @@ struct TcParams {
     void* out;             // dense: [T, N_out] bf16 or fp32
     int out_fp32;
     int n_out;             // dense: N_out (row length of out); expert: width of hb / y rows
-    uint16_t* hb;          // UP: h in bf16 [P, f]
+    float* hf;             // UP: h in fp32 [P, f]
     uint32_t* h_amax;      // UP: max |h| per row (fp32 bits)
     float* y;              // DOWN: [P, d]
     WsHeader* hdr;
@@ -444,9 +444,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             const float g = v1[i] * exp2i(eref1 - 127 + xe);
                             const float u = v3[i] * exp2i(eref3 - 127 + xe);
                             const float h = silu_f32(g) * u;
-                            const uint16_t hb = f32_to_bf16(h);
-                            if (valid) p.hb[static_cast<size_t>(pr) * p.n_out + r] = hb;
-                            const float a = warp_max(valid ? fabsf(bf16_to_f32(hb)) : 0.0f);
+                            if (valid) p.hf[static_cast<size_t>(pr) * p.n_out + r] = h;
+                            const float a = warp_max(valid ? fabsf(h) : 0.0f);
                             if (lane == 0) atomicMax(p.h_amax + pr, __float_as_uint(a));
                         }
                     } else {
@@ -573,26 +572,25 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ p
     }
 }
 
-// hp[r] = f16(hb[r] * 2^-ex), ex = floor(log2(h_amax[r])); one warp per row
+// hp[r] = f16(hf[r] * 2^-ex), ex = floor(log2(h_amax[r])); one warp per row
 __global__ void __launch_bounds__(256)
-convert_h_kernel(const uint16_t* __restrict__ hb, const uint32_t* __restrict__ h_amax, int P, int f,
+convert_h_kernel(const float* __restrict__ hf, const uint32_t* __restrict__ h_amax, int P, int f,
                  uint16_t* __restrict__ hp, int32_t* __restrict__ hexp) {
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= P) return;
     const int ex = ilog2f(__uint_as_float(h_amax[r]));
     const float sc = exp2i(-ex);
-    const uint16_t* src = hb + static_cast<size_t>(r) * f;
+    const float* src = hf + static_cast<size_t>(r) * f;
     uint16_t* dst = hp + static_cast<size_t>(r) * f;
     for (int c = lane * 8; c < f; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const float4 a = *reinterpret_cast<const float4*>(src + c);
+        const float4 b = *reinterpret_cast<const float4*>(src + c + 4);
         uint4 o;
-        uint32_t* oo = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            oo[j] = f32x2_to_f16x2(__uint_as_float(w[j] << 16) * sc,
-                                   __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+        o.x = f32x2_to_f16x2(a.x * sc, a.y * sc);
+        o.y = f32x2_to_f16x2(a.z * sc, a.w * sc);
+        o.z = f32x2_to_f16x2(b.x * sc, b.y * sc);
+        o.w = f32x2_to_f16x2(b.z * sc, b.w * sc);
         *reinterpret_cast<uint4*>(dst + c) = o;
     }
     if (lane == 0) hexp[r] = ex;
@@ -742,12 +740,12 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     p.units = units;
     p.bexp = g.xp_exp;
     p.n_out = g.f;
-    p.hb = g.hb;
+    p.hf = g.hf;
     p.h_amax = g.h_amax;
     p.hdr = g.hdr;
     if ((e = launch_tc<UP>(t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
-    convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hb, g.h_amax, P, g.f, g.hp, g.hp_exp);
+    convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp);
     trace_mark("convert_h", s);
 
     // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y, int nslots, size_t slot_stride,
                const float* __restrict__ wts, const int32_t* __restrict__ inv, int k, int d,
                uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int c = (blockIdx.x * 256 + threadIdx.x) * 4;
     if (c >= d) return;
@@ -106,9 +108,10 @@ cudaError_t launch_combine(const float* y, int nslots, const float* wts, const i
     if (T <= 0) return cudaSuccess;
     dim3 grid((d + 1023) / 1024, T);
     const size_t slot_stride = static_cast<size_t>(T) * k * d;
-    combine_kernel<<<grid, 256, 0, s>>>(y, nslots, slot_stride, wts, inv, k, d, out);
+    const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, s, y, nslots, slot_stride,
+                                     wts, inv, k, d, out);
     trace_mark("combine", s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace k3

@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(256)
 route_small_kernel(RouteArgs a) {
     __shared__ int32_t sel[256];
     __shared__ uint32_t ticket_s;
+    // the next kernel of the forward may start launching now: it waits for
+    // this grid's completion (griddepcontrol.wait) before reading its outputs
+    pdl_trigger();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int e = blockIdx.x * 8 + wid;
     if (e < a.E) {
@@ -230,6 +233,12 @@ route_small_kernel(RouteArgs a) {
     __syncthreads();
     if (a.counts)
         permute_small(sel, a.T, a.k, a.E, a.counts, a.offsets, a.perm, a.inv, a.active);
+    if (a.x16)
+        for (int t = wid; t < a.T; t += 8) {
+            const int ex = row_to_f16(a.x + static_cast<size_t>(t) * a.d_r, a.d_r,
+                                      a.x16 + static_cast<size_t>(t) * a.d_r);
+            if (lane == 0) a.xexp[t] = ex;
+        }
 }
 
 __global__ void __launch_bounds__(256)

@@ -108,3 +108,22 @@ def test_forward_host_buffers(k3):
     out_host = k3.k3moe_forward_host(layer, x_host)
     out_dev = k3.k3moe_forward(layer, x_host.cuda())
     assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+
+
+def test_graph_replay_matches_forward(k3):
+    """k3moe_graph_create / k3moe_graph_launch reproduce k3moe_forward bit for bit."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=3, E=64, k=8, d=768, f=1152, seed_index=13)
+    layer, dense, expert, _ = make_layer(cfg, path=0)
+    x = to_dev(dense["hidden"], "cuda")
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))
+    ref = k3.k3moe_forward(layer, x, ws=ws).clone()
+    out = torch.zeros_like(ref)
+    graph = k3.ForwardGraph(layer, x, out, ws)
+    out.zero_()
+    graph.launch()
+    graph.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    graph.close()

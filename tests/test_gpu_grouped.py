@@ -128,3 +128,17 @@ def test_chunk_t512_full_sampled(k3):
     rng = np.random.default_rng(5)
     toks = np.sort(rng.choice(cfg.T, 4, replace=False))
     compare_forward(k3, cfg, 0, tokens=toks)
+
+
+def test_block_t8192_full_sampled(k3):
+    """The full latent block at T = 8192, D = 7168 (Zipf-skewed routing): the
+    whole batch runs on the GPU, 4 seeded token rows are checked."""
+    cfg = synth.CONFIGS["block_t8192"]
+    rng = np.random.default_rng(6)
+    toks = np.sort(rng.choice(cfg.T, 4, replace=False))
+    compare_forward(k3, cfg, 0, tokens=toks)
+
+
+def test_verify_t8_grouped_path(k3):
+    """The full-size K3 layer through the tcgen05 path at T = 8 (hot experts)."""
+    compare_forward(k3, synth.CONFIGS["verify_t8"], 2)
