@@ -252,7 +252,7 @@ k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status);
  * them).  k3moe_trace_read waits for the last event and fills up to `max`
  * entries with the kernel names (static strings) and the milliseconds between
  * consecutive events of the most recently traced forward; it returns the
- * number of entries.  Tracing is process-wide and meant for one host thread;
+ * number of entries, or 0 if the events cannot be read.  Tracing is process-wide and meant for one host thread;
  * it is off by default.  k3moe_trace returns the previous setting. */
 int k3moe_trace(int enable);
 int k3moe_trace_read(int max, const char** names, float* ms);

@@ -150,12 +150,23 @@ struct Trace {
 };
 Trace g_trace;
 
+// Inside a stream capture a plain event record is only a dependency of the
+// capture; an external record becomes a node that records the event each
+// time the graph runs, so its timing can be read afterwards.
+void trace_record(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, s);
+}
+
 void trace_begin(cudaStream_t s) {
     if (!g_trace.on) return;
     g_trace.n = 0;
     if (!g_trace.ev[0])
         for (auto& e : g_trace.ev) cudaEventCreate(&e);
-    cudaEventRecord(g_trace.ev[0], s);
+    trace_record(g_trace.ev[0], s);
 }
 
 void trace_end() {
@@ -174,7 +185,7 @@ bool pdl_enabled() { return pdl_on(); }
 void trace_mark(const char* name, cudaStream_t s) {
     if (!g_trace.on || g_trace.n >= 32) return;
     g_trace.names[g_trace.n] = name;
-    cudaEventRecord(g_trace.ev[g_trace.n + 1], s);
+    trace_record(g_trace.ev[g_trace.n + 1], s);
     ++g_trace.n;
 }
 }  // namespace k3
@@ -192,10 +203,16 @@ int k3moe_trace_read(int max, const char** names, float* ms) {
     std::lock_guard<std::mutex> lock(g_trace.mu);
     if (g_trace.n_last > 0) {
         const int n = g_trace.n_last;
-        cudaEventSynchronize(g_trace.ev[n]);
+        if (cudaEventSynchronize(g_trace.ev[n]) != cudaSuccess) {
+            cudaGetLastError();  // leave no pending error behind
+            return 0;
+        }
         for (int i = 0; i < n; ++i) {
             float t = 0.0f;
-            cudaEventElapsedTime(&t, g_trace.ev[i], g_trace.ev[i + 1]);
+            if (cudaEventElapsedTime(&t, g_trace.ev[i], g_trace.ev[i + 1]) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
             g_trace.ms_last[i] = t;
         }
     }

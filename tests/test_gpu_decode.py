@@ -127,3 +127,25 @@ def test_graph_replay_matches_forward(k3):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     graph.close()
+
+
+def test_trace_of_graph_replay(k3):
+    """Kernel tracing inside a library graph: every kernel of the forward
+    reports a positive duration after a replay."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=2, E=64, k=8, d=768, f=1152, seed_index=14)
+    layer, dense, expert, _ = make_layer(cfg, path=0)
+    x = to_dev(dense["hidden"], "cuda")
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))
+    out = torch.empty_like(x)
+    k3.k3moe_trace(True)
+    graph = k3.ForwardGraph(layer, x, out, ws)
+    k3.k3moe_trace(False)
+    graph.launch()
+    tr = k3.k3moe_trace_read()
+    torch.cuda.synchronize()
+    names = [n for n, _ in tr]
+    assert "route_small" in names and "decode_up" in names and "combine" in names
+    assert all(ms > 0 for _, ms in tr)
+    graph.close()
