@@ -165,6 +165,33 @@ k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16
                          float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* k3moe_route without a workspace, for callers that cannot allocate device
+ * memory or hand the library a scratch buffer: code whose device memory must
+ * all come from a framework-owned pool, or a latency-critical decode loop in
+ * which cudaMalloc (which can synchronise the whole device) is not allowed.
+ * The paper has no counterpart: this is an integration convenience of this
+ * library, computing exactly what k3moe_route computes (same kernel).
+ *
+ * Scratch: a file-scope device array of 33,024 bytes (a 256-byte header plus
+ * room for 8 x 1024 fp32 logits), part of the library's module image, so every
+ * GPU that loads the library holds it until the process exits.  Limits:
+ * T <= 8 and E <= 1024; larger sizes return K3MOE_ERR_SHAPE (use k3moe_route
+ * with a workspace).  No cudaMalloc, cudaFree or other allocation happens in
+ * the call.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call shares the array and it
+ * keeps the last call's contents: each call clears the header on `stream`
+ * before its kernel, and calls whose work overlaps on the GPU (different
+ * streams, or different host threads) race on it, so order them.  Device-side
+ * errors (a non-finite logit) are not reported by this entry point.
+ * Arguments, layouts and the other errors are those of k3moe_route. */
+k3moe_status k3moe_route_noalloc(const uint16_t* x, int32_t T, int32_t d_r,
+                                 const uint16_t* router_w, const float* bias, int32_t E,
+                                 int32_t k, int32_t* idx_out, float* w_out, float* logits_out,
+                                 void* stream);
+
 /* Expert histogram, exclusive scan and token permutation of a selection.
  * Pairs are numbered p = t*k + j.
  *   idx      [T, k] int32 in [0, E)

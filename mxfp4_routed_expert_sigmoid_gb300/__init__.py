@@ -34,7 +34,8 @@ STATUS = {
 #: every symbol the C header declares (checked by the CPU test suite)
 EXPORTS = (
     "k3moe_abi_version", "k3moe_status_string", "k3moe_repack_mxfp4", "k3moe_unpack_mxfp4",
-    "k3moe_route_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_rmsnorm",
+    "k3moe_route_workspace_size", "k3moe_route", "k3moe_route_noalloc", "k3moe_permute",
+    "k3moe_rmsnorm",
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
         "k3moe_unpack_mxfp4": ([vp, i64, i64, vp, vp, vp], ctypes.c_int),
         "k3moe_route_workspace_size": ([i32, i32], sz),
         "k3moe_route": ([vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_route_noalloc": ([vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp], ctypes.c_int),
         "k3moe_permute": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "k3moe_rmsnorm": ([vp, i32, i32, vp, f32, vp, vp], ctypes.c_int),
         "k3moe_gemm_bf16": ([vp, vp, i32, i32, i32, vp, i32, vp], ctypes.c_int),

@@ -296,6 +296,24 @@ k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16
     return cuda_status(launch_topk(a, s));
 }
 
+k3moe_status k3moe_route_noalloc(const uint16_t* x, int32_t T, int32_t d_r,
+                                 const uint16_t* router_w, const float* bias, int32_t E,
+                                 int32_t k, int32_t* idx_out, float* w_out, float* logits_out,
+                                 void* stream) {
+    if (!x || !router_w || !bias || !idx_out || !w_out) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || d_r < 1 || E < 1 || k < 1) return K3MOE_ERR_INVALID_ARG;
+    if (T > kNoAllocMaxT || E > kNoAllocMaxE) return K3MOE_ERR_SHAPE;
+    if (k > E || k > 32 || d_r % 64) return K3MOE_ERR_SHAPE;
+    const void* ptrs[] = {x, router_w, bias, idx_out, w_out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+    if (logits_out && !aligned16(logits_out)) return K3MOE_ERR_ALIGN;
+    RouteArgs a{};
+    a.x = x; a.T = T; a.d_r = d_r; a.w = router_w; a.bias = bias; a.E = E; a.k = k;
+    a.idx = idx_out; a.wts = w_out; a.logits = logits_out;
+    return cuda_status(launch_route_noalloc(a, static_cast<cudaStream_t>(stream)));
+}
+
 k3moe_status k3moe_permute(const int32_t* idx, int32_t T, int32_t k, int32_t E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
                            size_t ws_bytes, void* stream) {

@@ -237,6 +237,10 @@ cudaError_t launch_unpack(const uint8_t* blocks, int64_t nblocks, uint8_t* packe
 
 // small T: GEMV logits + (last CTA) top-k [+ permutation if args.counts]
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s);
+// the same with library-owned static scratch (no caller workspace)
+constexpr int kNoAllocMaxT = 8;
+constexpr int kNoAllocMaxE = 1024;
+cudaError_t launch_route_noalloc(RouteArgs a, cudaStream_t s);
 // any T: logits already in a.logits -> top-k
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s);
 // SIMT GEMV/GEMM logits for moderate T (no top-k)

@@ -16,6 +16,8 @@
 // Permutation: histogram of the selection, exclusive scan, and a stable
 // scatter that lists each expert's pairs in ascending token order, plus the
 // inverse map and the ascending list of experts that received any token.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace k3 {
@@ -387,6 +389,54 @@ cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
     route_small_kernel<<<grid, 256, 0, s>>>(a);
     trace_mark("route_small", s);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Router with library-owned scratch (k3moe_route_noalloc).
+//
+// The small-T router needs a completion counter and, when the caller does
+// not want the logits, a [T, E] fp32 buffer for them.  This variant keeps
+// both in one file-scope device array instead of a caller workspace: it is
+// part of the module image, so every GPU that loads the library holds these
+// bytes until the process exits, and every call shares them.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratch =
+    sizeof(WsHeader) + static_cast<size_t>(kNoAllocMaxT) * kNoAllocMaxE * sizeof(float);
+static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratch];
+
+// Device address of g_route_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+static cudaError_t route_scratch_address(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_route_noalloc(RouteArgs a, cudaStream_t s) {
+    void* scratch = nullptr;
+    cudaError_t e = route_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    // the header (completion counter, status) must start at zero: clear it on
+    // the caller's stream, so it is ordered after any earlier call there
+    e = cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s);
+    if (e != cudaSuccess) return e;
+    a.hdr = static_cast<WsHeader*>(scratch);
+    if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(scratch) + sizeof(WsHeader));
+    a.counts = nullptr;
+    return launch_route_small(a, s);
 }
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s) {
