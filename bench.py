@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 decode, 2 grouped")
     ap.add_argument("--E", type=int, default=0,
                     help="fewer resident experts (small profiling captures only; not a bench line)")
+    ap.add_argument("--T", type=int, default=0,
+                    help="other token count (small profiling captures only; not a bench line)")
     return ap.parse_args()
 
 
@@ -57,6 +59,8 @@ def bench_config(args):
     cfg = synth.CONFIGS[args.config]
     if args.E:
         cfg = synth.custom(cfg.name, E=args.E)
+    if args.T:
+        cfg = synth.custom(cfg.name, E=cfg.E, T=args.T)
     return cfg
 
 
@@ -208,6 +212,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest value over all ranks (the job takes as long as its slowest rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / (max_total_ms / 1e3)
+
+
 def reference_arm(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -317,13 +338,8 @@ def ours_arm(args):
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = cfg.T * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_tokens_per_s(cfg.T, args.steps, world, total_ms)
 
     # ---- per-kernel durations (traced pass over the same steps) ----
     tgraphs = capture(True)

@@ -98,8 +98,8 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     p.h_amax = c.take(P * 4);
     p.hp = c.take(P * d->f * 2);
     p.hp_exp = c.take(P * 4);
-    p.tiles_cap = static_cast<int>(grouped_tile_cap(T, d->E, d->k));
-    p.tiles = c.take(static_cast<size_t>(p.tiles_cap) * 4 * 4);
+    p.tiles_cap = static_cast<int>(grouped_tile_cap(T, d->E, d->k, d->d, d->f));
+    p.tiles = c.take(2 * (static_cast<size_t>(p.tiles_cap) + 1) * 16);
     if (d->D > 0) {
         p.hn = c.take(static_cast<size_t>(T) * d->D * 2);
         p.z = c.take(static_cast<size_t>(T) * d->d * 2);

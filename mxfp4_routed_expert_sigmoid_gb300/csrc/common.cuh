@@ -297,13 +297,13 @@ struct GroupedArgs {
     uint16_t* hp;            // [T*k, f] f16 prescaled h
     int32_t* hp_exp;         // [T*k]
     float* y;                // [T*k, d] fp32
-    int32_t* tiles;          // tile list scratch
+    int32_t* tiles;          // two tile lists (up, down), tiles_cap + 1 int4 entries each
     int tiles_cap;
     uint16_t* out;           // [T, d] bf16
     WsHeader* hdr;
     int num_sms;
 };
-size_t grouped_tile_cap(int T, int E, int k);
+size_t grouped_tile_cap(int T, int E, int k, int d, int f);
 cudaError_t launch_grouped(const GroupedArgs& a, cudaStream_t s);
 
 // dense bf16 GEMM (tcgen05): out[t, n] = sum_c x[t, c] w[n, c]

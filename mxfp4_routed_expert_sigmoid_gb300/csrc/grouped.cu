@@ -1,11 +1,13 @@
 // tcgen05 GEMMs: the grouped expert GEMMs of the routed layer and the dense
 // bf16 GEMM used for the latent projections and the router at large T.
 //
-// One persistent, warp-specialised kernel template computes
+// Two persistent, warp-specialised kernels compute
 //     D[m, n] = sum_c A[m, c] * B[n, c]       (A: weights, B: token rows)
 // with M = 128 weight rows per tile (TMEM lanes), N = up to BN token rows
 // per tile (TMEM columns, fp32), K in stages of 64 (128 bytes of f16/bf16
-// per row: the 128-byte swizzled K-major shared-memory layout of tcgen05).
+// per row: the 128-byte swizzled K-major shared-memory layout of tcgen05):
+// tc_dense_kernel (bf16 operands, both by TMA) and tc_expert_kernel (MXFP4
+// weights dequantised to f16 in shared memory, f16 token rows by TMA).
 //
 // Roles (warps):
 //   0      producer: TMA loads of B (tokens) and of A (dense mode) or of the
@@ -37,6 +39,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -44,8 +47,6 @@
 
 namespace k3 {
 namespace {
-
-enum Mode { DENSE = 0, UP = 1, DOWN = 2 };
 
 constexpr int BM = 128;
 constexpr int BK = 64;
@@ -177,51 +178,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // ---------------------------------------------------------------------------
-// kernel parameters
+// Dense bf16 GEMM: out[t, n] = sum_c x[t, c] * w[n, c]
+//
+// A = w (128 output rows per tile, TMEM lanes), B = x (256 token rows per
+// tile, TMEM columns), both by TMA with 128-byte swizzle, 4 stages of 48 KB.
+// Warp 0 producer, warp 1 MMA issuer, warp 2 TMEM owner, warps 4..7
+// epilogue (bf16 or fp32 stores, coalesced along the output features).
 // ---------------------------------------------------------------------------
-struct TcParams {
-    int K;                 // reduction length (multiple of 64)
-    int rows_per_expert;   // expert modes: rows of one expert matrix (f or d)
-    int m_tiles;           // 128-row tiles per expert matrix (or over N_out in dense mode)
-    int T;                 // dense: token rows
-    int n_tiles;           // dense: token tiles
-    const uint8_t* s1;     // expert: E8M0 scales of A (w1 or w2), [E * rows, K / 32]
-    const uint8_t* s3;     // UP: scales of w3
-    const int4* units;     // expert: units[0].x = count; units[1 + u] = (e, row0, nrows, 0)
-    const int32_t* bexp;   // expert: per B row power-of-two exponent
-    void* out;             // dense: [T, N_out] bf16 or fp32
+struct DenseParams {
+    int K;        // reduction length (multiple of 64)
+    int m_tiles;  // 128-row tiles over N_out
+    int T;        // token rows
+    int n_tiles;  // token tiles
+    void* out;    // [T, N_out] bf16 or fp32
     int out_fp32;
-    int n_out;             // dense: N_out (row length of out); expert: width of hb / y rows
-    float* hf;             // UP: h in fp32 [P, f]
-    uint32_t* h_amax;      // UP: max |h| per row (fp32 bits)
-    float* y;              // DOWN: [P, d]
+    int n_out;
     WsHeader* hdr;
 };
 
-template <int MODE>
-struct Cfg;
-template <>
-struct Cfg<DENSE> {
-    static constexpr int NA = 1, BN = 256, STAGES = 4, THREADS = 256, TMEM_COLS = 512;
-};
-template <>
-struct Cfg<UP> {
-    static constexpr int NA = 2, BN = 128, STAGES = 3, THREADS = 512, TMEM_COLS = 512;
-};
-template <>
-struct Cfg<DOWN> {
-    static constexpr int NA = 1, BN = 128, STAGES = 4, THREADS = 512, TMEM_COLS = 256;
-};
+constexpr int kDenseBN = 256, kDenseStages = 4, kDenseThreads = 256, kDenseTmemCols = 512;
 
-template <int MODE>
-constexpr size_t smem_bytes() {
-    using C = Cfg<MODE>;
-    size_t b = 1024;  // alignment slack
-    b += static_cast<size_t>(C::STAGES) * C::NA * kTileA;
-    b += static_cast<size_t>(C::STAGES) * C::BN * BK * 2;
-    if (MODE != DENSE) b += static_cast<size_t>(C::STAGES) * C::NA * kTileRaw;
-    b += 256;  // barriers, flags
-    return b;
+constexpr size_t dense_smem_bytes() {
+    return 1024 + static_cast<size_t>(kDenseStages) * (kTileA + kDenseBN * BK * 2) + 256;
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
@@ -246,60 +224,250 @@ __device__ __forceinline__ int row_emax(const uint8_t* srow, int nb) {
     return m;
 }
 
-// tile -> (expert, first B row, B rows, m tile); returns false past the end
-template <int MODE>
-__device__ __forceinline__ bool tile_info(const TcParams& p, int tile, int n_tiles, int& e,
-                                          int& row0, int& nrows, int& mt) {
-    if (tile >= n_tiles) return false;
-    mt = tile % p.m_tiles;
-    const int u = tile / p.m_tiles;
-    if (MODE == DENSE) {
-        e = 0;
-        row0 = u * Cfg<DENSE>::BN;
-        nrows = min(Cfg<DENSE>::BN, p.T - row0);
-    } else {
-        const int4 un = p.units[1 + u];
-        e = un.x;
-        row0 = un.y;
-        nrows = un.z;
-    }
-    return true;
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
-               const __grid_constant__ CUtensorMap tmB, TcParams p) {
-    using C = Cfg<MODE>;
-    constexpr int NA = C::NA, BN = C::BN, STAGES = C::STAGES;
+__global__ void __launch_bounds__(kDenseThreads, 1)
+tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                DenseParams p) {
+    constexpr int BN = kDenseBN, STAGES = kDenseStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;                                          // [STAGES][NA][16 KB]
-    uint8_t* sB = sA + STAGES * NA * kTileA;                     // [STAGES][BN * 128]
-    uint8_t* sRaw = sB + STAGES * BN * BK * 2;                   // [STAGES][NA][4 KB]
-    uint8_t* tail = sRaw + (MODE != DENSE ? STAGES * NA * kTileRaw : 0);
-    uint64_t* full_b = reinterpret_cast<uint64_t*>(tail);        // TMA B (+A in dense mode)
-    uint64_t* full_raw = full_b + STAGES;                        // TMA raw A
-    uint64_t* full_a = full_raw + STAGES;                        // dequantised A ready
-    uint64_t* empty = full_a + STAGES;                           // MMA done with stage
-    uint64_t* acc_full = empty + STAGES;                         // [2]
-    uint64_t* acc_empty = acc_full + 2;                          // [2]
+    uint8_t* sA = smem;                     // [STAGES][16 KB]
+    uint8_t* sB = sA + STAGES * kTileA;     // [STAGES][BN * 128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * BN * BK * 2);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;    // [2]
+    uint64_t* acc_empty = acc_full + 2;     // [2]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = (MODE == DENSE) ? p.n_tiles * p.m_tiles : p.units[0].x * p.m_tiles;
-
+    const int n_tiles = p.n_tiles * p.m_tiles;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full_b[s], 1);
-            mbar_init(&full_raw[s], 1);
-            mbar_init(&full_a[s], 8);
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(kDenseTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int k_stages = p.K / BK;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const int mt = tile % p.m_tiles, row0 = (tile / p.m_tiles) * BN;
+                bool ok = true;
+                for (int ks = 0; ks < k_stages; ++ks) {
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 10)) { ok = false; break; }
+                    mbar_expect_tx(&full[s], kTileA + BN * BK * 2);
+                    tma_load_2d(sA + s * kTileA, &tmA, &full[s], ks * BK, mt * BM);
+                    tma_load_2d(sB + s * BN * BK * 2, &tmB, &full[s], ks * BK, row0);
+                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            const uint32_t idesc = idesc_f16(1, BM, BN);
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_ph = (it >> 1) & 1;
+                if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort_flag, p.hdr, 20)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int ks = 0; ks < k_stages; ++ks) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, p.hdr, 21)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * kTileA);
+                    const uint32_t b_addr = smem_u32(sB + s * BN * BK * 2);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(d0, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
+                                (ks > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[acc]);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue ------------------------------
+        const int wr = warp & 3;
+        const int m = wr * 32 + lane;  // accumulator lane = output feature in the tile
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int mt = tile % p.m_tiles, row0 = (tile / p.m_tiles) * BN;
+            const int nrows = min(BN, p.T - row0);
+            const int acc = it & 1;
+            const uint32_t acc_ph = (it >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_ph, abort_flag, p.hdr, 30)))
+                break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wr * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            const int col = mt * BM + m;
+            for (int n0 = 0; n0 < BN; n0 += 16) {
+                float v[16];
+                tmem_ld16(tbase + n0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = row0 + n0 + i;
+                    if (n0 + i < nrows) {
+                        if (p.out_fp32)
+                            static_cast<float*>(p.out)[static_cast<size_t>(t) * p.n_out + col] = v[i];
+                        else
+                            static_cast<uint16_t*>(p.out)[static_cast<size_t>(t) * p.n_out + col] =
+                                f32_to_bf16(v[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kDenseTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Expert GEMM kernel (UP: NA = 2 matrices w1/w3, DOWN: NA = 1 matrix w2)
+//
+// Warps: 0 raw-weight producer (TMA into an RS-deep ring of packed E2M1
+// tiles), 1 MMA issuer, 2 TMEM owner and exponent helper (computes each
+// tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
+// token producer (TMA of the tile's token rows in 16-row boxes, only as many
+// as the tile has, into a BS-deep ring), 4..7 epilogue, 8..15
+// dequantisation (raw ring -> f16 A stages of an AS-deep ring).  Three rings
+// with their own full/empty barriers: the raw weights and the token rows are
+// fetched several stages ahead (HBM and L2 latency), while the f16 stages
+// only have to cover the dequantise -> MMA hand-off.
+// ---------------------------------------------------------------------------
+template <int NA>
+struct ExpCfg;
+// RS: raw-weight stages, AS: dequantised A stages, BS: token (B) stages
+template <>
+struct ExpCfg<2> {
+    static constexpr int BN = 128, RS = 8, AS = 2, BS = 4, TMEM_COLS = 512;
+};
+template <>
+struct ExpCfg<1> {
+    static constexpr int BN = 128, RS = 8, AS = 4, BS = 4, TMEM_COLS = 256;
+};
+constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
+constexpr int kBoxRows = 16;    // token rows per TMA box
+constexpr int kExpThreads = 512;
+
+struct ExpParams {
+    int K;                // reduction length (multiple of 64)
+    int rows_per_expert;  // rows of one expert matrix
+    const uint8_t* s1;    // E8M0 of A (w1 or w2), [E * rows, K / 32]
+    const uint8_t* s3;    // UP: E8M0 of w3
+    const int4* tiles;    // tiles[0].x = count; tiles[1 + i] = (e, first B row, B rows, m tile)
+    const int32_t* bexp;  // per B row power-of-two exponent
+    int n_out;            // row length of hf / y
+    float* hf;            // UP: h in fp32 [P, f]
+    uint32_t* h_amax;     // UP: max |h| per row (fp32 bits)
+    float* y;             // DOWN: [P, d]
+    WsHeader* hdr;
+};
+
+template <int NA>
+constexpr size_t exp_smem_bytes() {
+    using C = ExpCfg<NA>;
+    size_t b = 1024;
+    b += static_cast<size_t>(C::AS) * NA * kTileA;
+    b += static_cast<size_t>(C::BS) * C::BN * BK * 2;
+    b += static_cast<size_t>(C::RS) * NA * kTileRaw;
+    b += static_cast<size_t>(kES) * NA * BM * 4;
+    b += 512;
+    return b;
+}
+
+template <int NA>
+__global__ void __launch_bounds__(kExpThreads, 1)
+tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
+                 const __grid_constant__ CUtensorMap tmB, ExpParams p) {
+    using C = ExpCfg<NA>;
+    constexpr int BN = C::BN, RS = C::RS, AS = C::AS, BS = C::BS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;                                // [AS][NA][16 KB]
+    uint8_t* sB = sA + AS * NA * kTileA;               // [BS][BN * 128]
+    uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RS][NA][4 KB]
+    int* sE = reinterpret_cast<int*>(sRaw + RS * NA * kTileRaw);  // [kES][NA][128]
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(sE + kES * NA * BM);
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* b_full = raw_empty + RS;
+    uint64_t* b_empty = b_full + BS;
+    uint64_t* a_full = b_empty + BS;
+    uint64_t* a_empty = a_full + AS;
+    uint64_t* acc_full = a_empty + AS;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* eref_full = acc_empty + 2;
+    uint64_t* eref_empty = eref_full + kES;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(eref_empty + kES);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = p.tiles[0].x;
+    const int k_stages = p.K / BK;
+    const int nb = p.K / 32;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], 8);
+        }
+        for (int i = 0; i < BS; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < AS; ++i) {
+            mbar_init(&a_full[i], 8);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        for (int i = 0; i < kES; ++i) {
+            mbar_init(&eref_full[i], 1);
+            mbar_init(&eref_empty[i], 12);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -314,186 +482,209 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (MODE == UP) prefetch_tmap(&tmA3);
+        if (NA == 2) prefetch_tmap(&tmA3);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int k_stages = p.K / BK;
 
     if (warp == 0) {
-        // ------------------------------ producer ------------------------------
+        // ---------------------------- raw-weight producer --------------------
         if (lane == 0) {
-            int s = 0;
+            int r = 0;
             uint32_t ph = 0;
-            for (int tile = blockIdx.x;; tile += gridDim.x) {
-                int e, row0, nrows, mt;
-                if (!tile_info<MODE>(p, tile, n_tiles, e, row0, nrows, mt)) break;
-                const int arow = (MODE == DENSE) ? mt * BM : e * p.rows_per_expert + mt * BM;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const int4 tl = p.tiles[1 + tile];
+                const int arow = tl.x * p.rows_per_expert + tl.w * BM;
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 10)) { ok = false; break; }
-                    if (MODE == DENSE) {
-                        mbar_expect_tx(&full_b[s], kTileA + BN * BK * 2);
-                        tma_load_2d(sA + s * kTileA, &tmA, &full_b[s], ks * BK, arow);
-                        tma_load_2d(sB + s * BN * BK * 2, &tmB, &full_b[s], ks * BK, row0);
-                    } else {
-                        mbar_expect_tx(&full_raw[s], NA * kTileRaw);
-                        tma_load_2d(sRaw + (s * NA) * kTileRaw, &tmA, &full_raw[s], ks * BK / 2, arow);
-                        if (MODE == UP)
-                            tma_load_2d(sRaw + (s * NA + 1) * kTileRaw, &tmA3, &full_raw[s], ks * BK / 2,
-                                        arow);
-                        mbar_expect_tx(&full_b[s], BN * BK * 2);
-                        tma_load_2d(sB + s * BN * BK * 2, &tmB, &full_b[s], ks * BK, row0);
-                    }
-                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                    if (!mbar_wait(&raw_empty[r], ph ^ 1, abort_flag, p.hdr, 50)) { ok = false; break; }
+                    mbar_expect_tx(&raw_full[r], NA * kTileRaw);
+                    tma_load_2d(sRaw + (r * NA) * kTileRaw, &tmA, &raw_full[r], ks * BK / 2, arow);
+                    if (NA == 2)
+                        tma_load_2d(sRaw + (r * NA + 1) * kTileRaw, &tmA3, &raw_full[r], ks * BK / 2, arow);
+                    if (++r == RS) { r = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 3) {
+        // ---------------------------- token producer -------------------------
+        if (lane == 0) {
+            int b = 0;
+            uint32_t ph = 0;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const int4 tl = p.tiles[1 + tile];
+                const int nbox = (tl.z + kBoxRows - 1) / kBoxRows;
+                bool ok = true;
+                for (int ks = 0; ks < k_stages; ++ks) {
+                    if (!mbar_wait(&b_empty[b], ph ^ 1, abort_flag, p.hdr, 51)) { ok = false; break; }
+                    mbar_expect_tx(&b_full[b], nbox * kBoxRows * BK * 2);
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d(sB + b * BN * BK * 2 + i * kBoxRows * BK * 2, &tmB, &b_full[b], ks * BK,
+                                    tl.y + i * kBoxRows);
+                    if (++b == BS) { b = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
         }
     } else if (warp == 1) {
-        // ------------------------------ MMA issuer ----------------------------
+        // ---------------------------- MMA issuer -----------------------------
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
+            int a = 0, b = 0;
+            uint32_t aph = 0, bph = 0;
             int it = 0;
-            const int fmt = (MODE == DENSE) ? 1 : 0;
-            for (int tile = blockIdx.x;; tile += gridDim.x, ++it) {
-                int e, row0, nrows, mt;
-                if (!tile_info<MODE>(p, tile, n_tiles, e, row0, nrows, mt)) break;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int4 tl = p.tiles[1 + tile];
                 const int acc = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
-                const int n_mma = (MODE == DENSE) ? BN : ((nrows + 15) / 16) * 16;
-                const uint32_t idesc = idesc_f16(fmt, BM, n_mma);
-                if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort_flag, p.hdr, 20)) break;
+                const int n_mma = ((tl.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
+                const uint32_t idesc = idesc_f16(0, BM, n_mma);
+                if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort_flag, p.hdr, 52)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * NA * BN);
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&full_b[s], ph, abort_flag, p.hdr, 21)) { ok = false; break; }
-                    if (MODE != DENSE && !mbar_wait(&full_a[s], ph, abort_flag, p.hdr, 22)) { ok = false; break; }
+                    if (!mbar_wait(&b_full[b], bph, abort_flag, p.hdr, 53) ||
+                        !mbar_wait(&a_full[a], aph, abort_flag, p.hdr, 54)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    const uint32_t b_addr = smem_u32(sB + s * BN * BK * 2);
+                    const uint32_t b_addr = smem_u32(sB + b * BN * BK * 2);
 #pragma unroll
-                    for (int a = 0; a < NA; ++a) {
-                        const uint32_t a_addr = smem_u32(sA + (s * NA + a) * kTileA);
+                    for (int m = 0; m < NA; ++m) {
+                        const uint32_t a_addr = smem_u32(sA + (a * NA + m) * kTileA);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_f16(d0 + a * BN, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                            mma_f16(d0 + m * BN, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
                                     idesc, (ks > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&empty[s]);
-                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                    mma_commit(&a_empty[a]);
+                    mma_commit(&b_empty[b]);
+                    if (++a == AS) { a = 0; aph ^= 1; }
+                    if (++b == BS) { b = 0; bph ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[acc]);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------ epilogue ------------------------------
-        const int wr = warp & 3;
-        const int m = wr * 32 + lane;  // accumulator lane = weight row in the tile
+    } else if (warp == 2) {
+        // ---------------------------- exponent helper ------------------------
         int it = 0;
-        for (int tile = blockIdx.x;; tile += gridDim.x, ++it) {
-            int e, row0, nrows, mt;
-            if (!tile_info<MODE>(p, tile, n_tiles, e, row0, nrows, mt)) break;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int4 tl = p.tiles[1 + tile];
+            const int slot = it % kES;
+            const uint32_t eph = (it / kES) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&eref_empty[slot], eph ^ 1, abort_flag, p.hdr, 55)))
+                break;
+#pragma unroll
+            for (int m = 0; m < NA; ++m) {
+                const uint8_t* sm_ = m == 0 ? p.s1 : p.s3;
+                for (int i = lane; i < BM; i += 32) {
+                    const int r = tl.w * BM + i;
+                    sE[(slot * NA + m) * BM + i] =
+                        r < p.rows_per_expert
+                            ? row_emax(sm_ + (static_cast<size_t>(tl.x) * p.rows_per_expert + r) * nb, nb)
+                            : 0;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&eref_full[slot]);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------- epilogue -------------------------------
+        const int wr = warp & 3;
+        const int m = wr * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int4 tl = p.tiles[1 + tile];
             const int acc = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_ph, abort_flag, p.hdr, 30)))
+            const int slot = it % kES;
+            const uint32_t eph = (it / kES) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_ph, abort_flag, p.hdr, 56) &&
+                                             mbar_wait(&eref_full[slot], eph, abort_flag, p.hdr, 57)))
                 break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wr * 32) << 16) +
                                    static_cast<uint32_t>(acc * NA * BN);
-            const int n_used = (MODE == DENSE) ? BN : ((nrows + 15) / 16) * 16;
-            if (MODE == DENSE) {
-                const int col = mt * BM + m;  // output feature
-                for (int n0 = 0; n0 < n_used; n0 += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + n0, v);
+            const int nrows = tl.z, row0 = tl.y;
+            const int n_used = ((nrows + kBoxRows - 1) / kBoxRows) * kBoxRows;
+            const int r = tl.w * BM + m;
+            const bool valid = r < p.rows_per_expert;
+            const int eref1 = sE[(slot * NA + 0) * BM + m];
+            const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + m] : 0;
+            for (int n0 = 0; n0 < n_used; n0 += 16) {
+                float v1[16];
+                tmem_ld16(tbase + n0, v1);
+                if (NA == 2) {
+                    float v3[16];
+                    tmem_ld16(tbase + BN + n0, v3);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int t = row0 + n0 + i;
-                        if (n0 + i < nrows) {
-                            if (p.out_fp32)
-                                static_cast<float*>(p.out)[static_cast<size_t>(t) * p.n_out + col] = v[i];
-                            else
-                                static_cast<uint16_t*>(p.out)[static_cast<size_t>(t) * p.n_out + col] =
-                                    f32_to_bf16(v[i]);
-                        }
+                        if (n0 + i >= nrows) break;
+                        const int pr = row0 + n0 + i;
+                        const int xe = p.bexp[pr];
+                        const float gg = v1[i] * exp2i(eref1 - 127 + xe);
+                        const float u = v3[i] * exp2i(eref3 - 127 + xe);
+                        const float h = silu_f32(gg) * u;
+                        if (valid) p.hf[static_cast<size_t>(pr) * p.n_out + r] = h;
+                        const float amx = warp_max(valid ? fabsf(h) : 0.0f);
+                        if (lane == 0) atomicMax(p.h_amax + pr, __float_as_uint(amx));
                     }
-                }
-            } else {
-                const int r = mt * BM + m;  // row of the expert matrix
-                const bool valid = r < p.rows_per_expert;
-                const int nb = p.K / 32;
-                const size_t srow = (static_cast<size_t>(e) * p.rows_per_expert + (valid ? r : 0)) * nb;
-                const int eref1 = row_emax(p.s1 + srow, nb);
-                const int eref3 = (MODE == UP) ? row_emax(p.s3 + srow, nb) : 0;
-                for (int n0 = 0; n0 < n_used; n0 += 16) {
-                    float v1[16];
-                    tmem_ld16(tbase + n0, v1);
-                    if (MODE == UP) {
-                        float v3[16];
-                        tmem_ld16(tbase + BN + n0, v3);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (n0 + i >= nrows) break;
-                            const int pr = row0 + n0 + i;
-                            const int xe = p.bexp[pr];
-                            const float g = v1[i] * exp2i(eref1 - 127 + xe);
-                            const float u = v3[i] * exp2i(eref3 - 127 + xe);
-                            const float h = silu_f32(g) * u;
-                            if (valid) p.hf[static_cast<size_t>(pr) * p.n_out + r] = h;
-                            const float a = warp_max(valid ? fabsf(h) : 0.0f);
-                            if (lane == 0) atomicMax(p.h_amax + pr, __float_as_uint(a));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (n0 + i >= nrows) break;
-                            const int pr = row0 + n0 + i;
-                            const float y = v1[i] * exp2i(eref1 - 127 + p.bexp[pr]);
-                            if (valid) p.y[static_cast<size_t>(pr) * p.n_out + r] = y;
-                        }
+                    for (int i = 0; i < 16; ++i) {
+                        if (n0 + i >= nrows) break;
+                        const int pr = row0 + n0 + i;
+                        const float yv = v1[i] * exp2i(eref1 - 127 + p.bexp[pr]);
+                        if (valid) p.y[static_cast<size_t>(pr) * p.n_out + r] = yv;
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[acc]);
+                mbar_arrive(&eref_empty[slot]);
+            }
         }
-    } else if (MODE != DENSE && warp >= 8) {
-        // ------------------------------ dequantisation ------------------------
+    } else if (warp >= 8) {
+        // ---------------------------- dequantisation -------------------------
         const int dt = threadIdx.x - 256;  // 0..255
         const int row = dt >> 1, half = dt & 1;
-        const int nb = p.K / 32;
-        int s = 0;
-        uint32_t ph = 0;
-        for (int tile = blockIdx.x;; tile += gridDim.x) {
-            int e, row0, nrows, mt;
-            if (!tile_info<MODE>(p, tile, n_tiles, e, row0, nrows, mt)) break;
-            int r = mt * BM + row;
-            if (r >= p.rows_per_expert) r = p.rows_per_expert - 1;  // padding rows: any finite data
-            const size_t srow = (static_cast<size_t>(e) * p.rows_per_expert + r) * nb;
+        int r = 0, a = 0;
+        uint32_t rph = 0, aph = 0;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int4 tl = p.tiles[1 + tile];
+            const int slot = it % kES;
+            const uint32_t eph = (it / kES) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&eref_full[slot], eph, abort_flag, p.hdr, 58))) break;
+            int rr = tl.w * BM + row;
+            if (rr >= p.rows_per_expert) rr = p.rows_per_expert - 1;  // padding rows: any finite data
+            const size_t srow = (static_cast<size_t>(tl.x) * p.rows_per_expert + rr) * nb;
             const uint8_t* sc1 = p.s1 + srow;
-            const uint8_t* sc3 = (MODE == UP) ? p.s3 + srow : nullptr;
-            const int eref1 = row_emax(sc1, nb);
-            const int eref3 = (MODE == UP) ? row_emax(sc3, nb) : 0;
+            const uint8_t* sc3 = NA == 2 ? p.s3 + srow : nullptr;
+            const int eref1 = sE[(slot * NA + 0) * BM + row];
+            const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + row] : 0;
             bool ok = true;
             for (int ks = 0; ks < k_stages; ++ks) {
                 const int blk = 2 * ks + half;
                 const int e1 = sc1[blk];
-                const int e3 = (MODE == UP) ? sc3[blk] : 0;
-                if (!__all_sync(0xffffffffu, mbar_wait(&full_raw[s], ph, abort_flag, p.hdr, 40))) {
+                const int e3 = NA == 2 ? sc3[blk] : 0;
+                if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59) &&
+                                                 mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
                     break;
                 }
 #pragma unroll
-                for (int a = 0; a < NA; ++a) {
+                for (int mm = 0; mm < NA; ++mm) {
                     const uint4 raw =
-                        *reinterpret_cast<const uint4*>(sRaw + (s * NA + a) * kTileRaw + row * 32 + half * 16);
-                    const uint16_t sh = f16_pow2((a == 0 ? e1 - eref1 : e3 - eref3));
+                        *reinterpret_cast<const uint4*>(sRaw + (r * NA + mm) * kTileRaw + row * 32 + half * 16);
+                    const uint16_t sh = f16_pow2(mm == 0 ? e1 - eref1 : e3 - eref3);
                     const uint32_t sc2 = static_cast<uint32_t>(sh) | (static_cast<uint32_t>(sh) << 16);
                     uint32_t w[16];
                     e2m1x8_to_f16x8(raw.x, w[0], w[1], w[2], w[3]);
@@ -502,7 +693,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     e2m1x8_to_f16x8(raw.w, w[12], w[13], w[14], w[15]);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[i] = hmul2(w[i], sc2);
-                    uint8_t* dst = sA + (s * NA + a) * kTileA + row * 128;
+                    uint8_t* dst = sA + (a * NA + mm) * kTileA + row * 128;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int chunk = (half * 4 + c) ^ (row & 7);
@@ -512,10 +703,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_a[s]);
-                if (++s == STAGES) { s = 0; ph ^= 1; }
+                if (lane == 0) {
+                    mbar_arrive(&a_full[a]);
+                    mbar_arrive(&raw_empty[r]);
+                }
+                if (++r == RS) { r = 0; rph ^= 1; }
+                if (++a == AS) { a = 0; aph ^= 1; }
             }
             if (!ok) break;
+            if (lane == 0) mbar_arrive(&eref_empty[slot]);
         }
     }
 
@@ -596,10 +792,15 @@ convert_h_kernel(const float* __restrict__ hf, const uint32_t* __restrict__ h_am
     if (lane == 0) hexp[r] = ex;
 }
 
-// units of at most bn rows per expert: units[0].x = count, units[1 + u] = (e, row0, nrows, 0)
-__global__ void __launch_bounds__(256)
-build_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
-                   int bn, int4* units, int cap) {
+// Tile lists of the expert GEMMs: for every expert with tokens, its token
+// rows are cut into chunks of at most bn rows, and each (m tile, chunk) pair
+// is one tile.  Order: expert, then m tile, then chunk, so the chunks that
+// share one weight tile are consecutive (neighbouring CTAs read the same
+// weight bytes, mostly from L2).  list[0].x = count; list[1 + i] =
+// (expert, first row, rows, m tile).
+__global__ void __launch_bounds__(1024)
+build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
+                   int bn, int m_up, int m_dn, int4* up, int4* dn, int cap) {
     __shared__ int base[1024 + 1];
     for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = (counts[e] + bn - 1) / bn;
     __syncthreads();
@@ -611,14 +812,31 @@ build_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
             run += c;
         }
         base[E] = run;
-        units[0] = make_int4(min(run, cap), 0, 0, 0);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int cnt = counts[e];
-        for (int c = 0; c * bn < cnt; ++c) {
-            const int u = base[e] + c;
-            if (u < cap) units[1 + u] = make_int4(e, offsets[e] + c * bn, min(bn, cnt - c * bn), 0);
+    const int U = base[E];
+    const int n_up = min(U * m_up, cap), n_dn = min(U * m_dn, cap);
+    if (threadIdx.x == 0) {
+        up[0] = make_int4(n_up, 0, 0, 0);
+        dn[0] = make_int4(n_dn, 0, 0, 0);
+    }
+    for (int pass = 0; pass < 2; ++pass) {
+        const int mt_n = pass == 0 ? m_up : m_dn;
+        const int n = pass == 0 ? n_up : n_dn;
+        int4* list = pass == 0 ? up : dn;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            // expert of entry i: largest e with base[e] * mt_n <= i
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (base[mid] * mt_n <= i) lo = mid; else hi = mid - 1;
+            }
+            const int e = lo;
+            const int nch = base[e + 1] - base[e];
+            const int local = i - base[e] * mt_n;
+            const int mt = local / nch, c = local % nch;
+            const int cnt = counts[e];
+            list[1 + i] = make_int4(e, offsets[e] + c * bn, min(bn, cnt - c * bn), mt);
         }
     }
 }
@@ -656,10 +874,9 @@ bool make_tmap(CUtensorMap* tm, const void* base, CUtensorMapDataType dt, int el
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
-cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                      const TcParams& p, int grid, cudaStream_t s, const char* name) {
-    constexpr size_t smem = smem_bytes<MODE>();
+cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const DenseParams& p,
+                         int grid, cudaStream_t s) {
+    constexpr size_t smem = dense_smem_bytes();
     static_assert(smem <= 232448, "shared memory budget");
     // the attribute is per device; set it once per device (not inside graph captures)
     static std::atomic<uint64_t> done{0};
@@ -667,23 +884,45 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& a3, const CUtenso
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
+        cudaError_t e = cudaFuncSetAttribute(tc_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        done.fetch_or(bit);
+    }
+    tc_dense_kernel<<<grid, kDenseThreads, smem, s>>>(a, b, p);
+    trace_mark("gemm_bf16", s);
+    return cudaGetLastError();
+}
+
+constexpr int kUnitRows = 128;  // == ExpCfg<1>::BN == ExpCfg<2>::BN
+
+template <int NA>
+cudaError_t launch_expert(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
+                          const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+    constexpr size_t smem = exp_smem_bytes<NA>();
+    static_assert(smem <= 232448, "shared memory budget");
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<NA>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
-    tc_gemm_kernel<MODE><<<grid, Cfg<MODE>::THREADS, smem, s>>>(a, a3, b, p);
+    tc_expert_kernel<NA><<<grid, kExpThreads, smem, s>>>(a, a3, b, p);
     trace_mark(name, s);
     return cudaGetLastError();
 }
 
-constexpr int kUnitRows = 128;  // == Cfg<UP>::BN == Cfg<DOWN>::BN
-
 }  // namespace
 
-size_t grouped_tile_cap(int T, int E, int k) {
-    return static_cast<size_t>(E) + (static_cast<size_t>(T) * k + 15) / 16 + 2;
+size_t grouped_tile_cap(int T, int E, int k, int d, int f) {
+    const size_t units = static_cast<size_t>(E) + (static_cast<size_t>(T) * k + kUnitRows - 1) / kUnitRows + 1;
+    const size_t mt = static_cast<size_t>(std::max((f + BM - 1) / BM, (d + BM - 1) / BM));
+    return units * mt;
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t* x, const uint16_t* w, int T, int N, int K, void* out,
@@ -693,80 +932,80 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const uint16_t* w, int T, int N,
     if (!make_tmap(&ta, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, BK, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
-    if (!make_tmap(&tb, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, T, BK, Cfg<DENSE>::BN,
+    if (!make_tmap(&tb, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, T, BK, kDenseBN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
-    TcParams p{};
+    DenseParams p{};
     p.K = K;
     p.m_tiles = N / BM;
     p.T = T;
-    p.n_tiles = (T + Cfg<DENSE>::BN - 1) / Cfg<DENSE>::BN;
+    p.n_tiles = (T + kDenseBN - 1) / kDenseBN;
     p.out = out;
     p.out_fp32 = out_fp32;
     p.n_out = N;
     p.hdr = hdr;
     const int tiles = p.n_tiles * p.m_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    return launch_tc<DENSE>(ta, ta, tb, p, grid, s, "gemm_bf16");
+    return launch_dense(ta, tb, p, grid, s);
 }
 
 cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     const int P = g.T * g.k;
-    int4* units = reinterpret_cast<int4*>(g.tiles);
-    const int cap = g.tiles_cap - 1;
+    const int cap = g.tiles_cap;
+    int4* tiles_up = reinterpret_cast<int4*>(g.tiles);
+    int4* tiles_dn = tiles_up + (cap + 1);
     cudaError_t e;
     gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.x, g.perm, P, g.k, g.d, g.xp, g.xp_exp, g.h_amax);
     trace_mark("gather_rows", s);
-    build_units_kernel<<<1, 256, 0, s>>>(g.counts, g.offsets, g.E, kUnitRows, units, cap);
-    trace_mark("build_units", s);
+    build_tiles_kernel<<<1, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUnitRows, (g.f + BM - 1) / BM,
+                                          (g.d + BM - 1) / BM, tiles_up, tiles_dn, cap);
+    trace_mark("build_tiles", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    // UP: A = w1 / w3 raw bytes [E*f, d/2], B = xp [P, d] f16
+    // UP: A = w1 / w3 raw bytes [E*f, d/2], B = xp [P, d] f16 in 16-row boxes
     CUtensorMap t1, t3, tb;
     const uint64_t rows_up = static_cast<uint64_t>(g.E) * g.f;
     if (!make_tmap(&t1, g.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap(&t3, g.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kUnitRows,
+        !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
-    TcParams p{};
+    ExpParams p{};
     p.K = g.d;
     p.rows_per_expert = g.f;
-    p.m_tiles = (g.f + BM - 1) / BM;
     p.s1 = g.w1_s;
     p.s3 = g.w3_s;
-    p.units = units;
+    p.tiles = tiles_up;
     p.bexp = g.xp_exp;
     p.n_out = g.f;
     p.hf = g.hf;
     p.h_amax = g.h_amax;
     p.hdr = g.hdr;
-    if ((e = launch_tc<UP>(t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
+    if ((e = launch_expert<2>(t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
     convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp);
     trace_mark("convert_h", s);
 
-    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16
+    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16 in 16-row boxes
     CUtensorMap t2, th;
     const uint64_t rows_dn = static_cast<uint64_t>(g.E) * g.d;
     if (!make_tmap(&t2, g.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.f / 2, rows_dn, BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap(&th, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kUnitRows,
+        !make_tmap(&th, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
-    TcParams q{};
+    ExpParams q{};
     q.K = g.f;
     q.rows_per_expert = g.d;
-    q.m_tiles = (g.d + BM - 1) / BM;
     q.s1 = g.w2_s;
-    q.units = units;
+    q.tiles = tiles_dn;
     q.bexp = g.hp_exp;
     q.n_out = g.d;
     q.y = g.y;
     q.hdr = g.hdr;
-    if ((e = launch_tc<DOWN>(t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
+    if ((e = launch_expert<1>(t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
 
     return launch_combine(g.y, 1, g.wts, g.inv, g.T, g.k, g.d, g.out, s);
 }

@@ -62,26 +62,37 @@ rmsnorm_kernel(const uint16_t* __restrict__ h, int D, const uint16_t* __restrict
     }
 }
 
-// 256 threads x 4 columns per CTA; grid (ceil(d / 1024), T)
-__global__ void __launch_bounds__(256)
+// 128 threads x 4 columns per CTA; grid (ceil(d / 512), T).  The token's k
+// (row, weight) pairs are staged in shared memory first, so the loads of the
+// k rows are independent and issue together.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ y, int nslots, size_t slot_stride,
                const float* __restrict__ wts, const int32_t* __restrict__ inv, int k, int d,
                uint16_t* __restrict__ out) {
+    __shared__ int rows[32];
+    __shared__ float wk[32];
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
-    const int c = (blockIdx.x * 256 + threadIdx.x) * 4;
+    if (threadIdx.x < k) {
+        rows[threadIdx.x] = inv[t * k + threadIdx.x];
+        wk[threadIdx.x] = wts[t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int c = (blockIdx.x * kCombineThreads + threadIdx.x) * 4;
     if (c >= d) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
-        const int row = inv[t * k + j];
-        const float w = wts[t * k + j];
-        const float* yr = y + static_cast<size_t>(row) * d + c;
+        const float* yr = y + static_cast<size_t>(rows[j]) * d + c;
         float4 v = *reinterpret_cast<const float4*>(yr);
-        for (int s = 1; s < nslots; ++s) {
-            const float4 v2 = *reinterpret_cast<const float4*>(yr + s * slot_stride);
+        if (nslots > 1) {
+            const float4 v2 = *reinterpret_cast<const float4*>(yr + slot_stride);
             v.x += v2.x; v.y += v2.y; v.z += v2.z; v.w += v2.w;
         }
+        const float w = wk[j];
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -106,9 +117,9 @@ cudaError_t launch_rmsnorm(const uint16_t* h, int T, int D, const uint16_t* gamm
 cudaError_t launch_combine(const float* y, int nslots, const float* wts, const int32_t* inv, int T,
                            int k, int d, uint16_t* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    dim3 grid((d + 1023) / 1024, T);
+    dim3 grid((d + 4 * kCombineThreads - 1) / (4 * kCombineThreads), T);
     const size_t slot_stride = static_cast<size_t>(T) * k * d;
-    const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, s, y, nslots, slot_stride,
+    const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, nslots, slot_stride,
                                      wts, inv, k, d, out);
     trace_mark("combine", s);
     return e;

@@ -33,57 +33,118 @@ __device__ __forceinline__ uint32_t order_bits(float v) {
 
 __device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
 
-// top-k of one token by one warp; logits row in global memory.  Writes idx/w
-// (global) and optionally the selection into shared memory.
-__device__ void topk_token(const float* lrow, const float* __restrict__ bias, int E,
-                           int k, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
-                           int32_t* sel_smem, WsHeader* hdr) {
+__device__ __forceinline__ uint64_t expert_key(float l, float b, int e) {
+    // order-preserving bits of s + b in the high word, ~e in the low word: the
+    // larger key is the larger score, and equal scores go to the lower index
+    return (static_cast<uint64_t>(order_bits(sigmoid_f32(l) + b)) << 32) |
+           static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ int key_expert(uint64_t key) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
+}
+
+// The k largest of the (unique) keys held by the warp, KPL per lane: k rounds
+// of a warp-wide max; lane j < k returns the j-th largest.
+template <int KPL>
+__device__ __forceinline__ uint64_t warp_topk(uint64_t (&key)[KPL], int k) {
     const int lane = threadIdx.x & 31;
-    uint64_t key[kKeysPerLane];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < kKeysPerLane; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = 0;
-        if (e < E) {
-            const float l = lrow[e];
-            bad |= !isfinite(l);
-            const float beta = sigmoid_f32(l) + bias[e];
-            key[i] = (static_cast<uint64_t>(order_bits(beta)) << 32) |
-                     static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
-        }
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(hdr, K3MOE_ERR_NONFINITE, 1);
-    float s_mine = 0.0f;  // lane j keeps the score of slot j
-    int e_mine = 0;
+    uint64_t mine = 0;
     for (int j = 0; j < k; ++j) {
         uint64_t best = 0;
 #pragma unroll
-        for (int i = 0; i < kKeysPerLane; ++i) best = key[i] > best ? key[i] : best;
+        for (int i = 0; i < KPL; ++i) best = key[i] > best ? key[i] : best;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
             best = other > best ? other : best;
         }
-        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
-        // the owner lane removes the winner
-        if ((e & 31) == lane) {
 #pragma unroll
-            for (int i = 0; i < kKeysPerLane; ++i)
-                if (key[i] == best) key[i] = 0;
-        }
-        if (lane == j) {
-            e_mine = e;
-            s_mine = sigmoid_f32(lrow[e]);
+        for (int i = 0; i < KPL; ++i)
+            if (key[i] == best) key[i] = 0;
+        if (lane == j) mine = best;
+    }
+    return mine;
+}
+
+// The k best experts among [e0, e1) of one token's logits (one warp; at most
+// 32 * KPL candidates); lane j < k returns the j-th key.
+template <int KPL>
+__device__ uint64_t topk_slice(const float* lrow, const float* __restrict__ bias, int e0, int e1,
+                               int k, WsHeader* hdr) {
+    const int lane = threadIdx.x & 31;
+    uint64_t key[KPL];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        const int e = e0 + lane + 32 * i;
+        key[i] = 0;
+        if (e < e1) {
+            const float l = lrow[e];
+            bad |= !isfinite(l);
+            key[i] = expert_key(l, bias[e], e);
         }
     }
-    // renormalise over the selection, summing in slot order
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(hdr, K3MOE_ERR_NONFINITE, 1);
+    return warp_topk<KPL>(key, k);
+}
+
+// Writes the selection of one token from its k winning keys (lane j holds the
+// j-th): idx, and the weights s / sum(s) summed in slot order.
+__device__ void write_selection(uint64_t mine, const float* lrow, int k, int32_t* __restrict__ idx_out,
+                                float* __restrict__ w_out, int32_t* sel_smem) {
+    const int lane = threadIdx.x & 31;
+    const int e = key_expert(mine);
+    const float s_mine = lane < k ? sigmoid_f32(lrow[e]) : 0.0f;
     float sum = 0.0f;
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, s_mine, j);
     if (lane < k) {
-        idx_out[lane] = e_mine;
+        idx_out[lane] = e;
         w_out[lane] = s_mine / sum;
-        if (sel_smem) sel_smem[lane] = e_mine;
+        if (sel_smem) sel_smem[lane] = e;
+    }
+}
+
+// top-k of one token by one warp over all E experts
+__device__ void topk_token(const float* lrow, const float* __restrict__ bias, int E,
+                           int k, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                           int32_t* sel_smem, WsHeader* hdr) {
+    const uint64_t mine = topk_slice<kKeysPerLane>(lrow, bias, 0, E, k, hdr);
+    write_selection(mine, lrow, k, idx_out, w_out, sel_smem);
+}
+
+// top-k of T <= 8 tokens by the 8 warps of a CTA: G = 8 / T' warps per token
+// (T' = T rounded up to a power of two) each keep the k best of a slice of the
+// experts, then one warp per token merges the G * k candidates.
+template <int G>
+__device__ void topk_tokens_cta(const RouteArgs& a, int32_t* sel, uint64_t (*cand)[32]) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int t = wid / G, gw = wid % G;
+    const int slice = (a.E + G - 1) / G;
+    const float* lrow = a.logits + static_cast<size_t>(t) * a.E;
+    if (t < a.T) {
+        const int e0 = gw * slice, e1 = min(a.E, e0 + slice);
+        const uint64_t mine = topk_slice<32 / G>(lrow, a.bias, e0, e1, a.k, a.hdr);
+        if (G == 1) {
+            write_selection(mine, lrow, a.k, a.idx + static_cast<size_t>(t) * a.k,
+                            a.wts + static_cast<size_t>(t) * a.k, sel + t * a.k);
+        } else if (lane < a.k) {
+            cand[wid][lane] = mine;
+        }
+    }
+    if (G == 1) return;
+    __syncthreads();
+    if (t < a.T && gw == 0) {
+        constexpr int KPL = (G * 32 + 31) / 32;  // G * k <= G * 32 candidates
+        uint64_t key[KPL];
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+            const int c = lane + 32 * i;  // candidate c = (warp c / k, rank c % k)
+            key[i] = c < G * a.k ? cand[wid + c / a.k][c % a.k] : 0;
+        }
+        const uint64_t mine = warp_topk<KPL>(key, a.k);
+        write_selection(mine, lrow, a.k, a.idx + static_cast<size_t>(t) * a.k,
+                        a.wts + static_cast<size_t>(t) * a.k, sel + t * a.k);
     }
 }
 
@@ -171,45 +232,99 @@ __device__ void permute_small(const int32_t* sel, int T, int k, int E, int32_t* 
 
 // Logits by GEMV (one warp per expert, all T tokens), then the last CTA to
 // finish runs top-k for every token and, if requested, the permutation.
+// Each warp issues all loads of its weight row before it needs them; the T
+// token rows are staged once per CTA in shared memory.  With x16 requested,
+// CTA b also writes token rows b, b + gridDim.x, ... as f16 with their
+// exponents, which the decode kernels read.
+constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
+
 __global__ void __launch_bounds__(256)
 route_small_kernel(RouteArgs a) {
+    extern __shared__ __align__(16) uint4 xs[];  // [T * d_r / 8]
     __shared__ int32_t sel[256];
     __shared__ uint32_t ticket_s;
+    __shared__ float red[8];
     // the next kernel of the forward may start launching now: it waits for
     // this grid's completion (griddepcontrol.wait) before reading its outputs
     pdl_trigger();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int e = blockIdx.x * 8 + wid;
+    const uint16_t* wrow = a.w + static_cast<size_t>(e < a.E ? e : 0) * a.d_r;
+    uint4 wv[kRouteChunks];
+#pragma unroll
+    for (int i = 0; i < kRouteChunks; ++i) {
+        const int c = i * 256 + lane * 8;
+        wv[i] = (e < a.E && c < a.d_r) ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+    }
+    const int nvec = a.T * a.d_r / 8;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x)
+        xs[v] = reinterpret_cast<const uint4*>(a.x)[v];
+    __syncthreads();
+
+    // token rows blockIdx.x, blockIdx.x + gridDim.x, ... -> f16 * 2^-e with
+    // e = floor(log2(max |x|)) (CTA-uniform loop; every CTA has the rows staged)
+    for (int t = blockIdx.x; a.x16 && t < a.T; t += gridDim.x) {
+        const uint4* row = xs + t * (a.d_r / 8);
+        float amax = 0.0f;
+        for (int v = threadIdx.x; v < a.d_r / 8; v += blockDim.x) {
+            const uint4 q = row[v];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j2] << 16)),
+                                         fabsf(__uint_as_float(w[j2] & 0xFFFF0000u))));
+        }
+        amax = warp_max(amax);
+        if (lane == 0) red[wid] = amax;
+        __syncthreads();
+        float m = 0.0f;
+        for (int w2 = 0; w2 < 8; ++w2) m = fmaxf(m, red[w2]);
+        const int ex = ilog2f(m);
+        const float sc = exp2i(-ex);
+        uint4* dst = reinterpret_cast<uint4*>(a.x16 + static_cast<size_t>(t) * a.d_r);
+        for (int v = threadIdx.x; v < a.d_r / 8; v += blockDim.x) {
+            const uint4 q = row[v];
+            uint4 o;
+            o.x = f32x2_to_f16x2(__uint_as_float(q.x << 16) * sc, __uint_as_float(q.x & 0xFFFF0000u) * sc);
+            o.y = f32x2_to_f16x2(__uint_as_float(q.y << 16) * sc, __uint_as_float(q.y & 0xFFFF0000u) * sc);
+            o.z = f32x2_to_f16x2(__uint_as_float(q.z << 16) * sc, __uint_as_float(q.z & 0xFFFF0000u) * sc);
+            o.w = f32x2_to_f16x2(__uint_as_float(q.w << 16) * sc, __uint_as_float(q.w & 0xFFFF0000u) * sc);
+            dst[v] = o;
+        }
+        if (threadIdx.x == 0) a.xexp[t] = ex;
+        __syncthreads();  // red[] is reused by the next row
+    }
+
     if (e < a.E) {
         float acc[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
-        const uint16_t* wrow = a.w + static_cast<size_t>(e) * a.d_r;
-        for (int c0 = 0; c0 < a.d_r; c0 += 256 * 4) {
-            uint4 wv[4];
+        for (int base = 0; base < a.d_r; base += 256 * kRouteChunks) {
+            if (base > 0) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u * 256 + lane * 8;
-                wv[u] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < kRouteChunks; ++i) {
+                    const int c = base + i * 256 + lane * 8;
+                    wv[i] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u * 256 + lane * 8;
-                if (c >= a.d_r) continue;
-                const uint32_t wq[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+            for (int i = 0; i < kRouteChunks; ++i) {
+                const int c = base + i * 256 + lane * 8;
+                if (c >= a.d_r) break;
+                const uint32_t wq[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     if (t >= a.T) break;
-                    const uint4 xv = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.d_r + c);
+                    const uint4 xv = xs[(t * a.d_r + c) / 8];
                     const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
-                    float s = acc[t];
+                    float sacc = acc[t];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        s = fmaf(__uint_as_float(wq[i] << 16), __uint_as_float(xq[i] << 16), s);
-                        s = fmaf(__uint_as_float(wq[i] & 0xFFFF0000u),
-                                 __uint_as_float(xq[i] & 0xFFFF0000u), s);
+                    for (int q = 0; q < 4; ++q) {
+                        sacc = fmaf(__uint_as_float(wq[q] << 16), __uint_as_float(xq[q] << 16), sacc);
+                        sacc = fmaf(__uint_as_float(wq[q] & 0xFFFF0000u),
+                                    __uint_as_float(xq[q] & 0xFFFF0000u), sacc);
                     }
-                    acc[t] = s;
+                    acc[t] = sacc;
                 }
             }
         }
@@ -228,19 +343,16 @@ route_small_kernel(RouteArgs a) {
     if (ticket_s != gridDim.x - 1) return;
     if (threadIdx.x == 0) a.hdr->counters[CTR_ROUTE] = 0;
     __threadfence();
-    for (int t = wid; t < a.T; t += 8)
-        topk_token(a.logits + static_cast<size_t>(t) * a.E, a.bias, a.E, a.k,
-                   a.idx + static_cast<size_t>(t) * a.k, a.wts + static_cast<size_t>(t) * a.k,
-                   sel + t * a.k, a.hdr);
+    {
+        __shared__ uint64_t cand[8][32];
+        if (a.T == 1) topk_tokens_cta<8>(a, sel, cand);
+        else if (a.T == 2) topk_tokens_cta<4>(a, sel, cand);
+        else if (a.T <= 4) topk_tokens_cta<2>(a, sel, cand);
+        else topk_tokens_cta<1>(a, sel, cand);
+    }
     __syncthreads();
     if (a.counts)
         permute_small(sel, a.T, a.k, a.E, a.counts, a.offsets, a.perm, a.inv, a.active);
-    if (a.x16)
-        for (int t = wid; t < a.T; t += 8) {
-            const int ex = row_to_f16(a.x + static_cast<size_t>(t) * a.d_r, a.d_r,
-                                      a.x16 + static_cast<size_t>(t) * a.d_r);
-            if (lane == 0) a.xexp[t] = ex;
-        }
 }
 
 __global__ void __launch_bounds__(256)
@@ -386,7 +498,14 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
 
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
     const int grid = (a.E + 7) / 8;
-    route_small_kernel<<<grid, 256, 0, s>>>(a);
+    const size_t smem = static_cast<size_t>(a.T) * a.d_r * 2;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    route_small_kernel<<<grid, 256, smem, s>>>(a);
     trace_mark("route_small", s);
     return cudaGetLastError();
 }
