@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define K3MOE_ABI_VERSION 1
+#define K3MOE_ABI_VERSION 2
 
 typedef enum k3moe_status {
     K3MOE_OK = 0,
@@ -68,7 +68,9 @@ typedef enum k3moe_act {
 } k3moe_act;
 
 /* Expert-path selector.  AUTO picks DECODE for T <= 8 and GROUPED otherwise.
- *   DECODE : streaming GEMV over the selected experts' bytes (CUDA cores).
+ *   DECODE : block-scaled tcgen05 MMAs (kind::mxf8f6f4) streaming the
+ *            selected experts' E2M1 codes by TMA, E8M0 scales applied by the
+ *            tensor cores, activations as E4M3 terms; split over the SMs.
  *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
  *            dequantisation, TMA-fed, TMEM accumulators. */
 typedef enum k3moe_path {
@@ -83,11 +85,16 @@ typedef enum k3moe_path {
  * Expert weights ([PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact"):
  * compressed-tensors MXFP4, logical [out, in] per expert; `*_q` holds two
  * E2M1 codes per byte (element 2i in the low nibble, sign in bit 3,
- * magnitudes [0,.5,1,1.5,2,3,4,6]); `*_s` holds one E8M0 byte e per 32
- * consecutive inputs, value 2^(e-127) (e = 255 is not allowed).
- *   w1_q [E, f, d/2]  w1_s [E, f, d/32]   gate projection
- *   w3_q [E, f, d/2]  w3_s [E, f, d/32]   up projection
- *   w2_q [E, d, f/2]  w2_s [E, d, f/32]   down projection
+ * magnitudes [0,.5,1,1.5,2,3,4,6]) and is 32-byte aligned:
+ *   w1_q [E, f, d/2]   gate projection
+ *   w3_q [E, f, d/2]   up projection
+ *   w2_q [E, d, f/2]   down projection
+ * The E8M0 block scales (one byte e per 32 consecutive inputs, value
+ * 2^(e-127), e = 255 not allowed) are passed in the prepared layout that
+ * k3moe_prepare_scales writes from the canonical [rows, in/32] arrays, one
+ * prepared array per matrix (E * rows * in / 32 bytes each):
+ *   w1_sf  from w1_s [E, f, d/32]     w3_sf  from w3_s [E, f, d/32]
+ *   w2_sf  from w2_s [E, d, f/32]
  * Router ([PR26185], GrEarl, "Dry run"): logits l = x_r W_r^T, scores
  * s = sigmoid(l); the k experts with the largest s + b are selected (ties to
  * the lower index, slots listed in that order); combine weights are
@@ -98,8 +105,8 @@ typedef enum k3moe_path {
 typedef struct k3moe_layer_desc {
     int32_t E;          /* routed experts (896) */
     int32_t k;          /* experts per token (16), 1 <= k <= min(E, 32) */
-    int32_t d;          /* latent width (3584), multiple of 64 (of 128 in block mode) */
-    int32_t f;          /* expert hidden width (3072), multiple of 64 */
+    int32_t d;          /* latent width (3584), multiple of 128 */
+    int32_t f;          /* expert hidden width (3072), multiple of 128 */
     int32_t d_router;   /* router input width: d (latent mode) or D (block mode) */
     int32_t act;        /* k3moe_act */
     int32_t path;       /* k3moe_path */
@@ -107,11 +114,11 @@ typedef struct k3moe_layer_desc {
     float eps;          /* block mode: RMSNorm epsilon (1e-5 per [PR573]) */
     int32_t reserved;   /* must be 0 */
     const uint8_t* w1_q;
-    const uint8_t* w1_s;
     const uint8_t* w3_q;
-    const uint8_t* w3_s;
     const uint8_t* w2_q;
-    const uint8_t* w2_s;
+    const uint8_t* w1_sf;        /* prepared scales of w1 */
+    const uint8_t* w3_sf;        /* prepared scales of w3 */
+    const uint8_t* w2_sf;        /* prepared scales of w2 */
     const uint16_t* router_w;    /* [E, d_router] bf16 */
     const float* router_b;       /* [E] fp32 selection bias (exp_probs_b) */
     const uint16_t* norm_gamma;  /* block mode: [D] bf16 (ffn_routed_norm) */
@@ -143,6 +150,25 @@ k3moe_status k3moe_repack_mxfp4(const uint8_t* packed, const uint8_t* scale, int
  *   aligned); scale_out [rows, cols/32].  Errors as for the repack. */
 k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t cols,
                                 uint8_t* packed_out, uint8_t* scale_out, void* stream);
+
+/* Block-scale preparation for the tensor-core kernels.  A canonical E8M0
+ * array (one byte per row and 32 inputs) is regrouped into 512-byte atoms,
+ * one per tile of 128 rows and 128-wide input chunk; byte 16 (m % 32) +
+ * 4 (m / 32) + b of an atom holds row m of the tile and block b of the chunk
+ * (the order in which tcgen05.cp spreads scales over the TMEM lanes that the
+ * block-scaled MMA reads: row m from lane m, column m / 32).  The atom of
+ * (tile, chunk) starts at byte (tile * cols/128 + chunk) * 512.
+ *   scale [rows, cols/32] uint8 (device; rows stacked over the experts)
+ *   sf    [rows * cols/32] uint8 (device)
+ * A byte permutation: bit-exact, deterministic.  rows and cols multiples of
+ * 128.  The paper stores scales row by row; the atoms are this library's
+ * layout.  Errors: INVALID_ARG, SHAPE, ALIGN (16-byte), CUDA. */
+k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t rows, int64_t cols, uint8_t* sf,
+                                  void* stream);
+
+/* Inverse of k3moe_prepare_scales (prepared atoms -> canonical array). */
+k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* scale,
+                                    void* stream);
 
 /* Workspace bytes that k3moe_route needs for T tokens and E experts. */
 size_t k3moe_route_workspace_size(int32_t T, int32_t E);

@@ -39,7 +39,7 @@ EXPORTS = (
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
-    "k3moe_trace_read",
+    "k3moe_trace_read", "k3moe_prepare_scales", "k3moe_unprepare_scales",
 )
 
 
@@ -56,8 +56,8 @@ class LayerDesc(ctypes.Structure):
         ("f", ctypes.c_int32), ("d_router", ctypes.c_int32), ("act", ctypes.c_int32),
         ("path", ctypes.c_int32), ("D", ctypes.c_int32), ("eps", ctypes.c_float),
         ("reserved", ctypes.c_int32),
-        ("w1_q", ctypes.c_void_p), ("w1_s", ctypes.c_void_p), ("w3_q", ctypes.c_void_p),
-        ("w3_s", ctypes.c_void_p), ("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
+        ("w1_q", ctypes.c_void_p), ("w3_q", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
+        ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
         ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
         ("norm_gamma", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
     ]
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
         "k3moe_graph_destroy": ([vp], ctypes.c_int),
         "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                               ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+        "k3moe_prepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
+        "k3moe_unprepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -244,13 +246,37 @@ def k3moe_gemm_bf16(x, w, out_fp32: bool = False, out=None, stream=None):
     return out
 
 
+def k3moe_prepare_scales(scale, stream=None):
+    """Canonical E8M0 scales [..., rows, cols/32] (rows stacked over any
+    leading dims) -> the prepared atoms the kernels read, a flat uint8 tensor."""
+    _dev(scale, "scale")
+    rows = scale.numel() // scale.shape[-1]
+    cols = 32 * scale.shape[-1]
+    sf = torch.empty(scale.numel(), dtype=torch.uint8, device=scale.device)
+    _check(lib().k3moe_prepare_scales(_p(scale), rows, cols, _p(sf), _stream(stream)))
+    return sf
+
+
+def k3moe_unprepare_scales(sf, shape, stream=None):
+    """Inverse of k3moe_prepare_scales: the canonical array of ``shape``."""
+    scale = torch.empty(shape, dtype=torch.uint8, device=sf.device)
+    rows = scale.numel() // scale.shape[-1]
+    _check(lib().k3moe_unprepare_scales(_p(sf), rows, 32 * scale.shape[-1], _p(scale), _stream(stream)))
+    return scale
+
+
 class MoELayer:
-    """Device tensors of one layer plus the ``k3moe_layer_desc`` that points at them."""
+    """Device tensors of one layer plus the ``k3moe_layer_desc`` that points at them.
+
+    Takes the canonical scale arrays (w*_s, one E8M0 byte per row and 32
+    inputs) and keeps the prepared atoms that the kernels read
+    (k3moe_prepare_scales, run once here on the current stream)."""
 
     def __init__(self, *, w1_q, w1_s, w3_q, w3_s, w2_q, w2_s, router_w, router_b, k: int,
                  norm_gamma=None, w_down=None, w_up=None, eps: float = 1e-5,
                  path: int = PATH_AUTO, act: int = ACT_SILU_GATED):
-        self.tensors = dict(w1_q=w1_q, w1_s=w1_s, w3_q=w3_q, w3_s=w3_s, w2_q=w2_q, w2_s=w2_s,
+        self.tensors = dict(w1_q=w1_q, w3_q=w3_q, w2_q=w2_q, w1_sf=k3moe_prepare_scales(w1_s),
+                            w3_sf=k3moe_prepare_scales(w3_s), w2_sf=k3moe_prepare_scales(w2_s),
                             router_w=_bf16(router_w, "router_w"), router_b=router_b)
         E, f, half_d = w1_q.shape
         d = 2 * half_d

@@ -1,6 +1,7 @@
 // Host side of the k3moe C ABI: argument checks, workspace layout, dispatch.
 // Every step of the layer runs in the kernels of this library; nothing here
 // computes on the host.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -14,6 +15,7 @@ namespace {
 constexpr int kDecodeMaxT = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int device_sms() {
     static std::mutex mu;
@@ -29,7 +31,21 @@ int device_sms() {
     return cache[dev];
 }
 
-k3moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA; }
+// K3MOE_DEBUG=1 in the environment prints the CUDA error behind a
+// K3MOE_ERR_CUDA status to stderr (read once)
+bool debug_on() {
+    static const bool on = [] {
+        const char* v = getenv("K3MOE_DEBUG");
+        return v && v[0] && v[0] != '0';
+    }();
+    return on;
+}
+
+k3moe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return K3MOE_OK;
+    if (debug_on()) fprintf(stderr, "k3moe: CUDA error %d (%s)\n", static_cast<int>(e), cudaGetErrorString(e));
+    return K3MOE_ERR_CUDA;
+}
 
 // PDL is on unless K3MOE_NO_PDL is set in the environment (read once)
 bool pdl_on() {
@@ -89,9 +105,8 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     p.inv = c.take(P * 4);
     p.chunk = c.take(permute_scratch_bytes(T, d->E));
     const int Td = std::min(T, kDecodeMaxT);
-    const size_t Pd = static_cast<size_t>(Td) * d->k;
-    p.dec = c.take(decode_scratch_bytes(Td, d->k, d->d, d->f));
-    p.y = c.take(std::max(P, 2 * Pd) * d->d * 4);  // grouped: 1 slot; decode: 2 slots
+    p.dec = c.take(mx_decode_scratch_bytes(Td, d->E, d->k, d->d, d->f));
+    p.y = c.take(P * d->d * 4);  // grouped path
     p.xp = c.take(P * d->d * 2);
     p.xp_exp = c.take(P * 4);
     p.hb = c.take(P * d->f * 4);
@@ -114,7 +129,7 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
     if (d->E < 1 || d->k < 1 || d->d < 1 || d->f < 1 || d->d_router < 1) return K3MOE_ERR_INVALID_ARG;
     if (d->reserved != 0) return K3MOE_ERR_INVALID_ARG;
     if (d->k > d->E || d->k > 32 || d->E > 1024) return K3MOE_ERR_SHAPE;
-    if (d->d % 64 || d->f % 64) return K3MOE_ERR_SHAPE;
+    if (d->d % 128 || d->f % 128) return K3MOE_ERR_SHAPE;
     if (d->D < 0) return K3MOE_ERR_SHAPE;
     if (d->D > 0) {
         if (d->D % 128 || d->d % 128 || d->d_router != d->D) return K3MOE_ERR_SHAPE;
@@ -127,11 +142,13 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
     }
     if (d->act != K3MOE_ACT_SILU_GATED) return K3MOE_ERR_UNSUPPORTED;
     if (d->path < K3MOE_PATH_AUTO || d->path > K3MOE_PATH_GROUPED) return K3MOE_ERR_INVALID_ARG;
-    const void* ptrs[] = {d->w1_q, d->w1_s, d->w3_q, d->w3_s, d->w2_q, d->w2_s, d->router_w, d->router_b};
+    const void* ptrs[] = {d->w1_q, d->w3_q, d->w2_q, d->w1_sf, d->w3_sf, d->w2_sf, d->router_w, d->router_b};
     for (const void* p : ptrs) {
         if (!p) return K3MOE_ERR_INVALID_ARG;
         if (!aligned16(p)) return K3MOE_ERR_ALIGN;
     }
+    // E2M1 codes are read by TMA in 16-byte slots: 32-byte aligned bases
+    if (!aligned32(d->w1_q) || !aligned32(d->w3_q) || !aligned32(d->w2_q)) return K3MOE_ERR_ALIGN;
     return K3MOE_OK;
 }
 
@@ -257,6 +274,24 @@ k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t col
     if (!aligned16(packed_out)) return K3MOE_ERR_ALIGN;
     return cuda_status(launch_unpack(blocks, rows * (cols / 32), packed_out, scale_out,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t rows, int64_t cols, uint8_t* sf,
+                                  void* stream) {
+    if (!scale || !sf || rows < 1 || cols < 1) return K3MOE_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return K3MOE_ERR_SHAPE;
+    if (!aligned16(scale) || !aligned16(sf)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_prepare_sf(scale, rows, static_cast<int>(cols), sf, 0,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* scale,
+                                    void* stream) {
+    if (!scale || !sf || rows < 1 || cols < 1) return K3MOE_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return K3MOE_ERR_SHAPE;
+    if (!aligned16(scale) || !aligned16(sf)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_prepare_sf(scale, rows, static_cast<int>(cols), const_cast<uint8_t*>(sf), 1,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 size_t k3moe_route_workspace_size(int32_t T, int32_t E) {
@@ -414,7 +449,8 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_DECODE && desc->D == 0;
     if (T <= kDecodeMaxT) {
         r.counts = counts; r.offsets = offsets; r.perm = perm; r.inv = inv; r.active = active;
-        if (fuse_prep) decode_x16_slots(at(p.dec), T, desc->d, &r.x16, &r.xexp);
+        if (fuse_prep)
+            mx_decode_xq_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.xq, &r.xsf, &r.xq_n);
         if ((e = launch_route_small(r, s))) return K3MOE_ERR_CUDA;
     } else {
         if (T >= 64 && desc->E % 128 == 0) {
@@ -432,20 +468,21 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     }
 
     if (path == K3MOE_PATH_DECODE) {
-        DecodeArgs a{};
-        a.w1_q = desc->w1_q; a.w1_s = desc->w1_s; a.w3_q = desc->w3_q; a.w3_s = desc->w3_s;
-        a.w2_q = desc->w2_q; a.w2_s = desc->w2_s;
-        a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
-        a.x16_ready = fuse_prep ? 1 : 0;
-        a.offsets = offsets; a.perm = perm; a.active = active; a.wts = r.wts; a.inv = inv;
+        MxDecodeArgs a{};
+        a.w1_q = desc->w1_q; a.w3_q = desc->w3_q; a.w2_q = desc->w2_q;
+        a.w1_sf = desc->w1_sf; a.w3_sf = desc->w3_sf; a.w2_sf = desc->w2_sf;
+        a.x = x_expert; a.xq_ready = fuse_prep ? 1 : 0;
+        a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
+        a.active = active; a.idx = r.idx; a.wts = r.wts;
         a.scratch = at(p.dec);
-        a.y = static_cast<float*>(at(p.y));
         a.out = latent_out; a.hdr = hdr; a.num_sms = sms;
-        if ((e = launch_decode(a, s))) return K3MOE_ERR_CUDA;
+        e = launch_mx_decode(a, s);
+        if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+        if (e) return cuda_status(e);
     } else {
         GroupedArgs g{};
-        g.w1_q = desc->w1_q; g.w1_s = desc->w1_s; g.w3_q = desc->w3_q; g.w3_s = desc->w3_s;
-        g.w2_q = desc->w2_q; g.w2_s = desc->w2_s;
+        g.w1_q = desc->w1_q; g.w3_q = desc->w3_q; g.w2_q = desc->w2_q;
+        g.w1_sf = desc->w1_sf; g.w3_sf = desc->w3_sf; g.w2_sf = desc->w2_sf;
         g.x = x_expert; g.T = T; g.E = desc->E; g.k = desc->k; g.d = desc->d; g.f = desc->f;
         g.counts = counts; g.offsets = offsets; g.perm = perm; g.inv = inv; g.wts = r.wts;
         g.xp = static_cast<uint16_t*>(at(p.xp));

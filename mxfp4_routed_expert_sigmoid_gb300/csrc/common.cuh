@@ -152,6 +152,89 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// Activations for the block-scaled tensor-core path: every 32-element block
+// of a row is written as kTerms E4M3 codes per element, each term with its
+// own E8M0 block scale, so that v ~= sum_j e4m3(q_j) * 2^(s_j - 127).  Term
+// j + 1 encodes what term j left over (exactly: the remainder of a
+// round-to-nearest is representable), so each term adds about four bits.
+// ---------------------------------------------------------------------------
+constexpr int kTerms = 3;
+
+// Smallest e with amax * 2^-e <= 448 (the largest finite E4M3), from the
+// exponent and mantissa fields: amax = (1 + m) 2^E fits at e = E - 8 iff
+// 1 + m <= 1.75.  Zero and subnormal amax give -127 (the smallest scale).
+__device__ __forceinline__ int e4m3_scale_exp(float amax) {
+    const uint32_t u = __float_as_uint(amax);
+    const int ef = static_cast<int>((u >> 23) & 0xFFu);
+    if (ef == 0) return -127;
+    return ef - 127 - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+
+// fp32 -> E4M3 code (round to nearest even, saturating to +-448)
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
+    return r & 0xFFu;
+}
+
+// E4M3 code -> fp32 (exact)
+__device__ __forceinline__ float e4m3_float(uint32_t code) {
+    uint32_t h;
+    const uint16_t in = static_cast<uint16_t>(code | (code << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+    return f16x2_to_f32x2(h).x;
+}
+
+// One 32-element block held by a warp (lane = element) -> kTerms codes of
+// this lane's element and the kTerms scale bytes (warp-uniform).
+__device__ __forceinline__ void quantize_terms(float v, uint32_t (&q)[kTerms], uint32_t (&sb)[kTerms]) {
+    float res = v;
+#pragma unroll
+    for (int j = 0; j < kTerms; ++j) {
+        const float amax = warp_max(fabsf(res));
+        const int e = e4m3_scale_exp(amax);
+        q[j] = e4m3_code(res * exp2i(-e));
+        sb[j] = static_cast<uint32_t>(e + 127);
+        res = res - e4m3_float(q[j]) * exp2i(e);
+    }
+}
+
+// B operand layout of the block-scaled MMA, per 128-wide K stage:
+//   codes : N rows x 128 bytes, row n = kTerms * token + term, stored with the
+//           128-byte swizzle of the tensor-core K-major layout (16-byte chunk
+//           c of row n at chunk c ^ (n % 8)), so one bulk copy lands it in
+//           shared memory ready for the MMA;
+//   scales: a 512-byte atom, byte 16 (n % 32) + 4 (n / 32) + kb for row n and
+//           32-block kb of the stage (the layout tcgen05.cp 32x128b.warpx4
+//           spreads over the TMEM lanes that the MMA reads).
+__device__ __forceinline__ uint32_t b_code_offset(int n, int k) {
+    return static_cast<uint32_t>(n * 128 + ((((k >> 4) ^ (n & 7)) & 7) << 4) + (k & 15));
+}
+__device__ __forceinline__ uint32_t sf_atom_offset(int n, int kb) {
+    return static_cast<uint32_t>(16 * (n & 31) + 4 * (n >> 5) + kb);
+}
+
+// Writes the quantised block (warp, lane = element) of row t into the B
+// layout: block kb (0..3) of the stage whose codes start at `codes` and whose
+// scale atom starts at `scales`.  Lanes 4i..4i+3 combine their bytes into one
+// 32-bit store.
+__device__ __forceinline__ void store_terms(const uint32_t (&q)[kTerms], const uint32_t (&sb)[kTerms],
+                                            int t, int kb, uint8_t* codes, uint8_t* scales) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < kTerms; ++j) {
+        uint32_t w = q[j];
+        w |= __shfl_down_sync(0xffffffffu, q[j], 1) << 8;
+        w |= __shfl_down_sync(0xffffffffu, q[j], 2) << 16;
+        w |= __shfl_down_sync(0xffffffffu, q[j], 3) << 24;
+        const int n = kTerms * t + j;
+        if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(codes + b_code_offset(n, 32 * kb + lane)) = w;
+        if (lane == 0) scales[sf_atom_offset(n, kb)] = static_cast<uint8_t>(sb[j]);
+    }
+}
+
 }  // namespace k3
 
 // ---------------------------------------------------------------------------
@@ -196,39 +279,13 @@ struct RouteArgs {
     int32_t* perm;     // [T*k]
     int32_t* inv;      // [T*k]
     int32_t* active;   // [E] ascending experts with count > 0; active[E] = n_active (at index E)
-    // optional (decode, latent mode): the router input as f16 rows with one
-    // power-of-two exponent per row, written by the last CTA
-    uint16_t* x16;     // [T, d_r]
-    int32_t* xexp;     // [T]
+    // optional (decode, latent mode): the router input quantised for the
+    // block-scaled expert kernels (codes [d_r / 128][xq_n][128], scale atoms
+    // [d_r / 128][512]); the CTAs share the work
+    uint8_t* xq;
+    uint8_t* xsf;
+    int xq_n;          // MMA N: rows per stage (>= kTerms * T)
 };
-
-// one warp: row (K bf16) -> f16 * 2^-e with e = floor(log2(max |row|)); returns e
-__device__ __forceinline__ int row_to_f16(const uint16_t* src, int K, uint16_t* dst) {
-    const int lane = threadIdx.x & 31;
-    float amax = 0.0f;
-    for (int c = lane * 8; c < K; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
-                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
-    }
-    amax = warp_max(amax);
-    const int ex = ilog2f(amax);
-    const float sc = exp2i(-ex);
-    for (int c = lane * 8; c < K; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint4 o;
-        o.x = f32x2_to_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
-        o.y = f32x2_to_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
-        o.z = f32x2_to_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
-        o.w = f32x2_to_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
-        *reinterpret_cast<uint4*>(dst + c) = o;
-    }
-    return ex;
-}
 
 cudaError_t launch_repack(const uint8_t* packed, const uint8_t* scale, int64_t nblocks,
                           uint8_t* out, cudaStream_t s);
@@ -258,31 +315,35 @@ cudaError_t launch_rmsnorm(const uint16_t* h, int T, int D, const uint16_t* gamm
 cudaError_t launch_combine(const float* y, int nslots, const float* wts, const int32_t* inv, int T,
                            int k, int d, uint16_t* out, cudaStream_t s);
 
-// decode path
-struct DecodeArgs {
-    const uint8_t *w1_q, *w1_s, *w3_q, *w3_s, *w2_q, *w2_s;
-    const uint16_t* x;     // [T, d] bf16 expert input
-    int x16_ready;         // 1: the router already wrote the f16 rows into the scratch
+
+// block-scaled tensor-core decode path (mx.cu)
+struct MxDecodeArgs {
+    const uint8_t *w1_q, *w3_q, *w2_q;  // E2M1 codes
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
+    const uint16_t* x;        // [T, d] bf16 expert input (read when !xq_ready)
+    int xq_ready;             // 1: the router already wrote the E4M3 terms
     int T, E, k, d, f;
-    const int32_t* offsets;  // [E+1]
-    const int32_t* perm;     // [T*k]
-    const int32_t* active;   // [E+1] list + count at [E]
-    const float* wts;        // [T, k]
-    const int32_t* inv;      // [T*k]
-    void* scratch;           // decode_scratch_bytes(T, k, d, f)
-    float* y;                // [2 slots][T*k, d] fp32 partial sums, rows in permuted order
-    uint16_t* out;           // [T, d] bf16
+    const int32_t* active;    // [E + 1] active experts ascending, count at [E]
+    const int32_t* idx;       // [T, k]
+    const float* wts;         // [T, k]
+    void* scratch;            // mx_decode_scratch_bytes(T, E, k, d, f)
+    uint16_t* out;            // [T, d] bf16
     WsHeader* hdr;
     int num_sms;
 };
-size_t decode_scratch_bytes(int T, int k, int d, int f);
-// where the decode scratch keeps the f16 token rows and their exponents
-void decode_x16_slots(void* scratch, int T, int d, uint16_t** x16, int32_t** xexp);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f);
+// where the decode scratch keeps the quantised token rows (router output)
+void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_t** xq, uint8_t** xsf,
+                        int* N);
+cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s);
+// canonical E8M0 scales [rows, K/32] <-> prepared atoms (inverse = 1: atoms -> canonical)
+cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
+                              cudaStream_t s);
 
 // grouped (tcgen05) path
 struct GroupedArgs {
-    const uint8_t *w1_q, *w1_s, *w3_q, *w3_s, *w2_q, *w2_s;
+    const uint8_t *w1_q, *w3_q, *w2_q;  // E2M1 codes
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
     const uint16_t* x;       // [T, d] bf16 expert input
     int T, E, k, d, f;
     const int32_t* counts;   // [E]

@@ -44,138 +44,17 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace k3 {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kTileA = BM * BK * 2;   // 16 KB of f16/bf16
 constexpr int kTileRaw = BM * BK / 2; // 4 KB of packed E2M1
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: false if the CTA is aborting or the limit expired.
-__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
-                          int where) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            if (hdr) set_error(hdr, K3MOE_ERR_TIMEOUT, where);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, uint64_t* bar, int x,
-                                            int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
-    d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset
-    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, A/B f16 (fmt 0) or
-// bf16 (fmt 1), both K-major, shape M x N.
-__device__ __forceinline__ uint32_t idesc_f16(int fmt, int M, int N) {
-    return (1u << 4) | (static_cast<uint32_t>(fmt) << 7) | (static_cast<uint32_t>(fmt) << 10) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // ---------------------------------------------------------------------------
 // Dense bf16 GEMM: out[t, n] = sum_c x[t, c] * w[n, c]
@@ -204,22 +83,23 @@ constexpr size_t dense_smem_bytes() {
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-// largest E8M0 exponent of a weight row of nb bytes (16-byte loads when the
-// row length allows it; rows are then 16-byte aligned because the scale
-// array is)
-__device__ __forceinline__ int row_emax(const uint8_t* srow, int nb) {
+// Prepared scale atoms: row r of expert e is row m = r % 128 of atom tile
+// e * rows / 128 + r / 128; its block b sits at + (b / 4) * 512 + b % 4 from
+// the returned pointer.
+__device__ __forceinline__ const uint8_t* sf_row(const uint8_t* sf, int e, int r, int rows_per_expert,
+                                                 int KS) {
+    const int tile = e * (rows_per_expert / 128) + r / 128;
+    const int m = r % 128;
+    return sf + static_cast<size_t>(tile) * KS * 512 + 16 * (m & 31) + 4 * (m >> 5);
+}
+
+// largest exponent of a row from its prepared atoms (four blocks per word)
+__device__ __forceinline__ int row_emax_sf(const uint8_t* srow, int KS) {
     int m = 0;
-    if ((nb & 15) == 0) {
-        for (int i = 0; i < nb; i += 16) {
-            const uint4 v = *reinterpret_cast<const uint4*>(srow + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int s = 0; s < KS; ++s) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(srow + static_cast<size_t>(s) * 512);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) m = max(m, static_cast<int>((w[j] >> (8 * b)) & 0xFF));
-        }
-    } else {
-        for (int i = 0; i < nb; ++i) m = max(m, static_cast<int>(srow[i]));
+        for (int b = 0; b < 4; ++b) m = max(m, static_cast<int>((w >> (8 * b)) & 0xFF));
     }
     return m;
 }
@@ -395,8 +275,8 @@ constexpr int kExpThreads = 512;
 struct ExpParams {
     int K;                // reduction length (multiple of 64)
     int rows_per_expert;  // rows of one expert matrix
-    const uint8_t* s1;    // E8M0 of A (w1 or w2), [E * rows, K / 32]
-    const uint8_t* s3;    // UP: E8M0 of w3
+    const uint8_t* s1;    // prepared E8M0 atoms of A (w1 or w2)
+    const uint8_t* s3;    // UP: prepared E8M0 atoms of w3
     const int4* tiles;    // tiles[0].x = count; tiles[1 + i] = (e, first B row, B rows, m tile)
     const int32_t* bexp;  // per B row power-of-two exponent
     int n_out;            // row length of hf / y
@@ -446,7 +326,6 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = p.tiles[0].x;
     const int k_stages = p.K / BK;
-    const int nb = p.K / 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -586,7 +465,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const int r = tl.w * BM + i;
                     sE[(slot * NA + m) * BM + i] =
                         r < p.rows_per_expert
-                            ? row_emax(sm_ + (static_cast<size_t>(tl.x) * p.rows_per_expert + r) * nb, nb)
+                            ? row_emax_sf(sf_row(sm_, tl.x, r, p.rows_per_expert, p.K / 128), p.K / 128)
                             : 0;
                 }
             }
@@ -665,16 +544,16 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!__all_sync(0xffffffffu, mbar_wait(&eref_full[slot], eph, abort_flag, p.hdr, 58))) break;
             int rr = tl.w * BM + row;
             if (rr >= p.rows_per_expert) rr = p.rows_per_expert - 1;  // padding rows: any finite data
-            const size_t srow = (static_cast<size_t>(tl.x) * p.rows_per_expert + rr) * nb;
-            const uint8_t* sc1 = p.s1 + srow;
-            const uint8_t* sc3 = NA == 2 ? p.s3 + srow : nullptr;
+            const uint8_t* sc1 = sf_row(p.s1, tl.x, rr, p.rows_per_expert, p.K / 128);
+            const uint8_t* sc3 = NA == 2 ? sf_row(p.s3, tl.x, rr, p.rows_per_expert, p.K / 128) : nullptr;
             const int eref1 = sE[(slot * NA + 0) * BM + row];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + row] : 0;
             bool ok = true;
             for (int ks = 0; ks < k_stages; ++ks) {
                 const int blk = 2 * ks + half;
-                const int e1 = sc1[blk];
-                const int e3 = NA == 2 ? sc3[blk] : 0;
+                const int so = (blk >> 2) * 512 + (blk & 3);
+                const int e1 = sc1[so];
+                const int e3 = NA == 2 ? sc3[so] : 0;
                 if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59) &&
                                                  mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
@@ -844,36 +723,6 @@ build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// 2-D tensor map over a row-major [outer, inner] array
-bool make_tmap(CUtensorMap* tm, const void* base, CUtensorMapDataType dt, int elem_bytes,
-               uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle sw) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_bytes)};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const DenseParams& p,
                          int grid, cudaStream_t s) {
     constexpr size_t smem = dense_smem_bytes();
@@ -975,8 +824,8 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     ExpParams p{};
     p.K = g.d;
     p.rows_per_expert = g.f;
-    p.s1 = g.w1_s;
-    p.s3 = g.w3_s;
+    p.s1 = g.w1_sf;
+    p.s3 = g.w3_sf;
     p.tiles = tiles_up;
     p.bexp = g.xp_exp;
     p.n_out = g.f;
@@ -999,7 +848,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     ExpParams q{};
     q.K = g.f;
     q.rows_per_expert = g.d;
-    q.s1 = g.w2_s;
+    q.s1 = g.w2_sf;
     q.tiles = tiles_dn;
     q.bexp = g.hp_exp;
     q.n_out = g.d;

@@ -1,0 +1,612 @@
+// Block-scaled tensor-core path of the routed experts (decode, T <= 8), and
+// the scale-factor layout it reads.
+//
+// The experts' MXFP4 weights reach the tensor cores as they are stored:
+// tcgen05.mma kind::mxf8f6f4 multiplies E2M1 weight codes by E4M3 activation
+// codes and applies both operands' E8M0 block scales (one per 32 inputs) in
+// hardware, accumulating in fp32 in TMEM; nothing is dequantised in software
+// (llama.cpp PR #26185 "model: add Kimi-K3 text model", review by GrEarl,
+// section "repack_mxfp4_blocks is bit-exact": the MXFP4 format; section "Dry
+// run": 896 experts, 16 used, latent width 3584, expert width 3072).
+//
+// Operands of one MMA (M = 128 weight rows, N = 16 or 32 token-term rows,
+// K = 32), staged per 128-wide K chunk, four chunks to a pipeline stage (the
+// TMA engines reach the copy bandwidth of HBM only with that many bytes per
+// stage: about 3.4 TB/s with one chunk, 6 TB/s with four, measured on GB300):
+//   A  E2M1 codes by TMA (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B: each 8 bytes
+//      of packed codes land in a 16-byte shared-memory slot, the container
+//      layout of 4-bit operands in kind::f8f6f4), 128-byte swizzle;
+//   SFA the 512-byte scale atom of the 128 rows x 4 blocks (prepared layout,
+//      below), copied to TMEM by tcgen05.cp 32x128b.warpx4: row m is read
+//      from lane m, column m / 32, byte = the K block (scale id in idesc);
+//   B  activations as kTerms E4M3 terms per token (rows 3t, 3t+1, 3t+2;
+//      see quantize_terms), pre-swizzled in global memory, one bulk copy;
+//   SFB their 512-byte scale atom (column n from lane n % 32, column n / 32).
+// The kTerms partial products of a token are summed in fp32 by the epilogue.
+//
+// Up projection: W1 and W3 are separate units (128-row tiles of one matrix),
+// so every TMA box is 128 rows tall; the finish kernel pairs g = W1 x with
+// u = W3 x.  Down projection: 128-row tiles of W2.
+//
+// Work split (stream-K): the units (active expert, row tile, K stage) are cut
+// into one contiguous range per CTA, every range at least one tile long, so a
+// tile is shared by at most two CTAs.  The CTA that starts a tile writes its
+// partial sums to slot 0 and the other to slot 1 (a CTA that owns the whole
+// tile writes zeros to slot 1); consumers add slot 0 and slot 1 in that order,
+// so results do not depend on timing.
+//
+// Kernels of one decode forward (after the router, which also writes the
+// token rows as E4M3 terms): up -> finish (h = silu(g) * u from both slots,
+// quantised to E4M3 terms) -> down -> combine (weights in slot order).
+//
+// Roles of the streaming kernel (192 threads, one CTA per SM):
+//   warp 0     producer: TMA / bulk copies into a ring of stages;
+//   warp 1     TMEM owner and MMA issuer (one thread);
+//   warps 2..5 epilogue: tcgen05.ld of the accumulator quadrant (warp % 4).
+// Every wait is bounded (kWaitLimitNs); on expiry the CTA records
+// K3MOE_ERR_TIMEOUT, every role stops, copies in flight are waited for (with
+// a limit) and TMEM is released.
+#include <atomic>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace k3 {
+namespace {
+
+using namespace tc;
+
+constexpr int kMxThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kChunks = 4;             // 128-wide K chunks per stage (a stage covers K = 512)
+constexpr int kSfStages = 1;           // stages whose scale slots live in TMEM at once
+constexpr int kChunkA = 16384;         // 128 rows x 128 bytes (E2M1 in 8-bit slots)
+constexpr uint32_t kTxChunkA = 8192;   // packed bytes the TMA moves per A chunk
+constexpr int kStageA = kChunks * kChunkA;
+constexpr int kSfBase = 64;            // TMEM: accumulators in columns 0..63, scale slots above
+// every scale slot starts on a 32-column boundary (A at +0, B at +32)
+static_assert(kSfBase + kSfStages * kChunks * 64 <= 512, "scale slots fit in TMEM");
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+struct MxArgs {
+    const uint8_t* sf[2];   // prepared scale atoms of the matrices (W1, W3 or W2)
+    int nmat;               // matrices per expert in this pass (2 up, 1 down)
+    const uint8_t* bq;      // B codes [unit][KS][N][128] (up: one shared unit)
+    const uint8_t* bsf;     // B scale atoms [unit][KS][512]
+    size_t bq_ustride;      // bytes per unit (0 when all units share B)
+    size_t bsf_ustride;
+    const int32_t* active;  // [E + 1]: active experts ascending, count at [E]
+    int E;
+    int rows;               // weight rows per expert (f up, d down)
+    int tiles;              // 128-row tiles per expert
+    int KC;                 // 128-wide K chunks (K / 128)
+    int KS;                 // stages of kChunks chunks (the last one may be shorter)
+    int N;                  // MMA N (16 or 32)
+    int T;                  // tokens
+    int RS;                 // stages in the ring
+    uint32_t stage_bytes;
+    float* part;            // [slot][mat][umax][T][rows_out]
+    int umax;
+    int rows_out;           // f (up) or d (down)
+    WsHeader* hdr;
+};
+
+// position (unit, matrix, row tile, stage) in the sequence of stages
+struct Cursor {
+    int u, mat, tile, ks;
+    __device__ Cursor(int w, int nmat, int tiles, int KS) {
+        const int per_m = tiles * KS, per_u = nmat * per_m;
+        u = w / per_u;
+        int r = w - u * per_u;
+        mat = r / per_m;
+        r -= mat * per_m;
+        tile = r / KS;
+        ks = r - tile * KS;
+    }
+    __device__ void next(int nmat, int tiles, int KS) {
+        if (++ks == KS) {
+            ks = 0;
+            if (++tile == tiles) {
+                tile = 0;
+                if (++mat == nmat) {
+                    mat = 0;
+                    ++u;
+                }
+            }
+        }
+    }
+};
+
+__global__ void __launch_bounds__(kMxThreads, 1)
+mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
+                 MxArgs p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_holder;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t NB = static_cast<uint32_t>(p.N) * 128;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.RS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);
+        }
+        abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 1) tmem_alloc(&tmem_holder, kTmemCols);
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        if (p.nmat > 1) prefetch_tmap(&tmA3);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_holder;
+
+    // the router / finish kernel before this one wrote the active list and B
+    pdl_wait();
+    pdl_trigger();
+    const int U = p.active[p.E];
+    const long long W = static_cast<long long>(U) * p.nmat * p.tiles * p.KS;
+    const int w0 = static_cast<int>(W * blockIdx.x / gridDim.x);
+    const int w1 = static_cast<int>(W * (blockIdx.x + 1) / gridDim.x);
+
+    if (warp == 0) {
+        if (lane == 0 && w0 < w1) {
+            // ------------------------------ producer ------------------------------
+            Cursor c(w0, p.nmat, p.tiles, p.KS);
+            int e = p.active[c.u];
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            for (int w = w0; w < w1; ++w) {
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70)) break;
+                uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+                const int c0 = c.ks * kChunks;
+                const int nch = min(kChunks, p.KC - c0);
+                mbar_expect_tx(&full[s], static_cast<uint32_t>(nch) * (kTxChunkA + NB + 1024));
+                const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
+                const int y = e * p.rows + c.tile * 128;
+                for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, &full[s], (c0 + cc) * 128, y);
+                uint8_t* sb = st + kStageA;
+                bulk_load(sb, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, &full[s]);
+                bulk_load(sb + kChunks * NB,
+                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.KC + c0) * 512, nch * 512,
+                          &full[s]);
+                bulk_load(sb + kChunks * NB + kChunks * 512,
+                          p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(c0) * 512, nch * 512, &full[s]);
+                ++issued;
+                if (++s == p.RS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+                const int u_prev = c.u;
+                c.next(p.nmat, p.tiles, p.KS);
+                if (c.u != u_prev && w + 1 < w1) e = p.active[c.u];
+            }
+            // copies still in flight (after an abort) finish before the CTA exits
+            for (int j = issued > p.RS ? issued - p.RS : 0; j < issued; ++j) {
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&full[j % p.RS], (j / p.RS) & 1) &&
+                       global_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && w0 < w1) {
+            // ------------------------------ MMA issuer ----------------------------
+            int ks = Cursor(w0, p.nmat, p.tiles, p.KS).ks;
+            int s = 0, seg = 0, ps = 0;
+            uint32_t ph = 0, pph = 0;
+            const uint32_t id0 = idesc_mx(128, p.N, 0, 0);
+            for (int i = 0, w = w0; w < w1; ++i, ++w) {
+                const bool seg_start = (w == w0) || ks == 0;
+                const bool seg_end = (w + 1 == w1) || ks == p.KS - 1;
+                const int a = seg & 1;
+                if (seg_start && !mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71))
+                    break;
+                if (!mbar_wait(&full[s], ph, abort_flag, p.hdr, 72)) break;
+                // scale slots of stage i are reused from stage i - kSfStages: its MMAs
+                // have finished reading them
+                if (i >= kSfStages) {
+                    if (!mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73)) break;
+                    if (++ps == p.RS) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
+                }
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+                const uint32_t sb = st + kStageA;
+                const int nch = min(kChunks, p.KC - ks * kChunks);
+                const uint32_t slot0 = tmem + kSfBase + (i % kSfStages) * kChunks * 64;
+                for (int cc = 0; cc < nch; ++cc) {
+                    tmem_cp_sf(slot0 + 64 * cc, sb + kChunks * NB + 512 * cc);
+                    tmem_cp_sf(slot0 + 64 * cc + 32, sb + kChunks * NB + kChunks * 512 + 512 * cc);
+                }
+                const uint32_t d_t = tmem + a * 32;
+                for (int cc = 0; cc < nch; ++cc) {
+                    const uint64_t ad = sw128_desc(st + cc * kChunkA), bd = sw128_desc(sb + cc * NB);
+                    const uint32_t sfa = slot0 + 64 * cc, sfb = sfa + 32;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_mx(d_t, ad + 2 * j, bd + 2 * j,
+                               id0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29), sfa,
+                               sfb, (seg_start && cc == 0 && j == 0) ? 0u : 1u);
+                }
+                mma_commit(&empty[s]);
+                if (seg_end) {
+                    mma_commit(&acc_full[a]);
+                    ++seg;
+                }
+                if (++s == p.RS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+                if (++ks == p.KS) ks = 0;
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ---------------------------------
+        const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
+        Cursor c(w0 < w1 ? w0 : 0, p.nmat, p.tiles, p.KS);
+        int seg = 0;
+        for (int w = w0; w < w1;) {
+            const int ks_begin = c.ks;
+            const int len = min(p.KS - c.ks, w1 - w);
+            const bool whole = ks_begin == 0 && len == p.KS;
+            const int a = seg & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, p.hdr, 74)))
+                break;
+            tc_fence_after();
+            float v[32];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * 32;
+            if (p.N == 16) {
+                float v16[16];
+                tmem_ld16(taddr, v16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = v16[i];
+#pragma unroll
+                for (int i = 16; i < 32; ++i) v[i] = 0.0f;
+            } else {
+                tmem_ld32(taddr, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            const int mat = c.mat, mats = p.nmat;
+            const int row = c.tile * 128 + q * 32 + lane;
+            const size_t plane = static_cast<size_t>(p.umax) * p.T * p.rows_out;
+            float* dst = p.part + static_cast<size_t>((ks_begin == 0 ? 0 : 1) * mats + mat) * plane +
+                         static_cast<size_t>(c.u) * p.T * p.rows_out + row;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t >= p.T) break;
+                const float sum = v[kTerms * t] + v[kTerms * t + 1] + v[kTerms * t + 2];
+                dst[static_cast<size_t>(t) * p.rows_out] = sum;
+                if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
+            }
+            w += len;
+            ++seg;
+            c.ks = 0;
+            if (++c.tile == p.tiles) {
+                c.tile = 0;
+                if (++c.mat == p.nmat) {
+                    c.mat = 0;
+                    ++c.u;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E4M3 terms in
+// the B layout of the down projection.  One warp per (unit, token, 32-block).
+__global__ void __launch_bounds__(256)
+mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
+                 const int32_t* __restrict__ active, int E, uint8_t* __restrict__ hq,
+                 uint8_t* __restrict__ hsf) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int nb = f / 32;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int u = i / (T * nb);
+    if (u >= active[E]) return;
+    const int r = i - u * T * nb;
+    const int t = r / nb, b = r - t * nb;
+    const size_t plane = static_cast<size_t>(umax) * T * f;
+    const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
+    const float g = part[o] + part[2 * plane + o];
+    const float uu = part[plane + o] + part[3 * plane + o];
+    uint32_t q[kTerms], sb[kTerms];
+    quantize_terms(silu_f32(g) * uu, q, sb);
+    const int KS = f / 128;
+    store_terms(q, sb, t, b & 3, hq + (static_cast<size_t>(u) * KS + (b >> 2)) * N * 128,
+                hsf + (static_cast<size_t>(u) * KS + (b >> 2)) * 512);
+}
+
+// Token rows (bf16) -> kTerms E4M3 terms in the B layout (used when the
+// router did not write them).  One warp per (token, 32-block).
+__global__ void __launch_bounds__(256)
+mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int T, int K, int N, uint8_t* __restrict__ xq,
+                        uint8_t* __restrict__ xsf) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (i >= T * nb) return;
+    const int t = i / nb, b = i - t * nb;
+    uint32_t q[kTerms], sb[kTerms];
+    quantize_terms(bf16_to_f32(x[static_cast<size_t>(t) * K + 32 * b + lane]), q, sb);
+    store_terms(q, sb, t, b & 3, xq + static_cast<size_t>(b >> 2) * N * 128,
+                xsf + static_cast<size_t>(b >> 2) * 512);
+}
+
+// out[t, :] = bf16(sum_j w[t, j] * (y0 + y1)[unit(idx[t, j]), t, :]), j in slot
+// order; the unit of an expert is its position in the active list.  A CTA
+// owns 128 columns of one token: its 8 warps load the k slots' rows at once
+// (warp g takes slots g, g + 8, ...; a lane takes 4 columns), park the
+// weighted rows in shared memory, and one thread per column adds them in
+// slot order.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCols = 128;
+constexpr int kCombineMaxUnits = 256;  // decode: T * k <= 8 * 32
+
+__global__ void __launch_bounds__(kCombineThreads)
+mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const float* __restrict__ wts,
+                  const int32_t* __restrict__ idx, const int32_t* __restrict__ active, int E, int k,
+                  uint16_t* __restrict__ out) {
+    __shared__ int rows[32];
+    __shared__ float wk[32];
+    __shared__ int act[kCombineMaxUnits];
+    __shared__ __align__(16) float part[32][kCombineCols];
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.y;
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int U = active[E];
+    for (int i = threadIdx.x; i < U; i += blockDim.x) act[i] = active[i];
+    __syncthreads();
+    if (threadIdx.x < k) {
+        const int e = idx[t * k + threadIdx.x];
+        int lo = 0, hi = U - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (act[mid] < e) lo = mid + 1;
+            else hi = mid;
+        }
+        rows[threadIdx.x] = lo * T + t;
+        wk[threadIdx.x] = wts[t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int c0 = blockIdx.x * kCombineCols;
+    const size_t slot = static_cast<size_t>(umax) * T * d;
+    if (c0 + lane * 4 < d) {
+#pragma unroll 4
+        for (int j = g; j < k; j += kCombineThreads / 32) {
+            const float* yr = y + static_cast<size_t>(rows[j]) * d + c0 + lane * 4;
+            const float4 v = *reinterpret_cast<const float4*>(yr);
+            const float4 v2 = *reinterpret_cast<const float4*>(yr + slot);
+            const float w = wk[j];
+            *reinterpret_cast<float4*>(&part[j][lane * 4]) =
+                make_float4(w * (v.x + v2.x), w * (v.y + v2.y), w * (v.z + v2.z), w * (v.w + v2.w));
+        }
+    }
+    __syncthreads();
+    const int c = c0 + threadIdx.x;
+    if (threadIdx.x < kCombineCols && c < d) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) acc += part[j][threadIdx.x];
+        out[static_cast<size_t>(t) * d + c] = f32_to_bf16(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prepared scale-factor layout.  For a weight matrix with R rows (stacked over
+// the experts) and K inputs, the E8M0 bytes are grouped per tile of 128 rows
+// and 128-wide input chunk into 512-byte atoms, byte 16 (m % 32) + 4 (m / 32)
+// + b holding row m of the tile and block b of the chunk; the atom of (tile,
+// chunk) starts at (tile * K/128 + chunk) * 512.  One thread per 4-byte word
+// (the four blocks of one row and chunk).
+// ---------------------------------------------------------------------------
+__global__ void prepare_sf_kernel(uint8_t* __restrict__ canon, int64_t n_words, int K,
+                                  uint8_t* __restrict__ atoms, int inverse) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n_words) return;
+    const int KC = K / 128, nb = K / 32;
+    const int64_t atom = i / 128;            // 128 words per atom
+    const int wi = static_cast<int>(i - atom * 128);
+    const int64_t tile = atom / KC;
+    const int chunk = static_cast<int>(atom - tile * KC);
+    const int r = wi >> 2, qd = wi & 3;      // word at byte 16 r + 4 qd: row m = 32 qd + r
+    const int64_t row = tile * 128 + 32 * qd + r;
+    uint32_t* cw = reinterpret_cast<uint32_t*>(canon + row * nb + 4 * chunk);
+    uint32_t* aw = reinterpret_cast<uint32_t*>(atoms + atom * 512 + 16 * r + 4 * qd);
+    if (inverse) *cw = *aw;
+    else *aw = *cw;
+}
+
+}  // namespace
+
+cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
+                              cudaStream_t s) {
+    const int64_t n_words = rows * (K / 32) / 4;
+    if (n_words <= 0) return cudaSuccess;
+    const int64_t blocks = (n_words + 255) / 256;
+    prepare_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(const_cast<uint8_t*>(canon), n_words, K,
+                                                                    atoms, inverse);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// host: decode forward
+// ---------------------------------------------------------------------------
+namespace {
+
+int mx_n(int T) { return kTerms * T <= 16 ? 16 : 32; }
+
+struct MxScratch {
+    uint8_t *xq, *xsf, *hq, *hsf;
+    float *up, *y;
+    int umax, N;
+};
+
+MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
+    MxScratch m{};
+    m.umax = std::min(E, T * k);
+    m.N = mx_n(T);
+    char* b = static_cast<char*>(scratch);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        char* r = b + o;
+        o += align_up(bytes);
+        return r;
+    };
+    m.xq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 128) * m.N * 128));
+    m.xsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 128) * 512));
+    m.up = reinterpret_cast<float*>(take(4ull * m.umax * T * f * 4));
+    m.hq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 128) * m.N * 128));
+    m.hsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 128) * 512));
+    m.y = reinterpret_cast<float*>(take(2ull * m.umax * T * d * 4));
+    return m;
+}
+
+cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p, int grid, cudaStream_t s,
+                          const char* name) {
+    p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 1024), 1024));
+    p.RS = std::min(kMaxStages, static_cast<int>((226 * 1024) / p.stage_bytes));
+    if (p.RS <= kSfStages) return cudaErrorNotSupported;  // the scale-slot ring trails the stage ring
+    const size_t smem = 1024 + static_cast<size_t>(p.RS) * p.stage_bytes;
+    // the attribute is per device: raise it once per device to the largest
+    // ring any call asks for (not inside graph captures in practice: the
+    // first forward runs uncaptured)
+    static std::atomic<int> set_bytes[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::atomic<int>& cur = set_bytes[dev & 63];
+    if (cur.load() < static_cast<int>(smem)) {
+        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        cur.store(static_cast<int>(smem));
+    }
+    const cudaError_t e = launch_pdl(mx_stream_kernel, dim3(grid), dim3(kMxThreads), smem, s, a, a3, p);
+    trace_mark(name, s);
+    return e;
+}
+
+}  // namespace
+
+size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f) {
+    const size_t umax = std::min(E, T * k);
+    const size_t N = mx_n(T);
+    return align_up(static_cast<size_t>(d / 128) * N * 128) + align_up(static_cast<size_t>(d / 128) * 512) +
+           align_up(4 * umax * T * f * 4) + align_up(umax * (f / 128) * N * 128) +
+           align_up(umax * (f / 128) * 512) + align_up(2 * umax * T * d * 4);
+}
+
+void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_t** xq, uint8_t** xsf,
+                        int* N) {
+    const MxScratch m = mx_carve(scratch, T, E, k, d, f);
+    *xq = m.xq;
+    *xsf = m.xsf;
+    *N = m.N;
+}
+
+cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
+    const MxScratch m = mx_carve(a.scratch, a.T, a.E, a.k, a.d, a.f);
+    cudaError_t e;
+    if (!a.xq_ready) {
+        const int warps = a.T * (a.d / 32);
+        e = launch_pdl(mx_quantize_rows_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, a.x, a.T, a.d, m.N,
+                       m.xq, m.xsf);
+        trace_mark("quantize_x", s);
+        if (e != cudaSuccess) return e;
+    }
+    // A operands: E2M1 codes as [E * rows, K] nibbles, boxes of 128 inputs x 128 rows
+    CUtensorMap t1, t3, t2;
+    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.d / 2, a.d,
+                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.d / 2, a.d,
+                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.f / 2, a.f,
+                        static_cast<uint64_t>(a.E) * a.d, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorNotSupported;
+
+    MxArgs up{};
+    up.sf[0] = a.w1_sf;
+    up.sf[1] = a.w3_sf;
+    up.nmat = 2;
+    up.bq = m.xq;
+    up.bsf = m.xsf;
+    up.bq_ustride = 0;
+    up.bsf_ustride = 0;
+    up.active = a.active;
+    up.E = a.E;
+    up.rows = a.f;
+    up.tiles = a.f / 128;
+    up.KC = a.d / 128;
+    up.KS = (up.KC + kChunks - 1) / kChunks;
+    up.N = m.N;
+    up.T = a.T;
+    up.part = m.up;
+    up.umax = m.umax;
+    up.rows_out = a.f;
+    up.hdr = a.hdr;
+    // every CTA's range must be at least one tile long: at least k experts are active
+    const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
+    if ((e = launch_stream(t1, t3, up, grid_up, s, "decode_up"))) return e;
+
+    const int warps = m.umax * a.T * (a.f / 32);
+    e = launch_pdl(mx_finish_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, static_cast<const float*>(m.up),
+                   m.umax, a.T, a.f, m.N, a.active, a.E, m.hq, m.hsf);
+    trace_mark("decode_finish_up", s);
+    if (e != cudaSuccess) return e;
+
+    MxArgs dn = up;
+    dn.sf[0] = a.w2_sf;
+    dn.sf[1] = a.w2_sf;
+    dn.nmat = 1;
+    dn.bq = m.hq;
+    dn.bsf = m.hsf;
+    dn.bq_ustride = static_cast<size_t>(a.f / 128) * m.N * 128;
+    dn.bsf_ustride = static_cast<size_t>(a.f / 128) * 512;
+    dn.rows = a.d;
+    dn.tiles = a.d / 128;
+    dn.KC = a.f / 128;
+    dn.KS = (dn.KC + kChunks - 1) / kChunks;
+    dn.part = m.y;
+    dn.rows_out = a.d;
+    const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
+    if ((e = launch_stream(t2, t2, dn, grid_dn, s, "decode_down"))) return e;
+
+    dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
+    e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
+                   m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, a.out);
+    trace_mark("combine", s);
+    return e;
+}
+
+}  // namespace k3

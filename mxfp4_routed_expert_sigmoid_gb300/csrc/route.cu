@@ -233,9 +233,8 @@ __device__ void permute_small(const int32_t* sel, int T, int k, int E, int32_t* 
 // Logits by GEMV (one warp per expert, all T tokens), then the last CTA to
 // finish runs top-k for every token and, if requested, the permutation.
 // Each warp issues all loads of its weight row before it needs them; the T
-// token rows are staged once per CTA in shared memory.  With x16 requested,
-// CTA b also writes token rows b, b + gridDim.x, ... as f16 with their
-// exponents, which the decode kernels read.
+// token rows are staged once per CTA in shared memory.  With xq requested,
+// the CTAs also write the rows as E4M3 terms for the expert kernels.
 constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
 
 __global__ void __launch_bounds__(256)
@@ -243,7 +242,6 @@ route_small_kernel(RouteArgs a) {
     extern __shared__ __align__(16) uint4 xs[];  // [T * d_r / 8]
     __shared__ int32_t sel[256];
     __shared__ uint32_t ticket_s;
-    __shared__ float red[8];
     // the next kernel of the forward may start launching now: it waits for
     // this grid's completion (griddepcontrol.wait) before reading its outputs
     pdl_trigger();
@@ -261,38 +259,19 @@ route_small_kernel(RouteArgs a) {
         xs[v] = reinterpret_cast<const uint4*>(a.x)[v];
     __syncthreads();
 
-    // token rows blockIdx.x, blockIdx.x + gridDim.x, ... -> f16 * 2^-e with
-    // e = floor(log2(max |x|)) (CTA-uniform loop; every CTA has the rows staged)
-    for (int t = blockIdx.x; a.x16 && t < a.T; t += gridDim.x) {
-        const uint4* row = xs + t * (a.d_r / 8);
-        float amax = 0.0f;
-        for (int v = threadIdx.x; v < a.d_r / 8; v += blockDim.x) {
-            const uint4 q = row[v];
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j2 = 0; j2 < 4; ++j2)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j2] << 16)),
-                                         fabsf(__uint_as_float(w[j2] & 0xFFFF0000u))));
+    // router input -> E4M3 terms for the block-scaled expert kernels: one warp
+    // per 32-element block, blocks spread over all warps of the grid (the
+    // rows are staged in every CTA)
+    if (a.xq) {
+        const int nb = a.d_r / 32;
+        for (int i = blockIdx.x * 8 + wid; i < a.T * nb; i += gridDim.x * 8) {
+            const int t = i / nb, b = i - t * nb;
+            const uint16_t* row = reinterpret_cast<const uint16_t*>(xs) + static_cast<size_t>(t) * a.d_r;
+            uint32_t q[kTerms], sb[kTerms];
+            quantize_terms(bf16_to_f32(row[32 * b + lane]), q, sb);
+            store_terms(q, sb, t, b & 3, a.xq + static_cast<size_t>(b >> 2) * a.xq_n * 128,
+                        a.xsf + static_cast<size_t>(b >> 2) * 512);
         }
-        amax = warp_max(amax);
-        if (lane == 0) red[wid] = amax;
-        __syncthreads();
-        float m = 0.0f;
-        for (int w2 = 0; w2 < 8; ++w2) m = fmaxf(m, red[w2]);
-        const int ex = ilog2f(m);
-        const float sc = exp2i(-ex);
-        uint4* dst = reinterpret_cast<uint4*>(a.x16 + static_cast<size_t>(t) * a.d_r);
-        for (int v = threadIdx.x; v < a.d_r / 8; v += blockDim.x) {
-            const uint4 q = row[v];
-            uint4 o;
-            o.x = f32x2_to_f16x2(__uint_as_float(q.x << 16) * sc, __uint_as_float(q.x & 0xFFFF0000u) * sc);
-            o.y = f32x2_to_f16x2(__uint_as_float(q.y << 16) * sc, __uint_as_float(q.y & 0xFFFF0000u) * sc);
-            o.z = f32x2_to_f16x2(__uint_as_float(q.z << 16) * sc, __uint_as_float(q.z & 0xFFFF0000u) * sc);
-            o.w = f32x2_to_f16x2(__uint_as_float(q.w << 16) * sc, __uint_as_float(q.w & 0xFFFF0000u) * sc);
-            dst[v] = o;
-        }
-        if (threadIdx.x == 0) a.xexp[t] = ex;
-        __syncthreads();  // red[] is reused by the next row
     }
 
     if (e < a.E) {

@@ -35,7 +35,7 @@ def test_exports_match_header(k3):
     L = k3.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert k3.k3moe_abi_version() == 1
+    assert k3.k3moe_abi_version() == 2
 
 
 def test_status_strings(k3):
@@ -72,7 +72,7 @@ def desc(k3, **over):
     d = k3.LayerDesc()
     d.E, d.k, d.d, d.f, d.d_router = 896, 16, 3584, 3072, 3584
     d.act, d.path, d.D, d.eps, d.reserved = 0, 0, 0, 0.0, 0
-    for name in ("w1_q", "w1_s", "w3_q", "w3_s", "w2_q", "w2_s", "router_w", "router_b"):
+    for name in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf", "router_w", "router_b"):
         setattr(d, name, A16)
     for k_, v in over.items():
         setattr(d, k_, v)
@@ -87,6 +87,17 @@ def test_repack_validation(k3):
     assert L.k3moe_repack_mxfp4(A1, A16, 4, 64, A16, None) == 3
     assert L.k3moe_unpack_mxfp4(A16, 4, 40, A16, A16, None) == 2
     assert L.k3moe_unpack_mxfp4(A16, 4, 64, A1, A16, None) == 3
+
+
+def test_prepare_scales_validation(k3):
+    L = k3.lib()
+    assert L.k3moe_prepare_scales(None, 128, 256, A16, None) == 1
+    assert L.k3moe_prepare_scales(A16, 0, 256, A16, None) == 1
+    assert L.k3moe_prepare_scales(A16, 192, 256, A16, None) == 2
+    assert L.k3moe_prepare_scales(A16, 128, 320, A16, None) == 2
+    assert L.k3moe_prepare_scales(A1, 128, 256, A16, None) == 3
+    assert L.k3moe_unprepare_scales(A16, 128, 64, A16, None) == 2
+    assert L.k3moe_unprepare_scales(A16, 128, 256, None, None) == 1
 
 
 def test_route_validation(k3):
@@ -118,8 +129,11 @@ def test_forward_validation(k3):
     assert fwd(desc(k3, act=1)) == 8
     assert fwd(desc(k3, reserved=1)) == 1
     assert fwd(desc(k3, path=7)) == 1
-    assert fwd(desc(k3, w2_s=None)) == 1
+    assert fwd(desc(k3, w2_sf=None)) == 1
+    assert fwd(desc(k3, d=192, d_router=192)) == 2  # the tensor-core stages are 128 wide
+    assert fwd(desc(k3, f=3072 + 64)) == 2
     assert fwd(desc(k3, w3_q=A1)) == 3
+    assert fwd(desc(k3, w2_q=A16 + 16)) == 3  # E2M1 codes: 32-byte aligned for TMA
     assert fwd(desc(k3, d_router=7168)) == 2
     assert fwd(desc(k3, D=7168, d_router=7168)) == 1  # block mode without its tensors
     assert fwd(desc(k3), h=A1) == 3

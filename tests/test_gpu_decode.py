@@ -17,6 +17,8 @@ from gpu_util import bf16_tensor_to_np, make_layer, oracle_forward, rel_err_rows
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
+# the tiny workload at the smallest width the tensor-core stages take (128)
+TINY = dict(d=128, f=128)
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +60,7 @@ def run_and_compare(k3, cfg, path, tokens=None, tol=TOL, layer_bundle=None):
 
 @pytest.mark.parametrize("T", [1, 3, 4, 8])
 def test_tiny_decode(k3, T):
-    cfg = synth.custom("tiny", T=T)
+    cfg = synth.custom("tiny", T=T, **TINY)
     run_and_compare(k3, cfg, 1)
 
 
@@ -102,7 +104,7 @@ def test_power_of_two_invariant_decode(k3):
 def test_forward_host_buffers(k3):
     import torch
 
-    cfg = synth.custom("tiny", T=2)
+    cfg = synth.custom("tiny", T=2, **TINY)
     layer, dense, expert, _ = make_layer(cfg, path=1)
     x_host = torch.from_numpy(dense["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     out_host = k3.k3moe_forward_host(layer, x_host)

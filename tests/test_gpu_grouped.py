@@ -17,6 +17,7 @@ from gpu_util import bf16_tensor_to_np, make_layer, oracle_forward, rel_err_rows
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
+TINY = dict(d=128, f=128)
 
 
 @pytest.fixture(scope="module")
@@ -75,7 +76,7 @@ def compare_forward(k3, cfg, path, tokens=None, bundle=None, tol=TOL):
 
 @pytest.mark.parametrize("T", [4, 9, 33])
 def test_tiny_grouped(k3, T):
-    compare_forward(k3, synth.custom("tiny", T=T), 2)
+    compare_forward(k3, synth.custom("tiny", T=T, **TINY), 2)
 
 
 @pytest.mark.parametrize("T", [8, 40, 300])

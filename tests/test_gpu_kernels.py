@@ -56,6 +56,24 @@ def test_repack_unpack_bit_exact(k3, rows, cols):
     _repack_case(k3, packed, scale, misalign_out=True)
 
 
+def prepared_atoms_np(s):
+    """The prepared scale layout written out with numpy: per tile of 128 rows
+    and 128-wide input chunk, a 512-byte atom with row m = 32 q + r, block b at
+    byte 16 r + 4 q + b."""
+    R, nb = s.shape
+    KC = nb // 4
+    return s.reshape(R // 128, 4, 32, KC, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 256), (5 * 1152, 768)])
+def test_prepare_scales_bit_exact(k3, rows, cols):
+    s = synth.random_bytes(rows * 3 + cols, rows * cols // 32).reshape(rows, cols // 32)
+    sf = k3.k3moe_prepare_scales(to_dev(s, "cuda"))
+    assert np.array_equal(sf.cpu().numpy(), prepared_atoms_np(s))
+    back = k3.k3moe_unprepare_scales(sf, s.shape)
+    assert np.array_equal(back.cpu().numpy(), s)
+
+
 def test_repack_worked_check_shape(k3):
     """The pages' [3072, 3584] check: GPU blocks decode to the same values."""
     rows, cols = 3072, 3584
