@@ -68,9 +68,9 @@ typedef enum k3moe_act {
 } k3moe_act;
 
 /* Expert-path selector.  AUTO picks DECODE for T <= 8 and GROUPED otherwise.
- *   DECODE : block-scaled tcgen05 MMAs (kind::mxf8f6f4) streaming the
- *            selected experts' E2M1 codes by TMA, E8M0 scales applied by the
- *            tensor cores, activations as E4M3 terms; split over the SMs.
+ *   DECODE : block-scaled tcgen05 MMAs (kind::mxf4) streaming the selected
+ *            experts' E2M1 codes by TMA, E8M0 scales applied by the tensor
+ *            cores, activations as E2M1 terms; split over the SMs.
  *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
  *            dequantisation, TMA-fed, TMEM accumulators. */
 typedef enum k3moe_path {
@@ -105,8 +105,8 @@ typedef enum k3moe_path {
 typedef struct k3moe_layer_desc {
     int32_t E;          /* routed experts (896) */
     int32_t k;          /* experts per token (16), 1 <= k <= min(E, 32) */
-    int32_t d;          /* latent width (3584), multiple of 128 */
-    int32_t f;          /* expert hidden width (3072), multiple of 128 */
+    int32_t d;          /* latent width (3584), multiple of 256 */
+    int32_t f;          /* expert hidden width (3072), multiple of 256 */
     int32_t d_router;   /* router input width: d (latent mode) or D (block mode) */
     int32_t act;        /* k3moe_act */
     int32_t path;       /* k3moe_path */

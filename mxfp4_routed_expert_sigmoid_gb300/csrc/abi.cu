@@ -129,7 +129,7 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
     if (d->E < 1 || d->k < 1 || d->d < 1 || d->f < 1 || d->d_router < 1) return K3MOE_ERR_INVALID_ARG;
     if (d->reserved != 0) return K3MOE_ERR_INVALID_ARG;
     if (d->k > d->E || d->k > 32 || d->E > 1024) return K3MOE_ERR_SHAPE;
-    if (d->d % 128 || d->f % 128) return K3MOE_ERR_SHAPE;
+    if (d->d % 256 || d->f % 256) return K3MOE_ERR_SHAPE;  // 256-wide K chunks of the MMAs
     if (d->D < 0) return K3MOE_ERR_SHAPE;
     if (d->D > 0) {
         if (d->D % 128 || d->d % 128 || d->d_router != d->D) return K3MOE_ERR_SHAPE;

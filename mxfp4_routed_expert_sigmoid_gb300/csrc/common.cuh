@@ -154,35 +154,37 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 
 // ---------------------------------------------------------------------------
 // Activations for the block-scaled tensor-core path: every 32-element block
-// of a row is written as kTerms E4M3 codes per element, each term with its
-// own E8M0 block scale, so that v ~= sum_j e4m3(q_j) * 2^(s_j - 127).  Term
+// of a row is written as kTerms E2M1 codes per element, each term with its
+// own E8M0 block scale, so that v ~= sum_j e2m1(q_j) * 2^(s_j - 127).  Term
 // j + 1 encodes what term j left over (exactly: the remainder of a
-// round-to-nearest is representable), so each term adds about four bits.
+// round-to-nearest is representable), so each term adds about 3.3 bits; five
+// terms put the layer output within about 1e-4 of its RMS.
 // ---------------------------------------------------------------------------
-constexpr int kTerms = 3;
+constexpr int kTerms = 5;
 
-// Smallest e with amax * 2^-e <= 448 (the largest finite E4M3), from the
-// exponent and mantissa fields: amax = (1 + m) 2^E fits at e = E - 8 iff
-// 1 + m <= 1.75.  Zero and subnormal amax give -127 (the smallest scale).
-__device__ __forceinline__ int e4m3_scale_exp(float amax) {
+// Smallest e with amax * 2^-e <= 6 (the largest E2M1 magnitude), from the
+// exponent and mantissa fields: amax = (1 + m) 2^E fits at e = E - 2 iff
+// 1 + m <= 1.5.  Zero and subnormal amax give -127 (the smallest scale).
+__device__ __forceinline__ int e2m1_scale_exp(float amax) {
     const uint32_t u = __float_as_uint(amax);
     const int ef = static_cast<int>((u >> 23) & 0xFFu);
     if (ef == 0) return -127;
-    return ef - 127 - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return ef - 127 - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
 }
 
-// fp32 -> E4M3 code (round to nearest even, saturating to +-448)
-__device__ __forceinline__ uint32_t e4m3_code(float v) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
-    return r & 0xFFu;
+// fp32 -> E2M1 code (round to nearest even, saturating to +-6), low 4 bits
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    uint32_t r;
+    asm("{ .reg .b8 c; cvt.rn.satfinite.e2m1x2.f32 c, %1, %1; mov.b32 %0, {c, c, c, c}; }" : "=r"(r) : "f"(v));
+    return r & 0xFu;
 }
 
-// E4M3 code -> fp32 (exact)
-__device__ __forceinline__ float e4m3_float(uint32_t code) {
+// E2M1 code -> fp32 (exact)
+__device__ __forceinline__ float e2m1_float(uint32_t code) {
     uint32_t h;
-    const uint16_t in = static_cast<uint16_t>(code | (code << 8));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+    asm("{ .reg .b8 c0, c1, c2, c3; mov.b32 {c0, c1, c2, c3}, %1; cvt.rn.f16x2.e2m1x2 %0, c0; }"
+        : "=r"(h)
+        : "r"(code));
     return f16x2_to_f32x2(h).x;
 }
 
@@ -193,45 +195,45 @@ __device__ __forceinline__ void quantize_terms(float v, uint32_t (&q)[kTerms], u
 #pragma unroll
     for (int j = 0; j < kTerms; ++j) {
         const float amax = warp_max(fabsf(res));
-        const int e = e4m3_scale_exp(amax);
-        q[j] = e4m3_code(res * exp2i(-e));
+        const int e = e2m1_scale_exp(amax);
+        q[j] = e2m1_code(res * exp2i(-e));
         sb[j] = static_cast<uint32_t>(e + 127);
-        res = res - e4m3_float(q[j]) * exp2i(e);
+        res = res - e2m1_float(q[j]) * exp2i(e);
     }
 }
 
-// B operand layout of the block-scaled MMA, per 128-wide K stage:
+// B operand layout of the block-scaled MMA (kind::mxf4: packed E2M1, two
+// codes per byte, element 2i in the low nibble), per 256-wide K chunk:
 //   codes : N rows x 128 bytes, row n = kTerms * token + term, stored with the
 //           128-byte swizzle of the tensor-core K-major layout (16-byte chunk
-//           c of row n at chunk c ^ (n % 8)), so one bulk copy lands it in
-//           shared memory ready for the MMA;
-//   scales: a 512-byte atom, byte 16 (n % 32) + 4 (n / 32) + kb for row n and
-//           32-block kb of the stage (the layout tcgen05.cp 32x128b.warpx4
-//           spreads over the TMEM lanes that the MMA reads).
-__device__ __forceinline__ uint32_t b_code_offset(int n, int k) {
-    return static_cast<uint32_t>(n * 128 + ((((k >> 4) ^ (n & 7)) & 7) << 4) + (k & 15));
-}
+//           c of row n at chunk c ^ (n % 8); a 32-element block is exactly one
+//           16-byte chunk), so one bulk copy lands it ready for the MMA;
+//   scales: per 128-wide K group a 512-byte atom, byte 16 (n % 32) + 4 (n / 32)
+//           + kb for row n and 32-block kb of the group (the layout tcgen05.cp
+//           32x128b.warpx4 spreads over the TMEM lanes the MMA reads).
 __device__ __forceinline__ uint32_t sf_atom_offset(int n, int kb) {
     return static_cast<uint32_t>(16 * (n & 31) + 4 * (n >> 5) + kb);
 }
 
-// Writes the quantised block (warp, lane = element) of row t into the B
-// layout: block kb (0..3) of the stage whose codes start at `codes` and whose
-// scale atom starts at `scales`.  Lanes 4i..4i+3 combine their bytes into one
-// 32-bit store.
+// Writes the quantised block (warp, lane = element) of token t into the B
+// layout: 32-block kb (0..7) of the 256-wide chunk whose codes start at
+// `codes`; `scales` is the atom of the chunk's first 128-wide group (the
+// second follows 512 bytes later).  Lane pairs share a byte, lanes 8i..8i+7
+// one 32-bit store.
 __device__ __forceinline__ void store_terms(const uint32_t (&q)[kTerms], const uint32_t (&sb)[kTerms],
                                             int t, int kb, uint8_t* codes, uint8_t* scales) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int j = 0; j < kTerms; ++j) {
-        uint32_t w = q[j];
-        w |= __shfl_down_sync(0xffffffffu, q[j], 1) << 8;
-        w |= __shfl_down_sync(0xffffffffu, q[j], 2) << 16;
-        w |= __shfl_down_sync(0xffffffffu, q[j], 3) << 24;
+        const uint32_t b = q[j] | (__shfl_down_sync(0xffffffffu, q[j], 1) << 4);   // even lanes
+        uint32_t w = b;
+        w |= __shfl_down_sync(0xffffffffu, b, 2) << 8;
+        w |= __shfl_down_sync(0xffffffffu, b, 4) << 16;
+        w |= __shfl_down_sync(0xffffffffu, b, 6) << 24;
         const int n = kTerms * t + j;
-        if ((lane & 3) == 0)
-            *reinterpret_cast<uint32_t*>(codes + b_code_offset(n, 32 * kb + lane)) = w;
-        if (lane == 0) scales[sf_atom_offset(n, kb)] = static_cast<uint8_t>(sb[j]);
+        if ((lane & 7) == 0)
+            *reinterpret_cast<uint32_t*>(codes + n * 128 + (((kb ^ (n & 7)) & 7) << 4) + (lane >> 1)) = w;
+        if (lane == 0) scales[(kb >> 2) * 512 + sf_atom_offset(n, kb & 3)] = static_cast<uint8_t>(sb[j]);
     }
 }
 
@@ -280,7 +282,7 @@ struct RouteArgs {
     int32_t* inv;      // [T*k]
     int32_t* active;   // [E] ascending experts with count > 0; active[E] = n_active (at index E)
     // optional (decode, latent mode): the router input quantised for the
-    // block-scaled expert kernels (codes [d_r / 128][xq_n][128], scale atoms
+    // block-scaled expert kernels (codes [d_r / 256][xq_n][128], scale atoms
     // [d_r / 128][512]); the CTAs share the work
     uint8_t* xq;
     uint8_t* xsf;
@@ -321,7 +323,7 @@ struct MxDecodeArgs {
     const uint8_t *w1_q, *w3_q, *w2_q;  // E2M1 codes
     const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
     const uint16_t* x;        // [T, d] bf16 expert input (read when !xq_ready)
-    int xq_ready;             // 1: the router already wrote the E4M3 terms
+    int xq_ready;             // 1: the router already wrote the E2M1 terms
     int T, E, k, d, f;
     const int32_t* active;    // [E + 1] active experts ascending, count at [E]
     const int32_t* idx;       // [T, k]

@@ -2,42 +2,44 @@
 // the scale-factor layout it reads.
 //
 // The experts' MXFP4 weights reach the tensor cores as they are stored:
-// tcgen05.mma kind::mxf8f6f4 multiplies E2M1 weight codes by E4M3 activation
-// codes and applies both operands' E8M0 block scales (one per 32 inputs) in
-// hardware, accumulating in fp32 in TMEM; nothing is dequantised in software
-// (llama.cpp PR #26185 "model: add Kimi-K3 text model", review by GrEarl,
-// section "repack_mxfp4_blocks is bit-exact": the MXFP4 format; section "Dry
-// run": 896 experts, 16 used, latent width 3584, expert width 3072).
+// tcgen05.mma kind::mxf4 multiplies packed E2M1 weight codes by packed E2M1
+// activation codes and applies both operands' E8M0 block scales (one per 32
+// inputs) in hardware, accumulating in fp32 in TMEM; nothing is dequantised
+// in software (llama.cpp PR #26185 "model: add Kimi-K3 text model", review by
+// GrEarl, section "repack_mxfp4_blocks is bit-exact": the MXFP4 format;
+// section "Dry run": 896 experts, 16 used, latent width 3584, expert width
+// 3072).
 //
-// Operands of one MMA (M = 128 weight rows, N = 16 or 32 token-term rows,
-// K = 32), staged per 128-wide K chunk, four chunks to a pipeline stage (the
-// TMA engines reach the copy bandwidth of HBM only with that many bytes per
-// stage: about 3.4 TB/s with one chunk, 6 TB/s with four, measured on GB300):
-//   A  E2M1 codes by TMA (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B: each 8 bytes
-//      of packed codes land in a 16-byte shared-memory slot, the container
-//      layout of 4-bit operands in kind::f8f6f4), 128-byte swizzle;
-//   SFA the 512-byte scale atom of the 128 rows x 4 blocks (prepared layout,
-//      below), copied to TMEM by tcgen05.cp 32x128b.warpx4: row m is read
-//      from lane m, column m / 32, byte = the K block (scale id in idesc);
-//   B  activations as kTerms E4M3 terms per token (rows 3t, 3t+1, 3t+2;
-//      see quantize_terms), pre-swizzled in global memory, one bulk copy;
-//   SFB their 512-byte scale atom (column n from lane n % 32, column n / 32).
+// Operands of one MMA (M = 128 weight rows, N = 16..64 token-term rows,
+// K = 64), staged per 256-wide K chunk (128 bytes of codes per row, the
+// 128-byte swizzled K-major layout), two chunks to a pipeline stage:
+//   A  weight codes by TMA, 16 KB per chunk, as stored in global memory;
+//   SFA two 512-byte scale atoms per chunk (prepared layout, below), copied
+//      to TMEM by tcgen05.cp 32x128b.warpx4: row m is read from lane m,
+//      column m / 32; an MMA reads two bytes of a column (scale id 0 for the
+//      first 64 inputs of an atom, 2 for the second);
+//   B  activations as kTerms E2M1 terms per token (rows kTerms t + j; see
+//      quantize_terms), pre-swizzled in global memory, one bulk copy;
+//   SFB their scale atoms (column n from lane n % 32, column n / 32).
 // The kTerms partial products of a token are summed in fp32 by the epilogue.
+// Why kind::mxf4: one tcgen05.mma with M = 128 takes about 58 ns on GB300
+// whatever N up to 128 (measured), so the weight bytes an instruction covers
+// set the speed limit: 4 KB with K = 64 here, twice kind::mxf8f6f4's K = 32.
 //
-// Up projection: W1 and W3 are separate units (128-row tiles of one matrix),
-// so every TMA box is 128 rows tall; the finish kernel pairs g = W1 x with
-// u = W3 x.  Down projection: 128-row tiles of W2.
+// Up projection: W1 and W3 are separate units (128-row tiles of one matrix);
+// the finish kernel pairs g = W1 x with u = W3 x.  Down projection: 128-row
+// tiles of W2.
 //
-// Work split (stream-K): the units (active expert, row tile, K stage) are cut
-// into one contiguous range per CTA, every range at least one tile long, so a
-// tile is shared by at most two CTAs.  The CTA that starts a tile writes its
-// partial sums to slot 0 and the other to slot 1 (a CTA that owns the whole
-// tile writes zeros to slot 1); consumers add slot 0 and slot 1 in that order,
-// so results do not depend on timing.
+// Work split (stream-K): the units (active expert, matrix, row tile, stage)
+// are cut into one contiguous range per CTA, every range at least one tile
+// long, so a tile is shared by at most two CTAs.  The CTA that starts a tile
+// writes its partial sums to slot 0 and the other to slot 1 (a CTA that owns
+// the whole tile writes zeros to slot 1); consumers add slot 0 and slot 1 in
+// that order, so results do not depend on timing.
 //
 // Kernels of one decode forward (after the router, which also writes the
-// token rows as E4M3 terms): up -> finish (h = silu(g) * u from both slots,
-// quantised to E4M3 terms) -> down -> combine (weights in slot order).
+// token rows as E2M1 terms): up -> finish (h = silu(g) * u from both slots,
+// quantised to E2M1 terms) -> down -> combine (weights in slot order).
 //
 // Roles of the streaming kernel (192 threads, one CTA per SM):
 //   warp 0     producer: TMA / bulk copies into a ring of stages;
@@ -58,32 +60,49 @@ using namespace tc;
 
 constexpr int kMxThreads = 192;
 constexpr int kMaxStages = 8;
-constexpr int kChunks = 4;             // 128-wide K chunks per stage (a stage covers K = 512)
-constexpr int kSfStages = 1;           // stages whose scale slots live in TMEM at once
-constexpr int kChunkA = 16384;         // 128 rows x 128 bytes (E2M1 in 8-bit slots)
-constexpr uint32_t kTxChunkA = 8192;   // packed bytes the TMA moves per A chunk
+constexpr int kChunks = 2;             // 256-wide K chunks per stage (a stage covers K = 512)
+constexpr int kChunkA = 16384;         // 128 rows x 128 bytes of packed E2M1
 constexpr int kStageA = kChunks * kChunkA;
-constexpr int kSfBase = 64;            // TMEM: accumulators in columns 0..63, scale slots above
-// every scale slot starts on a 32-column boundary (A at +0, B at +32)
-static_assert(kSfBase + kSfStages * kChunks * 64 <= 512, "scale slots fit in TMEM");
+constexpr int kMaxN = 64;              // MMA N: kTerms * T rounded up to 16
+constexpr int kSfBase = 2 * kMaxN;     // TMEM: two accumulators, then the scale slots
+// every scale slot starts on a 32-column boundary: per chunk two atoms of A
+// (+0, +64) and two of B (+32, +96)
+static_assert(kSfBase + kChunks * 128 <= 512, "scale slots fit in TMEM");
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+// Instruction descriptor, kind::mxf4: A = B = E2M1 (format 1), E8M0 scales,
+// K-major, M x N; sa / sb = scale id (0: blocks 0, 1 of the atom column; 2:
+// blocks 2, 3).
+__device__ __forceinline__ uint32_t idesc_f4(int M, int N, int sa, int sb) {
+    return (static_cast<uint32_t>(sb) << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sa) << 29);
+}
+
+__device__ __forceinline__ void mma_f4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5],"
+        " p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
 struct MxArgs {
     const uint8_t* sf[2];   // prepared scale atoms of the matrices (W1, W3 or W2)
     int nmat;               // matrices per expert in this pass (2 up, 1 down)
-    const uint8_t* bq;      // B codes [unit][KS][N][128] (up: one shared unit)
-    const uint8_t* bsf;     // B scale atoms [unit][KS][512]
+    const uint8_t* bq;      // B codes [unit][K / 256][N][128] (up: one shared unit)
+    const uint8_t* bsf;     // B scale atoms [unit][K / 128][512]
     size_t bq_ustride;      // bytes per unit (0 when all units share B)
     size_t bsf_ustride;
     const int32_t* active;  // [E + 1]: active experts ascending, count at [E]
     int E;
     int rows;               // weight rows per expert (f up, d down)
     int tiles;              // 128-row tiles per expert
-    int KC;                 // 128-wide K chunks (K / 128)
+    int KC;                 // 256-wide K chunks (K / 256)
     int KS;                 // stages of kChunks chunks (the last one may be shorter)
-    int N;                  // MMA N (16 or 32)
+    int N;                  // MMA N
     int T;                  // tokens
     int RS;                 // stages in the ring
     uint32_t stage_bytes;
@@ -130,7 +149,9 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __shared__ int abort_s;
     volatile int* abort_flag = &abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t NB = static_cast<uint32_t>(p.N) * 128;
+    const uint32_t NB = static_cast<uint32_t>(p.N) * 128;  // B bytes per chunk
+    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms
+    const uint32_t offB = kStageA, offSA = kStageA + kChunks * NB, offSB = offSA + kChunks * 1024;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.RS; ++s) {
@@ -176,17 +197,16 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
                 const int c0 = c.ks * kChunks;
                 const int nch = min(kChunks, p.KC - c0);
-                mbar_expect_tx(&full[s], static_cast<uint32_t>(nch) * (kTxChunkA + NB + 1024));
+                mbar_expect_tx(&full[s], static_cast<uint32_t>(nch) * (kChunkA + NB + 2048));
                 const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
                 const int y = e * p.rows + c.tile * 128;
                 for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, &full[s], (c0 + cc) * 128, y);
-                uint8_t* sb = st + kStageA;
-                bulk_load(sb, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, &full[s]);
-                bulk_load(sb + kChunks * NB,
-                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.KC + c0) * 512, nch * 512,
+                bulk_load(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, &full[s]);
+                bulk_load(st + offSA,
+                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
+                          nch * 1024, &full[s]);
+                bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024,
                           &full[s]);
-                bulk_load(sb + kChunks * NB + kChunks * 512,
-                          p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(c0) * 512, nch * 512, &full[s]);
                 ++issued;
                 if (++s == p.RS) {
                     s = 0;
@@ -210,7 +230,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int ks = Cursor(w0, p.nmat, p.tiles, p.KS).ks;
             int s = 0, seg = 0, ps = 0;
             uint32_t ph = 0, pph = 0;
-            const uint32_t id0 = idesc_mx(128, p.N, 0, 0);
+            const uint32_t id0 = idesc_f4(128, p.N, 0, 0);
             for (int i = 0, w = w0; w < w1; ++i, ++w) {
                 const bool seg_start = (w == w0) || ks == 0;
                 const bool seg_end = (w + 1 == w1) || ks == p.KS - 1;
@@ -218,9 +238,9 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (seg_start && !mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71))
                     break;
                 if (!mbar_wait(&full[s], ph, abort_flag, p.hdr, 72)) break;
-                // scale slots of stage i are reused from stage i - kSfStages: its MMAs
-                // have finished reading them
-                if (i >= kSfStages) {
+                // one set of scale slots: the MMAs of the previous stage have
+                // finished reading it
+                if (i > 0) {
                     if (!mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73)) break;
                     if (++ps == p.RS) {
                         ps = 0;
@@ -229,22 +249,21 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 tc_fence_after();
                 const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
-                const uint32_t sb = st + kStageA;
                 const int nch = min(kChunks, p.KC - ks * kChunks);
-                const uint32_t slot0 = tmem + kSfBase + (i % kSfStages) * kChunks * 64;
-                for (int cc = 0; cc < nch; ++cc) {
-                    tmem_cp_sf(slot0 + 64 * cc, sb + kChunks * NB + 512 * cc);
-                    tmem_cp_sf(slot0 + 64 * cc + 32, sb + kChunks * NB + kChunks * 512 + 512 * cc);
+                for (int g = 0; g < 2 * nch; ++g) {  // atoms: 2 per chunk
+                    tmem_cp_sf(tmem + kSfBase + 64 * g, st + offSA + 512 * g);
+                    tmem_cp_sf(tmem + kSfBase + 64 * g + 32, st + offSB + 512 * g);
                 }
-                const uint32_t d_t = tmem + a * 32;
+                const uint32_t d_t = tmem + a * kMaxN;
                 for (int cc = 0; cc < nch; ++cc) {
-                    const uint64_t ad = sw128_desc(st + cc * kChunkA), bd = sw128_desc(sb + cc * NB);
-                    const uint32_t sfa = slot0 + 64 * cc, sfb = sfa + 32;
+                    const uint64_t ad = sw128_desc(st + cc * kChunkA), bd = sw128_desc(st + offB + cc * NB);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_mx(d_t, ad + 2 * j, bd + 2 * j,
-                               id0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29), sfa,
-                               sfb, (seg_start && cc == 0 && j == 0) ? 0u : 1u);
+                    for (int j = 0; j < 4; ++j) {  // K = 64 each: atom 2 cc + j / 2, scale id 2 (j % 2)
+                        const uint32_t sfa = tmem + kSfBase + 64 * (2 * cc + (j >> 1));
+                        const uint32_t id = static_cast<uint32_t>(2 * (j & 1));
+                        mma_f4(d_t, ad + 2 * j, bd + 2 * j, id0 | (id << 4) | (id << 29), sfa, sfa + 32,
+                               (seg_start && cc == 0 && j == 0) ? 0u : 1u);
+                    }
                 }
                 mma_commit(&empty[s]);
                 if (seg_end) {
@@ -271,17 +290,19 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, p.hdr, 74)))
                 break;
             tc_fence_after();
-            float v[32];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * 32;
-            if (p.N == 16) {
-                float v16[16];
-                tmem_ld16(taddr, v16);
+            float v[kMaxN];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * kMaxN;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = v16[i];
+            for (int c16 = 0; c16 < kMaxN / 16; ++c16) {
+                if (c16 * 16 < p.N) {
+                    float v16[16];
+                    tmem_ld16(taddr + c16 * 16, v16);
 #pragma unroll
-                for (int i = 16; i < 32; ++i) v[i] = 0.0f;
-            } else {
-                tmem_ld32(taddr, v);
+                    for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = v16[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = 0.0f;
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -294,7 +315,9 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 if (t >= p.T) break;
-                const float sum = v[kTerms * t] + v[kTerms * t + 1] + v[kTerms * t + 2];
+                float sum = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kTerms; ++j) sum += v[kTerms * t + j];
                 dst[static_cast<size_t>(t) * p.rows_out] = sum;
                 if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
             }
@@ -319,7 +342,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-// h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E4M3 terms in
+// h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E2M1 terms in
 // the B layout of the down projection.  One warp per (unit, token, 32-block).
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
@@ -340,12 +363,12 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     const float uu = part[plane + o] + part[3 * plane + o];
     uint32_t q[kTerms], sb[kTerms];
     quantize_terms(silu_f32(g) * uu, q, sb);
-    const int KS = f / 128;
-    store_terms(q, sb, t, b & 3, hq + (static_cast<size_t>(u) * KS + (b >> 2)) * N * 128,
-                hsf + (static_cast<size_t>(u) * KS + (b >> 2)) * 512);
+    const int KC = f / 256;
+    store_terms(q, sb, t, b & 7, hq + (static_cast<size_t>(u) * KC + (b >> 3)) * N * 128,
+                hsf + (static_cast<size_t>(u) * KC + (b >> 3)) * 1024);
 }
 
-// Token rows (bf16) -> kTerms E4M3 terms in the B layout (used when the
+// Token rows (bf16) -> kTerms E2M1 terms in the B layout (used when the
 // router did not write them).  One warp per (token, 32-block).
 __global__ void __launch_bounds__(256)
 mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int T, int K, int N, uint8_t* __restrict__ xq,
@@ -359,8 +382,8 @@ mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int T, int K, int N, uin
     const int t = i / nb, b = i - t * nb;
     uint32_t q[kTerms], sb[kTerms];
     quantize_terms(bf16_to_f32(x[static_cast<size_t>(t) * K + 32 * b + lane]), q, sb);
-    store_terms(q, sb, t, b & 3, xq + static_cast<size_t>(b >> 2) * N * 128,
-                xsf + static_cast<size_t>(b >> 2) * 512);
+    store_terms(q, sb, t, b & 7, xq + static_cast<size_t>(b >> 3) * N * 128,
+                xsf + static_cast<size_t>(b >> 3) * 1024);
 }
 
 // out[t, :] = bf16(sum_j w[t, j] * (y0 + y1)[unit(idx[t, j]), t, :]), j in slot
@@ -464,7 +487,7 @@ cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t
 // ---------------------------------------------------------------------------
 namespace {
 
-int mx_n(int T) { return kTerms * T <= 16 ? 16 : 32; }
+int mx_n(int T) { return (kTerms * T + 15) / 16 * 16; }
 
 struct MxScratch {
     uint8_t *xq, *xsf, *hq, *hsf;
@@ -483,10 +506,10 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
         o += align_up(bytes);
         return r;
     };
-    m.xq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 128) * m.N * 128));
+    m.xq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 256) * m.N * 128));
     m.xsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 128) * 512));
     m.up = reinterpret_cast<float*>(take(4ull * m.umax * T * f * 4));
-    m.hq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 128) * m.N * 128));
+    m.hq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 256) * m.N * 128));
     m.hsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 128) * 512));
     m.y = reinterpret_cast<float*>(take(2ull * m.umax * T * d * 4));
     return m;
@@ -494,9 +517,9 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
 
 cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p, int grid, cudaStream_t s,
                           const char* name) {
-    p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 1024), 1024));
+    p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 2048), 1024));
     p.RS = std::min(kMaxStages, static_cast<int>((226 * 1024) / p.stage_bytes));
-    if (p.RS <= kSfStages) return cudaErrorNotSupported;  // the scale-slot ring trails the stage ring
+    if (p.RS < 2 || p.N > kMaxN) return cudaErrorNotSupported;
     const size_t smem = 1024 + static_cast<size_t>(p.RS) * p.stage_bytes;
     // the attribute is per device: raise it once per device to the largest
     // ring any call asks for (not inside graph captures in practice: the
@@ -522,8 +545,8 @@ cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p,
 size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f) {
     const size_t umax = std::min(E, T * k);
     const size_t N = mx_n(T);
-    return align_up(static_cast<size_t>(d / 128) * N * 128) + align_up(static_cast<size_t>(d / 128) * 512) +
-           align_up(4 * umax * T * f * 4) + align_up(umax * (f / 128) * N * 128) +
+    return align_up(static_cast<size_t>(d / 256) * N * 128) + align_up(static_cast<size_t>(d / 128) * 512) +
+           align_up(4 * umax * T * f * 4) + align_up(umax * (f / 256) * N * 128) +
            align_up(umax * (f / 128) * 512) + align_up(2 * umax * T * d * 4);
 }
 
@@ -545,13 +568,14 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
         trace_mark("quantize_x", s);
         if (e != cudaSuccess) return e;
     }
-    // A operands: E2M1 codes as [E * rows, K] nibbles, boxes of 128 inputs x 128 rows
+    // A operands: packed E2M1 codes as [E * rows, K / 2] bytes, boxes of 128 bytes
+    // (256 inputs) x 128 rows
     CUtensorMap t1, t3, t2;
-    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.d / 2, a.d,
+    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
                         static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.d / 2, a.d,
+        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
                         static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.f / 2, a.f,
+        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2,
                         static_cast<uint64_t>(a.E) * a.d, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
 
@@ -567,7 +591,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     up.E = a.E;
     up.rows = a.f;
     up.tiles = a.f / 128;
-    up.KC = a.d / 128;
+    up.KC = a.d / 256;
     up.KS = (up.KC + kChunks - 1) / kChunks;
     up.N = m.N;
     up.T = a.T;
@@ -591,11 +615,11 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     dn.nmat = 1;
     dn.bq = m.hq;
     dn.bsf = m.hsf;
-    dn.bq_ustride = static_cast<size_t>(a.f / 128) * m.N * 128;
+    dn.bq_ustride = static_cast<size_t>(a.f / 256) * m.N * 128;
     dn.bsf_ustride = static_cast<size_t>(a.f / 128) * 512;
     dn.rows = a.d;
     dn.tiles = a.d / 128;
-    dn.KC = a.f / 128;
+    dn.KC = a.f / 256;
     dn.KS = (dn.KC + kChunks - 1) / kChunks;
     dn.part = m.y;
     dn.rows_out = a.d;

@@ -234,7 +234,7 @@ __device__ void permute_small(const int32_t* sel, int T, int k, int E, int32_t* 
 // finish runs top-k for every token and, if requested, the permutation.
 // Each warp issues all loads of its weight row before it needs them; the T
 // token rows are staged once per CTA in shared memory.  With xq requested,
-// the CTAs also write the rows as E4M3 terms for the expert kernels.
+// the CTAs also write the rows as E2M1 terms for the expert kernels.
 constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
 
 __global__ void __launch_bounds__(256)
@@ -259,7 +259,7 @@ route_small_kernel(RouteArgs a) {
         xs[v] = reinterpret_cast<const uint4*>(a.x)[v];
     __syncthreads();
 
-    // router input -> E4M3 terms for the block-scaled expert kernels: one warp
+    // router input -> E2M1 terms for the block-scaled expert kernels: one warp
     // per 32-element block, blocks spread over all warps of the grid (the
     // rows are staged in every CTA)
     if (a.xq) {
@@ -269,8 +269,8 @@ route_small_kernel(RouteArgs a) {
             const uint16_t* row = reinterpret_cast<const uint16_t*>(xs) + static_cast<size_t>(t) * a.d_r;
             uint32_t q[kTerms], sb[kTerms];
             quantize_terms(bf16_to_f32(row[32 * b + lane]), q, sb);
-            store_terms(q, sb, t, b & 3, a.xq + static_cast<size_t>(b >> 2) * a.xq_n * 128,
-                        a.xsf + static_cast<size_t>(b >> 2) * 512);
+            store_terms(q, sb, t, b & 7, a.xq + static_cast<size_t>(b >> 3) * a.xq_n * 128,
+                        a.xsf + static_cast<size_t>(b >> 3) * 1024);
         }
     }
 

@@ -130,8 +130,9 @@ def test_forward_validation(k3):
     assert fwd(desc(k3, reserved=1)) == 1
     assert fwd(desc(k3, path=7)) == 1
     assert fwd(desc(k3, w2_sf=None)) == 1
-    assert fwd(desc(k3, d=192, d_router=192)) == 2  # the tensor-core stages are 128 wide
+    assert fwd(desc(k3, d=192, d_router=192)) == 2  # the tensor-core K chunks are 256 wide
     assert fwd(desc(k3, f=3072 + 64)) == 2
+    assert fwd(desc(k3, f=3072 + 128)) == 2
     assert fwd(desc(k3, w3_q=A1)) == 3
     assert fwd(desc(k3, w2_q=A16 + 16)) == 3  # E2M1 codes: 32-byte aligned for TMA
     assert fwd(desc(k3, d_router=7168)) == 2

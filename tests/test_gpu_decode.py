@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
 # the tiny workload at the smallest width the tensor-core stages take (128)
-TINY = dict(d=128, f=128)
+TINY = dict(d=256, f=256)
 
 
 @pytest.fixture(scope="module")
@@ -67,7 +67,7 @@ def test_tiny_decode(k3, T):
 @pytest.mark.parametrize("T", [1, 5, 8])
 def test_mid_decode(k3, T):
     # several row tiles per expert, ragged lane use (K/32 = 24 blocks), many experts
-    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1152, seed_index=11)
+    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1280, seed_index=11)
     run_and_compare(k3, cfg, 1)
 
 
@@ -89,7 +89,7 @@ def test_power_of_two_invariant_decode(k3):
     """Adding 1 to every W2 exponent doubles the output bit-exactly."""
     import torch
 
-    cfg = synth.custom("decode_t1", T=4, E=32, k=4, d=512, f=384, seed_index=12)
+    cfg = synth.custom("decode_t1", T=4, E=32, k=4, d=512, f=512, seed_index=12)
     layer, dense, expert, ex = make_layer(cfg, path=1)
     x = to_dev(dense["hidden"], "cuda")
     out1 = k3.k3moe_forward(layer, x)
@@ -116,7 +116,7 @@ def test_graph_replay_matches_forward(k3):
     """k3moe_graph_create / k3moe_graph_launch reproduce k3moe_forward bit for bit."""
     import torch
 
-    cfg = synth.custom("decode_t1", T=3, E=64, k=8, d=768, f=1152, seed_index=13)
+    cfg = synth.custom("decode_t1", T=3, E=64, k=8, d=768, f=1280, seed_index=13)
     layer, dense, expert, _ = make_layer(cfg, path=0)
     x = to_dev(dense["hidden"], "cuda")
     ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))
@@ -136,7 +136,7 @@ def test_trace_of_graph_replay(k3):
     reports a positive duration after a replay."""
     import torch
 
-    cfg = synth.custom("decode_t1", T=2, E=64, k=8, d=768, f=1152, seed_index=14)
+    cfg = synth.custom("decode_t1", T=2, E=64, k=8, d=768, f=1280, seed_index=14)
     layer, dense, expert, _ = make_layer(cfg, path=0)
     x = to_dev(dense["hidden"], "cuda")
     ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))

@@ -17,7 +17,7 @@ from gpu_util import bf16_tensor_to_np, make_layer, oracle_forward, rel_err_rows
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
-TINY = dict(d=128, f=128)
+TINY = dict(d=256, f=256)
 
 
 @pytest.fixture(scope="module")
@@ -82,7 +82,7 @@ def test_tiny_grouped(k3, T):
 @pytest.mark.parametrize("T", [8, 40, 300])
 def test_mid_grouped(k3, T):
     # several m-tiles, K stages and units; ragged expert segments
-    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1152, seed_index=21)
+    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1280, seed_index=21)
     compare_forward(k3, cfg, 2)
 
 
@@ -91,7 +91,7 @@ def test_paths_agree(k3):
     the oracle and of each other."""
     import torch
 
-    cfg = synth.custom("decode_t1", T=8, E=64, k=8, d=768, f=1152, seed_index=22)
+    cfg = synth.custom("decode_t1", T=8, E=64, k=8, d=768, f=1280, seed_index=22)
     bundle = make_layer(cfg, path=1)
     out_d, _, _ = compare_forward(k3, cfg, 1, bundle=bundle)
     layer_g = bundle[0].with_path(2)
@@ -103,7 +103,7 @@ def test_paths_agree(k3):
 def test_grouped_deterministic_and_power_of_two(k3):
     import torch
 
-    cfg = synth.custom("decode_t1", T=64, E=32, k=4, d=512, f=384, seed_index=23)
+    cfg = synth.custom("decode_t1", T=64, E=32, k=4, d=512, f=512, seed_index=23)
     layer, dense, expert, ex = make_layer(cfg, path=2)
     x = to_dev(dense["hidden"], "cuda")
     out1 = k3.k3moe_forward(layer, x)
@@ -120,7 +120,7 @@ def test_grouped_deterministic_and_power_of_two(k3):
 @pytest.mark.parametrize("T,path", [(4, 1), (4, 2), (300, 2)])
 def test_block_small(k3, T, path):
     """Full latent block (RMSNorm, projections, router at the model width)."""
-    cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=256, f=384, D=512, seed_index=24)
+    cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=256, f=512, D=512, seed_index=24)
     compare_forward(k3, cfg, path)
 
 
