@@ -448,10 +448,15 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     int32_t* active = static_cast<int32_t*>(at(p.active));
     const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_DECODE && desc->D == 0;
     if (T <= kDecodeMaxT) {
-        r.counts = counts; r.offsets = offsets; r.perm = perm; r.inv = inv; r.active = active;
+        // decode needs only the active experts (listed by the top-k kernel); the
+        // grouped path takes the full permutation
+        r.active = path == K3MOE_PATH_DECODE ? active : nullptr;
         if (fuse_prep)
             mx_decode_xq_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.xq, &r.xsf, &r.xq_n);
-        if ((e = launch_route_small(r, s))) return K3MOE_ERR_CUDA;
+        if ((e = launch_route_small(r, s))) return cuda_status(e);
+        if (path != K3MOE_PATH_DECODE &&
+            (e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s)))
+            return K3MOE_ERR_CUDA;
     } else {
         if (T >= 64 && desc->E % 128 == 0) {
             e = launch_gemm_bf16(x_router, desc->router_w, T, desc->E, desc->d_router, r.logits, 1,

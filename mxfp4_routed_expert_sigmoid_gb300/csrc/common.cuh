@@ -275,12 +275,9 @@ struct RouteArgs {
     float* wts;
     float* logits;     // [T, E] fp32 (always written; in the workspace if the caller passes none)
     WsHeader* hdr;
-    // fused permutation outputs (decode path) - may be null
-    int32_t* counts;   // [E]
-    int32_t* offsets;  // [E+1]
-    int32_t* perm;     // [T*k]
-    int32_t* inv;      // [T*k]
-    int32_t* active;   // [E] ascending experts with count > 0; active[E] = n_active (at index E)
+    // decode: the ascending experts that received any token, count at [E]
+    // (written by the small-T top-k kernel; null = not wanted)
+    int32_t* active;   // [E + 1]
     // optional (decode, latent mode): the router input quantised for the
     // block-scaled expert kernels (codes [d_r / 256][xq_n][128], scale atoms
     // [d_r / 128][512]); the CTAs share the work
@@ -294,7 +291,8 @@ cudaError_t launch_repack(const uint8_t* packed, const uint8_t* scale, int64_t n
 cudaError_t launch_unpack(const uint8_t* blocks, int64_t nblocks, uint8_t* packed,
                           uint8_t* scale, cudaStream_t s);
 
-// small T: GEMV logits + (last CTA) top-k [+ permutation if args.counts]
+// small T: GEMV logits (+ E2M1 terms of the rows if a.xq), then the top-k
+// kernel (+ active expert list if a.active)
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s);
 // the same with library-owned static scratch (no caller workspace)
 constexpr int kNoAllocMaxT = 8;

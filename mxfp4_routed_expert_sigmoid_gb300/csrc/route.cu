@@ -10,12 +10,16 @@
 // Top-k: each warp owns one token; every lane holds the keys of experts
 // lane, lane+32, ... as 64-bit integers (order-preserving fp32 bits of s + b
 // in the high word, ~expert in the low word, so the larger key wins and equal
-// scores fall to the lower index); k rounds of a warp-wide max extract the
-// selection in slot order.  Keys are unique, so the result is deterministic.
+// scores fall to the lower index).  The k-th largest of the 32 lane maxima
+// bounds the selection from below; the few keys above it are sorted (bitonic
+// network over the warp) and the first k are the selection in slot order.
+// Keys are unique, so the result is deterministic.
 //
 // Permutation: histogram of the selection, exclusive scan, and a stable
 // scatter that lists each expert's pairs in ascending token order, plus the
-// inverse map and the ascending list of experts that received any token.
+// inverse map and the ascending list of experts that received any token
+// (small selections: one block sort of (expert, pair) keys).
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -23,8 +27,7 @@
 namespace k3 {
 namespace {
 
-constexpr int kMaxE = 1024;   // experts handled by the in-register top-k
-constexpr int kKeysPerLane = kMaxE / 32;
+constexpr int kMaxE = 1024;   // experts handled by the one-key-per-thread top-k
 
 __device__ __forceinline__ uint32_t order_bits(float v) {
     uint32_t u = __float_as_uint(v);
@@ -40,112 +43,104 @@ __device__ __forceinline__ uint64_t expert_key(float l, float b, int e) {
            static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
-__device__ __forceinline__ int key_expert(uint64_t key) {
-    return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
-}
-
-// The k largest of the (unique) keys held by the warp, KPL per lane: k rounds
-// of a warp-wide max; lane j < k returns the j-th largest.
-template <int KPL>
-__device__ __forceinline__ uint64_t warp_topk(uint64_t (&key)[KPL], int k) {
-    const int lane = threadIdx.x & 31;
-    uint64_t mine = 0;
-    for (int j = 0; j < k; ++j) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-            best = other > best ? other : best;
-        }
-#pragma unroll
-        for (int i = 0; i < KPL; ++i)
-            if (key[i] == best) key[i] = 0;
-        if (lane == j) mine = best;
+// The top-k of one token by one CTA of kMaxE threads, thread e holding the
+// key of expert e (0 for e >= E).  The k-th largest high word H is found by
+// bisection on its bits with block-wide counts (32 steps); if more experts
+// share H than are still needed (equal s + b), a second bisection on the low
+// words keeps the lower experts.  Exactly k keys are chosen (keys are unique);
+// each is ranked by counting the chosen keys above it, which gives the slot.
+// Writes idx / w (w = s / sum(s), the sum in slot order) unless `dry`, and
+// returns whether this thread's expert was chosen.  Kept out of line so that
+// a dry run (before the logits exist) brings its code into the instruction
+// cache ahead of the real one.
+__device__ __noinline__ bool select_topk(uint64_t key, float s, int k, int32_t* idx_out, float* w_out,
+                                         bool dry) {
+    __shared__ uint64_t chosen_key[32];
+    __shared__ float chosen_s[32];
+    __shared__ int warp_count[kMaxE / 32];
+    const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+    const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
+    uint32_t H = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = H | (1u << bit);
+        if (__syncthreads_count(hi >= c) >= k) H = c;
     }
-    return mine;
-}
-
-// The k best experts among [e0, e1) of one token's logits (one warp; at most
-// 32 * KPL candidates); lane j < k returns the j-th key.
-template <int KPL>
-__device__ uint64_t topk_slice(const float* lrow, const float* __restrict__ bias, int e0, int e1,
-                               int k, WsHeader* hdr) {
-    const int lane = threadIdx.x & 31;
-    uint64_t key[KPL];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-        const int e = e0 + lane + 32 * i;
-        key[i] = 0;
-        if (e < e1) {
-            const float l = lrow[e];
-            bad |= !isfinite(l);
-            key[i] = expert_key(l, bias[e], e);
+    const int need = k - __syncthreads_count(hi > H);
+    uint32_t L = 0;
+    if (__syncthreads_count(hi == H) > need) {
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t c = L | (1u << bit);
+            if (__syncthreads_count(hi == H && lo >= c) >= need) L = c;
         }
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(hdr, K3MOE_ERR_NONFINITE, 1);
-    return warp_topk<KPL>(key, k);
-}
-
-// Writes the selection of one token from its k winning keys (lane j holds the
-// j-th): idx, and the weights s / sum(s) summed in slot order.
-__device__ void write_selection(uint64_t mine, const float* lrow, int k, int32_t* __restrict__ idx_out,
-                                float* __restrict__ w_out, int32_t* sel_smem) {
-    const int lane = threadIdx.x & 31;
-    const int e = key_expert(mine);
-    const float s_mine = lane < k ? sigmoid_f32(lrow[e]) : 0.0f;
-    float sum = 0.0f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, s_mine, j);
-    if (lane < k) {
-        idx_out[lane] = e;
-        w_out[lane] = s_mine / sum;
-        if (sel_smem) sel_smem[lane] = e;
-    }
-}
-
-// top-k of one token by one warp over all E experts
-__device__ void topk_token(const float* lrow, const float* __restrict__ bias, int E,
-                           int k, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
-                           int32_t* sel_smem, WsHeader* hdr) {
-    const uint64_t mine = topk_slice<kKeysPerLane>(lrow, bias, 0, E, k, hdr);
-    write_selection(mine, lrow, k, idx_out, w_out, sel_smem);
-}
-
-// top-k of T <= 8 tokens by the 8 warps of a CTA: G = 8 / T' warps per token
-// (T' = T rounded up to a power of two) each keep the k best of a slice of the
-// experts, then one warp per token merges the G * k candidates.
-template <int G>
-__device__ void topk_tokens_cta(const RouteArgs& a, int32_t* sel, uint64_t (*cand)[32]) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int t = wid / G, gw = wid % G;
-    const int slice = (a.E + G - 1) / G;
-    const float* lrow = a.logits + static_cast<size_t>(t) * a.E;
-    if (t < a.T) {
-        const int e0 = gw * slice, e1 = min(a.E, e0 + slice);
-        const uint64_t mine = topk_slice<32 / G>(lrow, a.bias, e0, e1, a.k, a.hdr);
-        if (G == 1) {
-            write_selection(mine, lrow, a.k, a.idx + static_cast<size_t>(t) * a.k,
-                            a.wts + static_cast<size_t>(t) * a.k, sel + t * a.k);
-        } else if (lane < a.k) {
-            cand[wid][lane] = mine;
-        }
-    }
-    if (G == 1) return;
+    const bool chosen = key != 0 && (hi > H || (hi == H && lo >= L));
+    const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
+    if (lane == 0) warp_count[wid] = __popc(bal);
     __syncthreads();
-    if (t < a.T && gw == 0) {
-        constexpr int KPL = (G * 32 + 31) / 32;  // G * k <= G * 32 candidates
-        uint64_t key[KPL];
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            const int c = lane + 32 * i;  // candidate c = (warp c / k, rank c % k)
-            key[i] = c < G * a.k ? cand[wid + c / a.k][c % a.k] : 0;
-        }
-        const uint64_t mine = warp_topk<KPL>(key, a.k);
-        write_selection(mine, lrow, a.k, a.idx + static_cast<size_t>(t) * a.k,
-                        a.wts + static_cast<size_t>(t) * a.k, sel + t * a.k);
+    if (chosen) {
+        int pos = __popc(bal & ((1u << lane) - 1u));
+        for (int w = 0; w < wid; ++w) pos += warp_count[w];
+        chosen_key[pos] = key;
     }
+    __syncthreads();
+    if (chosen) {
+        int rank = 0;
+        for (int j = 0; j < k; ++j) rank += chosen_key[j] > key ? 1 : 0;
+        chosen_s[rank] = s;
+        if (!dry) idx_out[rank] = e;
+    }
+    __syncthreads();
+    if (e < k) {
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j) sum += chosen_s[j];
+        if (!dry) w_out[e] = chosen_s[e] / sum;
+    }
+    __syncthreads();
+    return chosen;
+}
+
+// Top-k and weights of token blockIdx.x (blockDim.x == kMaxE).  With
+// a.active set (decode), every chosen expert is also marked in the bitmap kept
+// in the workspace header, and the last CTA turns the bitmap into the
+// ascending list of experts that received any token (count at active[E]) and
+// clears it.  The bias is read and the selection rehearsed on it before the
+// logits are awaited, so both overlap the logits kernel.
+__global__ void __launch_bounds__(kMaxE)
+route_topk_kernel(RouteArgs a) {
+    __shared__ uint32_t ticket_s;
+    const int t = blockIdx.x, e = threadIdx.x, lane = e & 31;
+    const bool valid = e < a.E;
+    const float b = valid ? a.bias[e] : 0.0f;
+    select_topk(valid ? expert_key(0.0f, b, e) : 0, 0.5f, a.k, nullptr, nullptr, true);
+    pdl_wait();
+    pdl_trigger();
+    const float l = valid ? a.logits[static_cast<size_t>(t) * a.E + e] : 0.0f;
+    if (__syncthreads_or(valid && !isfinite(l)) && e == 0) set_error(a.hdr, K3MOE_ERR_NONFINITE, 1);
+    const bool chosen = select_topk(valid ? expert_key(l, b, e) : 0, sigmoid_f32(l), a.k,
+                                    a.idx + static_cast<size_t>(t) * a.k,
+                                    a.wts + static_cast<size_t>(t) * a.k, false);
+    if (!a.active) return;
+    if (chosen) atomicOr(&a.hdr->pad[e >> 5], 1u << (e & 31));
+    __threadfence();
+    __syncthreads();
+    if (e == 0) ticket_s = atomicAdd(&a.hdr->counters[CTR_ROUTE], 1u);
+    __syncthreads();
+    if (ticket_s != gridDim.x - 1 || e >= 32) return;
+    __threadfence();
+    volatile uint32_t* bitmap = a.hdr->pad;
+    const uint32_t word = bitmap[lane];
+    const int c = __popc(word);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int pos = incl - c;
+    for (uint32_t w = word; w != 0; w &= w - 1) a.active[pos++] = 32 * lane + (__ffs(w) - 1);
+    if (lane == 31) a.active[a.E] = incl;
+    bitmap[lane] = 0;
+    if (lane == 0) a.hdr->counters[CTR_ROUTE] = 0;
 }
 
 // exclusive scan of n <= 4 * blockDim ints in shared memory (in place);
@@ -193,59 +188,33 @@ __device__ int block_exclusive_scan(int* data, int n) {
     return total_s;
 }
 
-// permutation of a small selection held in shared memory (T*k <= 256, E <= 1024)
-__device__ void permute_small(const int32_t* sel, int T, int k, int E, int32_t* counts,
-                              int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active) {
-    __shared__ int cnt[kMaxE];
-    __shared__ int off[kMaxE];
-    const int tid = threadIdx.x;
-    const int P = T * k;
-    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
-    for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cnt[sel[p]], 1);
-    __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) off[e] = cnt[e];
-    __syncthreads();
-    block_exclusive_scan(off, E);
-    for (int e = tid; e < E; e += blockDim.x) {
-        counts[e] = cnt[e];
-        offsets[e] = off[e];
-    }
-    if (tid == 0) offsets[E] = P;
-    for (int p = tid; p < P; p += blockDim.x) {
-        const int e = sel[p];
-        int rank = 0;
-        for (int q = 0; q < p; ++q) rank += (sel[q] == e);
-        const int row = off[e] + rank;
-        perm[row] = p;
-        inv[p] = row;
-    }
-    __syncthreads();
-    // ascending list of experts that received a token
-    for (int e = tid; e < E; e += blockDim.x) off[e] = cnt[e] > 0 ? 1 : 0;
-    __syncthreads();
-    const int n_active = block_exclusive_scan(off, E);
-    for (int e = tid; e < E; e += blockDim.x)
-        if (cnt[e] > 0) active[off[e]] = e;
-    if (tid == 0) active[E] = n_active;
-}
-
-// Logits by GEMV (one warp per expert, all T tokens), then the last CTA to
-// finish runs top-k for every token and, if requested, the permutation.
-// Each warp issues all loads of its weight row before it needs them; the T
-// token rows are staged once per CTA in shared memory.  With xq requested,
-// the CTAs also write the rows as E2M1 terms for the expert kernels.
+// Logits by GEMV (one warp per expert, all T tokens).  Each warp issues all
+// loads of its weight row before it needs them; the T token rows are staged
+// once per CTA in shared memory.  With xq requested, CTAs past the ceil(E / 8)
+// that compute logits write the token rows as E2M1 terms for the expert
+// kernels, one warp per 32-element block.
 constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
 
 __global__ void __launch_bounds__(256)
 route_small_kernel(RouteArgs a) {
     extern __shared__ __align__(16) uint4 xs[];  // [T * d_r / 8]
-    __shared__ int32_t sel[256];
-    __shared__ uint32_t ticket_s;
-    // the next kernel of the forward may start launching now: it waits for
-    // this grid's completion (griddepcontrol.wait) before reading its outputs
+    // the top-k kernel may start launching now: it waits for this grid's
+    // completion (griddepcontrol.wait) before reading the logits
     pdl_trigger();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int gemv_ctas = (a.E + 7) / 8;
+    if (static_cast<int>(blockIdx.x) >= gemv_ctas) {
+        const int nb = a.d_r / 32;
+        const int xq_ctas = gridDim.x - gemv_ctas;
+        for (int i = (blockIdx.x - gemv_ctas) * 8 + wid; i < a.T * nb; i += xq_ctas * 8) {
+            const int t = i / nb, b = i - t * nb;
+            uint32_t q[kTerms], sb[kTerms];
+            quantize_terms(bf16_to_f32(a.x[static_cast<size_t>(t) * a.d_r + 32 * b + lane]), q, sb);
+            store_terms(q, sb, t, b & 7, a.xq + static_cast<size_t>(b >> 3) * a.xq_n * 128,
+                        a.xsf + static_cast<size_t>(b >> 3) * 1024);
+        }
+        return;
+    }
     const int e = blockIdx.x * 8 + wid;
     const uint16_t* wrow = a.w + static_cast<size_t>(e < a.E ? e : 0) * a.d_r;
     uint4 wv[kRouteChunks];
@@ -258,21 +227,6 @@ route_small_kernel(RouteArgs a) {
     for (int v = threadIdx.x; v < nvec; v += blockDim.x)
         xs[v] = reinterpret_cast<const uint4*>(a.x)[v];
     __syncthreads();
-
-    // router input -> E2M1 terms for the block-scaled expert kernels: one warp
-    // per 32-element block, blocks spread over all warps of the grid (the
-    // rows are staged in every CTA)
-    if (a.xq) {
-        const int nb = a.d_r / 32;
-        for (int i = blockIdx.x * 8 + wid; i < a.T * nb; i += gridDim.x * 8) {
-            const int t = i / nb, b = i - t * nb;
-            const uint16_t* row = reinterpret_cast<const uint16_t*>(xs) + static_cast<size_t>(t) * a.d_r;
-            uint32_t q[kTerms], sb[kTerms];
-            quantize_terms(bf16_to_f32(row[32 * b + lane]), q, sb);
-            store_terms(q, sb, t, b & 7, a.xq + static_cast<size_t>(b >> 3) * a.xq_n * 128,
-                        a.xsf + static_cast<size_t>(b >> 3) * 1024);
-        }
-    }
 
     if (e < a.E) {
         float acc[8];
@@ -314,33 +268,6 @@ route_small_kernel(RouteArgs a) {
             if (lane == 0) a.logits[static_cast<size_t>(t) * a.E + e] = v;
         }
     }
-    // last CTA to finish does the selection
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) ticket_s = atomicAdd(&a.hdr->counters[CTR_ROUTE], 1u);
-    __syncthreads();
-    if (ticket_s != gridDim.x - 1) return;
-    if (threadIdx.x == 0) a.hdr->counters[CTR_ROUTE] = 0;
-    __threadfence();
-    {
-        __shared__ uint64_t cand[8][32];
-        if (a.T == 1) topk_tokens_cta<8>(a, sel, cand);
-        else if (a.T == 2) topk_tokens_cta<4>(a, sel, cand);
-        else if (a.T <= 4) topk_tokens_cta<2>(a, sel, cand);
-        else topk_tokens_cta<1>(a, sel, cand);
-    }
-    __syncthreads();
-    if (a.counts)
-        permute_small(sel, a.T, a.k, a.E, a.counts, a.offsets, a.perm, a.inv, a.active);
-}
-
-__global__ void __launch_bounds__(256)
-topk_kernel(RouteArgs a) {
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= a.T) return;
-    topk_token(a.logits + static_cast<size_t>(t) * a.E, a.bias, a.E, a.k,
-               a.idx + static_cast<size_t>(t) * a.k, a.wts + static_cast<size_t>(t) * a.k,
-               nullptr, a.hdr);
 }
 
 // Plain tiled SIMT logits for moderate T: 64 tokens x 64 experts per CTA.
@@ -475,8 +402,15 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
 
 }  // namespace
 
+cudaError_t launch_route_topk(const RouteArgs& a, cudaStream_t s) {
+    const cudaError_t e = launch_pdl(route_topk_kernel, dim3(a.T), dim3(kMaxE), 0, s, a);
+    trace_mark("route_topk", s);
+    return e;
+}
+
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
-    const int grid = (a.E + 7) / 8;
+    const int gemv_ctas = (a.E + 7) / 8;
+    const int xq_ctas = a.xq ? std::min(128, (a.T * (a.d_r / 32) + 7) / 8) : 0;
     const size_t smem = static_cast<size_t>(a.T) * a.d_r * 2;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
@@ -484,19 +418,22 @@ cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    route_small_kernel<<<grid, 256, smem, s>>>(a);
+    route_small_kernel<<<gemv_ctas + xq_ctas, 256, smem, s>>>(a);
     trace_mark("route_small", s);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_route_topk(a, s);
 }
 
 // ---------------------------------------------------------------------------
 // Router with library-owned scratch (k3moe_route_noalloc).
 //
-// The small-T router needs a completion counter and, when the caller does
-// not want the logits, a [T, E] fp32 buffer for them.  This variant keeps
-// both in one file-scope device array instead of a caller workspace: it is
-// part of the module image, so every GPU that loads the library holds these
-// bytes until the process exits, and every call shares them.
+// The small-T router needs a workspace header (its status word) and, when the
+// caller does not want the logits, a [T, E] fp32 buffer for them.  This
+// variant keeps both in one file-scope device array instead of a caller
+// workspace: it is part of the module image, so every GPU that loads the
+// library holds these bytes until the process exits, and every call shares
+// them.
 // ---------------------------------------------------------------------------
 constexpr size_t kNoAllocScratch =
     sizeof(WsHeader) + static_cast<size_t>(kNoAllocMaxT) * kNoAllocMaxE * sizeof(float);
@@ -533,14 +470,14 @@ cudaError_t launch_route_noalloc(RouteArgs a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     a.hdr = static_cast<WsHeader*>(scratch);
     if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(scratch) + sizeof(WsHeader));
-    a.counts = nullptr;
+    a.active = nullptr;
     return launch_route_small(a, s);
 }
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s) {
-    topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a);
-    trace_mark("topk", s);
-    return cudaGetLastError();
+    RouteArgs b = a;
+    b.active = nullptr;  // the permutation kernels list the active experts
+    return launch_route_topk(b, s);
 }
 
 cudaError_t launch_logits_simt(const RouteArgs& a, cudaStream_t s) {
