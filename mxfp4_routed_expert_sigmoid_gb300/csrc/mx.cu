@@ -41,10 +41,13 @@
 // token rows as E2M1 terms): up -> finish (h = silu(g) * u from both slots,
 // quantised to E2M1 terms) -> down -> combine (weights in slot order).
 //
-// Roles of the streaming kernel (192 threads, one CTA per SM):
+// Roles of the streaming kernel (224 threads, one CTA per SM):
 //   warp 0     producer: TMA / bulk copies into a ring of stages;
-//   warp 1     TMEM owner and MMA issuer (one thread);
-//   warps 2..5 epilogue: tcgen05.ld of the accumulator quadrant (warp % 4).
+//   warp 1     TMEM owner and MMA issuer of the first K chunk of each stage;
+//   warp 6     MMA issuer of the second chunk (one issuing thread reaches about
+//              60 % of the MMA rate of two, measured), into its own accumulator;
+//   warps 2..5 epilogue: tcgen05.ld of the accumulator quadrant (warp % 4),
+//              the two issuers' accumulators added in a fixed order.
 // Every wait is bounded (kWaitLimitNs); on expiry the CTA records
 // K3MOE_ERR_TIMEOUT, every role stops, copies in flight are waited for (with
 // a limit) and TMEM is released.
@@ -58,15 +61,17 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMxThreads = 192;
+constexpr int kMxThreads = 224;
 constexpr int kMaxStages = 8;
 constexpr int kChunks = 2;             // 256-wide K chunks per stage (a stage covers K = 512)
 constexpr int kChunkA = 16384;         // 128 rows x 128 bytes of packed E2M1
 constexpr int kStageA = kChunks * kChunkA;
 constexpr int kMaxN = 64;              // MMA N: kTerms * T rounded up to 16
-constexpr int kSfBase = 2 * kMaxN;     // TMEM: two accumulators, then the scale slots
-// every scale slot starts on a 32-column boundary: per chunk two atoms of A
-// (+0, +64) and two of B (+32, +96)
+// TMEM: accumulators (buffer a, issuer t) at (2 a + t) * kMaxN, then the scale
+// slots, each on a 32-column boundary: issuer t's atoms A0, B0, A1, B1 of its
+// chunk at kSfBase + 128 t + 32 g
+constexpr int kSfBase = 4 * kMaxN;
+static_assert(kChunks == 2, "one K chunk per MMA issuer");
 static_assert(kSfBase + kChunks * 128 <= 512, "scale slots fit in TMEM");
 constexpr uint32_t kTmemCols = 512;
 
@@ -156,10 +161,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.RS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);  // one commit per MMA issuer
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_full[a], 2);
             mbar_init(&acc_empty[a], 4);
         }
         abort_s = 0;
@@ -224,13 +229,15 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
         if (lane == 0 && w0 < w1) {
-            // ------------------------------ MMA issuer ----------------------------
+            // ------------------------------ MMA issuers ---------------------------
+            const int mt = warp == 1 ? 0 : 1;  // the stage's chunk this thread multiplies
             int ks = Cursor(w0, p.nmat, p.tiles, p.KS).ks;
             int s = 0, seg = 0, ps = 0;
             uint32_t ph = 0, pph = 0;
             const uint32_t id0 = idesc_f4(128, p.N, 0, 0);
+            const uint32_t slots = tmem + kSfBase + 128 * mt;
             for (int i = 0, w = w0; w < w1; ++i, ++w) {
                 const bool seg_start = (w == w0) || ks == 0;
                 const bool seg_end = (w + 1 == w1) || ks == p.KS - 1;
@@ -238,8 +245,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (seg_start && !mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71))
                     break;
                 if (!mbar_wait(&full[s], ph, abort_flag, p.hdr, 72)) break;
-                // one set of scale slots: the MMAs of the previous stage have
-                // finished reading it
+                // the scale slots are reused: the previous stage's MMAs have finished
                 if (i > 0) {
                     if (!mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73)) break;
                     if (++ps == p.RS) {
@@ -248,21 +254,21 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                 }
                 tc_fence_after();
-                const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
                 const int nch = min(kChunks, p.KC - ks * kChunks);
-                for (int g = 0; g < 2 * nch; ++g) {  // atoms: 2 per chunk
-                    tmem_cp_sf(tmem + kSfBase + 64 * g, st + offSA + 512 * g);
-                    tmem_cp_sf(tmem + kSfBase + 64 * g + 32, st + offSB + 512 * g);
-                }
-                const uint32_t d_t = tmem + a * kMaxN;
-                for (int cc = 0; cc < nch; ++cc) {
-                    const uint64_t ad = sw128_desc(st + cc * kChunkA), bd = sw128_desc(st + offB + cc * NB);
+                if (mt < nch) {
+                    const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+                    for (int h = 0; h < 2; ++h) {  // the chunk's two 128-wide scale groups
+                        tmem_cp_sf(slots + 64 * h, st + offSA + 512 * (2 * mt + h));
+                        tmem_cp_sf(slots + 64 * h + 32, st + offSB + 512 * (2 * mt + h));
+                    }
+                    const uint32_t d_t = tmem + (2 * a + mt) * kMaxN;
+                    const uint64_t ad = sw128_desc(st + mt * kChunkA), bd = sw128_desc(st + offB + mt * NB);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {  // K = 64 each: atom 2 cc + j / 2, scale id 2 (j % 2)
-                        const uint32_t sfa = tmem + kSfBase + 64 * (2 * cc + (j >> 1));
+                    for (int j = 0; j < 4; ++j) {  // K = 64 each: group j / 2, scale id 2 (j % 2)
+                        const uint32_t sfa = slots + 64 * (j >> 1);
                         const uint32_t id = static_cast<uint32_t>(2 * (j & 1));
                         mma_f4(d_t, ad + 2 * j, bd + 2 * j, id0 | (id << 4) | (id << 29), sfa, sfa + 32,
-                               (seg_start && cc == 0 && j == 0) ? 0u : 1u);
+                               (seg_start && j == 0) ? 0u : 1u);
                     }
                 }
                 mma_commit(&empty[s]);
@@ -290,8 +296,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, p.hdr, 74)))
                 break;
             tc_fence_after();
+            // the second issuer's accumulator holds data unless the segment is only
+            // a last stage with a single chunk
+            const bool has_d1 = (p.KC % kChunks) == 0 || ks_begin < p.KS - 1;
             float v[kMaxN];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * kMaxN;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * a * kMaxN;
 #pragma unroll
             for (int c16 = 0; c16 < kMaxN / 16; ++c16) {
                 if (c16 * 16 < p.N) {
@@ -299,6 +308,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tmem_ld16(taddr + c16 * 16, v16);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = v16[i];
+                    if (has_d1) {
+                        tmem_ld16(taddr + kMaxN + c16 * 16, v16);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[c16 * 16 + i] += v16[i];
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = 0.0f;
