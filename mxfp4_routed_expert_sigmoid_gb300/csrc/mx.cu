@@ -97,6 +97,7 @@ __device__ __forceinline__ void mma_f4(uint32_t d_tmem, uint64_t a, uint64_t b, 
 struct MxArgs {
     const uint8_t* sf[2];   // prepared scale atoms of the matrices (W1, W3 or W2)
     int nmat;               // matrices per expert in this pass (2 up, 1 down)
+    int early_a;            // 1: the active list is final before this grid's wait (down)
     const uint8_t* bq;      // B codes [unit][K / 256][N][128] (up: one shared unit)
     const uint8_t* bsf;     // B scale atoms [unit][K / 128][512]
     size_t bq_ustride;      // bytes per unit (0 when all units share B)
@@ -181,13 +182,58 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
 
-    // the router / finish kernel before this one wrote the active list and B
+    // The weight loads of the first stages need only the active list.  The down
+    // projection may issue them before waiting for the finish kernel: the list
+    // was written by the top-k kernel, which completed before the up projection
+    // (this grid's predecessor's predecessor) passed its own wait.
+    int U = 0, w0 = 0, w1 = 0;
+    auto split = [&]() {
+        U = p.active[p.E];
+        const long long W = static_cast<long long>(U) * p.nmat * p.tiles * p.KS;
+        w0 = static_cast<int>(W * blockIdx.x / gridDim.x);
+        w1 = static_cast<int>(W * (blockIdx.x + 1) / gridDim.x);
+    };
+    // stage j of this CTA's range: weight codes and their scales (A side) or the
+    // activation codes and scales (B side) into ring slot j % RS
+    auto issue_a = [&](const Cursor& c, int e, uint8_t* st, uint64_t* bar) {
+        const int c0 = c.ks * kChunks;
+        const int nch = min(kChunks, p.KC - c0);
+        const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
+        const int y = e * p.rows + c.tile * 128;
+        for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
+        bulk_load(st + offSA, p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
+                  nch * 1024, bar);
+    };
+    auto issue_b = [&](const Cursor& c, uint8_t* st, uint64_t* bar) {
+        const int c0 = c.ks * kChunks;
+        const int nch = min(kChunks, p.KC - c0);
+        bulk_load(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, bar);
+        bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024, bar);
+    };
+    auto a_bytes = [&](const Cursor& c) {
+        return static_cast<uint32_t>(min(kChunks, p.KC - c.ks * kChunks)) * (kChunkA + 1024);
+    };
+    auto b_bytes = [&](const Cursor& c) {
+        return static_cast<uint32_t>(min(kChunks, p.KC - c.ks * kChunks)) * (NB + 1024);
+    };
+    int early = 0;  // stages whose A side was issued before the wait
+    if (p.early_a) {
+        split();
+        if (warp == 0 && lane == 0 && w0 < w1) {
+            Cursor c(w0, p.nmat, p.tiles, p.KS);
+            early = min(p.RS, w1 - w0);
+            for (int j = 0; j < early; ++j) {
+                uint8_t* st = smem + static_cast<size_t>(j) * p.stage_bytes;
+                mbar_expect_tx_only(&full[j], a_bytes(c));
+                issue_a(c, p.active[c.u], st, &full[j]);
+                c.next(p.nmat, p.tiles, p.KS);
+            }
+        }
+    }
+    // the kernel before this one wrote the active list (up) or B (down)
     pdl_wait();
     pdl_trigger();
-    const int U = p.active[p.E];
-    const long long W = static_cast<long long>(U) * p.nmat * p.tiles * p.KS;
-    const int w0 = static_cast<int>(W * blockIdx.x / gridDim.x);
-    const int w1 = static_cast<int>(W * (blockIdx.x + 1) / gridDim.x);
+    if (!p.early_a) split();
 
     if (warp == 0) {
         if (lane == 0 && w0 < w1) {
@@ -198,20 +244,16 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t ph = 0;
             int issued = 0;
             for (int w = w0; w < w1; ++w) {
-                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70)) break;
                 uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-                const int c0 = c.ks * kChunks;
-                const int nch = min(kChunks, p.KC - c0);
-                mbar_expect_tx(&full[s], static_cast<uint32_t>(nch) * (kChunkA + NB + 2048));
-                const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
-                const int y = e * p.rows + c.tile * 128;
-                for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, &full[s], (c0 + cc) * 128, y);
-                bulk_load(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, &full[s]);
-                bulk_load(st + offSA,
-                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
-                          nch * 1024, &full[s]);
-                bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024,
-                          &full[s]);
+                if (issued < early) {
+                    mbar_expect_tx(&full[s], b_bytes(c));  // the arrival of the stage
+                    issue_b(c, st, &full[s]);
+                } else {
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70)) break;
+                    mbar_expect_tx(&full[s], a_bytes(c) + b_bytes(c));
+                    issue_a(c, e, st, &full[s]);
+                    issue_b(c, st, &full[s]);
+                }
                 ++issued;
                 if (++s == p.RS) {
                     s = 0;
@@ -627,6 +669,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     dn.sf[0] = a.w2_sf;
     dn.sf[1] = a.w2_sf;
     dn.nmat = 1;
+    dn.early_a = 1;
     dn.bq = m.hq;
     dn.bsf = m.hsf;
     dn.bq_ustride = static_cast<size_t>(a.f / 256) * m.N * 128;
