@@ -7,13 +7,13 @@
 //   selection key s + b (fp32), top-k with ties to the lower index, slots in
 //   key order, w = s / sum(s) over the selected experts (sum in slot order).
 //
-// Top-k: each warp owns one token; every lane holds the keys of experts
-// lane, lane+32, ... as 64-bit integers (order-preserving fp32 bits of s + b
-// in the high word, ~expert in the low word, so the larger key wins and equal
-// scores fall to the lower index).  The k-th largest of the 32 lane maxima
-// bounds the selection from below; the few keys above it are sorted (bitonic
-// network over the warp) and the first k are the selection in slot order.
-// Keys are unique, so the result is deterministic.
+// Top-k: one CTA per token, thread e holding the key of expert e as a 64-bit
+// integer (order-preserving fp32 bits of s + b in the high word, ~expert in
+// the low word, so the larger key wins and equal scores fall to the lower
+// index).  The k-th largest of the warp maxima bounds the selection from
+// below; the few keys above it are ranked by counting (bisection on
+// block-wide counts when too many qualify).  Keys are unique, so the result
+// is deterministic.
 //
 // Permutation: histogram of the selection, exclusive scan, and a stable
 // scatter that lists each expert's pairs in ascending token order, plus the
@@ -43,51 +43,116 @@ __device__ __forceinline__ uint64_t expert_key(float l, float b, int e) {
            static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
+constexpr int kCand = 64;  // candidate keys ranked by counting
+
 // The top-k of one token by one CTA of kMaxE threads, thread e holding the
-// key of expert e (0 for e >= E).  The k-th largest high word H is found by
-// bisection on its bits with block-wide counts (32 steps); if more experts
-// share H than are still needed (equal s + b), a second bisection on the low
-// words keeps the lower experts.  Exactly k keys are chosen (keys are unique);
-// each is ranked by counting the chosen keys above it, which gives the slot.
-// Writes idx / w (w = s / sum(s), the sum in slot order) unless `dry`, and
-// returns whether this thread's expert was chosen.  Kept out of line so that
-// a dry run (before the logits exist) brings its code into the instruction
-// cache ahead of the real one.
+// key of expert e (0 for e >= E).  Exactly k keys are chosen (keys are
+// unique), listed in key order: idx / w (w = s / sum(s), the sum in slot
+// order) are written unless `dry`; returns whether this thread's expert was
+// chosen.
+//
+// Fast path: the k-th largest of the 32 warp maxima, M, bounds the selection
+// from below (the k warps whose maxima are >= M hold k distinct keys >= M), so
+// the chosen keys are among those >= M.  When at most kCand keys qualify they
+// are ranked by counting.  Otherwise (equal or clustered scores) the k-th
+// largest high word is found by bisection on its bits with block-wide counts;
+// if more experts share it than are still needed, a second bisection on the
+// low words keeps the lower experts, and the chosen keys are ranked by
+// counting.  Both paths choose the same k keys.  Kept out of line so that a dry
+// run (before the logits exist) brings its code into the instruction cache
+// ahead of the real one.
 __device__ __noinline__ bool select_topk(uint64_t key, float s, int k, int32_t* idx_out, float* w_out,
                                          bool dry) {
-    __shared__ uint64_t chosen_key[32];
+    __shared__ uint64_t wmax_s[kMaxE / 32];
+    __shared__ uint64_t cand_key[kCand];
+    __shared__ float cand_s[kCand];
+    __shared__ uint64_t thr_s;
+    __shared__ int ncand_s;
+    __shared__ uint32_t chosen_bits[kMaxE / 32];
     __shared__ float chosen_s[32];
-    __shared__ int warp_count[kMaxE / 32];
+    constexpr uint32_t kFull = 0xffffffffu;
     const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
-    const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
-    uint32_t H = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t c = H | (1u << bit);
-        if (__syncthreads_count(hi >= c) >= k) H = c;
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    uint64_t m = key;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t v = __shfl_xor_sync(kFull, m, o);
+        m = v > m ? v : m;
     }
-    const int need = k - __syncthreads_count(hi > H);
-    uint32_t L = 0;
-    if (__syncthreads_count(hi == H) > need) {
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t c = L | (1u << bit);
-            if (__syncthreads_count(hi == H && lo >= c) >= need) L = c;
+    if (lane == 0) wmax_s[wid] = m;
+    if (e == 0) ncand_s = 0;
+    __syncthreads();
+    if (wid == 0) {
+        const uint64_t mine = wmax_s[lane];
+        int r = 0;
+#pragma unroll 8
+        for (int j = 0; j < kMaxE / 32; ++j) r += wmax_s[j] > mine ? 1 : 0;
+        // the k-th largest maximum; 0 (no bound) when fewer than k warps hold experts
+        const uint32_t at = __ballot_sync(kFull, r == k - 1);
+        const uint64_t M = at ? __shfl_sync(kFull, mine, __ffs(at) - 1) : 0;
+        if (lane == 0) thr_s = M;
+    }
+    __syncthreads();
+    const uint64_t M = thr_s;
+    const bool cand = M != 0 && key >= M;
+    const uint32_t cbal = __ballot_sync(kFull, cand);
+    int base = 0;
+    if (lane == 0 && cbal) base = atomicAdd(&ncand_s, __popc(cbal));
+    base = __shfl_sync(kFull, base, 0);
+    if (cand) {
+        const int pos = base + __popc(cbal & lanes_below);
+        if (pos < kCand) {
+            cand_key[pos] = key;
+            cand_s[pos] = s;
         }
     }
-    const bool chosen = key != 0 && (hi > H || (hi == H && lo >= L));
-    const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
-    if (lane == 0) warp_count[wid] = __popc(bal);
     __syncthreads();
-    if (chosen) {
-        int pos = __popc(bal & ((1u << lane) - 1u));
-        for (int w = 0; w < wid; ++w) pos += warp_count[w];
-        chosen_key[pos] = key;
-    }
-    __syncthreads();
-    if (chosen) {
-        int rank = 0;
-        for (int j = 0; j < k; ++j) rank += chosen_key[j] > key ? 1 : 0;
-        chosen_s[rank] = s;
-        if (!dry) idx_out[rank] = e;
+    const int n = ncand_s;
+    if (M != 0 && n <= kCand) {
+        if (e < 32) chosen_bits[e] = 0;
+        __syncthreads();
+        if (e < n) {
+            const uint64_t kk = cand_key[e];
+            int rank = 0;
+            for (int j = 0; j < n; ++j) rank += cand_key[j] > kk ? 1 : 0;
+            if (rank < k) {
+                const int ex = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
+                chosen_s[rank] = cand_s[e];
+                if (!dry) idx_out[rank] = ex;
+                atomicOr(&chosen_bits[ex >> 5], 1u << (ex & 31));
+            }
+        }
+    } else {
+        const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
+        uint32_t H = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t c = H | (1u << bit);
+            if (__syncthreads_count(hi >= c) >= k) H = c;
+        }
+        const int need = k - __syncthreads_count(hi > H);
+        uint32_t L = 0;
+        if (__syncthreads_count(hi == H) > need) {
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t c = L | (1u << bit);
+                if (__syncthreads_count(hi == H && lo >= c) >= need) L = c;
+            }
+        }
+        const bool chosen = key != 0 && (hi > H || (hi == H && lo >= L));
+        const uint32_t bal = __ballot_sync(kFull, chosen);
+        if (lane == 0) chosen_bits[wid] = bal;
+        __syncthreads();
+        if (chosen) {
+            int pos = __popc(bal & lanes_below);
+            for (int w = 0; w < wid; ++w) pos += __popc(chosen_bits[w]);
+            cand_key[pos] = key;
+        }
+        __syncthreads();
+        if (chosen) {
+            int rank = 0;
+            for (int j = 0; j < k; ++j) rank += cand_key[j] > key ? 1 : 0;
+            chosen_s[rank] = s;
+            if (!dry) idx_out[rank] = e;
+        }
     }
     __syncthreads();
     if (e < k) {
@@ -95,15 +160,16 @@ __device__ __noinline__ bool select_topk(uint64_t key, float s, int k, int32_t* 
         for (int j = 0; j < k; ++j) sum += chosen_s[j];
         if (!dry) w_out[e] = chosen_s[e] / sum;
     }
+    const bool mine = (chosen_bits[wid] >> lane) & 1u;
     __syncthreads();
-    return chosen;
+    return mine;
 }
 
 // Top-k and weights of token blockIdx.x (blockDim.x == kMaxE).  With
-// a.active set (decode), every chosen expert is also marked in the bitmap kept
-// in the workspace header, and the last CTA turns the bitmap into the
-// ascending list of experts that received any token (count at active[E]) and
-// clears it.  The bias is read and the selection rehearsed on it before the
+// a.active set (decode), the ascending list of experts that received any token
+// (count at active[E]) is written too: by the CTA itself for one token;
+// otherwise every chosen expert is marked in the bitmap kept in the workspace
+// header, and the last CTA turns the bitmap into the list and clears it.  The bias is read and the selection rehearsed on it before the
 // logits are awaited, so both overlap the logits kernel.
 __global__ void __launch_bounds__(kMaxE)
 route_topk_kernel(RouteArgs a) {
@@ -120,6 +186,24 @@ route_topk_kernel(RouteArgs a) {
                                     a.idx + static_cast<size_t>(t) * a.k,
                                     a.wts + static_cast<size_t>(t) * a.k, false);
     if (!a.active) return;
+    if (gridDim.x == 1) {
+        // one token: its selection, in ascending expert order, is the active list
+        __shared__ int wcount[kMaxE / 32];
+        const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
+        if (lane == 0) wcount[e >> 5] = __popc(bal);
+        __syncthreads();
+        if (chosen) {
+            int pos = __popc(bal & ((1u << lane) - 1u));
+            for (int w = 0; w < (e >> 5); ++w) pos += wcount[w];
+            a.active[pos] = e;
+        }
+        if (e == 0) {
+            int total = 0;
+            for (int w = 0; w < kMaxE / 32; ++w) total += wcount[w];
+            a.active[a.E] = total;
+        }
+        return;
+    }
     if (chosen) atomicOr(&a.hdr->pad[e >> 5], 1u << (e & 31));
     __threadfence();
     __syncthreads();
