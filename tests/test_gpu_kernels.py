@@ -139,6 +139,28 @@ def test_route_ties_lower_index(k3):
     assert np.allclose(wts.cpu().numpy(), 1.0 / k)
 
 
+@pytest.mark.parametrize("case", ["all_equal", "one_tied_per_warp"])
+def test_route_ties_wide(k3, case):
+    """Equal scores at the decode width (896 experts, top-16), both ways the
+    selection can run: all scores equal puts hundreds of keys above the
+    warp-maximum bound (bisection), one tied expert per warp puts exactly k
+    there (ranked directly).  Ties go to the lower index in both."""
+    import torch
+
+    E, k, T, d = 896, 16, 2, 64
+    x = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((E, d), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(E, dtype=torch.float32, device="cuda")
+    if case == "one_tied_per_warp":
+        b[5::32] = 1.0
+    idx, wts, _ = k3.k3moe_route(x, w, b, k)
+    want = list(range(k)) if case == "all_equal" else [32 * j + 5 for j in range(k)]
+    assert idx.cpu().tolist() == [want] * T
+    assert np.allclose(wts.cpu().numpy(), 1.0 / k)
+    r = oracle.select_experts(np.zeros((T, E)), b.cpu().numpy().astype(np.float32), k)
+    assert r["idx"].tolist() == [want] * T
+
+
 def test_route_nonfinite_flag(k3):
     import torch
 
