@@ -399,7 +399,9 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 // h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E2M1 terms in
-// the B layout of the down projection.  One warp per (unit, token, 32-block).
+// the B layout of the down projection.  One warp per (unit, token, 32-block),
+// grid-strided over the active units (the grid is sized for the SMs, not for
+// the largest possible number of units).
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
                  const int32_t* __restrict__ active, int E, uint8_t* __restrict__ hq,
@@ -408,20 +410,21 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int nb = f / 32;
-    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int u = i / (T * nb);
-    if (u >= active[E]) return;
-    const int r = i - u * T * nb;
-    const int t = r / nb, b = r - t * nb;
-    const size_t plane = static_cast<size_t>(umax) * T * f;
-    const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
-    const float g = part[o] + part[2 * plane + o];
-    const float uu = part[plane + o] + part[3 * plane + o];
-    uint32_t q[kTerms], sb[kTerms];
-    quantize_terms(silu_f32(g) * uu, q, sb);
     const int KC = f / 256;
-    store_terms(q, sb, t, b & 7, hq + (static_cast<size_t>(u) * KC + (b >> 3)) * N * 128,
-                hsf + (static_cast<size_t>(u) * KC + (b >> 3)) * 1024);
+    const int items = active[E] * T * nb;
+    const size_t plane = static_cast<size_t>(umax) * T * f;
+    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < items; i += gridDim.x * 8) {
+        const int u = i / (T * nb);
+        const int r = i - u * T * nb;
+        const int t = r / nb, b = r - t * nb;
+        const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
+        const float g = part[o] + part[2 * plane + o];
+        const float uu = part[plane + o] + part[3 * plane + o];
+        uint32_t q[kTerms], sb[kTerms];
+        quantize_terms(silu_f32(g) * uu, q, sb);
+        store_terms(q, sb, t, b & 7, hq + (static_cast<size_t>(u) * KC + (b >> 3)) * N * 128,
+                    hsf + (static_cast<size_t>(u) * KC + (b >> 3)) * 1024);
+    }
 }
 
 // Token rows (bf16) -> kTerms E2M1 terms in the B layout (used when the
@@ -657,10 +660,12 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     up.hdr = a.hdr;
     // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
+
     if ((e = launch_stream(t1, t3, up, grid_up, s, "decode_up"))) return e;
 
     const int warps = m.umax * a.T * (a.f / 32);
-    e = launch_pdl(mx_finish_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, static_cast<const float*>(m.up),
+    const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
+    e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
                    m.umax, a.T, a.f, m.N, a.active, a.E, m.hq, m.hsf);
     trace_mark("decode_finish_up", s);
     if (e != cudaSuccess) return e;
