@@ -22,7 +22,7 @@
 //      quantize_terms), pre-swizzled in global memory, one bulk copy;
 //   SFB their scale atoms (column n from lane n % 32, column n / 32).
 // The kTerms partial products of a token are summed in fp32 by the epilogue.
-// Why kind::mxf4: one tcgen05.mma with M = 128 takes about 58 ns on GB300
+// Why kind::mxf4: one tcgen05.mma with M = 128 takes about 55 ns on GB300
 // whatever N up to 128 (measured), so the weight bytes an instruction covers
 // set the speed limit: 4 KB with K = 64 here, twice kind::mxf8f6f4's K = 32.
 //
@@ -230,9 +230,14 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
     }
-    // the kernel before this one wrote the active list (up) or B (down)
+    // the kernel before this one wrote the active list (up) or B (down).  The
+    // down pass lets the combine launch at once (it reads nothing before its own
+    // wait); the up pass triggers only after its wait, because the down pass
+    // reads the active list before waiting and may launch as soon as the finish
+    // kernel has started
+    if (p.early_a) pdl_trigger();
     pdl_wait();
-    pdl_trigger();
+    if (!p.early_a) pdl_trigger();
     if (!p.early_a) split();
 
     if (warp == 0) {
@@ -406,8 +411,12 @@ __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
                  const int32_t* __restrict__ active, int E, uint8_t* __restrict__ hq,
                  uint8_t* __restrict__ hsf) {
-    pdl_wait();
+    // the down projection may launch now: its CTAs start on the SMs the up
+    // projection frees and issue their first weight loads during this kernel
+    // (this grid was launched after every up CTA passed its wait, so the active
+    // list they read is final)
     pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nb = f / 32;
     const int KC = f / 256;
