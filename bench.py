@@ -37,6 +37,11 @@ METRIC = "MoE-layer tokens/s; HBM GB/s at T=1/8, tensor TFLOPS at T=512/8192"
 EXPERT_MATRIX_BYTES = None  # filled per config
 
 
+# DRAM bytes (read + write) per launch of a kernel from an ncu capture of the
+# current kernel version (profiles/), by (workload, kernel); absent: not captured
+TRAFFIC = {}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,10 +408,19 @@ def ours_arm(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     mb = matrix_bytes(cfg)
     u_mean = sum(uniq) / len(uniq)
+    # algorithmic bytes per launch of the streaming kernels: every distinct
+    # selected expert's matrices once (units of the same expert re-read them)
     algo = {
         "decode_up": u_mean * 2 * mb,
         "decode_down": u_mean * mb,
+        "units_up": u_mean * 2 * mb,
+        "units_down": u_mean * mb,
         "route_small": cfg.E * cfg.d_router * 2 + cfg.T * cfg.d_router * 2 + cfg.T * cfg.E * 4,
+    }
+    # algorithmic flops of the grouped GEMMs: 2 f d per (token, expert) and matrix
+    flops = {
+        "expert_up": cfg.T * cfg.k * 2 * 2.0 * cfg.f * cfg.d,
+        "expert_down": cfg.T * cfg.k * 2.0 * cfg.f * cfg.d,
     }
     dom = max(kern_mean, key=kern_mean.get)
     roof = None
@@ -414,8 +428,17 @@ def ours_arm(args):
         achieved = algo[dom] / (kern_mean[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                 "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": None, "algorithmic_bytes_per_launch": algo[dom],
+                "traffic": TRAFFIC.get((cfg.name, dom)), "algorithmic_bytes_per_launch": algo[dom],
                 "avg_launch_ms": kern_mean[dom]}
+    elif dom in flops:
+        # f16 operands: the measured bf16 rate (same tensor-core rate); the kernel
+        # runs inside a step of several ms, so the sustained figure
+        tf_peak = peaks.get("bf16_tflops_sustained", 1700.0)
+        achieved = flops[dom] / (kern_mean[dom] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tf_peak,
+                "peak_source": ("measured bf16, sustained" if "bf16_tflops_sustained" in peaks else "fallback"),
+                "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": TRAFFIC.get((cfg.name, dom)),
+                "algorithmic_flops_per_launch": flops[dom], "avg_launch_ms": kern_mean[dom]}
     step_bytes = u_mean * 3 * mb + algo["route_small"]
     mean_ms = total_ms / args.steps
     line = {
@@ -449,7 +472,7 @@ def ours_arm(args):
 
 def dtype_of(T: int, path: int) -> str:
     """Arithmetic of the expert path the layer takes for T tokens."""
-    decode = path == 1 or (path == 0 and T <= 8)
+    decode = path == 1 or (path == 0 and T <= 1024)
     if decode:
         return ("e2m1 x e2m1 block-scaled tensor-core MMA (activations as five E2M1 terms), "
                 "fp32 accumulation")

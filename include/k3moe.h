@@ -67,10 +67,14 @@ typedef enum k3moe_act {
     K3MOE_ACT_SILU_GATED = 0
 } k3moe_act;
 
-/* Expert-path selector.  AUTO picks DECODE for T <= 8 and GROUPED otherwise.
+/* Expert-path selector.  AUTO picks DECODE for T <= 1024 and GROUPED
+ * otherwise; DECODE with T > 1024 returns K3MOE_ERR_UNSUPPORTED.
  *   DECODE : block-scaled tcgen05 MMAs (kind::mxf4) streaming the selected
  *            experts' E2M1 codes by TMA, E8M0 scales applied by the tensor
- *            cores, activations as E2M1 terms; split over the SMs.
+ *            cores, activations as E2M1 terms; split over the SMs.  Up to 8
+ *            tokens every active expert takes all tokens; beyond that each
+ *            expert's tokens are cut into units of at most 12 and an
+ *            expert's weights are streamed once per unit.
  *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
  *            dequantisation, TMA-fed, TMEM accumulators. */
 typedef enum k3moe_path {

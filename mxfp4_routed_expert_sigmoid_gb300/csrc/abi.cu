@@ -13,6 +13,10 @@ using namespace k3;
 namespace {
 
 constexpr int kDecodeMaxT = 8;
+// the block-scaled streaming kernels also take up to this many tokens, grouped
+// in units of at most 12 tokens of one expert (beyond it the experts see many
+// tokens each and the grouped GEMMs are the better fit)
+constexpr int kStreamMaxT = 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
@@ -85,6 +89,7 @@ RoutePlan route_plan(int T, int E) {
 struct FwdPlan {
     size_t logits, idx, wts, counts, offsets, active, perm, inv, chunk;
     size_t dec, y;                                  // decode scratch, shared y (fp32)
+    size_t units;                                   // unit-grouped streaming scratch
     size_t xp, xp_exp, hb, h_amax, hp, hp_exp, tiles;  // grouped
     size_t hn, z, m;                                // block mode
     size_t total;
@@ -106,6 +111,7 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     p.chunk = c.take(permute_scratch_bytes(T, d->E));
     const int Td = std::min(T, kDecodeMaxT);
     p.dec = c.take(mx_decode_scratch_bytes(Td, d->E, d->k, d->d, d->f));
+    if (T > kDecodeMaxT && T <= kStreamMaxT) p.units = c.take(mx_units_scratch_bytes(T, d->E, d->k, d->d, d->f));
     p.y = c.take(P * d->d * 4);  // grouped path
     p.xp = c.take(P * d->d * 2);
     p.xp_exp = c.take(P * 4);
@@ -406,8 +412,8 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     const FwdPlan p = fwd_plan(desc, T);
     if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
     int path = desc->path;
-    if (path == K3MOE_PATH_AUTO) path = T <= kDecodeMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
-    if (path == K3MOE_PATH_DECODE && T > kDecodeMaxT) return K3MOE_ERR_UNSUPPORTED;
+    if (path == K3MOE_PATH_AUTO) path = T <= kStreamMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
+    if (path == K3MOE_PATH_DECODE && T > kStreamMaxT) return K3MOE_ERR_UNSUPPORTED;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
@@ -472,7 +478,18 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
             return K3MOE_ERR_CUDA;
     }
 
-    if (path == K3MOE_PATH_DECODE) {
+    if (path == K3MOE_PATH_DECODE && T > kDecodeMaxT) {
+        MxUnitsArgs a{};
+        a.w1_q = desc->w1_q; a.w3_q = desc->w3_q; a.w2_q = desc->w2_q;
+        a.w1_sf = desc->w1_sf; a.w3_sf = desc->w3_sf; a.w2_sf = desc->w2_sf;
+        a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
+        a.counts = counts; a.offsets = offsets; a.perm = perm; a.inv = inv; a.idx = r.idx; a.wts = r.wts;
+        a.scratch = at(p.units);
+        a.out = latent_out; a.hdr = hdr; a.num_sms = sms;
+        e = launch_mx_units(a, s);
+        if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
+        if (e) return cuda_status(e);
+    } else if (path == K3MOE_PATH_DECODE) {
         MxDecodeArgs a{};
         a.w1_q = desc->w1_q; a.w3_q = desc->w3_q; a.w2_q = desc->w2_q;
         a.w1_sf = desc->w1_sf; a.w3_sf = desc->w3_sf; a.w2_sf = desc->w2_sf;

@@ -336,6 +336,27 @@ size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f);
 void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_t** xq, uint8_t** xsf,
                         int* N);
 cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s);
+// unit-grouped streaming forward (more tokens, few per expert): the experts'
+// sorted token lists (from the permutation) are cut into units of at most 12
+// tokens and streamed like the decode path
+struct MxUnitsArgs {
+    const uint8_t *w1_q, *w3_q, *w2_q;     // E2M1 codes
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
+    const uint16_t* x;        // [T, d] bf16 expert input
+    int T, E, k, d, f;
+    const int32_t* counts;    // [E]
+    const int32_t* offsets;   // [E + 1]
+    const int32_t* perm;      // [T k] sorted row -> (token, slot) pair
+    const int32_t* inv;       // [T k] pair -> sorted row
+    const int32_t* idx;       // [T, k]
+    const float* wts;         // [T, k]
+    void* scratch;            // mx_units_scratch_bytes(T, E, k, d, f)
+    uint16_t* out;            // [T, d] bf16
+    WsHeader* hdr;
+    int num_sms;
+};
+size_t mx_units_scratch_bytes(int T, int E, int k, int d, int f);
+cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s);
 // canonical E8M0 scales [rows, K/32] <-> prepared atoms (inverse = 1: atoms -> canonical)
 cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
                               cudaStream_t s);

@@ -102,7 +102,9 @@ struct MxArgs {
     const uint8_t* bsf;     // B scale atoms [unit][K / 128][512]
     size_t bq_ustride;      // bytes per unit (0 when all units share B)
     size_t bsf_ustride;
-    const int32_t* active;  // [E + 1]: active experts ascending, count at [E]
+    const int32_t* active;  // expert of each unit (decode: the active experts ascending)
+    const int32_t* count;   // number of units (decode: active + E)
+    const int32_t* ucnt;    // tokens of each unit (null: all T)
     int E;
     int rows;               // weight rows per expert (f up, d down)
     int tiles;              // 128-row tiles per expert
@@ -188,7 +190,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // (this grid's predecessor's predecessor) passed its own wait.
     int U = 0, w0 = 0, w1 = 0;
     auto split = [&]() {
-        U = p.active[p.E];
+        U = *p.count;
         const long long W = static_cast<long long>(U) * p.nmat * p.tiles * p.KS;
         w0 = static_cast<int>(W * blockIdx.x / gridDim.x);
         w1 = static_cast<int>(W * (blockIdx.x + 1) / gridDim.x);
@@ -373,9 +375,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const size_t plane = static_cast<size_t>(p.umax) * p.T * p.rows_out;
             float* dst = p.part + static_cast<size_t>((ks_begin == 0 ? 0 : 1) * mats + mat) * plane +
                          static_cast<size_t>(c.u) * p.T * p.rows_out + row;
+            const int tokens = p.ucnt ? p.ucnt[c.u] : p.T;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t >= p.T) break;
+            for (int t = 0; t < kMaxN / kTerms; ++t) {
+                if (t >= tokens) break;
                 float sum = 0.0f;
 #pragma unroll
                 for (int j = 0; j < kTerms; ++j) sum += v[kTerms * t + j];
@@ -409,7 +412,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // the largest possible number of units).
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
-                 const int32_t* __restrict__ active, int E, uint8_t* __restrict__ hq,
+                 const int32_t* __restrict__ count, const int32_t* __restrict__ ucnt, uint8_t* __restrict__ hq,
                  uint8_t* __restrict__ hsf) {
     // the down projection may launch now: its CTAs start on the SMs the up
     // projection frees and issue their first weight loads during this kernel
@@ -420,12 +423,14 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     const int lane = threadIdx.x & 31;
     const int nb = f / 32;
     const int KC = f / 256;
-    const int items = active[E] * T * nb;
+    const int items = *count * T * nb;
     const size_t plane = static_cast<size_t>(umax) * T * f;
     for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < items; i += gridDim.x * 8) {
         const int u = i / (T * nb);
         const int r = i - u * T * nb;
         const int t = r / nb, b = r - t * nb;
+        // tokens a unit does not have are skipped: their MMA columns are never read
+        if (ucnt && t >= ucnt[u]) continue;
         const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
         const float g = part[o] + part[2 * plane + o];
         const float uu = part[plane + o] + part[3 * plane + o];
@@ -467,7 +472,7 @@ constexpr int kCombineMaxUnits = 256;  // decode: T * k <= 8 * 32
 __global__ void __launch_bounds__(kCombineThreads)
 mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const float* __restrict__ wts,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ active, int E, int k,
-                  uint16_t* __restrict__ out) {
+                  const int32_t* __restrict__ rowmap, uint16_t* __restrict__ out) {
     __shared__ int rows[32];
     __shared__ float wk[32];
     __shared__ int act[kCombineMaxUnits];
@@ -476,19 +481,27 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
     pdl_trigger();
     const int t = blockIdx.y;
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
-    const int U = active[E];
-    for (int i = threadIdx.x; i < U; i += blockDim.x) act[i] = active[i];
-    __syncthreads();
-    if (threadIdx.x < k) {
-        const int e = idx[t * k + threadIdx.x];
-        int lo = 0, hi = U - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (act[mid] < e) lo = mid + 1;
-            else hi = mid;
+    if (rowmap) {
+        // unit-grouped: the row of every (token, slot) pair was listed with the units
+        if (threadIdx.x < k) {
+            rows[threadIdx.x] = rowmap[t * k + threadIdx.x];
+            wk[threadIdx.x] = wts[t * k + threadIdx.x];
         }
-        rows[threadIdx.x] = lo * T + t;
-        wk[threadIdx.x] = wts[t * k + threadIdx.x];
+    } else {
+        const int U = active[E];
+        for (int i = threadIdx.x; i < U; i += blockDim.x) act[i] = active[i];
+        __syncthreads();
+        if (threadIdx.x < k) {
+            const int e = idx[t * k + threadIdx.x];
+            int lo = 0, hi = U - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (act[mid] < e) lo = mid + 1;
+                else hi = mid;
+            }
+            rows[threadIdx.x] = lo * T + t;
+            wk[threadIdx.x] = wts[t * k + threadIdx.x];
+        }
     }
     __syncthreads();
     const int c0 = blockIdx.x * kCombineCols;
@@ -510,6 +523,126 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
         float acc = 0.0f;
         for (int j = 0; j < k; ++j) acc += part[j][threadIdx.x];
         out[static_cast<size_t>(t) * d + c] = f32_to_bf16(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Unit-grouped streaming (more tokens than the decode path takes, few per
+// expert): every expert's sorted token list (from the permutation) is cut into
+// units of at most kUnitTokens tokens, and the streaming kernels run over the
+// units exactly as the decode path runs over the active experts, with each
+// unit's own token rows as the B operand.  An expert's weights are read once
+// per unit.
+// ---------------------------------------------------------------------------
+constexpr int kUnitTokens = kMaxN / kTerms;  // 12: kTerms rows per token within N = 64
+
+// Unit list and the expert-output row of every (token, slot) pair.  One CTA of
+// 1024 threads (E <= 1024): units of expert e are ubase[e] .. ubase[e + 1) - 1.
+__global__ void __launch_bounds__(1024)
+mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                const int32_t* __restrict__ idx, const int32_t* __restrict__ inv, int E, int P,
+                int32_t* __restrict__ unit_exp, int32_t* __restrict__ unit_row0, int32_t* __restrict__ unit_cnt,
+                int32_t* __restrict__ nunits, int32_t* __restrict__ rowmap) {
+    __shared__ int ubase[1024 + 1];
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int n = tid < E ? (counts[tid] + kUnitTokens - 1) / kUnitTokens : 0;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_tot[lane], wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        warp_tot[lane] = wi - w;  // exclusive over warps
+    }
+    __syncthreads();
+    const int excl = warp_tot[wid] + incl - n;
+    if (tid < E) ubase[tid] = excl;
+    if (tid == blockDim.x - 1) ubase[E] = excl + n;  // blockDim.x >= E: the last thread sees the total
+    __syncthreads();
+    const int U = ubase[E];
+    if (tid == 0) *nunits = U;
+    for (int i = tid; i < U; i += blockDim.x) {
+        int lo = 0, hi = E - 1;  // expert of unit i: largest e with ubase[e] <= i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ubase[mid] <= i) lo = mid;
+            else hi = mid - 1;
+        }
+        const int g = i - ubase[lo];
+        unit_exp[i] = lo;
+        unit_row0[i] = offsets[lo] + g * kUnitTokens;
+        unit_cnt[i] = min(kUnitTokens, counts[lo] - g * kUnitTokens);
+    }
+    for (int q = tid; q < P; q += blockDim.x) {
+        const int e = idx[q];
+        const int local = inv[q] - offsets[e];
+        rowmap[q] = (ubase[e] + local / kUnitTokens) * kUnitTokens + local % kUnitTokens;
+    }
+}
+
+// Token rows as kTerms E2M1 terms, once per token (unswizzled): codes
+// [t][term][K / 2] (element 2i in the low nibble), E8M0 scales [t][term][K / 32].
+// One warp per (token, 32-block), grid-strided.
+__global__ void __launch_bounds__(256)
+mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __restrict__ tq,
+                      uint8_t* __restrict__ tsf) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32;
+    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < T * nb; i += gridDim.x * 8) {
+        const int t = i / nb, b = i - t * nb;
+        uint32_t q[kTerms], sb[kTerms];
+        quantize_terms(bf16_to_f32(x[static_cast<size_t>(t) * K + 32 * b + lane]), q, sb);
+#pragma unroll
+        for (int j = 0; j < kTerms; ++j) {
+            const uint32_t by = q[j] | (__shfl_down_sync(0xffffffffu, q[j], 1) << 4);  // even lanes
+            uint32_t w = by;
+            w |= __shfl_down_sync(0xffffffffu, by, 2) << 8;
+            w |= __shfl_down_sync(0xffffffffu, by, 4) << 16;
+            w |= __shfl_down_sync(0xffffffffu, by, 6) << 24;
+            const size_t row = static_cast<size_t>(t) * kTerms + j;
+            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(tq + row * (K / 2) + 16 * b + (lane >> 1)) = w;
+            if (lane == 0) tsf[row * nb + b] = static_cast<uint8_t>(sb[j]);
+        }
+    }
+}
+
+// B operand of the unit-grouped up projection: the term rows of token i of
+// unit u (sorted row unit_row0[u] + i) copied into the unit's swizzled layout;
+// tokens past unit_cnt[u] are left as they are (their MMA columns are never
+// read).  One thread per (unit, token, term, 32-block), grid-strided.
+__global__ void __launch_bounds__(256)
+mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__ tsf,
+                     const int32_t* __restrict__ perm, int k, int K, int N, const int32_t* __restrict__ nunits,
+                     const int32_t* __restrict__ unit_row0, const int32_t* __restrict__ unit_cnt,
+                     uint8_t* __restrict__ bq, uint8_t* __restrict__ bsf) {
+    const int nb = K / 32, KC = K / 256;
+    const int per_unit = kUnitTokens * kTerms * nb;
+    const long long items = static_cast<long long>(*nunits) * per_unit;
+    for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < items;
+         it += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int u = static_cast<int>(it / per_unit);
+        int r = static_cast<int>(it - static_cast<long long>(u) * per_unit);
+        const int i = r / (kTerms * nb);
+        r -= i * kTerms * nb;
+        const int j = r / nb, b = r - j * nb;
+        if (i >= unit_cnt[u]) continue;
+        const int tok = perm[unit_row0[u] + i] / k;
+        const size_t src = static_cast<size_t>(tok) * kTerms + j;
+        const int n = kTerms * i + j, c = b >> 3, g = b & 7;
+        const size_t cb = static_cast<size_t>(u) * KC + c;
+        *reinterpret_cast<uint4*>(bq + cb * N * 128 + n * 128 + ((g ^ (n & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(tq + src * (K / 2) + 16 * b);
+        bsf[cb * 1024 + (g >> 2) * 512 + sf_atom_offset(n, g & 3)] = tsf[src * nb + b];
     }
 }
 
@@ -656,6 +789,8 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     up.bq_ustride = 0;
     up.bsf_ustride = 0;
     up.active = a.active;
+    up.count = a.active + a.E;
+    up.ucnt = nullptr;
     up.E = a.E;
     up.rows = a.f;
     up.tiles = a.f / 128;
@@ -675,7 +810,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     const int warps = m.umax * a.T * (a.f / 32);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
     e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
-                   m.umax, a.T, a.f, m.N, a.active, a.E, m.hq, m.hsf);
+                   m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf);
     trace_mark("decode_finish_up", s);
     if (e != cudaSuccess) return e;
 
@@ -699,7 +834,147 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
 
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
-                   m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, a.out);
+                   m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, static_cast<const int32_t*>(nullptr), a.out);
+    trace_mark("combine", s);
+    return e;
+}
+
+// ---------------------------------------------------------------------------
+// host: unit-grouped streaming forward
+// ---------------------------------------------------------------------------
+namespace {
+
+struct MxUnitScratch {
+    int32_t *unit_exp, *unit_row0, *unit_cnt, *nunits, *rowmap;
+    uint8_t *tq, *tsf, *xq, *xsf, *hq, *hsf;
+    float *up, *y;
+    int umax, N;
+    size_t bytes;
+};
+
+// units <= min(T k, (T k + E (G - 1)) / G): ceil(c / G) <= (c + G - 1) / G per expert
+MxUnitScratch mx_units_carve(void* scratch, int T, int E, int k, int d, int f) {
+    MxUnitScratch m{};
+    const long long P = static_cast<long long>(T) * k;
+    m.umax = static_cast<int>(std::min<long long>(P, (P + static_cast<long long>(E) * (kUnitTokens - 1)) / kUnitTokens));
+    m.N = mx_n(kUnitTokens);
+    char* b = static_cast<char*>(scratch);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        char* r = b ? b + o : nullptr;
+        o += align_up(bytes);
+        return r;
+    };
+    const size_t U = static_cast<size_t>(m.umax);
+    m.unit_exp = reinterpret_cast<int32_t*>(take(U * 4));
+    m.unit_row0 = reinterpret_cast<int32_t*>(take(U * 4));
+    m.unit_cnt = reinterpret_cast<int32_t*>(take(U * 4));
+    m.nunits = reinterpret_cast<int32_t*>(take(4));
+    m.rowmap = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P) * 4));
+    m.tq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 2)));
+    m.tsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 32)));
+    m.xq = reinterpret_cast<uint8_t*>(take(U * (d / 256) * m.N * 128));
+    m.xsf = reinterpret_cast<uint8_t*>(take(U * (d / 128) * 512));
+    m.up = reinterpret_cast<float*>(take(4 * U * kUnitTokens * f * 4));
+    m.hq = reinterpret_cast<uint8_t*>(take(U * (f / 256) * m.N * 128));
+    m.hsf = reinterpret_cast<uint8_t*>(take(U * (f / 128) * 512));
+    m.y = reinterpret_cast<float*>(take(2 * U * kUnitTokens * d * 4));
+    m.bytes = o;
+    return m;
+}
+
+}  // namespace
+
+size_t mx_units_scratch_bytes(int T, int E, int k, int d, int f) {
+    return mx_units_carve(nullptr, T, E, k, d, f).bytes;
+}
+
+cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
+    const MxUnitScratch m = mx_units_carve(a.scratch, a.T, a.E, a.k, a.d, a.f);
+    if (a.E > 1024) return cudaErrorNotSupported;
+    const int P = a.T * a.k;
+    mx_units_kernel<<<1, 1024, 0, s>>>(a.counts, a.offsets, a.idx, a.inv, a.E, P, m.unit_exp, m.unit_row0,
+                                       m.unit_cnt, m.nunits, m.rowmap);
+    trace_mark("units", s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long twarps = static_cast<long long>(a.T) * (a.d / 32);
+    mx_token_terms_kernel<<<static_cast<int>(std::min<long long>((twarps + 7) / 8, 8LL * a.num_sms)), 256, 0, s>>>(
+        a.x, a.T, a.d, m.tq, m.tsf);
+    trace_mark("token_terms", s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const long long citems = static_cast<long long>(m.umax) * kUnitTokens * kTerms * (a.d / 32);
+    mx_unit_terms_kernel<<<static_cast<int>(std::min<long long>((citems + 255) / 256, 8LL * a.num_sms)), 256, 0,
+                           s>>>(m.tq, m.tsf, a.perm, a.k, a.d, m.N, m.nunits, m.unit_row0, m.unit_cnt, m.xq, m.xsf);
+    trace_mark("unit_terms", s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    CUtensorMap t1, t3, t2;
+    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
+                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
+                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2,
+                        static_cast<uint64_t>(a.E) * a.d, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorNotSupported;
+
+    MxArgs up{};
+    up.sf[0] = a.w1_sf;
+    up.sf[1] = a.w3_sf;
+    up.nmat = 2;
+    up.bq = m.xq;
+    up.bsf = m.xsf;
+    up.bq_ustride = static_cast<size_t>(a.d / 256) * m.N * 128;
+    up.bsf_ustride = static_cast<size_t>(a.d / 128) * 512;
+    up.active = m.unit_exp;
+    up.count = m.nunits;
+    up.ucnt = m.unit_cnt;
+    up.E = a.E;
+    up.rows = a.f;
+    up.tiles = a.f / 128;
+    up.KC = a.d / 256;
+    up.KS = (up.KC + kChunks - 1) / kChunks;
+    up.N = m.N;
+    up.T = kUnitTokens;
+    up.part = m.up;
+    up.umax = m.umax;
+    up.rows_out = a.f;
+    up.hdr = a.hdr;
+    // every CTA's range must be at least one tile long: there are at least k units
+    const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
+    if ((e = launch_stream(t1, t3, up, grid_up, s, "units_up"))) return e;
+
+    const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 32);
+    const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
+    e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
+                   kUnitTokens, a.f, m.N, static_cast<const int32_t*>(m.nunits),
+                   static_cast<const int32_t*>(m.unit_cnt), m.hq, m.hsf);
+    trace_mark("units_finish_up", s);
+    if (e != cudaSuccess) return e;
+
+    MxArgs dn = up;
+    dn.sf[0] = a.w2_sf;
+    dn.sf[1] = a.w2_sf;
+    dn.nmat = 1;
+    dn.early_a = 1;
+    dn.bq = m.hq;
+    dn.bsf = m.hsf;
+    dn.bq_ustride = static_cast<size_t>(a.f / 256) * m.N * 128;
+    dn.bsf_ustride = static_cast<size_t>(a.f / 128) * 512;
+    dn.rows = a.d;
+    dn.tiles = a.d / 128;
+    dn.KC = a.f / 256;
+    dn.KS = (dn.KC + kChunks - 1) / kChunks;
+    dn.part = m.y;
+    dn.rows_out = a.d;
+    const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
+    if ((e = launch_stream(t2, t2, dn, grid_dn, s, "units_down"))) return e;
+
+    // the y slots are strided by units x kUnitTokens rows; the grid's y index is the token
+    dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
+    e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y), m.umax,
+                   kUnitTokens, a.d, a.wts, a.idx, static_cast<const int32_t*>(nullptr), a.E, a.k,
+                   static_cast<const int32_t*>(m.rowmap), a.out);
     trace_mark("combine", s);
     return e;
 }

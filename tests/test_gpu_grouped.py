@@ -79,6 +79,48 @@ def test_tiny_grouped(k3, T):
     compare_forward(k3, synth.custom("tiny", T=T, **TINY), 2)
 
 
+@pytest.mark.parametrize("T", [9, 33])
+def test_tiny_units(k3, T):
+    """More than 8 tokens on the block-scaled streaming kernels (units of at
+    most 12 tokens of one expert)."""
+    compare_forward(k3, synth.custom("tiny", T=T, **TINY), 1)
+
+
+@pytest.mark.parametrize("T", [40, 300])
+def test_mid_units(k3, T):
+    # experts with 1..60 tokens: several units per expert, ragged last units
+    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1280, seed_index=21)
+    compare_forward(k3, cfg, 1)
+
+
+def test_units_deterministic_and_power_of_two(k3):
+    import torch
+
+    cfg = synth.custom("decode_t1", T=64, E=32, k=4, d=512, f=512, seed_index=23)
+    layer, dense, expert, ex = make_layer(cfg, path=1)
+    x = to_dev(dense["hidden"], "cuda")
+    out1 = k3.k3moe_forward(layer, x)
+    out2 = k3.k3moe_forward(layer, x)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    ex2 = dict(ex)
+    ex2["w2_s"] = ex["w2_s"] + 1
+    layer2 = k3.MoELayer(router_w=layer.tensors["router_w"], router_b=layer.tensors["router_b"],
+                         k=cfg.k, path=1, **ex2)
+    out3 = k3.k3moe_forward(layer2, x)
+    assert torch.equal(out3.float(), 2 * out1.float())
+
+
+def test_units_and_grouped_agree(k3):
+    """The streaming (units) and grouped GEMM paths on the same 300 tokens."""
+    cfg = synth.custom("decode_t1", T=300, E=64, k=8, d=768, f=1280, seed_index=25)
+    bundle = make_layer(cfg, path=1)
+    out_u, _, _ = compare_forward(k3, cfg, 1, bundle=bundle)
+    layer_g = bundle[0].with_path(2)
+    out_g, _, _ = compare_forward(k3, cfg, 2, bundle=(layer_g,) + tuple(bundle[1:]))
+    a, b = bf16_tensor_to_np(out_u), bf16_tensor_to_np(out_g)
+    assert np.all(rel_err_rows(a, b) <= 2 * TOL + 2.0 ** -8)
+
+
 @pytest.mark.parametrize("T", [8, 40, 300])
 def test_mid_grouped(k3, T):
     # several m-tiles, K stages and units; ragged expert segments
@@ -117,7 +159,7 @@ def test_grouped_deterministic_and_power_of_two(k3):
     assert torch.equal(out3.float(), 2 * out1.float())
 
 
-@pytest.mark.parametrize("T,path", [(4, 1), (4, 2), (300, 2)])
+@pytest.mark.parametrize("T,path", [(4, 1), (4, 2), (300, 1), (300, 2)])
 def test_block_small(k3, T, path):
     """Full latent block (RMSNorm, projections, router at the model width)."""
     cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=256, f=512, D=512, seed_index=24)
