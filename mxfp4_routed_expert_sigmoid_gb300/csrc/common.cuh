@@ -194,7 +194,8 @@ __device__ __forceinline__ void quantize_terms(float v, uint32_t (&q)[kTerms], u
     float res = v;
 #pragma unroll
     for (int j = 0; j < kTerms; ++j) {
-        const float amax = warp_max(fabsf(res));
+        // largest |res| of the block: non-negative floats order like their bits
+        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
         const int e = e2m1_scale_exp(amax);
         q[j] = e2m1_code(res * exp2i(-e));
         sb[j] = static_cast<uint32_t>(e + 127);

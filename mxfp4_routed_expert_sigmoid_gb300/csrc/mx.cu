@@ -105,6 +105,7 @@ struct MxArgs {
     const int32_t* active;  // expert of each unit (decode: the active experts ascending)
     const int32_t* count;   // number of units (decode: active + E)
     const int32_t* ucnt;    // tokens of each unit (null: all T)
+    const int32_t* ubase;   // unit-grouped: first unit of each expert, [E + 1] (null: decode)
     int E;
     int rows;               // weight rows per expert (f up, d down)
     int tiles;              // 128-row tiles per expert
@@ -120,29 +121,71 @@ struct MxArgs {
     WsHeader* hdr;
 };
 
-// position (unit, matrix, row tile, stage) in the sequence of stages
+// Position in the sequence of stages.  Decode: (unit, matrix, row tile,
+// stage), the unit being the position in the active list.  Unit-grouped
+// (ubase set): expert by expert, (matrix, row tile, unit of the expert,
+// stage), so that the units of one expert read each weight tile back to back
+// and all but the first find it in L2.
 struct Cursor {
     int u, mat, tile, ks;
-    __device__ Cursor(int w, int nmat, int tiles, int KS) {
-        const int per_m = tiles * KS, per_u = nmat * per_m;
-        u = w / per_u;
-        int r = w - u * per_u;
-        mat = r / per_m;
-        r -= mat * per_m;
-        tile = r / KS;
-        ks = r - tile * KS;
+    int e, grp, ngrp;  // expert (decode: the unit), unit within the expert, units of the expert
+    __device__ Cursor(int w, const MxArgs& p) {
+        if (!p.ubase) {
+            const int per_m = p.tiles * p.KS, per_u = p.nmat * per_m;
+            u = w / per_u;
+            int r = w - u * per_u;
+            mat = r / per_m;
+            r -= mat * per_m;
+            tile = r / p.KS;
+            ks = r - tile * p.KS;
+            e = u;
+            grp = 0;
+            ngrp = 1;
+        } else {
+            const int su = p.nmat * p.tiles * p.KS;  // stages per unit
+            int lo = 0, hi = p.E - 1;               // largest e with ubase[e] * su <= w
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.ubase[mid] * su <= w) lo = mid;
+                else hi = mid - 1;
+            }
+            e = lo;
+            ngrp = p.ubase[e + 1] - p.ubase[e];
+            int r = w - p.ubase[e] * su;
+            const int per_tile = ngrp * p.KS, per_m = p.tiles * per_tile;
+            mat = r / per_m;
+            r -= mat * per_m;
+            tile = r / per_tile;
+            r -= tile * per_tile;
+            grp = r / p.KS;
+            ks = r - grp * p.KS;
+            u = p.ubase[e] + grp;
+        }
     }
-    __device__ void next(int nmat, int tiles, int KS) {
-        if (++ks == KS) {
-            ks = 0;
-            if (++tile == tiles) {
+    // the first stage of the next (unit, matrix, row tile)
+    __device__ void next_segment(const MxArgs& p) {
+        ks = 0;
+        if (++grp == ngrp) {
+            grp = 0;
+            if (++tile == p.tiles) {
                 tile = 0;
-                if (++mat == nmat) {
+                if (++mat == p.nmat) {
                     mat = 0;
-                    ++u;
+                    if (p.ubase) {
+                        do {
+                            ++e;
+                        } while (e < p.E && p.ubase[e + 1] == p.ubase[e]);
+                        ngrp = e < p.E ? p.ubase[e + 1] - p.ubase[e] : 1;
+                    } else {
+                        ++e;
+                    }
                 }
             }
         }
+        u = p.ubase ? (e < p.E ? p.ubase[e] : 0) + grp : e;
+    }
+    __device__ void next(const MxArgs& p) {
+        if (++ks == p.KS) next_segment(p);
     }
 };
 
@@ -222,13 +265,13 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (p.early_a) {
         split();
         if (warp == 0 && lane == 0 && w0 < w1) {
-            Cursor c(w0, p.nmat, p.tiles, p.KS);
+            Cursor c(w0, p);
             early = min(p.RS, w1 - w0);
             for (int j = 0; j < early; ++j) {
                 uint8_t* st = smem + static_cast<size_t>(j) * p.stage_bytes;
                 mbar_expect_tx_only(&full[j], a_bytes(c));
                 issue_a(c, p.active[c.u], st, &full[j]);
-                c.next(p.nmat, p.tiles, p.KS);
+                c.next(p);
             }
         }
     }
@@ -245,7 +288,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0) {
         if (lane == 0 && w0 < w1) {
             // ------------------------------ producer ------------------------------
-            Cursor c(w0, p.nmat, p.tiles, p.KS);
+            Cursor c(w0, p);
             int e = p.active[c.u];
             int s = 0;
             uint32_t ph = 0;
@@ -267,7 +310,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     ph ^= 1;
                 }
                 const int u_prev = c.u;
-                c.next(p.nmat, p.tiles, p.KS);
+                c.next(p);
                 if (c.u != u_prev && w + 1 < w1) e = p.active[c.u];
             }
             // copies still in flight (after an abort) finish before the CTA exits
@@ -282,7 +325,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (lane == 0 && w0 < w1) {
             // ------------------------------ MMA issuers ---------------------------
             const int mt = warp == 1 ? 0 : 1;  // the stage's chunk this thread multiplies
-            int ks = Cursor(w0, p.nmat, p.tiles, p.KS).ks;
+            int ks = Cursor(w0, p).ks;
             int s = 0, seg = 0, ps = 0;
             uint32_t ph = 0, pph = 0;
             const uint32_t id0 = idesc_f4(128, p.N, 0, 0);
@@ -335,7 +378,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else {
         // ------------------------------ epilogue ---------------------------------
         const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
-        Cursor c(w0 < w1 ? w0 : 0, p.nmat, p.tiles, p.KS);
+        Cursor c(w0 < w1 ? w0 : 0, p);
         int seg = 0;
         for (int w = w0; w < w1;) {
             const int ks_begin = c.ks;
@@ -387,14 +430,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             w += len;
             ++seg;
-            c.ks = 0;
-            if (++c.tile == p.tiles) {
-                c.tile = 0;
-                if (++c.mat == p.nmat) {
-                    c.mat = 0;
-                    ++c.u;
-                }
-            }
+            c.next_segment(p);
         }
     }
 
@@ -425,19 +461,39 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     const int KC = f / 256;
     const int items = *count * T * nb;
     const size_t plane = static_cast<size_t>(umax) * T * f;
-    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < items; i += gridDim.x * 8) {
-        const int u = i / (T * nb);
-        const int r = i - u * T * nb;
-        const int t = r / nb, b = r - t * nb;
-        // tokens a unit does not have are skipped: their MMA columns are never read
-        if (ucnt && t >= ucnt[u]) continue;
-        const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
-        const float g = part[o] + part[2 * plane + o];
-        const float uu = part[plane + o] + part[3 * plane + o];
-        uint32_t q[kTerms], sb[kTerms];
-        quantize_terms(silu_f32(g) * uu, q, sb);
-        store_terms(q, sb, t, b & 7, hq + (static_cast<size_t>(u) * KC + (b >> 3)) * N * 128,
-                    hsf + (static_cast<size_t>(u) * KC + (b >> 3)) * 1024);
+    const int stride = gridDim.x * 8;
+    // two items per pass: the loads of both are in flight before either is quantised
+    for (int i0 = blockIdx.x * 8 + (threadIdx.x >> 5); i0 < items; i0 += 2 * stride) {
+        float h[2];
+        int uu[2], tt[2], bb[2];
+        bool ok[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int i = i0 + p * stride;
+            const int u = i / (T * nb);
+            const int r = i - u * T * nb;
+            const int t = r / nb, b = r - t * nb;
+            uu[p] = u;
+            tt[p] = t;
+            bb[p] = b;
+            // tokens a unit does not have are skipped: their MMA columns are never read
+            ok[p] = i < items && (!ucnt || t < ucnt[u]);
+            h[p] = 0.0f;
+            if (ok[p]) {
+                const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
+                const float g = part[o] + part[2 * plane + o];
+                const float up = part[plane + o] + part[3 * plane + o];
+                h[p] = silu_f32(g) * up;
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            if (!ok[p]) continue;
+            uint32_t q[kTerms], sb[kTerms];
+            quantize_terms(h[p], q, sb);
+            store_terms(q, sb, tt[p], bb[p] & 7, hq + (static_cast<size_t>(uu[p]) * KC + (bb[p] >> 3)) * N * 128,
+                        hsf + (static_cast<size_t>(uu[p]) * KC + (bb[p] >> 3)) * 1024);
+        }
     }
 }
 
@@ -542,7 +598,7 @@ __global__ void __launch_bounds__(1024)
 mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ idx, const int32_t* __restrict__ inv, int E, int P,
                 int32_t* __restrict__ unit_exp, int32_t* __restrict__ unit_row0, int32_t* __restrict__ unit_cnt,
-                int32_t* __restrict__ nunits, int32_t* __restrict__ rowmap) {
+                int32_t* __restrict__ nunits, int32_t* __restrict__ rowmap, int32_t* __restrict__ ubase_out) {
     __shared__ int ubase[1024 + 1];
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -571,6 +627,7 @@ mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
     __syncthreads();
     const int U = ubase[E];
     if (tid == 0) *nunits = U;
+    for (int e = tid; e <= E; e += blockDim.x) ubase_out[e] = ubase[e];
     for (int i = tid; i < U; i += blockDim.x) {
         int lo = 0, hi = E - 1;  // expert of unit i: largest e with ubase[e] <= i
         while (lo < hi) {
@@ -845,7 +902,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
 namespace {
 
 struct MxUnitScratch {
-    int32_t *unit_exp, *unit_row0, *unit_cnt, *nunits, *rowmap;
+    int32_t *unit_exp, *unit_row0, *unit_cnt, *nunits, *rowmap, *ubase;
     uint8_t *tq, *tsf, *xq, *xsf, *hq, *hsf;
     float *up, *y;
     int umax, N;
@@ -870,6 +927,7 @@ MxUnitScratch mx_units_carve(void* scratch, int T, int E, int k, int d, int f) {
     m.unit_row0 = reinterpret_cast<int32_t*>(take(U * 4));
     m.unit_cnt = reinterpret_cast<int32_t*>(take(U * 4));
     m.nunits = reinterpret_cast<int32_t*>(take(4));
+    m.ubase = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E + 1) * 4));
     m.rowmap = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P) * 4));
     m.tq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 2)));
     m.tsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 32)));
@@ -894,7 +952,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     if (a.E > 1024) return cudaErrorNotSupported;
     const int P = a.T * a.k;
     mx_units_kernel<<<1, 1024, 0, s>>>(a.counts, a.offsets, a.idx, a.inv, a.E, P, m.unit_exp, m.unit_row0,
-                                       m.unit_cnt, m.nunits, m.rowmap);
+                                       m.unit_cnt, m.nunits, m.rowmap, m.ubase);
     trace_mark("units", s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -929,6 +987,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     up.active = m.unit_exp;
     up.count = m.nunits;
     up.ucnt = m.unit_cnt;
+    up.ubase = m.ubase;
     up.E = a.E;
     up.rows = a.f;
     up.tiles = a.f / 128;
