@@ -203,6 +203,51 @@ __device__ __forceinline__ void quantize_terms(float v, uint32_t (&q)[kTerms], u
     }
 }
 
+// Two fp32 values -> one byte of E2M1 codes (lo in the low nibble; round to
+// nearest even, saturating), and the byte back to the two exact values.
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
+    uint32_t r;
+    asm("{ .reg .b8 c; cvt.rn.satfinite.e2m1x2.f32 c, %1, %2; mov.b32 %0, {c, c, c, c}; }"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r & 0xFFu;
+}
+__device__ __forceinline__ float2 e2m1x2_float(uint32_t byte) {
+    uint32_t h;
+    asm("{ .reg .b8 c0, c1, c2, c3; mov.b32 {c0, c1, c2, c3}, %1; cvt.rn.f16x2.e2m1x2 %0, c0; }"
+        : "=r"(h)
+        : "r"(byte));
+    return f16x2_to_f32x2(h);
+}
+
+// The same terms with 8 consecutive elements per lane: lanes 4m .. 4m + 3 hold
+// one 32-element block (lane 4m + r elements 8r .. 8r + 7), so a term's block
+// maximum takes two shuffles and its codes pack into one word per lane
+// (element 8r + i in nibble i).  v is left holding the residual.
+__device__ __forceinline__ void quantize8_terms(float (&v)[8], uint32_t (&w)[kTerms], uint32_t (&sb)[kTerms]) {
+#pragma unroll
+    for (int j = 0; j < kTerms; ++j) {
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = e2m1_scale_exp(m);
+        const float inv = exp2i(-e), sc = exp2i(e);
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const uint32_t byte = e2m1x2_code(v[i] * inv, v[i + 1] * inv);
+            const float2 d = e2m1x2_float(byte);
+            v[i] = fmaf(-d.x, sc, v[i]);
+            v[i + 1] = fmaf(-d.y, sc, v[i + 1]);
+            word |= byte << (4 * i);
+        }
+        w[j] = word;
+        sb[j] = static_cast<uint32_t>(e + 127);
+    }
+}
+
 // B operand layout of the block-scaled MMA (kind::mxf4: packed E2M1, two
 // codes per byte, element 2i in the low nibble), per 256-wide K chunk:
 //   codes : N rows x 128 bytes, row n = kTerms * token + term, stored with the

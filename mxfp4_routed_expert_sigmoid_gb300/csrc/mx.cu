@@ -442,10 +442,12 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-// h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E2M1 terms in
-// the B layout of the down projection.  One warp per (unit, token, 32-block),
-// grid-strided over the active units (the grid is sized for the SMs, not for
-// the largest possible number of units).
+// h = silu(g) * u from slot 0 + slot 1, quantised to kTerms E2M1 terms in the
+// B layout of the down projection.  One warp per (unit, token, 256-wide
+// chunk), grid-strided over the units: lane 4 kb + r takes elements 8 r ..
+// 8 r + 7 of 32-block kb (the grid is sized for the SMs, not for the largest
+// possible number of units).  Tokens a unit does not have are skipped: their
+// MMA columns are never read.
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
                  const int32_t* __restrict__ count, const int32_t* __restrict__ ucnt, uint8_t* __restrict__ hq,
@@ -456,43 +458,37 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     // list they read is final)
     pdl_trigger();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int nb = f / 32;
+    const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
     const int KC = f / 256;
-    const int items = *count * T * nb;
+    const int items = *count * T * KC;
     const size_t plane = static_cast<size_t>(umax) * T * f;
-    const int stride = gridDim.x * 8;
-    // two items per pass: the loads of both are in flight before either is quantised
-    for (int i0 = blockIdx.x * 8 + (threadIdx.x >> 5); i0 < items; i0 += 2 * stride) {
-        float h[2];
-        int uu[2], tt[2], bb[2];
-        bool ok[2];
+    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < items; i += gridDim.x * 8) {
+        const int u = i / (T * KC);
+        const int rr = i - u * T * KC;
+        const int t = rr / KC, c = rr - t * KC;
+        if (ucnt && t >= ucnt[u]) continue;
+        const float* g0 = part + (static_cast<size_t>(u) * T + t) * f + 256 * c + 32 * kb + 8 * r;
+        float a[8], b[8], cc[8], dd[8];
+        *reinterpret_cast<float4*>(a) = *reinterpret_cast<const float4*>(g0);
+        *reinterpret_cast<float4*>(a + 4) = *reinterpret_cast<const float4*>(g0 + 4);
+        *reinterpret_cast<float4*>(b) = *reinterpret_cast<const float4*>(g0 + plane);
+        *reinterpret_cast<float4*>(b + 4) = *reinterpret_cast<const float4*>(g0 + plane + 4);
+        *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(g0 + 2 * plane);
+        *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(g0 + 2 * plane + 4);
+        *reinterpret_cast<float4*>(dd) = *reinterpret_cast<const float4*>(g0 + 3 * plane);
+        *reinterpret_cast<float4*>(dd + 4) = *reinterpret_cast<const float4*>(g0 + 3 * plane + 4);
+        float v[8];
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const int i = i0 + p * stride;
-            const int u = i / (T * nb);
-            const int r = i - u * T * nb;
-            const int t = r / nb, b = r - t * nb;
-            uu[p] = u;
-            tt[p] = t;
-            bb[p] = b;
-            // tokens a unit does not have are skipped: their MMA columns are never read
-            ok[p] = i < items && (!ucnt || t < ucnt[u]);
-            h[p] = 0.0f;
-            if (ok[p]) {
-                const size_t o = (static_cast<size_t>(u) * T + t) * f + 32 * b + lane;
-                const float g = part[o] + part[2 * plane + o];
-                const float up = part[plane + o] + part[3 * plane + o];
-                h[p] = silu_f32(g) * up;
-            }
-        }
+        for (int q = 0; q < 8; ++q) v[q] = silu_f32(a[q] + cc[q]) * (b[q] + dd[q]);
+        uint32_t w[kTerms], sb[kTerms];
+        quantize8_terms(v, w, sb);
+        uint8_t* codes = hq + (static_cast<size_t>(u) * KC + c) * N * 128;
+        uint8_t* scales = hsf + (static_cast<size_t>(u) * KC + c) * 1024;
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            if (!ok[p]) continue;
-            uint32_t q[kTerms], sb[kTerms];
-            quantize_terms(h[p], q, sb);
-            store_terms(q, sb, tt[p], bb[p] & 7, hq + (static_cast<size_t>(uu[p]) * KC + (bb[p] >> 3)) * N * 128,
-                        hsf + (static_cast<size_t>(uu[p]) * KC + (bb[p] >> 3)) * 1024);
+        for (int j = 0; j < kTerms; ++j) {
+            const int n = kTerms * t + j;
+            *reinterpret_cast<uint32_t*>(codes + n * 128 + ((kb ^ (n & 7)) << 4) + 4 * r) = w[j];
+            if (r == 0) scales[(kb >> 2) * 512 + sf_atom_offset(n, kb & 3)] = static_cast<uint8_t>(sb[j]);
         }
     }
 }
@@ -649,26 +645,30 @@ mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
 
 // Token rows as kTerms E2M1 terms, once per token (unswizzled): codes
 // [t][term][K / 2] (element 2i in the low nibble), E8M0 scales [t][term][K / 32].
-// One warp per (token, 32-block), grid-strided.
+// One warp per (token, 256-wide chunk), lane 4 kb + r taking elements 8 r ..
+// 8 r + 7 of 32-block kb; grid-strided.
 __global__ void __launch_bounds__(256)
 mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __restrict__ tq,
                       uint8_t* __restrict__ tsf) {
-    const int lane = threadIdx.x & 31;
-    const int nb = K / 32;
-    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < T * nb; i += gridDim.x * 8) {
-        const int t = i / nb, b = i - t * nb;
-        uint32_t q[kTerms], sb[kTerms];
-        quantize_terms(bf16_to_f32(x[static_cast<size_t>(t) * K + 32 * b + lane]), q, sb);
+    const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
+    const int KC = K / 256, nb = K / 32;
+    for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < T * KC; i += gridDim.x * 8) {
+        const int t = i / KC, c = i - t * KC;
+        const uint4 raw = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * K + 256 * c + 32 * kb + 8 * r);
+        const uint32_t wr[4] = {raw.x, raw.y, raw.z, raw.w};
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[2 * q] = __uint_as_float(wr[q] << 16);
+            v[2 * q + 1] = __uint_as_float(wr[q] & 0xFFFF0000u);
+        }
+        uint32_t w[kTerms], sb[kTerms];
+        quantize8_terms(v, w, sb);
 #pragma unroll
         for (int j = 0; j < kTerms; ++j) {
-            const uint32_t by = q[j] | (__shfl_down_sync(0xffffffffu, q[j], 1) << 4);  // even lanes
-            uint32_t w = by;
-            w |= __shfl_down_sync(0xffffffffu, by, 2) << 8;
-            w |= __shfl_down_sync(0xffffffffu, by, 4) << 16;
-            w |= __shfl_down_sync(0xffffffffu, by, 6) << 24;
             const size_t row = static_cast<size_t>(t) * kTerms + j;
-            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(tq + row * (K / 2) + 16 * b + (lane >> 1)) = w;
-            if (lane == 0) tsf[row * nb + b] = static_cast<uint8_t>(sb[j]);
+            *reinterpret_cast<uint32_t*>(tq + row * (K / 2) + 128 * c + 16 * kb + 4 * r) = w[j];
+            if (r == 0) tsf[row * nb + 8 * c + kb] = static_cast<uint8_t>(sb[j]);
         }
     }
 }
@@ -864,7 +864,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
 
     if ((e = launch_stream(t1, t3, up, grid_up, s, "decode_up"))) return e;
 
-    const int warps = m.umax * a.T * (a.f / 32);
+    const int warps = m.umax * a.T * (a.f / 256);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
     e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
                    m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf);
@@ -956,7 +956,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     trace_mark("units", s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long twarps = static_cast<long long>(a.T) * (a.d / 32);
+    const long long twarps = static_cast<long long>(a.T) * (a.d / 256);
     mx_token_terms_kernel<<<static_cast<int>(std::min<long long>((twarps + 7) / 8, 8LL * a.num_sms)), 256, 0, s>>>(
         a.x, a.T, a.d, m.tq, m.tsf);
     trace_mark("token_terms", s);
@@ -1003,7 +1003,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
     if ((e = launch_stream(t1, t3, up, grid_up, s, "units_up"))) return e;
 
-    const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 32);
+    const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 256);
     const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
     e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
                    kUnitTokens, a.f, m.N, static_cast<const int32_t*>(m.nunits),
