@@ -73,8 +73,9 @@ typedef enum k3moe_act {
  *            experts' E2M1 codes by TMA, E8M0 scales applied by the tensor
  *            cores, activations as E2M1 terms; split over the SMs.  Up to 8
  *            tokens every active expert takes all tokens; beyond that each
- *            expert's tokens are cut into units of at most 12 and an
- *            expert's weights are streamed once per unit.
+ *            expert's tokens are cut into units of at most 16 (four E2M1
+ *            terms per token) and an expert's weights are streamed once per
+ *            unit.
  *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
  *            dequantisation, TMA-fed, TMEM accumulators. */
 typedef enum k3moe_path {

@@ -14,7 +14,7 @@ namespace {
 
 constexpr int kDecodeMaxT = 8;
 // the block-scaled streaming kernels also take up to this many tokens, grouped
-// in units of at most 12 tokens of one expert (beyond it the experts see many
+// in units of at most 16 tokens of one expert (beyond it the experts see many
 // tokens each and the grouped GEMMs are the better fit)
 constexpr int kStreamMaxT = 1024;
 

@@ -224,9 +224,10 @@ __device__ __forceinline__ float2 e2m1x2_float(uint32_t byte) {
 // one 32-element block (lane 4m + r elements 8r .. 8r + 7), so a term's block
 // maximum takes two shuffles and its codes pack into one word per lane
 // (element 8r + i in nibble i).  v is left holding the residual.
-__device__ __forceinline__ void quantize8_terms(float (&v)[8], uint32_t (&w)[kTerms], uint32_t (&sb)[kTerms]) {
+template <int TERMS>
+__device__ __forceinline__ void quantize8_terms(float (&v)[8], uint32_t (&w)[TERMS], uint32_t (&sb)[TERMS]) {
 #pragma unroll
-    for (int j = 0; j < kTerms; ++j) {
+    for (int j = 0; j < TERMS; ++j) {
         float m = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
@@ -383,7 +384,7 @@ void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_
                         int* N);
 cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s);
 // unit-grouped streaming forward (more tokens, few per expert): the experts'
-// sorted token lists (from the permutation) are cut into units of at most 12
+// sorted token lists (from the permutation) are cut into units of at most 16
 // tokens and streamed like the decode path
 struct MxUnitsArgs {
     const uint8_t *w1_q, *w3_q, *w2_q;     // E2M1 codes

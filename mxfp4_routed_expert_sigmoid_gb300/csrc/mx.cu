@@ -189,6 +189,7 @@ struct Cursor {
     }
 };
 
+template <int TERMS>
 __global__ void __launch_bounds__(kMxThreads, 1)
 mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                  MxArgs p) {
@@ -420,11 +421,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                          static_cast<size_t>(c.u) * p.T * p.rows_out + row;
             const int tokens = p.ucnt ? p.ucnt[c.u] : p.T;
 #pragma unroll
-            for (int t = 0; t < kMaxN / kTerms; ++t) {
+            for (int t = 0; t < kMaxN / TERMS; ++t) {
                 if (t >= tokens) break;
                 float sum = 0.0f;
 #pragma unroll
-                for (int j = 0; j < kTerms; ++j) sum += v[kTerms * t + j];
+                for (int j = 0; j < TERMS; ++j) sum += v[TERMS * t + j];
                 dst[static_cast<size_t>(t) * p.rows_out] = sum;
                 if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
             }
@@ -448,6 +449,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // 8 r + 7 of 32-block kb (the grid is sized for the SMs, not for the largest
 // possible number of units).  Tokens a unit does not have are skipped: their
 // MMA columns are never read.
+template <int TERMS>
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
                  const int32_t* __restrict__ count, const int32_t* __restrict__ ucnt, uint8_t* __restrict__ hq,
@@ -480,13 +482,13 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
         float v[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = silu_f32(a[q] + cc[q]) * (b[q] + dd[q]);
-        uint32_t w[kTerms], sb[kTerms];
-        quantize8_terms(v, w, sb);
+        uint32_t w[TERMS], sb[TERMS];
+        quantize8_terms<TERMS>(v, w, sb);
         uint8_t* codes = hq + (static_cast<size_t>(u) * KC + c) * N * 128;
         uint8_t* scales = hsf + (static_cast<size_t>(u) * KC + c) * 1024;
 #pragma unroll
-        for (int j = 0; j < kTerms; ++j) {
-            const int n = kTerms * t + j;
+        for (int j = 0; j < TERMS; ++j) {
+            const int n = TERMS * t + j;
             *reinterpret_cast<uint32_t*>(codes + n * 128 + ((kb ^ (n & 7)) << 4) + 4 * r) = w[j];
             if (r == 0) scales[(kb >> 2) * 512 + sf_atom_offset(n, kb & 3)] = static_cast<uint8_t>(sb[j]);
         }
@@ -586,7 +588,11 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
 // unit's own token rows as the B operand.  An expert's weights are read once
 // per unit.
 // ---------------------------------------------------------------------------
-constexpr int kUnitTokens = kMaxN / kTerms;  // 12: kTerms rows per token within N = 64
+// Units take four E2M1 terms per token (16 tokens within N = 64; an expert's
+// output within about 1.1e-3 of its RMS instead of 1.2e-4 with five), so that
+// most experts need a single unit at a few hundred tokens.
+constexpr int kUnitTerms = 4;
+constexpr int kUnitTokens = kMaxN / kUnitTerms;  // 16
 
 // Unit list and the expert-output row of every (token, slot) pair.  One CTA of
 // 1024 threads (E <= 1024): units of expert e are ubase[e] .. ubase[e + 1) - 1.
@@ -643,7 +649,7 @@ mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
     }
 }
 
-// Token rows as kTerms E2M1 terms, once per token (unswizzled): codes
+// Token rows as kUnitTerms E2M1 terms, once per token (unswizzled): codes
 // [t][term][K / 2] (element 2i in the low nibble), E8M0 scales [t][term][K / 32].
 // One warp per (token, 256-wide chunk), lane 4 kb + r taking elements 8 r ..
 // 8 r + 7 of 32-block kb; grid-strided.
@@ -662,11 +668,11 @@ mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __r
             v[2 * q] = __uint_as_float(wr[q] << 16);
             v[2 * q + 1] = __uint_as_float(wr[q] & 0xFFFF0000u);
         }
-        uint32_t w[kTerms], sb[kTerms];
-        quantize8_terms(v, w, sb);
+        uint32_t w[kUnitTerms], sb[kUnitTerms];
+        quantize8_terms<kUnitTerms>(v, w, sb);
 #pragma unroll
-        for (int j = 0; j < kTerms; ++j) {
-            const size_t row = static_cast<size_t>(t) * kTerms + j;
+        for (int j = 0; j < kUnitTerms; ++j) {
+            const size_t row = static_cast<size_t>(t) * kUnitTerms + j;
             *reinterpret_cast<uint32_t*>(tq + row * (K / 2) + 128 * c + 16 * kb + 4 * r) = w[j];
             if (r == 0) tsf[row * nb + 8 * c + kb] = static_cast<uint8_t>(sb[j]);
         }
@@ -683,19 +689,19 @@ mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__
                      const int32_t* __restrict__ unit_row0, const int32_t* __restrict__ unit_cnt,
                      uint8_t* __restrict__ bq, uint8_t* __restrict__ bsf) {
     const int nb = K / 32, KC = K / 256;
-    const int per_unit = kUnitTokens * kTerms * nb;
+    const int per_unit = kUnitTokens * kUnitTerms * nb;
     const long long items = static_cast<long long>(*nunits) * per_unit;
     for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < items;
          it += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int u = static_cast<int>(it / per_unit);
         int r = static_cast<int>(it - static_cast<long long>(u) * per_unit);
-        const int i = r / (kTerms * nb);
-        r -= i * kTerms * nb;
+        const int i = r / (kUnitTerms * nb);
+        r -= i * kUnitTerms * nb;
         const int j = r / nb, b = r - j * nb;
         if (i >= unit_cnt[u]) continue;
         const int tok = perm[unit_row0[u] + i] / k;
-        const size_t src = static_cast<size_t>(tok) * kTerms + j;
-        const int n = kTerms * i + j, c = b >> 3, g = b & 7;
+        const size_t src = static_cast<size_t>(tok) * kUnitTerms + j;
+        const int n = kUnitTerms * i + j, c = b >> 3, g = b & 7;
         const size_t cb = static_cast<size_t>(u) * KC + c;
         *reinterpret_cast<uint4*>(bq + cb * N * 128 + n * 128 + ((g ^ (n & 7)) << 4)) =
             *reinterpret_cast<const uint4*>(tq + src * (K / 2) + 16 * b);
@@ -745,7 +751,7 @@ cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t
 // ---------------------------------------------------------------------------
 namespace {
 
-int mx_n(int T) { return (kTerms * T + 15) / 16 * 16; }
+int mx_n(int T, int terms = kTerms) { return (terms * T + 15) / 16 * 16; }
 
 struct MxScratch {
     uint8_t *xq, *xsf, *hq, *hsf;
@@ -773,6 +779,7 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
     return m;
 }
 
+template <int TERMS>
 cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p, int grid, cudaStream_t s,
                           const char* name) {
     p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 2048), 1024));
@@ -787,13 +794,13 @@ cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p,
     cudaGetDevice(&dev);
     std::atomic<int>& cur = set_bytes[dev & 63];
     if (cur.load() < static_cast<int>(smem)) {
-        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel,
+        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel<TERMS>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cur.store(static_cast<int>(smem));
     }
-    const cudaError_t e = launch_pdl(mx_stream_kernel, dim3(grid), dim3(kMxThreads), smem, s, a, a3, p);
+    const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS>, dim3(grid), dim3(kMxThreads), smem, s, a, a3, p);
     trace_mark(name, s);
     return e;
 }
@@ -862,11 +869,11 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
 
-    if ((e = launch_stream(t1, t3, up, grid_up, s, "decode_up"))) return e;
+    if ((e = launch_stream<kTerms>(t1, t3, up, grid_up, s, "decode_up"))) return e;
 
     const int warps = m.umax * a.T * (a.f / 256);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
-    e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
+    e = launch_pdl(mx_finish_kernel<kTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
                    m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf);
     trace_mark("decode_finish_up", s);
     if (e != cudaSuccess) return e;
@@ -887,7 +894,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     dn.part = m.y;
     dn.rows_out = a.d;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream(t2, t2, dn, grid_dn, s, "decode_down"))) return e;
+    if ((e = launch_stream<kTerms>(t2, t2, dn, grid_dn, s, "decode_down"))) return e;
 
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
@@ -914,7 +921,7 @@ MxUnitScratch mx_units_carve(void* scratch, int T, int E, int k, int d, int f) {
     MxUnitScratch m{};
     const long long P = static_cast<long long>(T) * k;
     m.umax = static_cast<int>(std::min<long long>(P, (P + static_cast<long long>(E) * (kUnitTokens - 1)) / kUnitTokens));
-    m.N = mx_n(kUnitTokens);
+    m.N = mx_n(kUnitTokens, kUnitTerms);
     char* b = static_cast<char*>(scratch);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -929,8 +936,8 @@ MxUnitScratch mx_units_carve(void* scratch, int T, int E, int k, int d, int f) {
     m.nunits = reinterpret_cast<int32_t*>(take(4));
     m.ubase = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E + 1) * 4));
     m.rowmap = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P) * 4));
-    m.tq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 2)));
-    m.tsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kTerms * (d / 32)));
+    m.tq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kUnitTerms * (d / 2)));
+    m.tsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kUnitTerms * (d / 32)));
     m.xq = reinterpret_cast<uint8_t*>(take(U * (d / 256) * m.N * 128));
     m.xsf = reinterpret_cast<uint8_t*>(take(U * (d / 128) * 512));
     m.up = reinterpret_cast<float*>(take(4 * U * kUnitTokens * f * 4));
@@ -961,7 +968,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
         a.x, a.T, a.d, m.tq, m.tsf);
     trace_mark("token_terms", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long long citems = static_cast<long long>(m.umax) * kUnitTokens * kTerms * (a.d / 32);
+    const long long citems = static_cast<long long>(m.umax) * kUnitTokens * kUnitTerms * (a.d / 32);
     mx_unit_terms_kernel<<<static_cast<int>(std::min<long long>((citems + 255) / 256, 8LL * a.num_sms)), 256, 0,
                            s>>>(m.tq, m.tsf, a.perm, a.k, a.d, m.N, m.nunits, m.unit_row0, m.unit_cnt, m.xq, m.xsf);
     trace_mark("unit_terms", s);
@@ -1001,11 +1008,11 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     up.hdr = a.hdr;
     // every CTA's range must be at least one tile long: there are at least k units
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
-    if ((e = launch_stream(t1, t3, up, grid_up, s, "units_up"))) return e;
+    if ((e = launch_stream<kUnitTerms>(t1, t3, up, grid_up, s, "units_up"))) return e;
 
     const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 256);
     const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
-    e = launch_pdl(mx_finish_kernel, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
+    e = launch_pdl(mx_finish_kernel<kUnitTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
                    kUnitTokens, a.f, m.N, static_cast<const int32_t*>(m.nunits),
                    static_cast<const int32_t*>(m.unit_cnt), m.hq, m.hsf);
     trace_mark("units_finish_up", s);
@@ -1027,7 +1034,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     dn.part = m.y;
     dn.rows_out = a.d;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream(t2, t2, dn, grid_dn, s, "units_down"))) return e;
+    if ((e = launch_stream<kUnitTerms>(t2, t2, dn, grid_dn, s, "units_down"))) return e;
 
     // the y slots are strided by units x kUnitTokens rows; the grid's y index is the token
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);

@@ -82,7 +82,7 @@ def test_tiny_grouped(k3, T):
 @pytest.mark.parametrize("T", [9, 33])
 def test_tiny_units(k3, T):
     """More than 8 tokens on the block-scaled streaming kernels (units of at
-    most 12 tokens of one expert)."""
+    most 16 tokens of one expert)."""
     compare_forward(k3, synth.custom("tiny", T=T, **TINY), 1)
 
 
