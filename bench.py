@@ -38,8 +38,14 @@ EXPERT_MATRIX_BYTES = None  # filled per config
 
 
 # DRAM bytes (read + write) per launch of a kernel from an ncu capture of the
-# current kernel version (profiles/), by (workload, kernel); absent: not captured
-TRAFFIC = {}
+# current kernel version, by (workload, kernel); absent: not captured.  The
+# decode capture (profiles/mx_stream_kernel_decode_e128.md) ran a 128-expert
+# copy of the layer: one token touches 16 experts either way, so a launch moves
+# the same bytes as in the 896-expert layer.
+TRAFFIC = {
+    ("decode_t1", "decode_up"): 187_272_192 + 3_737_856,
+    ("decode_t1", "decode_down"): 94_225_920 + 2_310_400,
+}
 
 
 def parse():
