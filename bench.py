@@ -480,7 +480,8 @@ def dtype_of(T: int, path: int) -> str:
     """Arithmetic of the expert path the layer takes for T tokens."""
     decode = path == 1 or (path == 0 and T <= 1024)
     if decode:
-        return ("e2m1 x e2m1 block-scaled tensor-core MMA (activations as five E2M1 terms), "
+        terms = 4 if T > 8 else 5
+        return (f"e2m1 x e2m1 block-scaled tensor-core MMA (activations as {terms} E2M1 terms), "
                 "fp32 accumulation")
     return "f16 x f16 tensor-core MMA (E2M1 weights dequantised exactly), fp32 accumulation"
 
