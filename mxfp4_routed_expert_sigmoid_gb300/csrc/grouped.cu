@@ -259,14 +259,18 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // ---------------------------------------------------------------------------
 template <int NA>
 struct ExpCfg;
-// RS: raw-weight stages, AS: dequantised A stages, BS: token (B) stages
+// RS: raw-weight stages, AS: dequantised A stages, BS: token (B) stages,
+// NBUF: accumulator buffers in TMEM.  The down projection takes 256 token rows
+// per tile (each MMA, M = 128, N = 256, K = 16, then outlasts its issue cost);
+// the up projection keeps 128 so that its two accumulators (W1, W3) stay
+// double-buffered (with 256 and one buffer it measured 35 % slower).
 template <>
 struct ExpCfg<2> {
-    static constexpr int BN = 128, RS = 8, AS = 2, BS = 4, TMEM_COLS = 512;
+    static constexpr int BN = 128, RS = 8, AS = 2, BS = 4, NBUF = 2, TMEM_COLS = 512;
 };
 template <>
 struct ExpCfg<1> {
-    static constexpr int BN = 128, RS = 8, AS = 4, BS = 4, TMEM_COLS = 256;
+    static constexpr int BN = 256, RS = 8, AS = 4, BS = 3, NBUF = 2, TMEM_COLS = 512;
 };
 constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
 constexpr int kBoxRows = 16;    // token rows per TMA box
@@ -416,8 +420,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int it = 0;
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
                 const int4 tl = p.tiles[1 + tile];
-                const int acc = it & 1;
-                const uint32_t acc_ph = (it >> 1) & 1;
+                const int acc = C::NBUF == 2 ? (it & 1) : 0;
+                const uint32_t acc_ph = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 const int n_mma = ((tl.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
                 const uint32_t idesc = idesc_f16(0, BM, n_mma);
                 if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort_flag, p.hdr, 52)) break;
@@ -479,8 +483,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         int it = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
             const int4 tl = p.tiles[1 + tile];
-            const int acc = it & 1;
-            const uint32_t acc_ph = (it >> 1) & 1;
+            const int acc = C::NBUF == 2 ? (it & 1) : 0;
+            const uint32_t acc_ph = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
             const int slot = it % kES;
             const uint32_t eph = (it / kES) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_ph, abort_flag, p.hdr, 56) &&
@@ -679,30 +683,26 @@ convert_h_kernel(const float* __restrict__ hf, const uint32_t* __restrict__ h_am
 // (expert, first row, rows, m tile).
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
-                   int bn, int m_up, int m_dn, int4* up, int4* dn, int cap) {
+                   int bn_up, int bn_dn, int m_up, int m_dn, int4* up, int4* dn, int cap) {
     __shared__ int base[1024 + 1];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = (counts[e] + bn - 1) / bn;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int e = 0; e < E; ++e) {
-            const int c = base[e];
-            base[e] = run;
-            run += c;
-        }
-        base[E] = run;
-    }
-    __syncthreads();
-    const int U = base[E];
-    const int n_up = min(U * m_up, cap), n_dn = min(U * m_dn, cap);
-    if (threadIdx.x == 0) {
-        up[0] = make_int4(n_up, 0, 0, 0);
-        dn[0] = make_int4(n_dn, 0, 0, 0);
-    }
     for (int pass = 0; pass < 2; ++pass) {
+        const int bn = pass == 0 ? bn_up : bn_dn;
+        for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = (counts[e] + bn - 1) / bn;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int e = 0; e < E; ++e) {
+                const int c = base[e];
+                base[e] = run;
+                run += c;
+            }
+            base[E] = run;
+        }
+        __syncthreads();
         const int mt_n = pass == 0 ? m_up : m_dn;
-        const int n = pass == 0 ? n_up : n_dn;
+        const int n = min(base[E] * mt_n, cap);
         int4* list = pass == 0 ? up : dn;
+        if (threadIdx.x == 0) list[0] = make_int4(n, 0, 0, 0);
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             // expert of entry i: largest e with base[e] * mt_n <= i
             int lo = 0, hi = E - 1;
@@ -717,6 +717,7 @@ build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
             const int cnt = counts[e];
             list[1 + i] = make_int4(e, offsets[e] + c * bn, min(bn, cnt - c * bn), mt);
         }
+        __syncthreads();  // base[] is rebuilt for the next pass
     }
 }
 
@@ -743,7 +744,9 @@ cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const Dense
     return cudaGetLastError();
 }
 
-constexpr int kUnitRows = 128;  // == ExpCfg<1>::BN == ExpCfg<2>::BN
+// token rows per tile of the up (W1, W3) and down (W2) passes
+constexpr int kUpRows = ExpCfg<2>::BN, kDownRows = ExpCfg<1>::BN;
+constexpr int kUnitRows = kUpRows < kDownRows ? kUpRows : kDownRows;  // bounds the tile count
 
 template <int NA>
 cudaError_t launch_expert(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
@@ -806,7 +809,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     cudaError_t e;
     gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.x, g.perm, P, g.k, g.d, g.xp, g.xp_exp, g.h_amax);
     trace_mark("gather_rows", s);
-    build_tiles_kernel<<<1, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUnitRows, (g.f + BM - 1) / BM,
+    build_tiles_kernel<<<1, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUpRows, kDownRows, (g.f + BM - 1) / BM,
                                           (g.d + BM - 1) / BM, tiles_up, tiles_dn, cap);
     trace_mark("build_tiles", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
