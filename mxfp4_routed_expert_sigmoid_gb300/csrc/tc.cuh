@@ -152,19 +152,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-// Hints that pull a tensor box or a byte range into L2 ahead of its load
-// (no completion to track).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tm)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
-
 // Shared-memory descriptor without swizzle: 8-row x 16-byte core matrices,
 // rows 16 bytes apart, 8-row groups sbo bytes apart (source of tcgen05.cp).
 __device__ __forceinline__ uint64_t plain_desc(uint32_t saddr, uint32_t sbo) {
@@ -183,41 +170,7 @@ __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint32_t saddr) {
                  "l"(plain_desc(saddr, 128)));
 }
 
-// Instruction descriptor, kind::mxf8f6f4 with E8M0 block scales: A = E2M1
-// (format 5), B = E4M3 (format 0), fp32 accumulator implied, K-major, M x N;
-// sa / sb select the scale byte (K block of 32 within the 4-block group).
-__device__ __forceinline__ uint32_t idesc_mx(int M, int N, int sa, int sb) {
-    return (static_cast<uint32_t>(sb) << 4) | (5u << 7) | (0u << 10) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sa) << 29);
-}
 
-// D (+)= (A * sfA) (B * sfB), one K = 32 slice; scale factors in TMEM
-__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4],"
-        " [%5], p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t cols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
