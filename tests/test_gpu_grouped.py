@@ -86,6 +86,23 @@ def test_tiny_units(k3, T):
     compare_forward(k3, synth.custom("tiny", T=T, **TINY), 1)
 
 
+@pytest.mark.parametrize("T,path", [(1024, 1), (1025, 0)])
+def test_units_limit(k3, T, path):
+    """The largest batch the streaming kernels take (T = 1024; up to 128 tokens
+    per expert, eight units of 16) and the first one AUTO sends to the grouped
+    GEMMs (T = 1025); 6 seeded token rows checked."""
+    cfg = synth.custom("decode_t1", T=T, E=64, k=8, d=768, f=1280, seed_index=26)
+    rng = np.random.default_rng(T)
+    compare_forward(k3, cfg, path, tokens=np.sort(rng.choice(T, 6, replace=False)))
+
+
+@pytest.mark.parametrize("T", [4, 20])
+def test_every_expert_selected(k3, T):
+    """k = E: every expert takes every token (the dense gated MLP special case),
+    through the decode path (T = 4) and the units (T = 20, two units per expert)."""
+    compare_forward(k3, synth.custom("tiny", T=T, k=8, **TINY), 1)
+
+
 @pytest.mark.parametrize("T", [40, 300])
 def test_mid_units(k3, T):
     # experts with 1..60 tokens: several units per expert, ragged last units
