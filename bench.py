@@ -63,6 +63,9 @@ def parse():
                     help="fewer resident experts (small profiling captures only; not a bench line)")
     ap.add_argument("--T", type=int, default=0,
                     help="other token count (small profiling captures only; not a bench line)")
+    ap.add_argument("--cache-slots", type=int, default=0,
+                    help="host-resident experts behind a device cache of this many experts "
+                         "(k3moe_forward_cached); 0 = experts resident in HBM")
     return ap.parse_args()
 
 
@@ -476,6 +479,146 @@ def ours_arm(args):
         dist.destroy_process_group()
 
 
+def cached_arm(args):
+    """The layer with its experts in pinned host memory behind a device cache
+    of ``--cache-slots`` experts (k3moe_forward_cached): every step routes,
+    fetches the missing experts over the host link (NVLink-C2C on GB300) and
+    runs the expert kernels on the cache slots."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mxfp4_routed_expert_sigmoid_gb300 as k3
+
+    cfg = bench_config(args)
+    dense = synth.dense_inputs(cfg)
+
+    def dv(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    layer = k3.MoELayer(router_w=dv(dense["router_w"]), router_b=dv(dense["router_b"]), k=cfg.k,
+                        path=args.path, **synth.experts_torch(cfg, dev))
+    hlayer = k3.host_resident(layer)
+    del layer
+    torch.cuda.empty_cache()
+    S = args.cache_slots
+    cache = k3.ExpertCache(hlayer, S)
+    pool_np = token_pool(cfg, args.pool)
+    pool = [dv(pool_np[i]) for i in range(args.pool)]
+    ws = k3.workspace(k3.k3moe_workspace_size(hlayer, cfg.T), dev)
+    out = torch.empty_like(pool[0])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # link bandwidth for the roofline: copy-engine transfers of 2 GiB from the
+    # pinned expert buffer (host -> device), best of 3
+    nb = min(2 << 30, hlayer.host_buffer.numel())
+    dst = torch.empty(nb, dtype=torch.uint8, device=dev)
+    h2d = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(hlayer.host_buffer[:nb], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        h2d.append(nb / (a.elapsed_time(b) * 1e-3) / 1e9)
+    link_gbs = max(h2d)
+    del dst
+
+    # one pass over the pool fills the cache; graphs per batch (each
+    # set-up forward is a call of the cache too)
+    for i in range(args.pool):
+        k3.k3moe_forward_cached(hlayer, cache, pool[i], out=out, ws=ws)
+    graphs = [k3.ForwardGraph(hlayer, pool[i], out, ws, cache=cache) for i in range(args.pool)]
+    for i in range(max(args.warmup, 3)):
+        graphs[i % args.pool].launch(stream)
+    if k3.k3moe_get_status(ws) != 0:
+        raise RuntimeError("device status error during setup")
+    before = cache.stats()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with Clocks(0) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            graphs[(args.warmup + i) % args.pool].launch(stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    after = cache.stats()
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    value = job_tokens_per_s(cfg.T, args.steps, 1, total_ms)
+    calls = after["calls"] - before["calls"]
+    hits, misses = after["hits"] - before["hits"], after["misses"] - before["misses"]
+    fetched = (after["bytes"] - before["bytes"]) / max(calls, 1)
+
+    # per-kernel durations: traced direct launches over the same batches
+    k3.k3moe_trace(True)
+    per_kernel, launches = {}, 0
+    for i in range(args.steps):
+        flush.zero_()
+        k3.k3moe_forward_cached(hlayer, cache, pool[(args.warmup + i) % args.pool], out=out, ws=ws)
+        tr = k3.k3moe_trace_read()
+        launches = max(launches, len(tr))
+        for name, ms in tr:
+            per_kernel.setdefault(name, []).append(ms)
+    k3.k3moe_trace(False)
+    kern_mean = {n: sum(v) / len(v) for n, v in per_kernel.items()}
+    traced = cache.stats()
+    fill_bytes = (traced["bytes"] - after["bytes"]) / max(traced["calls"] - after["calls"], 1)
+
+    # end to end: pinned host input -> device, cached forward, result -> host
+    pool_host = [torch.from_numpy(pool_np[i].view(np.int16)).view(torch.bfloat16).pin_memory()
+                 for i in range(args.pool)]
+    out_host = torch.empty_like(pool_host[0]).pin_memory()
+    x_dev = torch.empty_like(pool[0])
+    e2e_s = 0.0
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        x_dev.copy_(pool_host[(args.warmup + i) % args.pool], non_blocking=True)
+        k3.k3moe_forward_cached(hlayer, cache, x_dev, out=out, ws=ws)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s += time.perf_counter() - t0
+
+    fill_ms = kern_mean.get("cache_fill", 0.0)
+    fill_gbs = fill_bytes / (fill_ms * 1e-3) / 1e9 if fill_ms > 0 else None
+    mb = matrix_bytes(cfg)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype_of(cfg.T, args.path),
+        "data": "synthetic (seeded; random-init weights of the K3 layer shapes)",
+        "config": dict(workload_config(cfg, args.pool), workload=cfg.name + "_host_experts",
+                       expert_bytes_resident=0, expert_bytes_host=3 * cfg.E * mb,
+                       cache_slots=S, cache_bytes=3 * S * mb),
+        "cache": {"hit_rate": hits / max(hits + misses, 1), "hits_per_step": hits / max(calls, 1),
+                  "misses_per_step": misses / max(calls, 1), "fetched_bytes_per_step": fetched},
+        "kernels_ms": kern_mean,
+        "kernels_ms_source": "direct launches (host launch gaps included)",
+        "roofline": {"kernel": "cache_fill", "bound": "c2c", "achieved": fill_gbs,
+                     "peak": link_gbs, "unit": "GB/s",
+                     "peak_source": "measured in this run: pinned host -> device copy-engine "
+                                    "transfer of 2 GiB",
+                     "frac": (fill_gbs / link_gbs) if fill_gbs else None, "traffic": None,
+                     "algorithmic_bytes_per_launch": fill_bytes, "avg_launch_ms": fill_ms},
+        "e2e": {"value": cfg.T * args.steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def dtype_of(T: int, path: int) -> str:
     """Arithmetic of the expert path the layer takes for T tokens."""
     decode = path == 1 or (path == 0 and T <= 1024)
@@ -490,6 +633,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         reference_arm(args)
+    elif args.cache_slots > 0:
+        cached_arm(args)
     else:
         ours_arm(args)
 

@@ -14,7 +14,10 @@
  *       17-byte block and the repack.
  *   [PR573]   Lucebox PR #573 "feat(kimi-k3): add DSpark Q8 artifact and shared
  *       speculative runtime", section "DSpark acceptance-contract
- *       correction": RMS epsilon 1e-5.
+ *       correction": RMS epsilon 1e-5; section "Runtime validation": SSD-routed
+ *       experts behind an 8 GiB device expert cache.
+ *   [K3-Stuff] the K3-Stuff model page, "llama-cpp-patches", change 2: the page
+ *       cache as the hot-expert cache (lazy fault-in, LRU eviction).
  *
  * Conventions for every entry point:
  *   - Every pointer argument is DEVICE memory owned by the caller unless the
@@ -46,7 +49,7 @@
 extern "C" {
 #endif
 
-#define K3MOE_ABI_VERSION 2
+#define K3MOE_ABI_VERSION 3
 
 typedef enum k3moe_status {
     K3MOE_OK = 0,
@@ -291,6 +294,87 @@ k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hi
                                 uint16_t* out, void* ws, size_t ws_bytes, void** graph_out);
 k3moe_status k3moe_graph_launch(void* graph, void* stream);
 k3moe_status k3moe_graph_destroy(void* graph);
+
+/* Host-resident experts behind a device expert cache.
+ *
+ * [K3-Stuff] (the K3-Stuff model page, "llama-cpp-patches", change 2) runs
+ * the model with its experts outside device memory: the page cache is the
+ * hot-expert cache, filled lazily and evicted least recently used; [PR573]
+ * ("Runtime validation") does the same with an 8 GiB device expert cache and
+ * batched verification routed per batch.  Here the six expert arrays of the
+ * layer stay in HOST memory and `slots` experts at a time live in device
+ * memory.  Each k3moe_forward_cached call, after routing, refreshes the
+ * stamps of the used experts that are resident (hits), gives each missing
+ * expert the least recently used slot that the call does not use (never-used
+ * slots first; equal stamps: lower slot first; the i-th missing expert in
+ * ascending index takes the i-th victim in ascending slot order), copies the
+ * missing experts' codes and scale atoms from host memory into their slots on
+ * the device (every SM reads the host arrays directly; on GB300 over
+ * NVLink-C2C), and then runs the expert kernels on the slots.  Every token of
+ * the call shares the fetch: an expert is fetched at most once per call (the
+ * union of the call's selections, as in a batch of draft tokens).  The result
+ * is bitwise the result of k3moe_forward on device-resident weights.
+ *
+ * All cache pointers are device memory owned by the caller:
+ *   w1_q  [slots, f, d/2]   w3_q [slots, f, d/2]   w2_q [slots, d, f/2]
+ *         (32-byte aligned)
+ *   w1_sf, w3_sf, w2_sf     prepared scale atoms, slots * f * d/32 bytes each
+ *   state                   bookkeeping, k3moe_cache_state_size(E, slots)
+ *                           bytes, set up by k3moe_cache_init before first use
+ * min(E, T*k) <= slots <= E for every call (K3MOE_ERR_SHAPE otherwise). */
+typedef struct k3moe_expert_cache {
+    int32_t slots;      /* experts the device holds at a time */
+    int32_t reserved;   /* must be 0 */
+    uint8_t* w1_q;
+    uint8_t* w3_q;
+    uint8_t* w2_q;
+    uint8_t* w1_sf;
+    uint8_t* w3_sf;
+    uint8_t* w2_sf;
+    void* state;
+} k3moe_expert_cache;
+
+/* Device bytes of the cache bookkeeping (a 256-byte header, the expert ->
+ * slot map and per-slot arrays); 0 for non-positive sizes. */
+size_t k3moe_cache_state_size(int32_t E, int32_t slots);
+
+/* Marks every slot empty and clears the counters (on `stream`).
+ * Errors: INVALID_ARG, SHAPE (slots > E or E > 1024), ALIGN, CUDA. */
+k3moe_status k3moe_cache_init(void* state, int32_t E, int32_t slots, void* stream);
+
+/* k3moe_forward with the expert weights in host memory.  desc->w1_q ...
+ * desc->w2_sf point to HOST arrays in the layouts k3moe_forward takes
+ * (codes, and the prepared scale atoms; k3moe_prepare_scales may write them
+ * through the mapped pointer), page-locked and mapped into the device
+ * address space (cudaHostAlloc, or cudaHostRegister with mapping); every
+ * other pointer is device memory.  The DECODE path only (T <= 1024).  The
+ * call keeps the cache state between calls; calls sharing a cache must be
+ * ordered on one stream.  Errors: those of k3moe_forward; INVALID_ARG (null
+ * host array, or one that is not page-locked host memory by
+ * cudaPointerGetAttributes, e.g. a device array; reserved != 0), SHAPE
+ * (slots), UNSUPPORTED (the
+ * GROUPED path); device: INVALID_ARG if the state was not initialised for
+ * (E, slots). */
+k3moe_status k3moe_forward_cached(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                                  const uint16_t* hidden, int32_t T, uint16_t* out, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* Counters of a cache since k3moe_cache_init: calls, expert hits and misses
+ * (a used expert counts once per call), bytes fetched from host memory, and
+ * the hits and misses of the last call.  Synchronises `stream`.
+ * Errors: INVALID_ARG (null, state not initialised), CUDA. */
+typedef struct k3moe_cache_stats {
+    uint64_t calls, hits, misses, bytes;
+    int32_t last_hits, last_misses;
+} k3moe_cache_stats;
+k3moe_status k3moe_cache_read_stats(const void* state, void* stream, k3moe_cache_stats* out);
+
+/* k3moe_graph_create for k3moe_forward_cached: every replay routes, updates
+ * the cache and fetches what is missing, like an eager call.  The set-up
+ * forward counts as a call of the cache (the capture itself runs nothing). */
+k3moe_status k3moe_graph_create_cached(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                                       const uint16_t* hidden, int32_t T, uint16_t* out, void* ws,
+                                       size_t ws_bytes, void** graph_out);
 
 /* Copy the routing of the last k3moe_forward that used `ws` (device to
  * device, on `stream`): idx_out [T, k] int32, w_out [T, k] fp32, logits_out

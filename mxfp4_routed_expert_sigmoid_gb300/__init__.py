@@ -40,6 +40,8 @@ EXPORTS = (
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
     "k3moe_trace_read", "k3moe_prepare_scales", "k3moe_unprepare_scales",
+    "k3moe_cache_state_size", "k3moe_cache_init", "k3moe_forward_cached",
+    "k3moe_cache_read_stats", "k3moe_graph_create_cached",
 )
 
 
@@ -60,6 +62,24 @@ class LayerDesc(ctypes.Structure):
         ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
         ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
         ("norm_gamma", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+    ]
+
+
+class CacheDesc(ctypes.Structure):
+    """Mirror of ``k3moe_expert_cache``."""
+    _fields_ = [
+        ("slots", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("w1_q", ctypes.c_void_p), ("w3_q", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
+        ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
+        ("state", ctypes.c_void_p),
+    ]
+
+
+class CacheStats(ctypes.Structure):
+    """Mirror of ``k3moe_cache_stats``."""
+    _fields_ = [
+        ("calls", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
+        ("bytes", ctypes.c_uint64), ("last_hits", ctypes.c_int32), ("last_misses", ctypes.c_int32),
     ]
 
 
@@ -103,6 +123,14 @@ def lib() -> ctypes.CDLL:
         "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                               ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
         "k3moe_prepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
+        "k3moe_cache_state_size": ([i32, i32], sz),
+        "k3moe_cache_init": ([vp, i32, i32, vp], ctypes.c_int),
+        "k3moe_forward_cached": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(CacheDesc), vp, i32,
+                                  vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_cache_read_stats": ([vp, vp, ctypes.POINTER(CacheStats)], ctypes.c_int),
+        "k3moe_graph_create_cached": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(CacheDesc), vp,
+                                       i32, vp, vp, sz, ctypes.POINTER(ctypes.c_void_p)],
+                                      ctypes.c_int),
         "k3moe_unprepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
@@ -375,15 +403,121 @@ def k3moe_trace_read(max_entries: int = 32):
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
-class ForwardGraph:
-    """A CUDA graph of one k3moe_forward with fixed buffers (k3moe_graph_create)."""
+EXPERT_ARRAYS = ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf")
 
-    def __init__(self, layer: MoELayer, hidden, out, ws):
+
+def host_resident(layer: MoELayer) -> MoELayer:
+    """A copy of ``layer`` whose six expert arrays (codes and prepared scale
+    atoms) live in one page-locked host buffer, for k3moe_forward_cached.  The
+    router and block-mode tensors stay shared with ``layer``; the device
+    expert arrays are referenced only by ``layer`` (drop it to free them)."""
+    align = 256
+    offs, total = [], 0
+    for n in EXPERT_ARRAYS:
+        offs.append(total)
+        total += (layer.tensors[n].numel() + align - 1) // align * align
+    buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    other = object.__new__(MoELayer)
+    other.__dict__.update(layer.__dict__)
+    other.tensors = dict(layer.tensors)
+    desc = LayerDesc.from_buffer_copy(layer.desc)
+    for n, off in zip(EXPERT_ARRAYS, offs):
+        src = layer.tensors[n]
+        view = buf[off:off + src.numel()].view(src.shape)
+        view.copy_(src)
+        other.tensors[n] = view
+        setattr(desc, n, view.data_ptr())
+    other.desc = desc
+    other.host_buffer = buf
+    return other
+
+
+class ExpertCache:
+    """Device slots and bookkeeping of a ``k3moe_expert_cache`` (initialised
+    here with k3moe_cache_init on the current stream)."""
+
+    def __init__(self, layer: MoELayer, slots: int, device=None, stream=None):
+        dev = device or "cuda"
+        E, d, f = layer.E, layer.d, layer.f
+        u8 = torch.uint8
+        self.tensors = dict(
+            w1_q=torch.empty((slots, f, d // 2), dtype=u8, device=dev),
+            w3_q=torch.empty((slots, f, d // 2), dtype=u8, device=dev),
+            w2_q=torch.empty((slots, d, f // 2), dtype=u8, device=dev),
+            w1_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
+            w3_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
+            w2_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
+            state=torch.zeros(max(int(lib().k3moe_cache_state_size(E, slots)), 256), dtype=u8,
+                              device=dev),
+        )
+        desc = CacheDesc()
+        desc.slots, desc.reserved = slots, 0
+        for name, t in self.tensors.items():
+            setattr(desc, name, t.data_ptr())
+        self.desc = desc
+        self.E, self.slots = E, slots
+        _check(lib().k3moe_cache_init(_p(self.tensors["state"]), E, slots, _stream(stream)))
+
+    def reset(self, stream=None):
+        _check(lib().k3moe_cache_init(_p(self.tensors["state"]), self.E, self.slots,
+                                      _stream(stream)))
+
+    def stats(self, stream=None) -> dict:
+        """k3moe_cache_read_stats (synchronises the stream)."""
+        st = CacheStats()
+        _check(lib().k3moe_cache_read_stats(_p(self.tensors["state"]), _stream(stream),
+                                            ctypes.byref(st)))
+        return {name: int(getattr(st, name)) for name, _ in CacheStats._fields_}
+
+    def maps(self):
+        """(slot_of [E], expert_of [S], stamp [S]) as device int tensors (views of the state)."""
+        st = self.tensors["state"]
+        E, S = self.E, self.slots
+        al = lambda n: (n * 4 + 255) // 256 * 256  # noqa: E731
+        o1 = 256
+        o2 = o1 + al(E)
+        o3 = o2 + al(S)
+        slot_of = st[o1:o1 + 4 * E].view(torch.int32)
+        expert_of = st[o2:o2 + 4 * S].view(torch.int32)
+        stamp = st[o3:o3 + 4 * S].view(torch.int32)
+        return slot_of, expert_of, stamp
+
+
+def k3moe_cache_state_size(E: int, slots: int) -> int:
+    return lib().k3moe_cache_state_size(E, slots)
+
+
+def k3moe_forward_cached(layer: MoELayer, cache: ExpertCache, hidden, out=None, ws=None,
+                         stream=None):
+    """k3moe_forward with host-resident expert arrays (``host_resident``) behind ``cache``."""
+    hidden = _bf16(hidden, "hidden")
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = workspace(k3moe_workspace_size(layer, T), hidden.device)
+    _check(lib().k3moe_forward_cached(ctypes.byref(layer.desc), ctypes.byref(cache.desc),
+                                      _p(hidden), T, _p(out), _p(ws), ws.numel(),
+                                      _stream(stream)))
+    return out
+
+
+class ForwardGraph:
+    """A CUDA graph of one k3moe_forward (or, with ``cache``, one
+    k3moe_forward_cached) with fixed buffers (k3moe_graph_create[_cached])."""
+
+    def __init__(self, layer: MoELayer, hidden, out, ws, cache: "ExpertCache | None" = None):
         hidden = _bf16(hidden, "hidden")
-        self._keep = (layer, hidden, out, ws)
+        self._keep = (layer, hidden, out, ws, cache)
         h = ctypes.c_void_p(None)
-        _check(lib().k3moe_graph_create(ctypes.byref(layer.desc), _p(hidden), hidden.shape[0],
-                                        _p(out), _p(ws), ws.numel(), ctypes.byref(h)))
+        if cache is None:
+            _check(lib().k3moe_graph_create(ctypes.byref(layer.desc), _p(hidden), hidden.shape[0],
+                                            _p(out), _p(ws), ws.numel(), ctypes.byref(h)))
+        else:
+            _check(lib().k3moe_graph_create_cached(ctypes.byref(layer.desc),
+                                                   ctypes.byref(cache.desc), _p(hidden),
+                                                   hidden.shape[0], _p(out), _p(ws), ws.numel(),
+                                                   ctypes.byref(h)))
         self.handle = h
 
     def launch(self, stream=None):

@@ -403,8 +403,57 @@ size_t k3moe_host_staging_size(const k3moe_layer_desc* desc, int32_t T) {
     return 2 * align_up(static_cast<size_t>(T) * width * 2);
 }
 
-k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
-                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+// The cached forward's view of the expert weights: the slot arrays, the
+// expert -> slot map, and the device addresses of the host-resident arrays.
+struct CachePlan {
+    const k3moe_expert_cache* c = nullptr;
+    CacheFillArgs fill{};
+};
+
+k3moe_status check_cache(const k3moe_layer_desc* d, const k3moe_expert_cache* c, int T, CachePlan* cp) {
+    if (!c || c->reserved != 0 || !c->state) return K3MOE_ERR_INVALID_ARG;
+    const long long need = std::min<long long>(d->E, static_cast<long long>(T) * d->k);
+    if (c->slots < 1 || c->slots > d->E || c->slots < need) return K3MOE_ERR_SHAPE;
+    uint8_t* dst[6] = {c->w1_q, c->w3_q, c->w2_q, c->w1_sf, c->w3_sf, c->w2_sf};
+    for (uint8_t* q : dst) {
+        if (!q) return K3MOE_ERR_INVALID_ARG;
+        if (!aligned16(q)) return K3MOE_ERR_ALIGN;
+    }
+    if (!aligned32(c->w1_q) || !aligned32(c->w3_q) || !aligned32(c->w2_q) || !aligned16(c->state))
+        return K3MOE_ERR_ALIGN;
+    // the expert arrays of the layer are host memory, page-locked and mapped
+    const void* src[6] = {d->w1_q, d->w3_q, d->w2_q, d->w1_sf, d->w3_sf, d->w2_sf};
+    const uint8_t* dev[6];
+    for (int i = 0; i < 6; ++i) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, src[i]) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+            !at.devicePointer || !at.hostPointer) {
+            cudaGetLastError();
+            return K3MOE_ERR_INVALID_ARG;
+        }
+        // the device address of the host byte src[i] (the allocation may start before it)
+        const uint8_t* p = static_cast<const uint8_t*>(at.devicePointer) +
+                           (static_cast<const uint8_t*>(src[i]) - static_cast<const uint8_t*>(at.hostPointer));
+        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+        dev[i] = p;
+    }
+    cp->c = c;
+    for (int i = 0; i < 3; ++i) {
+        cp->fill.src_q[i] = dev[i];
+        cp->fill.src_sf[i] = dev[3 + i];
+        cp->fill.dst_q[i] = dst[i];
+        cp->fill.dst_sf[i] = dst[3 + i];
+    }
+    cp->fill.q_bytes = static_cast<size_t>(d->f) * (d->d / 2);
+    cp->fill.sf_bytes = static_cast<size_t>(d->f) * (d->d / 32);
+    return K3MOE_OK;
+}
+
+k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                          const uint16_t* hidden, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
+                          void* stream) {
     k3moe_status st = check_desc(desc);
     if (st != K3MOE_OK) return st;
     if (!hidden || !out || !ws || T < 1) return K3MOE_ERR_INVALID_ARG;
@@ -414,6 +463,12 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     int path = desc->path;
     if (path == K3MOE_PATH_AUTO) path = T <= kStreamMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
     if (path == K3MOE_PATH_DECODE && T > kStreamMaxT) return K3MOE_ERR_UNSUPPORTED;
+    CachePlan cp;
+    if (cache) {
+        // the cache serves the streaming kernels only (few experts per call)
+        if (path != K3MOE_PATH_DECODE) return K3MOE_ERR_UNSUPPORTED;
+        if ((st = check_cache(desc, cache, T, &cp)) != K3MOE_OK) return st;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
@@ -478,10 +533,26 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
             return K3MOE_ERR_CUDA;
     }
 
+    // the weights the expert kernels read: the layer's arrays, or the cache's
+    // slots after the missing experts were fetched into them
+    const uint8_t *w1_q = desc->w1_q, *w3_q = desc->w3_q, *w2_q = desc->w2_q;
+    const uint8_t *w1_sf = desc->w1_sf, *w3_sf = desc->w3_sf, *w2_sf = desc->w2_sf;
+    const int32_t* slot_of = nullptr;
+    int nslots = desc->E;
+    if (cp.c) {
+        if ((e = launch_cache_update(cp.c->state, desc->E, cp.c->slots, active, cp.fill, hdr, sms, s)))
+            return cuda_status(e);
+        w1_q = cp.c->w1_q; w3_q = cp.c->w3_q; w2_q = cp.c->w2_q;
+        w1_sf = cp.c->w1_sf; w3_sf = cp.c->w3_sf; w2_sf = cp.c->w2_sf;
+        slot_of = cache_view(cp.c->state, desc->E, cp.c->slots).slot_of;
+        nslots = cp.c->slots;
+    }
+
     if (path == K3MOE_PATH_DECODE && T > kDecodeMaxT) {
         MxUnitsArgs a{};
-        a.w1_q = desc->w1_q; a.w3_q = desc->w3_q; a.w2_q = desc->w2_q;
-        a.w1_sf = desc->w1_sf; a.w3_sf = desc->w3_sf; a.w2_sf = desc->w2_sf;
+        a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
+        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
+        a.slot_of = slot_of; a.nslots = nslots;
         a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.counts = counts; a.offsets = offsets; a.perm = perm; a.inv = inv; a.idx = r.idx; a.wts = r.wts;
         a.scratch = at(p.units);
@@ -491,8 +562,9 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
         if (e) return cuda_status(e);
     } else if (path == K3MOE_PATH_DECODE) {
         MxDecodeArgs a{};
-        a.w1_q = desc->w1_q; a.w3_q = desc->w3_q; a.w2_q = desc->w2_q;
-        a.w1_sf = desc->w1_sf; a.w3_sf = desc->w3_sf; a.w2_sf = desc->w2_sf;
+        a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
+        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
+        a.slot_of = slot_of; a.nslots = nslots;
         a.x = x_expert; a.xq_ready = fuse_prep ? 1 : 0;
         a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.active = active; a.idx = r.idx; a.wts = r.wts;
@@ -530,6 +602,47 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
     return K3MOE_OK;
 }
 
+}  // namespace
+
+k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    return forward_impl(desc, nullptr, hidden, T, out, ws, ws_bytes, stream);
+}
+
+size_t k3moe_cache_state_size(int32_t E, int32_t slots) {
+    if (E < 1 || slots < 1) return 0;
+    return cache_state_bytes(E, slots);
+}
+
+k3moe_status k3moe_cache_init(void* state, int32_t E, int32_t slots, void* stream) {
+    if (!state || E < 1 || slots < 1) return K3MOE_ERR_INVALID_ARG;
+    if (slots > E || E > 1024) return K3MOE_ERR_SHAPE;
+    if (!aligned16(state)) return K3MOE_ERR_ALIGN;
+    return cuda_status(launch_cache_init(state, E, slots, static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_forward_cached(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                                  const uint16_t* hidden, int32_t T, uint16_t* out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+    if (!cache) return K3MOE_ERR_INVALID_ARG;
+    return forward_impl(desc, cache, hidden, T, out, ws, ws_bytes, stream);
+}
+
+k3moe_status k3moe_cache_read_stats(const void* state, void* stream, k3moe_cache_stats* out) {
+    if (!state || !out) return K3MOE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return K3MOE_ERR_CUDA;
+    CacheHeader h;
+    if (cudaMemcpy(&h, state, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (h.magic != kCacheMagic) return K3MOE_ERR_INVALID_ARG;
+    out->calls = h.calls;
+    out->hits = h.hits;
+    out->misses = h.misses;
+    out->bytes = h.bytes;
+    out->last_hits = h.last_hit;
+    out->last_misses = h.last_miss;
+    return K3MOE_OK;
+}
+
 k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hidden_host,
                                 int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,
                                 void* stream) {
@@ -559,14 +672,16 @@ struct ForwardGraph {
 };
 }  // namespace
 
-k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
-                                uint16_t* out, void* ws, size_t ws_bytes, void** graph_out) {
+namespace {
+k3moe_status graph_create(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                          const uint16_t* hidden, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
+                          void** graph_out) {
     if (!graph_out) return K3MOE_ERR_INVALID_ARG;
     *graph_out = nullptr;
     cudaStream_t cs = nullptr;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return K3MOE_ERR_CUDA;
     // one uncaptured forward: argument checks and one-time set-up
-    k3moe_status st = k3moe_forward(desc, hidden, T, out, ws, ws_bytes, cs);
+    k3moe_status st = forward_impl(desc, cache, hidden, T, out, ws, ws_bytes, cs);
     if (st == K3MOE_OK && cudaStreamSynchronize(cs) != cudaSuccess) st = K3MOE_ERR_CUDA;
     ForwardGraph* fg = nullptr;
     if (st == K3MOE_OK) {
@@ -574,7 +689,7 @@ k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hi
         if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
             st = K3MOE_ERR_CUDA;
         } else {
-            st = k3moe_forward(desc, hidden, T, out, ws, ws_bytes, cs);
+            st = forward_impl(desc, cache, hidden, T, out, ws, ws_bytes, cs);
             const cudaError_t e = cudaStreamEndCapture(cs, &fg->graph);
             if (st == K3MOE_OK && e != cudaSuccess) st = K3MOE_ERR_CUDA;
         }
@@ -593,6 +708,19 @@ k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hi
     }
     *graph_out = fg;
     return K3MOE_OK;
+}
+}  // namespace
+
+k3moe_status k3moe_graph_create(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                                uint16_t* out, void* ws, size_t ws_bytes, void** graph_out) {
+    return graph_create(desc, nullptr, hidden, T, out, ws, ws_bytes, graph_out);
+}
+
+k3moe_status k3moe_graph_create_cached(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
+                                       const uint16_t* hidden, int32_t T, uint16_t* out, void* ws,
+                                       size_t ws_bytes, void** graph_out) {
+    if (!cache) return K3MOE_ERR_INVALID_ARG;
+    return graph_create(desc, cache, hidden, T, out, ws, ws_bytes, graph_out);
 }
 
 k3moe_status k3moe_graph_launch(void* graph, void* stream) {

@@ -371,6 +371,8 @@ struct MxDecodeArgs {
     int xq_ready;             // 1: the router already wrote the E2M1 terms
     int T, E, k, d, f;
     const int32_t* active;    // [E + 1] active experts ascending, count at [E]
+    const int32_t* slot_of;   // expert -> weight slot of the w arrays (null: the expert itself)
+    int nslots;               // expert slots the w arrays hold (E without a cache)
     const int32_t* idx;       // [T, k]
     const float* wts;         // [T, k]
     void* scratch;            // mx_decode_scratch_bytes(T, E, k, d, f)
@@ -397,6 +399,8 @@ struct MxUnitsArgs {
     const int32_t* inv;       // [T k] pair -> sorted row
     const int32_t* idx;       // [T, k]
     const float* wts;         // [T, k]
+    const int32_t* slot_of;   // expert -> weight slot (null: the expert itself)
+    int nslots;               // expert slots the w arrays hold (E without a cache)
     void* scratch;            // mx_units_scratch_bytes(T, E, k, d, f)
     uint16_t* out;            // [T, d] bf16
     WsHeader* hdr;
@@ -404,6 +408,46 @@ struct MxUnitsArgs {
 };
 size_t mx_units_scratch_bytes(int T, int E, int k, int d, int f);
 cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s);
+// device expert cache (cache.cu).  The caller's state buffer holds a 256-byte
+// header, then slot_of [E], expert_of [S], stamp [S], miss_e [S], miss_slot [S]
+// (int32 / uint32, each array 256-byte aligned).
+constexpr uint32_t kCacheMagic = 0x4b33c4c1u;
+struct CacheHeader {
+    uint32_t magic;         // kCacheMagic after k3moe_cache_init
+    int32_t E, slots;
+    uint32_t clock;         // calls served; a slot's stamp is the clock of its last use
+    int32_t last_miss, last_hit;
+    int32_t pad0[2];
+    unsigned long long calls, hits, misses, bytes;  // totals since init
+    uint32_t pad[48];
+};
+static_assert(sizeof(CacheHeader) == 256, "cache header is 256 bytes");
+struct CacheView {
+    CacheHeader* h;
+    int32_t* slot_of;    // [E] slot holding the expert, -1 = not resident
+    int32_t* expert_of;  // [S] expert in the slot, -1 = empty
+    uint32_t* stamp;     // [S] clock of the slot's last use (0 = never)
+    int32_t* miss_e;     // [S] experts to fetch in this call, ascending
+    int32_t* miss_slot;  // [S] the slot each of them goes to
+};
+size_t cache_state_bytes(int E, int slots);
+CacheView cache_view(void* state, int E, int slots);
+// where the fetched bytes come from (device addresses of host-resident
+// arrays) and go to (the slot arrays); per expert and matrix q_bytes of
+// codes and sf_bytes of prepared scale atoms, in the order w1, w3, w2
+struct CacheFillArgs {
+    const uint8_t* src_q[3];
+    const uint8_t* src_sf[3];
+    uint8_t* dst_q[3];
+    uint8_t* dst_sf[3];
+    size_t q_bytes, sf_bytes;
+};
+cudaError_t launch_cache_init(void* state, int E, int slots, cudaStream_t s);
+// after the active list is final: slot assignment (one CTA), then the copy of
+// the missing experts into their slots (all SMs)
+cudaError_t launch_cache_update(void* state, int E, int slots, const int32_t* active,
+                                const CacheFillArgs& f, WsHeader* hdr, int num_sms, cudaStream_t s);
+
 // canonical E8M0 scales [rows, K/32] <-> prepared atoms (inverse = 1: atoms -> canonical)
 cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
                               cudaStream_t s);

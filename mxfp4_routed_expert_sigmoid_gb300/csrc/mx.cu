@@ -106,6 +106,8 @@ struct MxArgs {
     const int32_t* count;   // number of units (decode: active + E)
     const int32_t* ucnt;    // tokens of each unit (null: all T)
     const int32_t* ubase;   // unit-grouped: first unit of each expert, [E + 1] (null: decode)
+    const int32_t* slot_of; // expert -> slot of the weight arrays (null: the expert itself)
+    int nslots;             // slots the weight arrays hold
     int E;
     int rows;               // weight rows per expert (f up, d down)
     int tiles;              // 128-row tiles per expert
@@ -189,6 +191,19 @@ struct Cursor {
     }
 };
 
+// where expert e's weights sit in the weight arrays: its own index, or the
+// cache slot that holds it (a slot outside the arrays is an error: slot 0 is
+// read instead and the status word records it)
+__device__ __forceinline__ int weight_slot(const MxArgs& p, int e) {
+    if (!p.slot_of) return e;
+    const int s = p.slot_of[e];
+    if (s < 0 || s >= p.nslots) {
+        set_error(p.hdr, K3MOE_ERR_INVALID_ARG, 72);
+        return 0;
+    }
+    return s;
+}
+
 template <int TERMS>
 __global__ void __launch_bounds__(kMxThreads, 1)
 mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
@@ -271,7 +286,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (int j = 0; j < early; ++j) {
                 uint8_t* st = smem + static_cast<size_t>(j) * p.stage_bytes;
                 mbar_expect_tx_only(&full[j], a_bytes(c));
-                issue_a(c, p.active[c.u], st, &full[j]);
+                issue_a(c, weight_slot(p, p.active[c.u]), st, &full[j]);
                 c.next(p);
             }
         }
@@ -290,7 +305,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (lane == 0 && w0 < w1) {
             // ------------------------------ producer ------------------------------
             Cursor c(w0, p);
-            int e = p.active[c.u];
+            int e = weight_slot(p, p.active[c.u]);
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -312,7 +327,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 const int u_prev = c.u;
                 c.next(p);
-                if (c.u != u_prev && w + 1 < w1) e = p.active[c.u];
+                if (c.u != u_prev && w + 1 < w1) e = weight_slot(p, p.active[c.u]);
             }
             // copies still in flight (after an abort) finish before the CTA exits
             for (int j = issued > p.RS ? issued - p.RS : 0; j < issued; ++j) {
@@ -833,15 +848,16 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
         trace_mark("quantize_x", s);
         if (e != cudaSuccess) return e;
     }
-    // A operands: packed E2M1 codes as [E * rows, K / 2] bytes, boxes of 128 bytes
-    // (256 inputs) x 128 rows
+    // A operands: packed E2M1 codes as [slots * rows, K / 2] bytes (a slot per
+    // expert, or the cache's slots), boxes of 128 bytes (256 inputs) x 128 rows
+    const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
     CUtensorMap t1, t3, t2;
-    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
-                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
-                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2,
-                        static_cast<uint64_t>(a.E) * a.d, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2, nslots * a.d, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
 
     MxArgs up{};
@@ -855,6 +871,8 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     up.active = a.active;
     up.count = a.active + a.E;
     up.ucnt = nullptr;
+    up.slot_of = a.slot_of;
+    up.nslots = static_cast<int>(nslots);
     up.E = a.E;
     up.rows = a.f;
     up.tiles = a.f / 128;
@@ -974,13 +992,14 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     trace_mark("unit_terms", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+    const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
     CUtensorMap t1, t3, t2;
-    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
-                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2,
-                        static_cast<uint64_t>(a.E) * a.f, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2,
-                        static_cast<uint64_t>(a.E) * a.d, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2, nslots * a.d, 128, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
 
     MxArgs up{};
@@ -995,6 +1014,8 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     up.count = m.nunits;
     up.ucnt = m.unit_cnt;
     up.ubase = m.ubase;
+    up.slot_of = a.slot_of;
+    up.nslots = static_cast<int>(nslots);
     up.E = a.E;
     up.rows = a.f;
     up.tiles = a.f / 128;

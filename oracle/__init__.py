@@ -25,7 +25,11 @@ Sources (web pages; cited by title and section):
     both scale formulas and the worked check on a [3072, 3584] w1 tensor.
 * Lucebox PR #573 "feat(kimi-k3): add DSpark Q8 artifact and shared
   speculative runtime", section "DSpark acceptance-contract correction": RMS
-  epsilon 1e-5.
+  epsilon 1e-5; section "Runtime validation": an 8 GiB device expert cache
+  in front of SSD-routed experts.
+* The K3-Stuff model page, "llama-cpp-patches", change 2: the page cache as
+  the hot-expert cache with least-recently-used eviction (``cache.py``, the
+  slot policy of the host-resident expert path).
 
 Readings of points the pages leave open are stated in each function.
 

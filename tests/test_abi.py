@@ -35,7 +35,7 @@ def test_exports_match_header(k3):
     L = k3.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert k3.k3moe_abi_version() == 2
+    assert k3.k3moe_abi_version() == 3
 
 
 def test_status_strings(k3):
@@ -45,12 +45,16 @@ def test_status_strings(k3):
     assert L.k3moe_status_string(99) == b"unknown status"
 
 
-def test_desc_layout_matches_c(k3):
-    fields = [f for f, _ in k3.LayerDesc._fields_]
+@pytest.mark.parametrize("py,c", [("LayerDesc", "k3moe_layer_desc"),
+                                  ("CacheDesc", "k3moe_expert_cache"),
+                                  ("CacheStats", "k3moe_cache_stats")])
+def test_desc_layout_matches_c(k3, py, c):
+    struct = getattr(k3, py)
+    fields = [f for f, _ in struct._fields_]
     prog = "#include <stdio.h>\n#include <stddef.h>\n#include \"k3moe.h\"\nint main(void){\n"
-    prog += 'printf("%zu\\n", sizeof(k3moe_layer_desc));\n'
+    prog += f'printf("%zu\\n", sizeof({c}));\n'
     for f in fields:
-        prog += f'printf("%zu\\n", offsetof(k3moe_layer_desc, {f}));\n'
+        prog += f'printf("%zu\\n", offsetof({c}, {f}));\n'
     prog += "return 0;}\n"
     with tempfile.TemporaryDirectory() as d:
         src = os.path.join(d, "t.c")
@@ -59,9 +63,9 @@ def test_desc_layout_matches_c(k3):
         subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
         vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
                                                check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(k3.LayerDesc)
+    assert vals[0] == ctypes.sizeof(struct)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(k3.LayerDesc, f).offset == off, f
+        assert getattr(struct, f).offset == off, f
 
 
 A16 = 0x10000  # a fake 16-byte aligned address: validation rejects before any use
@@ -140,6 +144,46 @@ def test_forward_validation(k3):
     assert fwd(desc(k3), h=A1) == 3
     assert fwd(desc(k3), ws=16) == 4
     assert fwd(desc(k3, path=1), T=1025) == 8  # the streaming kernels take at most 1024 tokens
+
+
+def cache_desc(k3, **over):
+    c = k3.CacheDesc()
+    c.slots, c.reserved = 64, 0
+    for name in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf", "state"):
+        setattr(c, name, A16)
+    for k_, v in over.items():
+        setattr(c, k_, v)
+    return c
+
+
+def test_cache_validation(k3):
+    """Host checks of the cached forward and the cache set-up (no launch)."""
+    L = k3.lib()
+
+    def fwd(dsc, c, T=1):
+        return L.k3moe_forward_cached(ctypes.byref(dsc), None if c is None else ctypes.byref(c),
+                                      A16, T, A16, A16, 1 << 40, None)
+
+    assert fwd(desc(k3), None) == 1
+    assert fwd(desc(k3), cache_desc(k3, reserved=1)) == 1
+    assert fwd(desc(k3), cache_desc(k3, state=None)) == 1
+    assert fwd(desc(k3), cache_desc(k3, slots=15)) == 2   # fewer slots than one token's experts
+    assert fwd(desc(k3), cache_desc(k3, slots=897)) == 2  # more slots than experts
+    assert fwd(desc(k3), cache_desc(k3), T=8) == 2        # 8 tokens may use 128 experts
+    assert fwd(desc(k3), cache_desc(k3, w2_q=A16 + 16)) == 3
+    assert fwd(desc(k3), cache_desc(k3, w3_sf=A1)) == 3
+    assert fwd(desc(k3), cache_desc(k3, w1_q=None)) == 1
+    assert fwd(desc(k3, path=2), cache_desc(k3)) == 8     # the grouped path has no cache
+    assert fwd(desc(k3), cache_desc(k3), T=2000) == 8
+    assert fwd(desc(k3, k=40), cache_desc(k3)) == 2       # the layer checks come first
+    assert L.k3moe_cache_state_size(896, 0) == 0
+    st = L.k3moe_cache_state_size(896, 160)
+    assert st >= 256 + 896 * 4 + 4 * 160 * 4
+    assert L.k3moe_cache_init(None, 896, 160, None) == 1
+    assert L.k3moe_cache_init(A16, 896, 900, None) == 2
+    assert L.k3moe_cache_init(A16, 2000, 160, None) == 2
+    assert L.k3moe_cache_init(A1, 896, 160, None) == 3
+    assert L.k3moe_cache_read_stats(None, None, None) == 1
 
 
 def test_workspace_sizes(k3):
