@@ -63,6 +63,9 @@ def parse():
                     help="fewer resident experts (small profiling captures only; not a bench line)")
     ap.add_argument("--T", type=int, default=0,
                     help="other token count (small profiling captures only; not a bench line)")
+    ap.add_argument("--format", choices=["split", "ggml"], default="split",
+                    help="expert weight format: compressed-tensors codes + scales, or llama.cpp "
+                         "17-byte MXFP4 blocks read directly by the streaming kernels")
     ap.add_argument("--cache-slots", type=int, default=0,
                     help="host-resident experts behind a device cache of this many experts "
                          "(k3moe_forward_cached); 0 = experts resident in HBM")
@@ -299,6 +302,11 @@ def ours_arm(args):
         kw.update(norm_gamma=dv(dense["norm_gamma"]), w_down=dv(dense["w_down"]),
                   w_up=dv(dense["w_up"]), eps=dense["eps"])
     layer = k3.MoELayer(**kw)
+    del kw, ex
+    if args.format == "ggml":
+        layer = k3.ggml_layer(layer)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     pool_np = token_pool(cfg, args.pool)
     pool = [dv(pool_np[i]) for i in range(args.pool)]
     ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T) + k3.k3moe_host_staging_size(layer, cfg.T), dev)
@@ -437,7 +445,8 @@ def ours_arm(args):
         achieved = algo[dom] / (kern_mean[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                 "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": TRAFFIC.get((cfg.name, dom)), "algorithmic_bytes_per_launch": algo[dom],
+                "traffic": TRAFFIC.get((cfg.name, dom)) if args.format == "split" else None,
+                "algorithmic_bytes_per_launch": algo[dom],
                 "avg_launch_ms": kern_mean[dom]}
     elif dom in flops:
         # f16 operands: the measured bf16 rate (same tensor-core rate); the kernel
@@ -456,7 +465,8 @@ def ours_arm(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg.T, args.path),
         "data": "synthetic (seeded; random-init weights of the K3 layer shapes)",
-        "config": workload_config(cfg, args.pool),
+        "config": dict(workload_config(cfg, args.pool),
+                       **({"weight_format": "ggml 17-byte MXFP4 blocks"} if args.format == "ggml" else {})),
         "hbm_gbs_step": step_bytes / (mean_ms * 1e-3) / 1e9,
         "experts_touched_per_step": u_mean,
         "kernels_ms": kern_mean,

@@ -109,7 +109,25 @@ typedef enum k3moe_path {
  * s / sum(s) over the selected k (the bias only steers selection).
  * Block mode (D > 0): the input is h [T, D]; hn = RMSNorm(h) * gamma (eps),
  * the router reads hn (d_router = D), the experts read z = hn W_down^T
- * [T, d], and the output is W_up applied to the combined latent rows. */
+ * [T, d], and the output is W_up applied to the combined latent rows.
+ *
+ * Weight format (`format`):
+ *   K3MOE_FORMAT_SPLIT (0): the codes and prepared scales above.
+ *   K3MOE_FORMAT_GGML  (1): llama.cpp's MXFP4 blocks, as k3moe_repack_mxfp4
+ *     writes them ([PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact"):
+ *     w1_q [E, f, d/32, 17], w3_q [E, f, d/32, 17], w2_q [E, d, f/32, 17]
+ *     (byte 0 of a block = the E8M0 byte e, bytes 1..16 = element j in the
+ *     low and element j + 16 in the high nibble of byte j), 16-byte aligned;
+ *     w1_sf, w3_sf, w2_sf unused (may be NULL).  The streaming kernels read
+ *     the blocks as they are and convert them in shared memory; the result
+ *     is bitwise that of the SPLIT format on the same weights.  d and f
+ *     must be multiples of 512 (rows of whole 16-byte units); the DECODE
+ *     path only (T <= 1024) and no expert cache (UNSUPPORTED otherwise). */
+typedef enum k3moe_format {
+    K3MOE_FORMAT_SPLIT = 0,
+    K3MOE_FORMAT_GGML = 1
+} k3moe_format;
+
 typedef struct k3moe_layer_desc {
     int32_t E;          /* routed experts (896) */
     int32_t k;          /* experts per token (16), 1 <= k <= min(E, 32) */
@@ -120,7 +138,7 @@ typedef struct k3moe_layer_desc {
     int32_t path;       /* k3moe_path */
     int32_t D;          /* block mode: model width (7168), multiple of 128; 0 = latent mode */
     float eps;          /* block mode: RMSNorm epsilon (1e-5 per [PR573]) */
-    int32_t reserved;   /* must be 0 */
+    int32_t format;     /* k3moe_format of the expert weights */
     const uint8_t* w1_q;
     const uint8_t* w3_q;
     const uint8_t* w2_q;

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libk3moe.so")
 
 ACT_SILU_GATED = 0
 PATH_AUTO, PATH_DECODE, PATH_GROUPED = 0, 1, 2
+FORMAT_SPLIT, FORMAT_GGML = 0, 1
 
 STATUS = {
     0: "K3MOE_OK", 1: "K3MOE_ERR_INVALID_ARG", 2: "K3MOE_ERR_SHAPE", 3: "K3MOE_ERR_ALIGN",
@@ -57,7 +58,7 @@ class LayerDesc(ctypes.Structure):
         ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("d", ctypes.c_int32),
         ("f", ctypes.c_int32), ("d_router", ctypes.c_int32), ("act", ctypes.c_int32),
         ("path", ctypes.c_int32), ("D", ctypes.c_int32), ("eps", ctypes.c_float),
-        ("reserved", ctypes.c_int32),
+        ("format", ctypes.c_int32),
         ("w1_q", ctypes.c_void_p), ("w3_q", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
         ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
         ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
@@ -316,7 +317,7 @@ class MoELayer:
         desc = LayerDesc()
         desc.E, desc.k, desc.d, desc.f = E, k, d, f
         desc.d_router = D if block else d
-        desc.act, desc.path, desc.D, desc.eps, desc.reserved = act, path, D, eps, 0
+        desc.act, desc.path, desc.D, desc.eps, desc.format = act, path, D, eps, FORMAT_SPLIT
         for name, t in self.tensors.items():
             setattr(desc, name, t.data_ptr())
         self.desc = desc
@@ -404,6 +405,30 @@ def k3moe_trace_read(max_entries: int = 32):
 
 
 EXPERT_ARRAYS = ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf")
+
+
+def ggml_layer(layer: MoELayer, stream=None) -> MoELayer:
+    """A copy of ``layer`` whose expert matrices are llama.cpp's MXFP4 blocks
+    ([E, rows, K/32, 17], written by k3moe_repack_mxfp4 from the codes and the
+    canonical scales), descriptor format K3MOE_FORMAT_GGML.  Router and
+    block-mode tensors stay shared with ``layer``."""
+    other = object.__new__(MoELayer)
+    other.__dict__.update(layer.__dict__)
+    other.tensors = dict(layer.tensors)
+    desc = LayerDesc.from_buffer_copy(layer.desc)
+    for q, sf in (("w1_q", "w1_sf"), ("w3_q", "w3_sf"), ("w2_q", "w2_sf")):
+        codes = layer.tensors[q]
+        E, rows, half = codes.shape
+        K = 2 * half
+        canon = k3moe_unprepare_scales(layer.tensors[sf], (E * rows, K // 32), stream=stream)
+        blocks = k3moe_repack_mxfp4(codes.view(E * rows, half), canon, stream=stream)
+        other.tensors[q] = blocks.view(E, rows, K // 32, 17)
+        del other.tensors[sf]
+        setattr(desc, q, blocks.data_ptr())
+        setattr(desc, sf, None)
+    desc.format = FORMAT_GGML
+    other.desc = desc
+    return other
 
 
 def host_resident(layer: MoELayer) -> MoELayer:

@@ -133,7 +133,7 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
 k3moe_status check_desc(const k3moe_layer_desc* d) {
     if (!d) return K3MOE_ERR_INVALID_ARG;
     if (d->E < 1 || d->k < 1 || d->d < 1 || d->f < 1 || d->d_router < 1) return K3MOE_ERR_INVALID_ARG;
-    if (d->reserved != 0) return K3MOE_ERR_INVALID_ARG;
+    if (d->format != K3MOE_FORMAT_SPLIT && d->format != K3MOE_FORMAT_GGML) return K3MOE_ERR_INVALID_ARG;
     if (d->k > d->E || d->k > 32 || d->E > 1024) return K3MOE_ERR_SHAPE;
     if (d->d % 256 || d->f % 256) return K3MOE_ERR_SHAPE;  // 256-wide K chunks of the MMAs
     if (d->D < 0) return K3MOE_ERR_SHAPE;
@@ -148,10 +148,16 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
     }
     if (d->act != K3MOE_ACT_SILU_GATED) return K3MOE_ERR_UNSUPPORTED;
     if (d->path < K3MOE_PATH_AUTO || d->path > K3MOE_PATH_GROUPED) return K3MOE_ERR_INVALID_ARG;
-    const void* ptrs[] = {d->w1_q, d->w3_q, d->w2_q, d->w1_sf, d->w3_sf, d->w2_sf, d->router_w, d->router_b};
-    for (const void* p : ptrs) {
-        if (!p) return K3MOE_ERR_INVALID_ARG;
-        if (!aligned16(p)) return K3MOE_ERR_ALIGN;
+    const bool ggml = d->format == K3MOE_FORMAT_GGML;
+    const void* ptrs[] = {d->w1_q, d->w3_q, d->w2_q, d->router_w, d->router_b, d->w1_sf, d->w3_sf, d->w2_sf};
+    for (int i = 0; i < (ggml ? 5 : 8); ++i) {  // ggml blocks carry their scales
+        if (!ptrs[i]) return K3MOE_ERR_INVALID_ARG;
+        if (!aligned16(ptrs[i])) return K3MOE_ERR_ALIGN;
+    }
+    if (ggml) {
+        // rows of d/32 (f/32) 17-byte blocks are whole 16-byte units for TMA
+        if (d->d % 512 || d->f % 512) return K3MOE_ERR_SHAPE;
+        return K3MOE_OK;
     }
     // E2M1 codes are read by TMA in 16-byte slots: 32-byte aligned bases
     if (!aligned32(d->w1_q) || !aligned32(d->w3_q) || !aligned32(d->w2_q)) return K3MOE_ERR_ALIGN;
@@ -463,6 +469,8 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     int path = desc->path;
     if (path == K3MOE_PATH_AUTO) path = T <= kStreamMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
     if (path == K3MOE_PATH_DECODE && T > kStreamMaxT) return K3MOE_ERR_UNSUPPORTED;
+    // ggml blocks: the streaming kernels only, without a cache
+    if (desc->format == K3MOE_FORMAT_GGML && (path != K3MOE_PATH_DECODE || cache)) return K3MOE_ERR_UNSUPPORTED;
     CachePlan cp;
     if (cache) {
         // the cache serves the streaming kernels only (few experts per call)
@@ -553,6 +561,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
         a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
         a.slot_of = slot_of; a.nslots = nslots;
+        a.ggml = desc->format == K3MOE_FORMAT_GGML ? 1 : 0;
         a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.counts = counts; a.offsets = offsets; a.perm = perm; a.inv = inv; a.idx = r.idx; a.wts = r.wts;
         a.scratch = at(p.units);
@@ -565,6 +574,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
         a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
         a.slot_of = slot_of; a.nslots = nslots;
+        a.ggml = desc->format == K3MOE_FORMAT_GGML ? 1 : 0;
         a.x = x_expert; a.xq_ready = fuse_prep ? 1 : 0;
         a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.active = active; a.idx = r.idx; a.wts = r.wts;

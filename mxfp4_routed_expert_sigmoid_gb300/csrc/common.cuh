@@ -373,6 +373,7 @@ struct MxDecodeArgs {
     const int32_t* active;    // [E + 1] active experts ascending, count at [E]
     const int32_t* slot_of;   // expert -> weight slot of the w arrays (null: the expert itself)
     int nslots;               // expert slots the w arrays hold (E without a cache)
+    int ggml;                 // 1: w*_q hold ggml 17-byte blocks (w*_sf unused)
     const int32_t* idx;       // [T, k]
     const float* wts;         // [T, k]
     void* scratch;            // mx_decode_scratch_bytes(T, E, k, d, f)
@@ -401,6 +402,7 @@ struct MxUnitsArgs {
     const float* wts;         // [T, k]
     const int32_t* slot_of;   // expert -> weight slot (null: the expert itself)
     int nslots;               // expert slots the w arrays hold (E without a cache)
+    int ggml;                 // 1: w*_q hold ggml 17-byte blocks (w*_sf unused)
     void* scratch;            // mx_units_scratch_bytes(T, E, k, d, f)
     uint16_t* out;            // [T, d] bf16
     WsHeader* hdr;

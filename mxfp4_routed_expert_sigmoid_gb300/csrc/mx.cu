@@ -62,10 +62,17 @@ namespace {
 using namespace tc;
 
 constexpr int kMxThreads = 224;
+constexpr int kGgThreads = 128;        // ggml-block variant: one converting thread per tile row
+constexpr int kGgBar = 1;              // their named barrier
 constexpr int kMaxStages = 8;
 constexpr int kChunks = 2;             // 256-wide K chunks per stage (a stage covers K = 512)
 constexpr int kChunkA = 16384;         // 128 rows x 128 bytes of packed E2M1
 constexpr int kStageA = kChunks * kChunkA;
+// ggml 17-byte blocks: a stage of one tile row is 16 blocks = 272 bytes, the
+// tile's 128 rows 34,816 bytes = the A chunks and scale atoms they become
+constexpr int kGgRowBytes = 4 * kChunks * 2 * 17;
+constexpr int kGgStageBytes = 128 * kGgRowBytes;
+static_assert(kGgStageBytes == kStageA + kChunks * 1024, "a ggml stage converts in place");
 constexpr int kMaxN = 64;              // MMA N: kTerms * T rounded up to 16
 // TMEM: accumulators (buffer a, issuer t) at (2 a + t) * kMaxN, then the scale
 // slots, each on a 32-column boundary: issuer t's atoms A0, B0, A1, B1 of its
@@ -191,6 +198,80 @@ struct Cursor {
     }
 };
 
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// barrier over n threads that also ANDs a predicate across them
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// For a word q of ggml code bytes c_j | c_(j+16) << 4: bytes 0 and 2 of
+// *lo_pairs are c_0 | c_1 << 4 and c_2 | c_3 << 4 (the word's low nibbles
+// paired), bytes 0 and 2 of *hi_pairs the same for its high nibbles; bytes 1
+// and 3 are left over.
+__device__ __forceinline__ void nibble_pairs(uint32_t q, uint32_t* lo_pairs, uint32_t* hi_pairs) {
+    constexpr uint32_t lo = 0x0F0F0F0Fu;
+    const uint32_t t = q >> 4, u = q >> 8;
+    *lo_pairs = (q & lo) | (t & ~lo);
+    *hi_pairs = (t & lo) | (u & ~lo);
+}
+
+// One tile row of a stage stored as ggml blocks (llama.cpp PR #26185, review
+// by GrEarl, "repack_mxfp4_blocks is bit-exact": 17 bytes per 32 inputs, the
+// E8M0 byte unchanged, then byte j holding code j in the low and code j + 16
+// in the high nibble) -> the row of the two A chunks (128-byte swizzled, code
+// 2i in the low nibble of byte i, as the compressed-tensors layout stores
+// them) and the row's bytes of the stage's four scale atoms.  The stage is
+// converted in place: every row is read into registers before the barrier,
+// then written.
+__device__ __forceinline__ void gg_convert_row(uint8_t* st, int r, uint32_t offSA) {
+    uint32_t R[kGgRowBytes / 4 + 1];
+    const uint4* src = reinterpret_cast<const uint4*>(st + r * kGgRowBytes);
+#pragma unroll
+    for (int i = 0; i < kGgRowBytes / 16; ++i) {
+        const uint4 v = src[i];
+        R[4 * i] = v.x;
+        R[4 * i + 1] = v.y;
+        R[4 * i + 2] = v.z;
+        R[4 * i + 3] = v.w;
+    }
+    R[kGgRowBytes / 4] = 0;
+    named_bar_sync(kGgBar, kGgThreads);
+#pragma unroll
+    for (int b = 0; b < 4 * kChunks * 2; ++b) {
+        const int o = 17 * b + 1, wi = o >> 2, sh = 8 * (o & 3);
+        uint32_t L[4], H[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nibble_pairs(__funnelshift_r(R[wi + i], R[wi + i + 1], sh), &L[i], &H[i]);
+        uint4 n;
+        n.x = __byte_perm(L[0], L[1], 0x6420);  // codes 0..7
+        n.y = __byte_perm(L[2], L[3], 0x6420);  // codes 8..15
+        n.z = __byte_perm(H[0], H[1], 0x6420);  // codes 16..23
+        n.w = __byte_perm(H[2], H[3], 0x6420);  // codes 24..31
+        const int chunk = b >> 3, unit = b & 7;
+        *reinterpret_cast<uint4*>(st + chunk * kChunkA + r * 128 + ((unit ^ (r & 7)) << 4)) = n;
+    }
+#pragma unroll
+    for (int g = 0; g < 2 * kChunks; ++g) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int o = 17 * (4 * g + j);
+            v |= ((R[o >> 2] >> (8 * (o & 3))) & 0xFFu) << (8 * j);
+        }
+        *reinterpret_cast<uint32_t*>(st + offSA + g * 512 + 16 * (r & 31) + 4 * (r >> 5)) = v;
+    }
+}
+
 // where expert e's weights sit in the weight arrays: its own index, or the
 // cache slot that holds it (a slot outside the arrays is an error: slot 0 is
 // read instead and the status word records it)
@@ -204,26 +285,32 @@ __device__ __forceinline__ int weight_slot(const MxArgs& p, int e) {
     return s;
 }
 
-template <int TERMS>
-__global__ void __launch_bounds__(kMxThreads, 1)
+template <int TERMS, bool GG>
+__global__ void __launch_bounds__(GG ? kMxThreads + kGgThreads : kMxThreads, 1)
 mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                  MxArgs p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t raw[GG ? kMaxStages : 1];  // ggml: the stage's copies landed
     __shared__ uint32_t tmem_holder;
     __shared__ int abort_s;
     volatile int* abort_flag = &abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t NB = static_cast<uint32_t>(p.N) * 128;  // B bytes per chunk
-    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms
-    const uint32_t offB = kStageA, offSA = kStageA + kChunks * NB, offSB = offSA + kChunks * 1024;
+    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms;
+    // ggml weights: A chunks | SFA atoms | B chunks | SFB atoms, so that the
+    // stage's 17-byte blocks land on the A and SFA bytes they become
+    const uint32_t offB = GG ? kStageA + kChunks * 1024 : kStageA;
+    const uint32_t offSA = GG ? kStageA : kStageA + kChunks * NB;
+    const uint32_t offSB = GG ? offB + kChunks * NB : offSA + kChunks * 1024;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.RS; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1);   // the copies (or, ggml, the converting threads)
             mbar_init(&empty[s], 2);  // one commit per MMA issuer
+            if (GG) mbar_init(&raw[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 2);
@@ -261,6 +348,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int nch = min(kChunks, p.KC - c0);
         const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
         const int y = e * p.rows + c.tile * 128;
+        if (GG) {  // one box of 32-bit words: 128 rows x 272 bytes (K is a multiple of 512)
+            tma_load_2d(st, tm, bar, c.ks * (kGgRowBytes / 4), y);
+            return;
+        }
         for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
         bulk_load(st + offSA, p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
                   nch * 1024, bar);
@@ -272,8 +363,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024, bar);
     };
     auto a_bytes = [&](const Cursor& c) {
+        if (GG) return static_cast<uint32_t>(kGgStageBytes);
         return static_cast<uint32_t>(min(kChunks, p.KC - c.ks * kChunks)) * (kChunkA + 1024);
     };
+    // the barrier the stage's copies complete on
+    auto ld_bar = [&](int s) { return GG ? &raw[s] : &full[s]; };
     auto b_bytes = [&](const Cursor& c) {
         return static_cast<uint32_t>(min(kChunks, p.KC - c.ks * kChunks)) * (NB + 1024);
     };
@@ -285,8 +379,8 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             early = min(p.RS, w1 - w0);
             for (int j = 0; j < early; ++j) {
                 uint8_t* st = smem + static_cast<size_t>(j) * p.stage_bytes;
-                mbar_expect_tx_only(&full[j], a_bytes(c));
-                issue_a(c, weight_slot(p, p.active[c.u]), st, &full[j]);
+                mbar_expect_tx_only(ld_bar(j), a_bytes(c));
+                issue_a(c, weight_slot(p, p.active[c.u]), st, ld_bar(j));
                 c.next(p);
             }
         }
@@ -312,13 +406,13 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (int w = w0; w < w1; ++w) {
                 uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
                 if (issued < early) {
-                    mbar_expect_tx(&full[s], b_bytes(c));  // the arrival of the stage
-                    issue_b(c, st, &full[s]);
+                    mbar_expect_tx(ld_bar(s), b_bytes(c));  // the arrival of the stage
+                    issue_b(c, st, ld_bar(s));
                 } else {
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70)) break;
-                    mbar_expect_tx(&full[s], a_bytes(c) + b_bytes(c));
-                    issue_a(c, e, st, &full[s]);
-                    issue_b(c, st, &full[s]);
+                    mbar_expect_tx(ld_bar(s), a_bytes(c) + b_bytes(c));
+                    issue_a(c, e, st, ld_bar(s));
+                    issue_b(c, st, ld_bar(s));
                 }
                 ++issued;
                 if (++s == p.RS) {
@@ -332,7 +426,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             // copies still in flight (after an abort) finish before the CTA exits
             for (int j = issued > p.RS ? issued - p.RS : 0; j < issued; ++j) {
                 const uint64_t t0 = global_ns();
-                while (!mbar_try_wait(&full[j % p.RS], (j / p.RS) & 1) &&
+                while (!mbar_try_wait(ld_bar(j % p.RS), (j / p.RS) & 1) &&
                        global_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -389,6 +483,25 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     ph ^= 1;
                 }
                 if (++ks == p.KS) ks = 0;
+            }
+        }
+    } else if (GG && warp >= kMxThreads / 32) {
+        // ------------------------ ggml block conversion -----------------------
+        // thread r converts tile row r of every stage, in stage order, and the
+        // last of the 128 to finish hands the stage to the MMA issuers
+        const int r = threadIdx.x - kMxThreads;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int w = w0; w < w1; ++w) {
+            const bool ok = mbar_wait(&raw[s], ph, abort_flag, p.hdr, 76);
+            if (!named_bar_and(kGgBar, kGgThreads, ok)) break;
+            gg_convert_row(smem + static_cast<size_t>(s) * p.stage_bytes, r, offSA);
+            fence_proxy_async();  // the MMA and tcgen05.cp read these bytes through the async proxy
+            named_bar_sync(kGgBar, kGgThreads);
+            if (r == 0) mbar_arrive(&full[s]);
+            if (++s == p.RS) {
+                s = 0;
+                ph ^= 1;
             }
         }
     } else {
@@ -794,7 +907,7 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
     return m;
 }
 
-template <int TERMS>
+template <int TERMS, bool GG>
 cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p, int grid, cudaStream_t s,
                           const char* name) {
     p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 2048), 1024));
@@ -809,15 +922,47 @@ cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p,
     cudaGetDevice(&dev);
     std::atomic<int>& cur = set_bytes[dev & 63];
     if (cur.load() < static_cast<int>(smem)) {
-        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel<TERMS>,
+        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel<TERMS, GG>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cur.store(static_cast<int>(smem));
     }
-    const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS>, dim3(grid), dim3(kMxThreads), smem, s, a, a3, p);
+    const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS, GG>, dim3(grid),
+                                     dim3(GG ? kMxThreads + kGgThreads : kMxThreads), smem, s, a, a3, p);
     trace_mark(name, s);
     return e;
+}
+
+// A operands of the three matrices over `nslots` expert slots.  Compressed-
+// tensors codes: [slots * rows, K / 2] bytes, boxes of 128 bytes (256 inputs)
+// x 128 rows, 128-byte swizzle.  ggml blocks: [slots * rows, K / 32 * 17]
+// bytes as 32-bit words, boxes of 68 words (one 512-input stage) x 128 rows,
+// no swizzle (the converting threads swizzle).
+bool make_weight_maps(const uint8_t* w1, const uint8_t* w3, const uint8_t* w2, int d, int f, uint64_t nslots,
+                      bool ggml, CUtensorMap* t1, CUtensorMap* t3, CUtensorMap* t2) {
+    if (ggml) {
+        const uint64_t rb_d = static_cast<uint64_t>(d) / 32 * 17, rb_f = static_cast<uint64_t>(f) / 32 * 17;
+        return make_tmap_rows(t1, w1, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_d, rb_d / 4, nslots * f, kGgRowBytes / 4,
+                              128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+               make_tmap_rows(t3, w3, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_d, rb_d / 4, nslots * f, kGgRowBytes / 4,
+                              128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+               make_tmap_rows(t2, w2, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_f, rb_f / 4, nslots * d, kGgRowBytes / 4,
+                              128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    return make_tmap_rows(t1, w1, CU_TENSOR_MAP_DATA_TYPE_UINT8, d / 2, d / 2, nslots * f, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tmap_rows(t3, w3, CU_TENSOR_MAP_DATA_TYPE_UINT8, d / 2, d / 2, nslots * f, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tmap_rows(t2, w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, f / 2, f / 2, nslots * d, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int TERMS>
+cudaError_t launch_stream_fmt(bool ggml, const CUtensorMap& a, const CUtensorMap& a3, const MxArgs& p, int grid,
+                              cudaStream_t s, const char* name) {
+    return ggml ? launch_stream<TERMS, true>(a, a3, p, grid, s, name)
+                : launch_stream<TERMS, false>(a, a3, p, grid, s, name);
 }
 
 }  // namespace
@@ -848,16 +993,10 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
         trace_mark("quantize_x", s);
         if (e != cudaSuccess) return e;
     }
-    // A operands: packed E2M1 codes as [slots * rows, K / 2] bytes (a slot per
-    // expert, or the cache's slots), boxes of 128 bytes (256 inputs) x 128 rows
+    // A operands over a slot per expert, or over the cache's slots
     const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
     CUtensorMap t1, t3, t2;
-    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2, nslots * a.d, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_weight_maps(a.w1_q, a.w3_q, a.w2_q, a.d, a.f, nslots, a.ggml != 0, &t1, &t3, &t2))
         return cudaErrorNotSupported;
 
     MxArgs up{};
@@ -887,7 +1026,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
 
-    if ((e = launch_stream<kTerms>(t1, t3, up, grid_up, s, "decode_up"))) return e;
+    if ((e = launch_stream_fmt<kTerms>(a.ggml != 0, t1, t3, up, grid_up, s, "decode_up"))) return e;
 
     const int warps = m.umax * a.T * (a.f / 256);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
@@ -912,7 +1051,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     dn.part = m.y;
     dn.rows_out = a.d;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream<kTerms>(t2, t2, dn, grid_dn, s, "decode_down"))) return e;
+    if ((e = launch_stream_fmt<kTerms>(a.ggml != 0, t2, t2, dn, grid_dn, s, "decode_down"))) return e;
 
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
@@ -994,12 +1133,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
 
     const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
     CUtensorMap t1, t3, t2;
-    if (!make_tmap_rows(&t1, a.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t3, a.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.d / 2, a.d / 2, nslots * a.f, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_rows(&t2, a.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.f / 2, a.f / 2, nslots * a.d, 128, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_weight_maps(a.w1_q, a.w3_q, a.w2_q, a.d, a.f, nslots, a.ggml != 0, &t1, &t3, &t2))
         return cudaErrorNotSupported;
 
     MxArgs up{};
@@ -1029,7 +1163,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     up.hdr = a.hdr;
     // every CTA's range must be at least one tile long: there are at least k units
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
-    if ((e = launch_stream<kUnitTerms>(t1, t3, up, grid_up, s, "units_up"))) return e;
+    if ((e = launch_stream_fmt<kUnitTerms>(a.ggml != 0, t1, t3, up, grid_up, s, "units_up"))) return e;
 
     const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 256);
     const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
@@ -1055,7 +1189,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     dn.part = m.y;
     dn.rows_out = a.d;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream<kUnitTerms>(t2, t2, dn, grid_dn, s, "units_down"))) return e;
+    if ((e = launch_stream_fmt<kUnitTerms>(a.ggml != 0, t2, t2, dn, grid_dn, s, "units_down"))) return e;
 
     // the y slots are strided by units x kUnitTokens rows; the grid's y index is the token
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);

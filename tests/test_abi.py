@@ -75,7 +75,7 @@ A1 = 0x10001
 def desc(k3, **over):
     d = k3.LayerDesc()
     d.E, d.k, d.d, d.f, d.d_router = 896, 16, 3584, 3072, 3584
-    d.act, d.path, d.D, d.eps, d.reserved = 0, 0, 0, 0.0, 0
+    d.act, d.path, d.D, d.eps, d.format = 0, 0, 0, 0.0, 0
     for name in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf", "router_w", "router_b"):
         setattr(d, name, A16)
     for k_, v in over.items():
@@ -131,7 +131,14 @@ def test_forward_validation(k3):
     assert fwd(desc(k3, k=17, E=16)) == 2
     assert fwd(desc(k3, E=2000)) == 2
     assert fwd(desc(k3, act=1)) == 8
-    assert fwd(desc(k3, reserved=1)) == 1
+    assert fwd(desc(k3, format=2)) == 1
+    # ggml blocks: no separate scales; rows of whole 16-byte units; streaming path only
+    assert fwd(desc(k3, format=1, w2_sf=None, w3_sf=None, w1_sf=None, w1_q=A16 + 16), ws=16) == 4
+    assert fwd(desc(k3, format=1, d=3584 - 256, d_router=3584 - 256)) == 2
+    assert fwd(desc(k3, format=1, f=3072 + 256)) == 2
+    assert fwd(desc(k3, format=1, path=2)) == 8
+    assert fwd(desc(k3, format=1), T=1025) == 8
+    assert fwd(desc(k3, format=1, w2_q=A1)) == 3
     assert fwd(desc(k3, path=7)) == 1
     assert fwd(desc(k3, w2_sf=None)) == 1
     assert fwd(desc(k3, d=192, d_router=192)) == 2  # the tensor-core K chunks are 256 wide
