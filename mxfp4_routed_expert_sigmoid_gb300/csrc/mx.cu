@@ -348,13 +348,14 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int nch = min(kChunks, p.KC - c0);
         const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
         const int y = e * p.rows + c.tile * 128;
-        if (GG) {  // one box of 32-bit words: 128 rows x 272 bytes (K is a multiple of 512)
+        if constexpr (GG) {  // one box of 32-bit words: 128 rows x 272 bytes (K is a multiple of 512)
             tma_load_2d(st, tm, bar, c.ks * (kGgRowBytes / 4), y);
-            return;
+        } else {
+            for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
+            bulk_load(st + offSA,
+                      p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
+                      nch * 1024, bar);
         }
-        for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
-        bulk_load(st + offSA, p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
-                  nch * 1024, bar);
     };
     auto issue_b = [&](const Cursor& c, uint8_t* st, uint64_t* bar) {
         const int c0 = c.ks * kChunks;
