@@ -43,8 +43,8 @@ EXPERT_MATRIX_BYTES = None  # filled per config
 # copy of the layer: one token touches 16 experts either way, so a launch moves
 # the same bytes as in the 896-expert layer.
 TRAFFIC = {
-    ("decode_t1", "decode_up"): 187_272_192 + 3_737_856,
-    ("decode_t1", "decode_down"): 94_225_920 + 2_310_400,
+    ("decode_t1", "decode_up"): 187_269_376 + 3_475_968,
+    ("decode_t1", "decode_down"): 94_227_200 + 2_305_024,
 }
 
 
