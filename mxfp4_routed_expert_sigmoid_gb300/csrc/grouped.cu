@@ -296,7 +296,7 @@ constexpr size_t exp_smem_bytes() {
     size_t b = 1024;
     b += static_cast<size_t>(C::AS) * NA * kTileA;
     b += static_cast<size_t>(C::BS) * C::BN * BK * 2;
-    b += static_cast<size_t>(C::RS) * NA * kTileRaw;
+    b += static_cast<size_t>(C::RS) * NA * (kTileRaw + 512);
     b += static_cast<size_t>(kES) * NA * BM * 4;
     b += 512;
     return b;
@@ -313,7 +313,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint8_t* sA = smem;                                // [AS][NA][16 KB]
     uint8_t* sB = sA + AS * NA * kTileA;               // [BS][BN * 128]
     uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RS][NA][4 KB]
-    int* sE = reinterpret_cast<int*>(sRaw + RS * NA * kTileRaw);  // [kES][NA][128]
+    uint8_t* sRawSf = sRaw + RS * NA * kTileRaw;       // [RS][NA][512]: the stage's scale atom
+    int* sE = reinterpret_cast<int*>(sRawSf + RS * NA * 512);  // [kES][NA][128]
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(sE + kES * NA * BM);
     uint64_t* raw_empty = raw_full + RS;
     uint64_t* b_full = raw_empty + RS;
@@ -380,13 +381,19 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 const int4 tl = p.tiles[1 + tile];
                 const int arow = tl.x * p.rows_per_expert + tl.w * BM;
+                // the tile's prepared scale atoms, one per 128 inputs (two stages)
+                const size_t atoms = static_cast<size_t>(tl.x * (p.rows_per_expert / BM) + tl.w) * (p.K / 128) * 512;
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&raw_empty[r], ph ^ 1, abort_flag, p.hdr, 50)) { ok = false; break; }
-                    mbar_expect_tx(&raw_full[r], NA * kTileRaw);
+                    mbar_expect_tx(&raw_full[r], NA * (kTileRaw + 512));
+                    const size_t atom = atoms + static_cast<size_t>(ks >> 1) * 512;
                     tma_load_2d(sRaw + (r * NA) * kTileRaw, &tmA, &raw_full[r], ks * BK / 2, arow);
-                    if (NA == 2)
+                    bulk_load(sRawSf + (r * NA) * 512, p.s1 + atom, 512, &raw_full[r]);
+                    if (NA == 2) {
                         tma_load_2d(sRaw + (r * NA + 1) * kTileRaw, &tmA3, &raw_full[r], ks * BK / 2, arow);
+                        bulk_load(sRawSf + (r * NA + 1) * 512, p.s3 + atom, 512, &raw_full[r]);
+                    }
                     if (++r == RS) { r = 0; ph ^= 1; }
                 }
                 if (!ok) break;
@@ -546,23 +553,20 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int slot = it % kES;
             const uint32_t eph = (it / kES) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&eref_full[slot], eph, abort_flag, p.hdr, 58))) break;
-            int rr = tl.w * BM + row;
-            if (rr >= p.rows_per_expert) rr = p.rows_per_expert - 1;  // padding rows: any finite data
-            const uint8_t* sc1 = sf_row(p.s1, tl.x, rr, p.rows_per_expert, p.K / 128);
-            const uint8_t* sc3 = NA == 2 ? sf_row(p.s3, tl.x, rr, p.rows_per_expert, p.K / 128) : nullptr;
             const int eref1 = sE[(slot * NA + 0) * BM + row];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + row] : 0;
+            // this thread's byte of a scale atom: row `row`, block 2 ks + half
+            const int sfo = 16 * (row & 31) + 4 * (row >> 5);
             bool ok = true;
             for (int ks = 0; ks < k_stages; ++ks) {
                 const int blk = 2 * ks + half;
-                const int so = (blk >> 2) * 512 + (blk & 3);
-                const int e1 = sc1[so];
-                const int e3 = NA == 2 ? sc3[so] : 0;
                 if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59) &&
                                                  mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
                     break;
                 }
+                const int e1 = sRawSf[(r * NA) * 512 + sfo + (blk & 3)];
+                const int e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * 512 + sfo + (blk & 3)] : 0;
 #pragma unroll
                 for (int mm = 0; mm < NA; ++mm) {
                     const uint4 raw =
