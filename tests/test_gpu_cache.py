@@ -45,7 +45,7 @@ def small(k3):
 
 def batches(cfg, n, T, seed):
     """n distinct seeded token batches [T, d] (bf16 bits) of the config's distribution."""
-    big = synth.custom(cfg.name, T=T * n, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, seed_index=seed)
+    big = synth.custom(cfg.name, T=T * n, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, D=cfg.D, seed_index=seed)
     return synth.hidden(big).reshape(n, T, -1)
 
 
@@ -163,3 +163,29 @@ def test_cache_errors(k3, small):
         k3.k3moe_forward_cached(hlayer, cache, x8, ws=k3.workspace(k3.k3moe_workspace_size(hlayer, 8)))
     assert ex.value.status == 2
     assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("T", [1, 6])
+def test_cached_block_mode(k3, T):
+    """The full latent block (RMSNorm, down-projection, router on the normed
+    width, experts, up-projection) with host-resident experts: bitwise the
+    block on device-resident experts, call after call."""
+    import torch
+
+    cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=512, f=512, D=1024, seed_index=27)
+    layer, dense, expert, _ = make_layer(cfg, on_device_experts=False)
+    hlayer = k3.host_resident(layer)
+    cache = k3.ExpertCache(hlayer, min(cfg.E, T * cfg.k + 4))
+    st = CacheState.empty(cfg.E, cache.slots)
+    big = synth.custom(cfg.name, T=T * 4, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, D=cfg.D, seed_index=28)
+    xs = synth.hidden(big).reshape(4, T, -1)
+    ws_c = k3.workspace(k3.k3moe_workspace_size(hlayer, T))
+    ws_r = k3.workspace(k3.k3moe_workspace_size(layer, T))
+    for x_np in xs:
+        x = to_dev(x_np, "cuda")
+        got = k3.k3moe_forward_cached(hlayer, cache, x, ws=ws_c)
+        ref = k3.k3moe_forward(layer, x, ws=ws_r)
+        assert k3.k3moe_get_status(ws_c) == 0
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        idx, _, _ = k3.k3moe_forward_routing(hlayer, ws_c, T)
+        check_state(k3, cache, st, cache_call(st, np.unique(idx.cpu().numpy())))

@@ -56,7 +56,7 @@ def ggml_expert(k3, glayer):
 def run(k3, cfg, layer, glayer, dense, T, n, seed, check_oracle=True):
     import torch
 
-    big = synth.custom(cfg.name, T=T * n, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, seed_index=seed)
+    big = synth.custom(cfg.name, T=T * n, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, D=cfg.D, seed_index=seed)
     xs = synth.hidden(big).reshape(n, T, -1)
     ws_g = k3.workspace(k3.k3moe_workspace_size(glayer, T))
     ws_s = k3.workspace(k3.k3moe_workspace_size(layer, T))
@@ -116,3 +116,11 @@ def test_ggml_rejections(k3, small):
     with pytest.raises(k3.K3MoEError) as ex:  # no expert cache over ggml blocks
         k3.k3moe_forward_cached(glayer, cache, x[:1])
     assert ex.value.status == 8
+
+
+@pytest.mark.parametrize("T", [1, 6, 12])
+def test_ggml_block_mode(k3, T):
+    """The full latent block over ggml blocks: bitwise the split-layout block."""
+    cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=512, f=512, D=1024, seed_index=29)
+    layer, glayer, dense = layers(k3, cfg)
+    run(k3, cfg, layer, glayer, dense, T, n=2, seed=400 + T, check_oracle=False)
