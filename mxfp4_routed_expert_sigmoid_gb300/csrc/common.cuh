@@ -426,7 +426,7 @@ struct CacheHeader {
 static_assert(sizeof(CacheHeader) == 256, "cache header is 256 bytes");
 struct CacheView {
     CacheHeader* h;
-    int32_t* slot_of;    // [E] slot holding the expert, -1 = not resident
+    int32_t* slot_of;    // [E] slot holding the expert, -1 = not resident; right after the header
     int32_t* expert_of;  // [S] expert in the slot, -1 = empty
     uint32_t* stamp;     // [S] clock of the slot's last use (0 = never)
     int32_t* miss_e;     // [S] experts to fetch in this call, ascending

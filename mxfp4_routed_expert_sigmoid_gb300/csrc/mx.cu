@@ -273,10 +273,17 @@ __device__ __forceinline__ void gg_convert_row(uint8_t* st, int r, uint32_t offS
 }
 
 // where expert e's weights sit in the weight arrays: its own index, or the
-// cache slot that holds it (a slot outside the arrays is an error: slot 0 is
-// read instead and the status word records it)
+// cache slot that holds it.  The map is read only if the cache header in
+// front of it was set up for these sizes (the state buffer is then large
+// enough); otherwise, or for a slot outside the arrays, slot 0 is read
+// instead and the status word records the error.
 __device__ __forceinline__ int weight_slot(const MxArgs& p, int e) {
     if (!p.slot_of) return e;
+    const CacheHeader* h = reinterpret_cast<const CacheHeader*>(p.slot_of) - 1;
+    if (h->magic != kCacheMagic || h->E != p.E || h->slots != p.nslots) {
+        set_error(p.hdr, K3MOE_ERR_INVALID_ARG, 73);
+        return 0;
+    }
     const int s = p.slot_of[e];
     if (s < 0 || s >= p.nslots) {
         set_error(p.hdr, K3MOE_ERR_INVALID_ARG, 72);
