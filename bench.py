@@ -326,8 +326,7 @@ def ours_arm(args):
         step(i)
         idx, _, _ = k3.k3moe_forward_routing(layer, ws, cfg.T, with_logits=False)
         uniq.append(len(torch.unique(idx)))
-    if k3.k3moe_get_status(ws) != 0:
-        raise RuntimeError("device status error during setup")
+    check_status(k3, ws)
 
     # one CUDA graph per token batch: the forward's launches replay back to
     # back on the device, without host launch overhead between them
@@ -544,11 +543,11 @@ def cached_arm(args):
     # set-up forward is a call of the cache too)
     for i in range(args.pool):
         k3.k3moe_forward_cached(hlayer, cache, pool[i], out=out, ws=ws)
+    torch.cuda.synchronize()
     graphs = [k3.ForwardGraph(hlayer, pool[i], out, ws, cache=cache) for i in range(args.pool)]
     for i in range(max(args.warmup, 3)):
         graphs[i % args.pool].launch(stream)
-    if k3.k3moe_get_status(ws) != 0:
-        raise RuntimeError("device status error during setup")
+    check_status(k3, ws)
     before = cache.stats()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -627,6 +626,16 @@ def cached_arm(args):
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def check_status(k3, ws):
+    """Raise with the device status word and the place it was set, if any."""
+    import torch
+
+    torch.cuda.synchronize()
+    code, info = ws[:8].view(torch.int32).cpu().tolist()
+    if k3.k3moe_get_status(ws) != 0:
+        raise RuntimeError(f"device status {k3.STATUS.get(code, code)} (where: {info}) during setup")
 
 
 def dtype_of(T: int, path: int) -> str:

@@ -301,8 +301,10 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
 /* CUDA graph of one k3moe_forward with fixed buffers, for callers that run
  * the same layer call repeatedly (a decode loop): the graph replays every
  * kernel of the forward back to back on the device, without per-kernel host
- * launch overhead.  k3moe_graph_create runs the forward once on a private
- * stream (one-time set-up), then captures it (thread-local capture mode) and
+ * launch overhead.  k3moe_graph_create waits for the device to be idle
+ * (cudaDeviceSynchronize: earlier work on any stream may use the same
+ * workspace or cache), runs the forward once on a private stream (one-time
+ * set-up), then captures it (thread-local capture mode) and
  * instantiates the executable graph; it allocates the graph objects (host and
  * driver), which k3moe_graph_destroy frees.  The buffers named here must stay
  * valid while the graph exists; new inputs are written into `hidden` in place.

@@ -688,6 +688,9 @@ k3moe_status graph_create(const k3moe_layer_desc* desc, const k3moe_expert_cache
                           void** graph_out) {
     if (!graph_out) return K3MOE_ERR_INVALID_ARG;
     *graph_out = nullptr;
+    // the set-up forward runs on a private stream: work the caller queued on
+    // its own streams (which may use the same workspace or cache) finishes first
+    if (cudaDeviceSynchronize() != cudaSuccess) return K3MOE_ERR_CUDA;
     cudaStream_t cs = nullptr;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return K3MOE_ERR_CUDA;
     // one uncaptured forward: argument checks and one-time set-up

@@ -189,3 +189,28 @@ def test_cached_block_mode(k3, T):
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
         idx, _, _ = k3.k3moe_forward_routing(hlayer, ws_c, T)
         check_state(k3, cache, st, cache_call(st, np.unique(idx.cpu().numpy())))
+
+
+def test_graph_after_queued_calls(k3, small):
+    """Graph creation right after eager calls still queued on the caller's
+    stream: its set-up forward (on a private stream) must not overlap them."""
+    import torch
+
+    cfg, layer, hlayer, dense, expert = small
+    T, S = 1, 8
+    cache = k3.ExpertCache(hlayer, S)
+    xs = batches(cfg, 5, T, 88)
+    ws = k3.workspace(k3.k3moe_workspace_size(hlayer, T))
+    out = torch.empty((T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    idxs = []
+    for i in range(4):  # no synchronisation in between
+        k3.k3moe_forward_cached(hlayer, cache, to_dev(xs[i], "cuda"), out=out, ws=ws)
+        idxs.append(k3.k3moe_forward_routing(hlayer, ws, T, with_logits=False)[0])
+    g = k3.ForwardGraph(hlayer, to_dev(xs[4], "cuda"), out, ws, cache=cache)
+    idxs.append(k3.k3moe_forward_routing(hlayer, ws, T, with_logits=False)[0])
+    assert k3.k3moe_get_status(ws) == 0
+    st = CacheState.empty(cfg.E, S)
+    for idx in idxs:
+        call = cache_call(st, np.unique(idx.cpu().numpy()))
+    check_state(k3, cache, st, call)
+    g.close()
