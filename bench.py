@@ -12,7 +12,7 @@ than L2), and a 256 MB buffer is written between steps (outside the timed
 kernels) to flush L2 of the previous step's router and activation bytes.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-(the reference arm of this build) on the same workload instead.
+(the float64 NumPy statement of the layer) on the same workload instead.
 Multi-GPU (torchrun): every rank runs an independent replica with its own
 weights (the layer is data-parallel over tokens; no collective on the path).
 """
