@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--format", choices=["split", "ggml"], default="split",
                     help="expert weight format: compressed-tensors codes + scales, or llama.cpp "
                          "17-byte MXFP4 blocks read directly by the streaming kernels")
+    ap.add_argument("--prepared", action="store_true",
+                    help="hand the kernels the scales in the prepared atom layout instead of the "
+                         "checkpoint's canonical E8M0 rows")
     ap.add_argument("--cache-slots", type=int, default=0,
                     help="host-resident experts behind a device cache of this many experts "
                          "(k3moe_forward_cached); 0 = experts resident in HBM")
@@ -297,7 +300,7 @@ def ours_arm(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     kw = dict(router_w=dv(dense["router_w"]), router_b=dv(dense["router_b"]), k=cfg.k,
-              path=args.path, **ex)
+              path=args.path, prepared=args.prepared, **ex)
     if cfg.block:
         kw.update(norm_gamma=dv(dense["norm_gamma"]), w_down=dv(dense["w_down"]),
                   w_up=dv(dense["w_up"]), eps=dense["eps"])
@@ -465,7 +468,9 @@ def ours_arm(args):
         "dtype": dtype_of(cfg.T, args.path),
         "data": "synthetic (seeded; random-init weights of the K3 layer shapes)",
         "config": dict(workload_config(cfg, args.pool),
-                       **({"weight_format": "ggml 17-byte MXFP4 blocks"} if args.format == "ggml" else {})),
+                       weight_format=("ggml 17-byte MXFP4 blocks" if args.format == "ggml" else
+                                      "codes + E8M0 scales, " +
+                                      ("prepared atoms" if args.prepared else "canonical rows"))),
         "hbm_gbs_step": step_bytes / (mean_ms * 1e-3) / 1e9,
         "experts_touched_per_step": u_mean,
         "kernels_ms": kern_mean,
@@ -511,7 +516,7 @@ def cached_arm(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     layer = k3.MoELayer(router_w=dv(dense["router_w"]), router_b=dv(dense["router_b"]), k=cfg.k,
-                        path=args.path, **synth.experts_torch(cfg, dev))
+                        path=args.path, prepared=args.prepared, **synth.experts_torch(cfg, dev))
     hlayer = k3.host_resident(layer)
     del layer
     torch.cuda.empty_cache()

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define K3MOE_ABI_VERSION 3
+#define K3MOE_ABI_VERSION 4
 
 typedef enum k3moe_status {
     K3MOE_OK = 0,
@@ -70,39 +70,56 @@ typedef enum k3moe_act {
     K3MOE_ACT_SILU_GATED = 0
 } k3moe_act;
 
-/* Expert-path selector.  AUTO picks DECODE for T <= 1024 and GROUPED
- * otherwise; DECODE with T > 1024 returns K3MOE_ERR_UNSUPPORTED.
- *   DECODE : block-scaled tcgen05 MMAs (kind::mxf4) streaming the selected
- *            experts' E2M1 codes by TMA, E8M0 scales applied by the tensor
- *            cores, activations as E2M1 terms; split over the SMs.  Up to 8
- *            tokens every active expert takes all tokens; beyond that each
- *            expert's tokens are cut into units of at most 16 (four E2M1
- *            terms per token) and an expert's weights are streamed once per
- *            unit.
- *   GROUPED: tcgen05 grouped GEMMs with in-shared-memory MXFP4 -> f16
- *            dequantisation, TMA-fed, TMEM accumulators. */
+/* Expert-path selector.  AUTO picks BLOCK_SCALED for T <= 1024 and
+ * BF16_DEQUANT otherwise; BLOCK_SCALED with T > 1024 returns
+ * K3MOE_ERR_UNSUPPORTED.
+ *   BLOCK_SCALED: block-scaled tcgen05 MMAs (kind::mxf4) streaming the
+ *            selected experts' E2M1 codes by TMA, E8M0 scales applied by the
+ *            tensor cores, activations as E2M1 terms (five per token up to 8
+ *            tokens, four beyond: each term encodes what the previous ones
+ *            left over, with its own E8M0 scale per 32 inputs); split over
+ *            the SMs.  Up to 8 tokens every active expert takes all tokens;
+ *            beyond that each expert's tokens are cut into units of at most
+ *            16 and an expert's weights are streamed once per unit.  This is
+ *            the block-scaled option of the layer's design; activations
+ *            quantised once to MXFP8 (E4M3 elements) instead of E2M1 terms
+ *            leave an output error of several percent of the row RMS, over
+ *            the layer's bound, so they are not offered.
+ *   BF16_DEQUANT: tcgen05 grouped GEMMs with in-shared-memory dequantisation
+ *            of the MXFP4 weights to f16 (exact: an E2M1 value times a power
+ *            of two within f16's range; same tensor-core rate as bf16),
+ *            TMA-fed, TMEM accumulators; f16 token rows.
+ * DECODE and GROUPED are the names of ABI version 3 for the same values. */
 typedef enum k3moe_path {
     K3MOE_PATH_AUTO = 0,
-    K3MOE_PATH_DECODE = 1,
-    K3MOE_PATH_GROUPED = 2
+    K3MOE_PATH_BLOCK_SCALED = 1,
+    K3MOE_PATH_BF16_DEQUANT = 2,
+    K3MOE_PATH_DECODE = K3MOE_PATH_BLOCK_SCALED,
+    K3MOE_PATH_GROUPED = K3MOE_PATH_BF16_DEQUANT
 } k3moe_path;
 
 /* One MoE layer.  All pointers are device memory owned by the caller and must
  * stay valid while work that uses them is in flight.
  *
  * Expert weights ([PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact"):
- * compressed-tensors MXFP4, logical [out, in] per expert; `*_q` holds two
+ * compressed-tensors MXFP4, logical [out, in] per expert, exactly as the
+ * checkpoint stores each weight_packed / weight_scale pair.  `*_q` holds two
  * E2M1 codes per byte (element 2i in the low nibble, sign in bit 3,
- * magnitudes [0,.5,1,1.5,2,3,4,6]) and is 32-byte aligned:
- *   w1_q [E, f, d/2]   gate projection
- *   w3_q [E, f, d/2]   up projection
- *   w2_q [E, d, f/2]   down projection
- * The E8M0 block scales (one byte e per 32 consecutive inputs, value
- * 2^(e-127), e = 255 not allowed) are passed in the prepared layout that
- * k3moe_prepare_scales writes from the canonical [rows, in/32] arrays, one
- * prepared array per matrix (E * rows * in / 32 bytes each):
- *   w1_sf  from w1_s [E, f, d/32]     w3_sf  from w3_s [E, f, d/32]
- *   w2_sf  from w2_s [E, d, f/32]
+ * magnitudes [0,.5,1,1.5,2,3,4,6]) and is 32-byte aligned; `*_s` holds one
+ * E8M0 byte e per 32 consecutive inputs of a row (value 2^(e-127); e = 255,
+ * NaN in the format, is not allowed), 16-byte aligned:
+ *   w1_q [E, f, d/2]   w1_s [E, f, d/32]   gate projection
+ *   w3_q [E, f, d/2]   w3_s [E, f, d/32]   up projection
+ *   w2_q [E, d, f/2]   w2_s [E, d, f/32]   down projection
+ * d and f are multiples of 64.  When d and f are multiples of 512 the kernels
+ * read the scale rows as they are (a TMA box of 16 bytes x 128 rows per
+ * 512-input stage, re-laid in shared memory); otherwise each forward first
+ * rewrites all three scale arrays into the prepared layout in its workspace
+ * (1/32 of the expert bytes, read and written once per call).
+ * Optional fast path: w1_sf, w3_sf, w2_sf, the same scales in the prepared
+ * layout that k3moe_prepare_scales writes (all three or none; NULL = use the
+ * canonical arrays).  When given they are read instead of w*_s, which may
+ * then be NULL.
  * Router ([PR26185], GrEarl, "Dry run"): logits l = x_r W_r^T, scores
  * s = sigmoid(l); the k experts with the largest s + b are selected (ties to
  * the lower index, slots listed in that order); combine weights are
@@ -112,17 +129,18 @@ typedef enum k3moe_path {
  * [T, d], and the output is W_up applied to the combined latent rows.
  *
  * Weight format (`format`):
- *   K3MOE_FORMAT_SPLIT (0): the codes and prepared scales above.
+ *   K3MOE_FORMAT_SPLIT (0): the codes and scales above.
  *   K3MOE_FORMAT_GGML  (1): llama.cpp's MXFP4 blocks, as k3moe_repack_mxfp4
  *     writes them ([PR26185], GrEarl, "repack_mxfp4_blocks is bit-exact"):
  *     w1_q [E, f, d/32, 17], w3_q [E, f, d/32, 17], w2_q [E, d, f/32, 17]
  *     (byte 0 of a block = the E8M0 byte e, bytes 1..16 = element j in the
  *     low and element j + 16 in the high nibble of byte j), 16-byte aligned;
- *     w1_sf, w3_sf, w2_sf unused (may be NULL).  The streaming kernels read
- *     the blocks as they are and convert them in shared memory; the result
- *     is bitwise that of the SPLIT format on the same weights.  d and f
- *     must be multiples of 512 (rows of whole 16-byte units); the DECODE
- *     path only (T <= 1024) and no expert cache (UNSUPPORTED otherwise). */
+ *     the scale pointers are unused (may be NULL).  The streaming kernels
+ *     read the blocks as they are and convert them in shared memory; the
+ *     result is bitwise that of the SPLIT format on the same weights.  d and
+ *     f must be multiples of 512 (rows of whole 16-byte units); the
+ *     BLOCK_SCALED path only (T <= 1024) and no expert cache (UNSUPPORTED
+ *     otherwise). */
 typedef enum k3moe_format {
     K3MOE_FORMAT_SPLIT = 0,
     K3MOE_FORMAT_GGML = 1
@@ -131,8 +149,8 @@ typedef enum k3moe_format {
 typedef struct k3moe_layer_desc {
     int32_t E;          /* routed experts (896) */
     int32_t k;          /* experts per token (16), 1 <= k <= min(E, 32) */
-    int32_t d;          /* latent width (3584), multiple of 256 */
-    int32_t f;          /* expert hidden width (3072), multiple of 256 */
+    int32_t d;          /* latent width (3584), multiple of 64 */
+    int32_t f;          /* expert hidden width (3072), multiple of 64 */
     int32_t d_router;   /* router input width: d (latent mode) or D (block mode) */
     int32_t act;        /* k3moe_act */
     int32_t path;       /* k3moe_path */
@@ -142,9 +160,12 @@ typedef struct k3moe_layer_desc {
     const uint8_t* w1_q;
     const uint8_t* w3_q;
     const uint8_t* w2_q;
-    const uint8_t* w1_sf;        /* prepared scales of w1 */
-    const uint8_t* w3_sf;        /* prepared scales of w3 */
-    const uint8_t* w2_sf;        /* prepared scales of w2 */
+    const uint8_t* w1_s;         /* canonical E8M0 scales of w1 */
+    const uint8_t* w3_s;         /* canonical E8M0 scales of w3 */
+    const uint8_t* w2_s;         /* canonical E8M0 scales of w2 */
+    const uint8_t* w1_sf;        /* optional: prepared scales of w1 (NULL = use w1_s) */
+    const uint8_t* w3_sf;        /* optional: prepared scales of w3 */
+    const uint8_t* w2_sf;        /* optional: prepared scales of w2 */
     const uint16_t* router_w;    /* [E, d_router] bf16 */
     const float* router_b;       /* [E] fp32 selection bias (exp_probs_b) */
     const uint16_t* norm_gamma;  /* block mode: [D] bf16 (ffn_routed_norm) */
@@ -177,24 +198,30 @@ k3moe_status k3moe_repack_mxfp4(const uint8_t* packed, const uint8_t* scale, int
 k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t cols,
                                 uint8_t* packed_out, uint8_t* scale_out, void* stream);
 
-/* Block-scale preparation for the tensor-core kernels.  A canonical E8M0
- * array (one byte per row and 32 inputs) is regrouped into 512-byte atoms,
- * one per tile of 128 rows and 128-wide input chunk; byte 16 (m % 32) +
- * 4 (m / 32) + b of an atom holds row m of the tile and block b of the chunk
- * (the order in which tcgen05.cp spreads scales over the TMEM lanes that the
- * block-scaled MMA reads: row m from lane m, column m / 32).  The atom of
- * (tile, chunk) starts at byte (tile * cols/128 + chunk) * 512.
- *   scale [rows, cols/32] uint8 (device; rows stacked over the experts)
- *   sf    [rows * cols/32] uint8 (device)
- * A byte permutation: bit-exact, deterministic.  rows and cols multiples of
- * 128.  The paper stores scales row by row; the atoms are this library's
- * layout.  Errors: INVALID_ARG, SHAPE, ALIGN (16-byte), CUDA. */
-k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t rows, int64_t cols, uint8_t* sf,
-                                  void* stream);
+/* Block-scale preparation for the tensor-core kernels (an optional fast
+ * path: k3moe_forward also takes the canonical arrays).  The canonical E8M0
+ * array of a weight matrix, E experts of `rows` rows with one byte per 32 of
+ * the `cols` inputs, is regrouped per expert into 512-byte atoms, one per
+ * tile of 128 rows and 128-wide input group (ceil(rows / 128) tiles and
+ * ceil(cols / 128) groups per expert; rows past `rows` and blocks past
+ * cols / 32 are zero): byte 16 (m % 32) + 4 (m / 32) + b of an atom holds row
+ * m of the tile and block b of the group (the order in which tcgen05.cp
+ * spreads scales over the TMEM lanes that the block-scaled MMA reads: row m
+ * from lane m, column m / 32).  The atom of (expert, tile, group) starts at
+ * byte ((e * tiles + tile) * groups + group) * 512.
+ *   scale [E, rows, cols/32] uint8 (device)
+ *   sf    k3moe_prepared_scales_size(E, rows, cols) bytes (device)
+ * A byte permutation with zero padding: bit-exact, deterministic.  rows and
+ * cols multiples of 64.  The paper stores scales row by row; the atoms are
+ * this library's layout.  Errors: INVALID_ARG, SHAPE, ALIGN (16-byte), CUDA. */
+size_t k3moe_prepared_scales_size(int64_t E, int64_t rows, int64_t cols);
+k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t E, int64_t rows, int64_t cols,
+                                  uint8_t* sf, void* stream);
 
-/* Inverse of k3moe_prepare_scales (prepared atoms -> canonical array). */
-k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* scale,
-                                    void* stream);
+/* Inverse of k3moe_prepare_scales (prepared atoms -> canonical array; the
+ * padding is not read). */
+k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t E, int64_t rows, int64_t cols,
+                                    uint8_t* scale, void* stream);
 
 /* Workspace bytes that k3moe_route needs for T tokens and E experts. */
 size_t k3moe_route_workspace_size(int32_t T, int32_t E);
@@ -210,8 +237,9 @@ size_t k3moe_route_workspace_size(int32_t T, int32_t E);
  *   logits_out [T, E] fp32 or NULL  the fp32 logits the selection used
  *   ws, ws_bytes                 scratch >= k3moe_route_workspace_size(T, E)
  * Logits accumulate bf16 products in fp32; s = 1 / (1 + expf(-l)) and
- * s + b are fp32.  Errors: INVALID_ARG, SHAPE (k > 32, k > E, d_r % 8), ALIGN,
- * WORKSPACE, CUDA; device: NONFINITE (a logit was not finite). */
+ * s + b are fp32.  Errors: INVALID_ARG, SHAPE (k > 32, k > E, E > 1024,
+ * d_r not a multiple of 64), ALIGN, WORKSPACE, CUDA; device: NONFINITE (a
+ * logit was not finite). */
 k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16_t* router_w,
                          const float* bias, int32_t E, int32_t k, int32_t* idx_out,
                          float* w_out, float* logits_out, void* ws, size_t ws_bytes,
@@ -232,8 +260,11 @@ k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16
  * the call.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Every call shares the array and it
+ * (cudaGetSymbolAddress, with that device current) and caches it for the
+ * life of the process; make that first call before any stream capture.  The
+ * cached address belongs to the device's current context: after
+ * cudaDeviceReset on that device, do not call this entry point again in the
+ * same process.  Every call shares the array and it
  * keeps the last call's contents: each call clears the header on `stream`
  * before its kernel, and calls whose work overlaps on the GPU (different
  * streams, or different host threads) race on it, so order them.  Device-side
@@ -303,8 +334,10 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
  * kernel of the forward back to back on the device, without per-kernel host
  * launch overhead.  k3moe_graph_create waits for the device to be idle
  * (cudaDeviceSynchronize: earlier work on any stream may use the same
- * workspace or cache), runs the forward once on a private stream (one-time
- * set-up), then captures it (thread-local capture mode) and
+ * workspace or cache; no stream of the process may be capturing in global
+ * capture mode during the call, since that synchronisation would be refused
+ * and would invalidate that capture), runs the forward once on a private
+ * stream (one-time set-up), then captures it (thread-local capture mode) and
  * instantiates the executable graph; it allocates the graph objects (host and
  * driver), which k3moe_graph_destroy frees.  The buffers named here must stay
  * valid while the graph exists; new inputs are written into `hidden` in place.
@@ -338,7 +371,12 @@ k3moe_status k3moe_graph_destroy(void* graph);
  * All cache pointers are device memory owned by the caller:
  *   w1_q  [slots, f, d/2]   w3_q [slots, f, d/2]   w2_q [slots, d, f/2]
  *         (32-byte aligned)
- *   w1_sf, w3_sf, w2_sf     prepared scale atoms, slots * f * d/32 bytes each
+ *   w1_s, w3_s, w2_s        the slots' scales, in the layout the layer
+ *                           descriptor's scales use: canonical rows
+ *                           ([slots, f, d/32], [slots, d, f/32]; d and f
+ *                           multiples of 512) or, when the descriptor gives
+ *                           prepared scales, k3moe_prepared_scales_size(slots,
+ *                           f, d) bytes each
  *   state                   bookkeeping, k3moe_cache_state_size(E, slots)
  *                           bytes, set up by k3moe_cache_init before first use
  * min(E, T*k) <= slots <= E for every call (K3MOE_ERR_SHAPE otherwise). */
@@ -348,9 +386,9 @@ typedef struct k3moe_expert_cache {
     uint8_t* w1_q;
     uint8_t* w3_q;
     uint8_t* w2_q;
-    uint8_t* w1_sf;
-    uint8_t* w3_sf;
-    uint8_t* w2_sf;
+    uint8_t* w1_s;
+    uint8_t* w3_s;
+    uint8_t* w2_s;
     void* state;
 } k3moe_expert_cache;
 
@@ -362,19 +400,19 @@ size_t k3moe_cache_state_size(int32_t E, int32_t slots);
  * Errors: INVALID_ARG, SHAPE (slots > E or E > 1024), ALIGN, CUDA. */
 k3moe_status k3moe_cache_init(void* state, int32_t E, int32_t slots, void* stream);
 
-/* k3moe_forward with the expert weights in host memory.  desc->w1_q ...
- * desc->w2_sf point to HOST arrays in the layouts k3moe_forward takes
- * (codes, and the prepared scale atoms; k3moe_prepare_scales may write them
- * through the mapped pointer), page-locked and mapped into the device
- * address space (cudaHostAlloc, or cudaHostRegister with mapping); every
- * other pointer is device memory.  The DECODE path only (T <= 1024).  The
+/* k3moe_forward with the expert weights in host memory.  The descriptor's
+ * codes and scales (the canonical w*_s, or the prepared w*_sf when given)
+ * point to HOST arrays in the layouts k3moe_forward takes, page-locked and
+ * mapped into the device address space (cudaHostAlloc, or cudaHostRegister
+ * with mapping); every other pointer is device memory.  Canonical scales need
+ * d and f multiples of 512 here.  The BLOCK_SCALED path only (T <= 1024).  The
  * call keeps the cache state between calls; calls sharing a cache must be
  * ordered on one stream.  Errors: those of k3moe_forward; INVALID_ARG (null
  * host array, or one that is not page-locked host memory by
  * cudaPointerGetAttributes, e.g. a device array; reserved != 0), SHAPE
  * (slots), UNSUPPORTED (the
- * GROUPED path); device: INVALID_ARG if the state was not initialised for
- * (E, slots). */
+ * BF16_DEQUANT path, canonical scales with d or f not a multiple of 512);
+ * device: INVALID_ARG if the state was not initialised for (E, slots). */
 k3moe_status k3moe_forward_cached(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
                                   const uint16_t* hidden, int32_t T, uint16_t* out, void* ws,
                                   size_t ws_bytes, void* stream);

@@ -23,7 +23,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libk3moe.so")
 
 ACT_SILU_GATED = 0
-PATH_AUTO, PATH_DECODE, PATH_GROUPED = 0, 1, 2
+PATH_AUTO, PATH_BLOCK_SCALED, PATH_BF16_DEQUANT = 0, 1, 2
+PATH_DECODE, PATH_GROUPED = PATH_BLOCK_SCALED, PATH_BF16_DEQUANT  # ABI version 3 names
 FORMAT_SPLIT, FORMAT_GGML = 0, 1
 
 STATUS = {
@@ -40,7 +41,8 @@ EXPORTS = (
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
-    "k3moe_trace_read", "k3moe_prepare_scales", "k3moe_unprepare_scales",
+    "k3moe_trace_read", "k3moe_prepared_scales_size", "k3moe_prepare_scales",
+    "k3moe_unprepare_scales",
     "k3moe_cache_state_size", "k3moe_cache_init", "k3moe_forward_cached",
     "k3moe_cache_read_stats", "k3moe_graph_create_cached",
 )
@@ -60,6 +62,7 @@ class LayerDesc(ctypes.Structure):
         ("path", ctypes.c_int32), ("D", ctypes.c_int32), ("eps", ctypes.c_float),
         ("format", ctypes.c_int32),
         ("w1_q", ctypes.c_void_p), ("w3_q", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
+        ("w1_s", ctypes.c_void_p), ("w3_s", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
         ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
         ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
         ("norm_gamma", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
@@ -71,7 +74,7 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [
         ("slots", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("w1_q", ctypes.c_void_p), ("w3_q", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
-        ("w1_sf", ctypes.c_void_p), ("w3_sf", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p),
+        ("w1_s", ctypes.c_void_p), ("w3_s", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
         ("state", ctypes.c_void_p),
     ]
 
@@ -123,7 +126,8 @@ def lib() -> ctypes.CDLL:
         "k3moe_graph_destroy": ([vp], ctypes.c_int),
         "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                               ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
-        "k3moe_prepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
+        "k3moe_prepared_scales_size": ([i64, i64, i64], sz),
+        "k3moe_prepare_scales": ([vp, i64, i64, i64, vp, vp], ctypes.c_int),
         "k3moe_cache_state_size": ([i32, i32], sz),
         "k3moe_cache_init": ([vp, i32, i32, vp], ctypes.c_int),
         "k3moe_forward_cached": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(CacheDesc), vp, i32,
@@ -132,7 +136,7 @@ def lib() -> ctypes.CDLL:
         "k3moe_graph_create_cached": ([ctypes.POINTER(LayerDesc), ctypes.POINTER(CacheDesc), vp,
                                        i32, vp, vp, sz, ctypes.POINTER(ctypes.c_void_p)],
                                       ctypes.c_int),
-        "k3moe_unprepare_scales": ([vp, i64, i64, vp, vp], ctypes.c_int),
+        "k3moe_unprepare_scales": ([vp, i64, i64, i64, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -275,38 +279,49 @@ def k3moe_gemm_bf16(x, w, out_fp32: bool = False, out=None, stream=None):
     return out
 
 
+def k3moe_prepared_scales_size(E: int, rows: int, cols: int) -> int:
+    return lib().k3moe_prepared_scales_size(E, rows, cols)
+
+
 def k3moe_prepare_scales(scale, stream=None):
-    """Canonical E8M0 scales [..., rows, cols/32] (rows stacked over any
-    leading dims) -> the prepared atoms the kernels read, a flat uint8 tensor."""
+    """Canonical E8M0 scales [E, rows, cols/32] (or [rows, cols/32], one
+    expert) -> the prepared atoms the kernels can read instead, a flat uint8
+    tensor of k3moe_prepared_scales_size(E, rows, cols) bytes."""
     _dev(scale, "scale")
-    rows = scale.numel() // scale.shape[-1]
-    cols = 32 * scale.shape[-1]
-    sf = torch.empty(scale.numel(), dtype=torch.uint8, device=scale.device)
-    _check(lib().k3moe_prepare_scales(_p(scale), rows, cols, _p(sf), _stream(stream)))
+    E = scale.shape[0] if scale.dim() == 3 else 1
+    rows, cols = scale.shape[-2], 32 * scale.shape[-1]
+    sf = torch.empty(k3moe_prepared_scales_size(E, rows, cols), dtype=torch.uint8, device=scale.device)
+    _check(lib().k3moe_prepare_scales(_p(scale), E, rows, cols, _p(sf), _stream(stream)))
     return sf
 
 
 def k3moe_unprepare_scales(sf, shape, stream=None):
-    """Inverse of k3moe_prepare_scales: the canonical array of ``shape``."""
+    """Inverse of k3moe_prepare_scales: the canonical array of ``shape``
+    ([E, rows, cols/32] or [rows, cols/32])."""
     scale = torch.empty(shape, dtype=torch.uint8, device=sf.device)
-    rows = scale.numel() // scale.shape[-1]
-    _check(lib().k3moe_unprepare_scales(_p(sf), rows, 32 * scale.shape[-1], _p(scale), _stream(stream)))
+    E = scale.shape[0] if scale.dim() == 3 else 1
+    _check(lib().k3moe_unprepare_scales(_p(sf), E, scale.shape[-2], 32 * scale.shape[-1], _p(scale),
+                                        _stream(stream)))
     return scale
 
 
 class MoELayer:
     """Device tensors of one layer plus the ``k3moe_layer_desc`` that points at them.
 
-    Takes the canonical scale arrays (w*_s, one E8M0 byte per row and 32
-    inputs) and keeps the prepared atoms that the kernels read
-    (k3moe_prepare_scales, run once here on the current stream)."""
+    Takes the expert weights as the checkpoint stores them: codes (w*_q) and
+    canonical E8M0 scales (w*_s, one byte per row and 32 inputs).  With
+    ``prepared=True`` it also keeps the scales in the prepared atom layout
+    (k3moe_prepare_scales, run once here on the current stream), which the
+    kernels then read instead."""
 
     def __init__(self, *, w1_q, w1_s, w3_q, w3_s, w2_q, w2_s, router_w, router_b, k: int,
                  norm_gamma=None, w_down=None, w_up=None, eps: float = 1e-5,
-                 path: int = PATH_AUTO, act: int = ACT_SILU_GATED):
-        self.tensors = dict(w1_q=w1_q, w3_q=w3_q, w2_q=w2_q, w1_sf=k3moe_prepare_scales(w1_s),
-                            w3_sf=k3moe_prepare_scales(w3_s), w2_sf=k3moe_prepare_scales(w2_s),
+                 path: int = PATH_AUTO, act: int = ACT_SILU_GATED, prepared: bool = False):
+        self.tensors = dict(w1_q=w1_q, w3_q=w3_q, w2_q=w2_q, w1_s=w1_s, w3_s=w3_s, w2_s=w2_s,
                             router_w=_bf16(router_w, "router_w"), router_b=router_b)
+        if prepared:
+            self.tensors.update(w1_sf=k3moe_prepare_scales(w1_s), w3_sf=k3moe_prepare_scales(w3_s),
+                                w2_sf=k3moe_prepare_scales(w2_s))
         E, f, half_d = w1_q.shape
         d = 2 * half_d
         block = w_down is not None
@@ -322,6 +337,7 @@ class MoELayer:
             setattr(desc, name, t.data_ptr())
         self.desc = desc
         self.E, self.k, self.d, self.f, self.D = E, k, d, f, D
+        self.prepared = prepared
 
     def with_path(self, path: int) -> "MoELayer":
         other = object.__new__(MoELayer)
@@ -404,7 +420,11 @@ def k3moe_trace_read(max_entries: int = 32):
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
-EXPERT_ARRAYS = ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf")
+def expert_arrays(layer: MoELayer):
+    """Names of the six expert arrays the kernels read: the codes and either
+    the prepared or the canonical scales."""
+    sc = ("w1_sf", "w3_sf", "w2_sf") if layer.prepared else ("w1_s", "w3_s", "w2_s")
+    return ("w1_q", "w3_q", "w2_q") + sc
 
 
 def ggml_layer(layer: MoELayer, stream=None) -> MoELayer:
@@ -416,29 +436,33 @@ def ggml_layer(layer: MoELayer, stream=None) -> MoELayer:
     other.__dict__.update(layer.__dict__)
     other.tensors = dict(layer.tensors)
     desc = LayerDesc.from_buffer_copy(layer.desc)
-    for q, sf in (("w1_q", "w1_sf"), ("w3_q", "w3_sf"), ("w2_q", "w2_sf")):
-        codes = layer.tensors[q]
+    for m in ("w1", "w3", "w2"):
+        codes, canon = layer.tensors[m + "_q"], layer.tensors[m + "_s"]
         E, rows, half = codes.shape
         K = 2 * half
-        canon = k3moe_unprepare_scales(layer.tensors[sf], (E * rows, K // 32), stream=stream)
-        blocks = k3moe_repack_mxfp4(codes.view(E * rows, half), canon, stream=stream)
-        other.tensors[q] = blocks.view(E, rows, K // 32, 17)
-        del other.tensors[sf]
-        setattr(desc, q, blocks.data_ptr())
-        setattr(desc, sf, None)
+        blocks = k3moe_repack_mxfp4(codes.view(E * rows, half), canon.view(E * rows, K // 32),
+                                    stream=stream)
+        other.tensors[m + "_q"] = blocks.view(E, rows, K // 32, 17)
+        for sc in (m + "_s", m + "_sf"):
+            other.tensors.pop(sc, None)
+            setattr(desc, sc, None)
+        setattr(desc, m + "_q", blocks.data_ptr())
     desc.format = FORMAT_GGML
     other.desc = desc
+    other.prepared = False
     return other
 
 
 def host_resident(layer: MoELayer) -> MoELayer:
-    """A copy of ``layer`` whose six expert arrays (codes and prepared scale
-    atoms) live in one page-locked host buffer, for k3moe_forward_cached.  The
-    router and block-mode tensors stay shared with ``layer``; the device
-    expert arrays are referenced only by ``layer`` (drop it to free them)."""
+    """A copy of ``layer`` whose six expert arrays (codes and the scales the
+    kernels read) live in one page-locked host buffer, for
+    k3moe_forward_cached.  The router and block-mode tensors stay shared with
+    ``layer``; the device expert arrays are referenced only by ``layer``
+    (drop it to free them)."""
     align = 256
+    names = expert_arrays(layer)
     offs, total = [], 0
-    for n in EXPERT_ARRAYS:
+    for n in names:
         offs.append(total)
         total += (layer.tensors[n].numel() + align - 1) // align * align
     buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
@@ -446,7 +470,11 @@ def host_resident(layer: MoELayer) -> MoELayer:
     other.__dict__.update(layer.__dict__)
     other.tensors = dict(layer.tensors)
     desc = LayerDesc.from_buffer_copy(layer.desc)
-    for n, off in zip(EXPERT_ARRAYS, offs):
+    for n in ("w1_s", "w3_s", "w2_s", "w1_sf", "w3_sf", "w2_sf"):
+        if n not in names:  # the other scale layout is not kept on the host
+            other.tensors.pop(n, None)
+            setattr(desc, n, None)
+    for n, off in zip(names, offs):
         src = layer.tensors[n]
         view = buf[off:off + src.numel()].view(src.shape)
         view.copy_(src)
@@ -465,13 +493,15 @@ class ExpertCache:
         dev = device or "cuda"
         E, d, f = layer.E, layer.d, layer.f
         u8 = torch.uint8
+        # the slots' scales in the layer's layout: prepared atoms or canonical rows
+        nsc = k3moe_prepared_scales_size(slots, f, d) if layer.prepared else slots * f * d // 32
         self.tensors = dict(
             w1_q=torch.empty((slots, f, d // 2), dtype=u8, device=dev),
             w3_q=torch.empty((slots, f, d // 2), dtype=u8, device=dev),
             w2_q=torch.empty((slots, d, f // 2), dtype=u8, device=dev),
-            w1_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
-            w3_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
-            w2_sf=torch.empty(slots * f * d // 32, dtype=u8, device=dev),
+            w1_s=torch.empty(nsc, dtype=u8, device=dev),
+            w3_s=torch.empty(nsc, dtype=u8, device=dev),
+            w2_s=torch.empty(nsc, dtype=u8, device=dev),
             state=torch.zeros(max(int(lib().k3moe_cache_state_size(E, slots)), 256), dtype=u8,
                               device=dev),
         )

@@ -86,7 +86,18 @@ RoutePlan route_plan(int T, int E) {
     return p;
 }
 
+// Which scales the expert kernels read: the caller's prepared atoms, the
+// caller's canonical rows (d and f multiples of 512), or atoms that the
+// forward writes into its workspace from the canonical rows first.
+enum ScaleSource { SCALES_PREPARED = 0, SCALES_CANON = 1, SCALES_CANON_PREP = 2 };
+
+ScaleSource scale_source(const k3moe_layer_desc* d) {
+    if (d->w1_sf && d->w3_sf && d->w2_sf) return SCALES_PREPARED;
+    return (d->d % 512 == 0 && d->f % 512 == 0) ? SCALES_CANON : SCALES_CANON_PREP;
+}
+
 struct FwdPlan {
+    size_t sf1, sf3, sf2;                           // atoms written per call (SCALES_CANON_PREP)
     size_t logits, idx, wts, counts, offsets, active, perm, inv, chunk;
     size_t dec, y;                                  // decode scratch, shared y (fp32)
     size_t units;                                   // unit-grouped streaming scratch
@@ -100,6 +111,11 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     Carve c;
     FwdPlan p{};
     const size_t P = static_cast<size_t>(T) * d->k;
+    if (d->format == K3MOE_FORMAT_SPLIT && scale_source(d) == SCALES_CANON_PREP) {
+        p.sf1 = c.take(prepared_sf_bytes(d->E, d->f, d->d));
+        p.sf3 = c.take(prepared_sf_bytes(d->E, d->f, d->d));
+        p.sf2 = c.take(prepared_sf_bytes(d->E, d->d, d->f));
+    }
     p.logits = c.take(static_cast<size_t>(T) * d->E * 4);
     p.idx = c.take(P * 4);
     p.wts = c.take(P * 4);
@@ -135,7 +151,7 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
     if (d->E < 1 || d->k < 1 || d->d < 1 || d->f < 1 || d->d_router < 1) return K3MOE_ERR_INVALID_ARG;
     if (d->format != K3MOE_FORMAT_SPLIT && d->format != K3MOE_FORMAT_GGML) return K3MOE_ERR_INVALID_ARG;
     if (d->k > d->E || d->k > 32 || d->E > 1024) return K3MOE_ERR_SHAPE;
-    if (d->d % 256 || d->f % 256) return K3MOE_ERR_SHAPE;  // 256-wide K chunks of the MMAs
+    if (d->d % 64 || d->f % 64) return K3MOE_ERR_SHAPE;  // the MMAs take 64 inputs at a time
     if (d->D < 0) return K3MOE_ERR_SHAPE;
     if (d->D > 0) {
         if (d->D % 128 || d->d % 128 || d->d_router != d->D) return K3MOE_ERR_SHAPE;
@@ -147,12 +163,23 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
         return K3MOE_ERR_SHAPE;
     }
     if (d->act != K3MOE_ACT_SILU_GATED) return K3MOE_ERR_UNSUPPORTED;
-    if (d->path < K3MOE_PATH_AUTO || d->path > K3MOE_PATH_GROUPED) return K3MOE_ERR_INVALID_ARG;
+    if (d->path < K3MOE_PATH_AUTO || d->path > K3MOE_PATH_BF16_DEQUANT) return K3MOE_ERR_INVALID_ARG;
     const bool ggml = d->format == K3MOE_FORMAT_GGML;
-    const void* ptrs[] = {d->w1_q, d->w3_q, d->w2_q, d->router_w, d->router_b, d->w1_sf, d->w3_sf, d->w2_sf};
-    for (int i = 0; i < (ggml ? 5 : 8); ++i) {  // ggml blocks carry their scales
-        if (!ptrs[i]) return K3MOE_ERR_INVALID_ARG;
-        if (!aligned16(ptrs[i])) return K3MOE_ERR_ALIGN;
+    const void* ptrs[] = {d->w1_q, d->w3_q, d->w2_q, d->router_w, d->router_b};
+    for (const void* q : ptrs) {
+        if (!q) return K3MOE_ERR_INVALID_ARG;
+        if (!aligned16(q)) return K3MOE_ERR_ALIGN;
+    }
+    if (!ggml) {  // ggml blocks carry their scales
+        // prepared scales: all three or none; without them the canonical arrays
+        const int nsf = (d->w1_sf != nullptr) + (d->w3_sf != nullptr) + (d->w2_sf != nullptr);
+        if (nsf != 0 && nsf != 3) return K3MOE_ERR_INVALID_ARG;
+        const void* sc[] = {d->w1_sf, d->w3_sf, d->w2_sf};
+        const void* cs[] = {d->w1_s, d->w3_s, d->w2_s};
+        for (const void* q : nsf ? sc : cs) {
+            if (!q) return K3MOE_ERR_INVALID_ARG;
+            if (!aligned16(q)) return K3MOE_ERR_ALIGN;
+        }
     }
     if (ggml) {
         // rows of d/32 (f/32) 17-byte blocks are whole 16-byte units for TMA
@@ -288,22 +315,34 @@ k3moe_status k3moe_unpack_mxfp4(const uint8_t* blocks, int64_t rows, int64_t col
                                      static_cast<cudaStream_t>(stream)));
 }
 
-k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t rows, int64_t cols, uint8_t* sf,
+size_t k3moe_prepared_scales_size(int64_t E, int64_t rows, int64_t cols) {
+    if (E < 1 || rows < 1 || cols < 1 || rows > (1 << 30) || cols > (1 << 30)) return 0;
+    return prepared_sf_bytes(E, static_cast<int>(rows), static_cast<int>(cols));
+}
+
+namespace {
+k3moe_status check_prepare(const void* a, const void* b, int64_t E, int64_t rows, int64_t cols) {
+    if (!a || !b || E < 1 || rows < 1 || cols < 1) return K3MOE_ERR_INVALID_ARG;
+    if (rows % 64 || cols % 64 || rows > (1 << 30) || cols > (1 << 30)) return K3MOE_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(b)) return K3MOE_ERR_ALIGN;
+    return K3MOE_OK;
+}
+}  // namespace
+
+k3moe_status k3moe_prepare_scales(const uint8_t* scale, int64_t E, int64_t rows, int64_t cols, uint8_t* sf,
                                   void* stream) {
-    if (!scale || !sf || rows < 1 || cols < 1) return K3MOE_ERR_INVALID_ARG;
-    if (rows % 128 || cols % 128) return K3MOE_ERR_SHAPE;
-    if (!aligned16(scale) || !aligned16(sf)) return K3MOE_ERR_ALIGN;
-    return cuda_status(launch_prepare_sf(scale, rows, static_cast<int>(cols), sf, 0,
+    const k3moe_status st = check_prepare(scale, sf, E, rows, cols);
+    if (st != K3MOE_OK) return st;
+    return cuda_status(launch_prepare_sf(scale, E, static_cast<int>(rows), static_cast<int>(cols), sf, 0,
                                          static_cast<cudaStream_t>(stream)));
 }
 
-k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* scale,
+k3moe_status k3moe_unprepare_scales(const uint8_t* sf, int64_t E, int64_t rows, int64_t cols, uint8_t* scale,
                                     void* stream) {
-    if (!scale || !sf || rows < 1 || cols < 1) return K3MOE_ERR_INVALID_ARG;
-    if (rows % 128 || cols % 128) return K3MOE_ERR_SHAPE;
-    if (!aligned16(scale) || !aligned16(sf)) return K3MOE_ERR_ALIGN;
-    return cuda_status(launch_prepare_sf(scale, rows, static_cast<int>(cols), const_cast<uint8_t*>(sf), 1,
-                                         static_cast<cudaStream_t>(stream)));
+    const k3moe_status st = check_prepare(sf, scale, E, rows, cols);
+    if (st != K3MOE_OK) return st;
+    return cuda_status(launch_prepare_sf(scale, E, static_cast<int>(rows), static_cast<int>(cols),
+                                         const_cast<uint8_t*>(sf), 1, static_cast<cudaStream_t>(stream)));
 }
 
 size_t k3moe_route_workspace_size(int32_t T, int32_t E) {
@@ -422,7 +461,11 @@ k3moe_status check_cache(const k3moe_layer_desc* d, const k3moe_expert_cache* c,
     if (!c || c->reserved != 0 || !c->state) return K3MOE_ERR_INVALID_ARG;
     const long long need = std::min<long long>(d->E, static_cast<long long>(T) * d->k);
     if (c->slots < 1 || c->slots > d->E || c->slots < need) return K3MOE_ERR_SHAPE;
-    uint8_t* dst[6] = {c->w1_q, c->w3_q, c->w2_q, c->w1_sf, c->w3_sf, c->w2_sf};
+    // the slots hold the scales in the layout the kernels read: the caller's
+    // prepared atoms or the canonical rows (not a per-call preparation)
+    const ScaleSource ss = scale_source(d);
+    if (ss == SCALES_CANON_PREP) return K3MOE_ERR_UNSUPPORTED;
+    uint8_t* dst[6] = {c->w1_q, c->w3_q, c->w2_q, c->w1_s, c->w3_s, c->w2_s};
     for (uint8_t* q : dst) {
         if (!q) return K3MOE_ERR_INVALID_ARG;
         if (!aligned16(q)) return K3MOE_ERR_ALIGN;
@@ -430,7 +473,9 @@ k3moe_status check_cache(const k3moe_layer_desc* d, const k3moe_expert_cache* c,
     if (!aligned32(c->w1_q) || !aligned32(c->w3_q) || !aligned32(c->w2_q) || !aligned16(c->state))
         return K3MOE_ERR_ALIGN;
     // the expert arrays of the layer are host memory, page-locked and mapped
-    const void* src[6] = {d->w1_q, d->w3_q, d->w2_q, d->w1_sf, d->w3_sf, d->w2_sf};
+    const bool prep = ss == SCALES_PREPARED;
+    const void* src[6] = {d->w1_q, d->w3_q, d->w2_q, prep ? d->w1_sf : d->w1_s, prep ? d->w3_sf : d->w3_s,
+                          prep ? d->w2_sf : d->w2_s};
     const uint8_t* dev[6];
     for (int i = 0; i < 6; ++i) {
         cudaPointerAttributes at{};
@@ -453,7 +498,8 @@ k3moe_status check_cache(const k3moe_layer_desc* d, const k3moe_expert_cache* c,
         cp->fill.dst_sf[i] = dst[3 + i];
     }
     cp->fill.q_bytes = static_cast<size_t>(d->f) * (d->d / 2);
-    cp->fill.sf_bytes = static_cast<size_t>(d->f) * (d->d / 32);
+    // per expert, the same for all three matrices (w2 is [d, f], w1 and w3 [f, d])
+    cp->fill.sf_bytes = prep ? prepared_sf_bytes(1, d->f, d->d) : static_cast<size_t>(d->f) * (d->d / 32);
     return K3MOE_OK;
 }
 
@@ -467,14 +513,14 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     const FwdPlan p = fwd_plan(desc, T);
     if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
     int path = desc->path;
-    if (path == K3MOE_PATH_AUTO) path = T <= kStreamMaxT ? K3MOE_PATH_DECODE : K3MOE_PATH_GROUPED;
-    if (path == K3MOE_PATH_DECODE && T > kStreamMaxT) return K3MOE_ERR_UNSUPPORTED;
+    if (path == K3MOE_PATH_AUTO) path = T <= kStreamMaxT ? K3MOE_PATH_BLOCK_SCALED : K3MOE_PATH_BF16_DEQUANT;
+    if (path == K3MOE_PATH_BLOCK_SCALED && T > kStreamMaxT) return K3MOE_ERR_UNSUPPORTED;
     // ggml blocks: the streaming kernels only, without a cache
-    if (desc->format == K3MOE_FORMAT_GGML && (path != K3MOE_PATH_DECODE || cache)) return K3MOE_ERR_UNSUPPORTED;
+    if (desc->format == K3MOE_FORMAT_GGML && (path != K3MOE_PATH_BLOCK_SCALED || cache)) return K3MOE_ERR_UNSUPPORTED;
     CachePlan cp;
     if (cache) {
         // the cache serves the streaming kernels only (few experts per call)
-        if (path != K3MOE_PATH_DECODE) return K3MOE_ERR_UNSUPPORTED;
+        if (path != K3MOE_PATH_BLOCK_SCALED) return K3MOE_ERR_UNSUPPORTED;
         if ((st = check_cache(desc, cache, T, &cp)) != K3MOE_OK) return st;
     }
 
@@ -487,6 +533,15 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     struct TraceEnd { ~TraceEnd() { trace_end(); } } trace_end_guard;
     auto at = [&](size_t off) { return static_cast<void*>(base + off); };
     cudaError_t e = cudaSuccess;
+    const ScaleSource ss = desc->format == K3MOE_FORMAT_GGML ? SCALES_PREPARED : scale_source(desc);
+    if (ss == SCALES_CANON_PREP) {
+        // widths that are not whole 512-input stages: the canonical rows are
+        // rewritten as prepared atoms first (1/32 of the expert bytes)
+        if ((e = launch_prepare_sf(desc->w1_s, desc->E, desc->f, desc->d, static_cast<uint8_t*>(at(p.sf1)), 0, s)) ||
+            (e = launch_prepare_sf(desc->w3_s, desc->E, desc->f, desc->d, static_cast<uint8_t*>(at(p.sf3)), 0, s)) ||
+            (e = launch_prepare_sf(desc->w2_s, desc->E, desc->d, desc->f, static_cast<uint8_t*>(at(p.sf2)), 0, s)))
+            return cuda_status(e);
+    }
 
     const uint16_t* x_router = hidden;
     const uint16_t* x_expert = hidden;
@@ -515,15 +570,15 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     int32_t* perm = static_cast<int32_t*>(at(p.perm));
     int32_t* inv = static_cast<int32_t*>(at(p.inv));
     int32_t* active = static_cast<int32_t*>(at(p.active));
-    const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_DECODE && desc->D == 0;
+    const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED && desc->D == 0;
     if (T <= kDecodeMaxT) {
         // decode needs only the active experts (listed by the top-k kernel); the
         // grouped path takes the full permutation
-        r.active = path == K3MOE_PATH_DECODE ? active : nullptr;
+        r.active = path == K3MOE_PATH_BLOCK_SCALED ? active : nullptr;
         if (fuse_prep)
             mx_decode_xq_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.xq, &r.xsf, &r.xq_n);
         if ((e = launch_route_small(r, s))) return cuda_status(e);
-        if (path != K3MOE_PATH_DECODE &&
+        if (path != K3MOE_PATH_BLOCK_SCALED &&
             (e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s)))
             return K3MOE_ERR_CUDA;
     } else {
@@ -545,21 +600,30 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     // slots after the missing experts were fetched into them
     const uint8_t *w1_q = desc->w1_q, *w3_q = desc->w3_q, *w2_q = desc->w2_q;
     const uint8_t *w1_sf = desc->w1_sf, *w3_sf = desc->w3_sf, *w2_sf = desc->w2_sf;
+    int sf_canon = 0;
+    if (ss == SCALES_CANON) {
+        w1_sf = desc->w1_s; w3_sf = desc->w3_s; w2_sf = desc->w2_s;
+        sf_canon = 1;
+    } else if (ss == SCALES_CANON_PREP) {
+        w1_sf = static_cast<const uint8_t*>(at(p.sf1));
+        w3_sf = static_cast<const uint8_t*>(at(p.sf3));
+        w2_sf = static_cast<const uint8_t*>(at(p.sf2));
+    }
     const int32_t* slot_of = nullptr;
     int nslots = desc->E;
     if (cp.c) {
         if ((e = launch_cache_update(cp.c->state, desc->E, cp.c->slots, active, cp.fill, hdr, sms, s)))
             return cuda_status(e);
         w1_q = cp.c->w1_q; w3_q = cp.c->w3_q; w2_q = cp.c->w2_q;
-        w1_sf = cp.c->w1_sf; w3_sf = cp.c->w3_sf; w2_sf = cp.c->w2_sf;
+        w1_sf = cp.c->w1_s; w3_sf = cp.c->w3_s; w2_sf = cp.c->w2_s;
         slot_of = cache_view(cp.c->state, desc->E, cp.c->slots).slot_of;
         nslots = cp.c->slots;
     }
 
-    if (path == K3MOE_PATH_DECODE && T > kDecodeMaxT) {
+    if (path == K3MOE_PATH_BLOCK_SCALED && T > kDecodeMaxT) {
         MxUnitsArgs a{};
         a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
-        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
+        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf; a.sf_canon = sf_canon;
         a.slot_of = slot_of; a.nslots = nslots;
         a.ggml = desc->format == K3MOE_FORMAT_GGML ? 1 : 0;
         a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
@@ -569,10 +633,10 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         e = launch_mx_units(a, s);
         if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
         if (e) return cuda_status(e);
-    } else if (path == K3MOE_PATH_DECODE) {
+    } else if (path == K3MOE_PATH_BLOCK_SCALED) {
         MxDecodeArgs a{};
         a.w1_q = w1_q; a.w3_q = w3_q; a.w2_q = w2_q;
-        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf;
+        a.w1_sf = w1_sf; a.w3_sf = w3_sf; a.w2_sf = w2_sf; a.sf_canon = sf_canon;
         a.slot_of = slot_of; a.nslots = nslots;
         a.ggml = desc->format == K3MOE_FORMAT_GGML ? 1 : 0;
         a.x = x_expert; a.xq_ready = fuse_prep ? 1 : 0;
@@ -586,7 +650,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     } else {
         GroupedArgs g{};
         g.w1_q = desc->w1_q; g.w3_q = desc->w3_q; g.w2_q = desc->w2_q;
-        g.w1_sf = desc->w1_sf; g.w3_sf = desc->w3_sf; g.w2_sf = desc->w2_sf;
+        g.w1_sf = w1_sf; g.w3_sf = w3_sf; g.w2_sf = w2_sf; g.sf_canon = sf_canon;
         g.x = x_expert; g.T = T; g.E = desc->E; g.k = desc->k; g.d = desc->d; g.f = desc->f;
         g.counts = counts; g.offsets = offsets; g.perm = perm; g.inv = inv; g.wts = r.wts;
         g.xp = static_cast<uint16_t*>(at(p.xp));

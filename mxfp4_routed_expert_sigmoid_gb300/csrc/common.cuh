@@ -162,14 +162,16 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 // ---------------------------------------------------------------------------
 constexpr int kTerms = 5;
 
-// Smallest e with amax * 2^-e <= 6 (the largest E2M1 magnitude), from the
-// exponent and mantissa fields: amax = (1 + m) 2^E fits at e = E - 2 iff
-// 1 + m <= 1.5.  Zero and subnormal amax give -127 (the smallest scale).
+// Smallest e >= -127 with amax * 2^-e <= 6 (the largest E2M1 magnitude), from
+// the exponent and mantissa fields: amax = (1 + m) 2^E fits at e = E - 2 iff
+// 1 + m <= 1.5.  The E8M0 byte is e + 127, so e stays at -127 or above (byte
+// 255 is NaN): zero, subnormal and lowest-binade amax (below 2^-125) give
+// -127, where amax * 2^127 < 4 still fits.
 __device__ __forceinline__ int e2m1_scale_exp(float amax) {
     const uint32_t u = __float_as_uint(amax);
     const int ef = static_cast<int>((u >> 23) & 0xFFu);
-    if (ef == 0) return -127;
-    return ef - 127 - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    const int e = ef - 127 - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    return e < -127 ? -127 : e;
 }
 
 // fp32 -> E2M1 code (round to nearest even, saturating to +-6), low 4 bits
@@ -366,7 +368,8 @@ cudaError_t launch_combine(const float* y, int nslots, const float* wts, const i
 // block-scaled tensor-core decode path (mx.cu)
 struct MxDecodeArgs {
     const uint8_t *w1_q, *w3_q, *w2_q;  // E2M1 codes
-    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // E8M0 scales: prepared atoms, or canonical rows (sf_canon)
+    int sf_canon;             // 1: w*_sf are the canonical [rows, K / 32] arrays (d, f multiples of 512)
     const uint16_t* x;        // [T, d] bf16 expert input (read when !xq_ready)
     int xq_ready;             // 1: the router already wrote the E2M1 terms
     int T, E, k, d, f;
@@ -391,7 +394,8 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s);
 // tokens and streamed like the decode path
 struct MxUnitsArgs {
     const uint8_t *w1_q, *w3_q, *w2_q;     // E2M1 codes
-    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // E8M0 scales: prepared atoms, or canonical rows (sf_canon)
+    int sf_canon;             // 1: w*_sf are the canonical [rows, K / 32] arrays (d, f multiples of 512)
     const uint16_t* x;        // [T, d] bf16 expert input
     int T, E, k, d, f;
     const int32_t* counts;    // [E]
@@ -450,14 +454,17 @@ cudaError_t launch_cache_init(void* state, int E, int slots, cudaStream_t s);
 cudaError_t launch_cache_update(void* state, int E, int slots, const int32_t* active,
                                 const CacheFillArgs& f, WsHeader* hdr, int num_sms, cudaStream_t s);
 
-// canonical E8M0 scales [rows, K/32] <-> prepared atoms (inverse = 1: atoms -> canonical)
-cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
+// canonical E8M0 scales [E, R, K/32] <-> prepared atoms (inverse = 1: atoms -> canonical); the
+// atoms of an expert fill ceil(R / 128) x ceil(K / 128) atoms of 512 bytes (zero padding)
+size_t prepared_sf_bytes(int64_t E, int R, int K);
+cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t E, int R, int K, uint8_t* atoms, int inverse,
                               cudaStream_t s);
 
 // grouped (tcgen05) path
 struct GroupedArgs {
     const uint8_t *w1_q, *w3_q, *w2_q;  // E2M1 codes
-    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // prepared scale atoms
+    const uint8_t *w1_sf, *w3_sf, *w2_sf;  // E8M0 scales: prepared atoms, or canonical rows (sf_canon)
+    int sf_canon;            // 1: w*_sf are the canonical [rows, K / 32] arrays (d, f multiples of 512)
     const uint16_t* x;       // [T, d] bf16 expert input
     int T, E, k, d, f;
     const int32_t* counts;   // [E]

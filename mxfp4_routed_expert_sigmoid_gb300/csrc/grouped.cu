@@ -83,25 +83,41 @@ constexpr size_t dense_smem_bytes() {
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-// Prepared scale atoms: row r of expert e is row m = r % 128 of atom tile
-// e * rows / 128 + r / 128; its block b sits at + (b / 4) * 512 + b % 4 from
-// the returned pointer.
-__device__ __forceinline__ const uint8_t* sf_row(const uint8_t* sf, int e, int r, int rows_per_expert,
-                                                 int KS) {
-    const int tile = e * (rows_per_expert / 128) + r / 128;
+// Prepared scale atoms (per expert ceil(rows / 128) tiles of G = ceil(K / 128)
+// atoms, zero-padded): row r of expert e is row m = r % 128 of atom tile
+// e * tiles_e + r / 128; its block b sits at + (b / 4) * 512 + b % 4 from the
+// returned pointer.
+__device__ __forceinline__ const uint8_t* sf_row(const uint8_t* sf, int e, int r, int tiles_e, int G) {
+    const int tile = e * tiles_e + r / 128;
     const int m = r % 128;
-    return sf + static_cast<size_t>(tile) * KS * 512 + 16 * (m & 31) + 4 * (m >> 5);
+    return sf + static_cast<size_t>(tile) * G * 512 + 16 * (m & 31) + 4 * (m >> 5);
 }
 
 // largest exponent of a row from its prepared atoms (four blocks per word)
-__device__ __forceinline__ int row_emax_sf(const uint8_t* srow, int KS) {
+__device__ __forceinline__ int row_emax_sf(const uint8_t* srow, int G) {
     int m = 0;
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < G; ++s) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(srow + static_cast<size_t>(s) * 512);
 #pragma unroll
         for (int b = 0; b < 4; ++b) m = max(m, static_cast<int>((w >> (8 * b)) & 0xFF));
     }
     return m;
+}
+
+// largest exponent of a canonical E8M0 row (nv 16-byte vectors)
+__device__ __forceinline__ int row_emax_canon(const uint8_t* row, int nv) {
+    uint32_t m = 0;
+    for (int i = 0; i < nv; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * i);
+        m = __vmaxu4(m, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+    }
+    return static_cast<int>(max(max(m & 0xFF, (m >> 8) & 0xFF), max((m >> 16) & 0xFF, m >> 24)));
+}
+
+// byte i (0..15) of a 16-byte vector
+__device__ __forceinline__ int vec_byte(const uint4& v, int i) {
+    const uint32_t w = i < 8 ? (i < 4 ? v.x : v.y) : (i < 12 ? v.z : v.w);
+    return static_cast<int>((w >> (8 * (i & 3))) & 0xFF);
 }
 
 __global__ void __launch_bounds__(kDenseThreads, 1)
@@ -278,9 +294,11 @@ constexpr int kExpThreads = 512;
 
 struct ExpParams {
     int K;                // reduction length (multiple of 64)
-    int rows_per_expert;  // rows of one expert matrix
-    const uint8_t* s1;    // prepared E8M0 atoms of A (w1 or w2)
-    const uint8_t* s3;    // UP: prepared E8M0 atoms of w3
+    int rows_per_expert;  // rows of one expert matrix (multiple of 64)
+    int tiles_e;          // 128-row tiles per expert (the last may be partial)
+    int G;                // 128-wide scale groups per row (prepared atoms)
+    const uint8_t* s1;    // E8M0 scales of A (w1 or w2): prepared atoms, or canonical rows (SFC)
+    const uint8_t* s3;    // UP: the same for w3
     const int4* tiles;    // tiles[0].x = count; tiles[1 + i] = (e, first B row, B rows, m tile)
     const int32_t* bexp;  // per B row power-of-two exponent
     int n_out;            // row length of hf / y
@@ -302,7 +320,11 @@ constexpr size_t exp_smem_bytes() {
     return b;
 }
 
-template <int NA>
+// SFC = 0: the scales are prepared atoms, one 512-byte atom per stage copied
+// with the raw codes; SFC = 1: canonical E8M0 rows (K a multiple of 512), read
+// by each dequantising thread straight from global memory, 16 blocks (eight
+// stages) per 16-byte load, the next load issued eight stages ahead.
+template <int NA, int SFC>
 __global__ void __launch_bounds__(kExpThreads, 1)
 tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                  const __grid_constant__ CUtensorMap tmB, ExpParams p) {
@@ -382,17 +404,17 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int4 tl = p.tiles[1 + tile];
                 const int arow = tl.x * p.rows_per_expert + tl.w * BM;
                 // the tile's prepared scale atoms, one per 128 inputs (two stages)
-                const size_t atoms = static_cast<size_t>(tl.x * (p.rows_per_expert / BM) + tl.w) * (p.K / 128) * 512;
+                const size_t atoms = static_cast<size_t>(tl.x * p.tiles_e + tl.w) * p.G * 512;
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&raw_empty[r], ph ^ 1, abort_flag, p.hdr, 50)) { ok = false; break; }
-                    mbar_expect_tx(&raw_full[r], NA * (kTileRaw + 512));
+                    mbar_expect_tx(&raw_full[r], NA * (kTileRaw + (SFC ? 0 : 512)));
                     const size_t atom = atoms + static_cast<size_t>(ks >> 1) * 512;
                     tma_load_2d(sRaw + (r * NA) * kTileRaw, &tmA, &raw_full[r], ks * BK / 2, arow);
-                    bulk_load(sRawSf + (r * NA) * 512, p.s1 + atom, 512, &raw_full[r]);
+                    if (!SFC) bulk_load(sRawSf + (r * NA) * 512, p.s1 + atom, 512, &raw_full[r]);
                     if (NA == 2) {
                         tma_load_2d(sRaw + (r * NA + 1) * kTileRaw, &tmA3, &raw_full[r], ks * BK / 2, arow);
-                        bulk_load(sRawSf + (r * NA + 1) * 512, p.s3 + atom, 512, &raw_full[r]);
+                        if (!SFC) bulk_load(sRawSf + (r * NA + 1) * 512, p.s3 + atom, 512, &raw_full[r]);
                     }
                     if (++r == RS) { r = 0; ph ^= 1; }
                 }
@@ -474,10 +496,15 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const uint8_t* sm_ = m == 0 ? p.s1 : p.s3;
                 for (int i = lane; i < BM; i += 32) {
                     const int r = tl.w * BM + i;
-                    sE[(slot * NA + m) * BM + i] =
-                        r < p.rows_per_expert
-                            ? row_emax_sf(sf_row(sm_, tl.x, r, p.rows_per_expert, p.K / 128), p.K / 128)
-                            : 0;
+                    int em = 0;
+                    if (r < p.rows_per_expert) {
+                        if (SFC)
+                            em = row_emax_canon(sm_ + (static_cast<size_t>(tl.x) * p.rows_per_expert + r) * (p.K / 32),
+                                                p.K / 512);
+                        else
+                            em = row_emax_sf(sf_row(sm_, tl.x, r, p.tiles_e, p.G), p.G);
+                    }
+                    sE[(slot * NA + m) * BM + i] = em;
                 }
             }
             __syncwarp();
@@ -557,16 +584,42 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + row] : 0;
             // this thread's byte of a scale atom: row `row`, block 2 ks + half
             const int sfo = 16 * (row & 31) + 4 * (row >> 5);
+            // canonical scales: the row's 16-byte vectors, current and next (a
+            // row past the expert reads zeros: its products are never stored)
+            const int grow = tl.w * BM + row;
+            const bool rvalid = grow < p.rows_per_expert;
+            const int nvec = p.K / 512;
+            const uint8_t* c1 = p.s1 + (static_cast<size_t>(tl.x) * p.rows_per_expert + grow) * (p.K / 32);
+            const uint8_t* c3 = NA == 2 ? p.s3 + (c1 - p.s1) : nullptr;
+            uint4 v1 = make_uint4(0, 0, 0, 0), v3 = v1, n1 = v1, n3 = v1;
+            if (SFC && rvalid) {
+                n1 = ldg_nc_v4(c1);
+                if (NA == 2) n3 = ldg_nc_v4(c3);
+            }
             bool ok = true;
             for (int ks = 0; ks < k_stages; ++ks) {
                 const int blk = 2 * ks + half;
+                if (SFC && (ks & 7) == 0) {
+                    v1 = n1;
+                    v3 = n3;
+                    if (rvalid && (ks >> 3) + 1 < nvec) {
+                        n1 = ldg_nc_v4(c1 + 16 * ((ks >> 3) + 1));
+                        if (NA == 2) n3 = ldg_nc_v4(c3 + 16 * ((ks >> 3) + 1));
+                    }
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59) &&
                                                  mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
                     break;
                 }
-                const int e1 = sRawSf[(r * NA) * 512 + sfo + (blk & 3)];
-                const int e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * 512 + sfo + (blk & 3)] : 0;
+                int e1, e3;
+                if (SFC) {
+                    e1 = vec_byte(v1, blk & 15);
+                    e3 = NA == 2 ? vec_byte(v3, blk & 15) : 0;
+                } else {
+                    e1 = sRawSf[(r * NA) * 512 + sfo + (blk & 3)];
+                    e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * 512 + sfo + (blk & 3)] : 0;
+                }
 #pragma unroll
                 for (int mm = 0; mm < NA; ++mm) {
                     const uint4 raw =
@@ -752,9 +805,9 @@ cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const Dense
 constexpr int kUpRows = ExpCfg<2>::BN, kDownRows = ExpCfg<1>::BN;
 constexpr int kUnitRows = kUpRows < kDownRows ? kUpRows : kDownRows;  // bounds the tile count
 
-template <int NA>
-cudaError_t launch_expert(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                          const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+template <int NA, int SFC>
+cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
+                              const ExpParams& p, int grid, cudaStream_t s, const char* name) {
     constexpr size_t smem = exp_smem_bytes<NA>();
     static_assert(smem <= 232448, "shared memory budget");
     static std::atomic<uint64_t> done{0};
@@ -762,15 +815,22 @@ cudaError_t launch_expert(const CUtensorMap& a, const CUtensorMap& a3, const CUt
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<NA>,
+        cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<NA, SFC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
-    tc_expert_kernel<NA><<<grid, kExpThreads, smem, s>>>(a, a3, b, p);
+    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, p);
     trace_mark(name, s);
     return cudaGetLastError();
+}
+
+template <int NA>
+cudaError_t launch_expert(int sf_canon, const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
+                          const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+    return sf_canon ? launch_expert_sfc<NA, 1>(a, a3, b, p, grid, s, name)
+                    : launch_expert_sfc<NA, 0>(a, a3, b, p, grid, s, name);
 }
 
 }  // namespace
@@ -828,9 +888,12 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
         !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
+    if (g.sf_canon && (g.d % 512 || g.f % 512)) return cudaErrorNotSupported;
     ExpParams p{};
     p.K = g.d;
     p.rows_per_expert = g.f;
+    p.tiles_e = (g.f + BM - 1) / BM;
+    p.G = (g.d + 127) / 128;
     p.s1 = g.w1_sf;
     p.s3 = g.w3_sf;
     p.tiles = tiles_up;
@@ -839,7 +902,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     p.hf = g.hf;
     p.h_amax = g.h_amax;
     p.hdr = g.hdr;
-    if ((e = launch_expert<2>(t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
+    if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
     convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp);
     trace_mark("convert_h", s);
@@ -855,13 +918,15 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     ExpParams q{};
     q.K = g.f;
     q.rows_per_expert = g.d;
+    q.tiles_e = (g.d + BM - 1) / BM;
+    q.G = (g.f + 127) / 128;
     q.s1 = g.w2_sf;
     q.tiles = tiles_dn;
     q.bexp = g.hp_exp;
     q.n_out = g.d;
     q.y = g.y;
     q.hdr = g.hdr;
-    if ((e = launch_expert<1>(t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
+    if ((e = launch_expert<1>(g.sf_canon, t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
 
     return launch_combine(g.y, 1, g.wts, g.inv, g.T, g.k, g.d, g.out, s);
 }

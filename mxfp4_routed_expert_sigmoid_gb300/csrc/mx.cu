@@ -13,11 +13,17 @@
 // Operands of one MMA (M = 128 weight rows, N = 16..64 token-term rows,
 // K = 64), staged per 256-wide K chunk (128 bytes of codes per row, the
 // 128-byte swizzled K-major layout), two chunks to a pipeline stage:
-//   A  weight codes by TMA, 16 KB per chunk, as stored in global memory;
-//   SFA two 512-byte scale atoms per chunk (prepared layout, below), copied
-//      to TMEM by tcgen05.cp 32x128b.warpx4: row m is read from lane m,
-//      column m / 32; an MMA reads two bytes of a column (scale id 0 for the
-//      first 64 inputs of an atom, 2 for the second);
+//   A  weight codes by TMA, 16 KB per chunk, as stored in global memory (a
+//      chunk past the end of a row is zero-filled by the TMA unit, and MMAs
+//      past the row's last 64 inputs are not issued);
+//   SFA two 512-byte scale atoms per chunk, copied to TMEM by tcgen05.cp
+//      32x128b.warpx4: row m is read from lane m, column m / 32; an MMA reads
+//      two bytes of a column (scale id 0 for the first 64 inputs of an atom, 2
+//      for the second).  The atoms come either prepared (the layout written by
+//      k3moe_prepare_scales, one bulk copy per stage) or from the checkpoint's
+//      canonical E8M0 rows: one TMA box of 16 bytes x 128 rows per stage,
+//      which the two MMA issuer warps re-lay into atom order in shared memory
+//      (32 lanes each, their own chunk) before the tcgen05.cp;
 //   B  activations as kTerms E2M1 terms per token (rows kTerms t + j; see
 //      quantize_terms), pre-swizzled in global memory, one bulk copy;
 //   SFB their scale atoms (column n from lane n % 32, column n / 32).
@@ -81,6 +87,10 @@ constexpr int kSfBase = 4 * kMaxN;
 static_assert(kChunks == 2, "one K chunk per MMA issuer");
 static_assert(kSfBase + kChunks * 128 <= 512, "scale slots fit in TMEM");
 constexpr uint32_t kTmemCols = 512;
+// weight formats of the streaming kernel: compressed-tensors codes with
+// prepared scale atoms, ggml 17-byte blocks, or codes with canonical E8M0 rows
+constexpr int kWfAtoms = 0, kWfGgml = 1, kWfCanon = 2;
+constexpr int kRawSf = 2048;           // canonical: one stage's scale rows, 128 x 16 bytes
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
@@ -102,7 +112,7 @@ __device__ __forceinline__ void mma_f4(uint32_t d_tmem, uint64_t a, uint64_t b, 
 }
 
 struct MxArgs {
-    const uint8_t* sf[2];   // prepared scale atoms of the matrices (W1, W3 or W2)
+    const uint8_t* sf[2];   // prepared scale atoms of the matrices (W1, W3 or W2; atoms format)
     int nmat;               // matrices per expert in this pass (2 up, 1 down)
     int early_a;            // 1: the active list is final before this grid's wait (down)
     const uint8_t* bq;      // B codes [unit][K / 256][N][128] (up: one shared unit)
@@ -116,10 +126,12 @@ struct MxArgs {
     const int32_t* slot_of; // expert -> slot of the weight arrays (null: the expert itself)
     int nslots;             // slots the weight arrays hold
     int E;
-    int rows;               // weight rows per expert (f up, d down)
-    int tiles;              // 128-row tiles per expert
-    int KC;                 // 256-wide K chunks (K / 256)
+    int rows;               // weight rows per expert (f up, d down), a multiple of 64
+    int tiles;              // 128-row tiles per expert (the last may hold fewer rows)
+    int K;                  // inputs (d up, f down), a multiple of 64
+    int KC;                 // 256-wide K chunks (the last may be partial)
     int KS;                 // stages of kChunks chunks (the last one may be shorter)
+    int G;                  // 128-wide scale groups per row (prepared atoms per tile)
     int N;                  // MMA N
     int T;                  // tokens
     int RS;                 // stages in the ring
@@ -292,10 +304,27 @@ __device__ __forceinline__ int weight_slot(const MxArgs& p, int e) {
     return s;
 }
 
-template <int TERMS, bool GG>
-__global__ void __launch_bounds__(GG ? kMxThreads + kGgThreads : kMxThreads, 1)
+// The canonical scale rows of a stage (the TMA box puts row r's 16 E8M0 bytes,
+// blocks 16 ks .. 16 ks + 15, at byte 16 r) -> the two 512-byte atoms of chunk
+// mt (blocks 8 mt .. 8 mt + 3 and 8 mt + 4 .. 8 mt + 7 of the stage), byte
+// 16 (m % 32) + 4 (m / 32) + b for row m.  One warp: lane l moves rows l,
+// l + 32, l + 64 and l + 96.
+__device__ __forceinline__ void relay_sf(const uint8_t* raw, uint8_t* atoms, int mt, int lane) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint2 v = *reinterpret_cast<const uint2*>(raw + 16 * (lane + 32 * q) + 8 * mt);
+        *reinterpret_cast<uint32_t*>(atoms + 16 * lane + 4 * q) = v.x;
+        *reinterpret_cast<uint32_t*>(atoms + 512 + 16 * lane + 4 * q) = v.y;
+    }
+}
+
+template <int TERMS, int WF>
+__global__ void __launch_bounds__(WF == kWfGgml ? kMxThreads + kGgThreads : kMxThreads, 1)
 mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmS3,
                  MxArgs p) {
+    constexpr bool GG = WF == kWfGgml;
+    constexpr bool CANON = WF == kWfCanon;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -306,12 +335,14 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     volatile int* abort_flag = &abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t NB = static_cast<uint32_t>(p.N) * 128;  // B bytes per chunk
-    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms;
-    // ggml weights: A chunks | SFA atoms | B chunks | SFB atoms, so that the
-    // stage's 17-byte blocks land on the A and SFA bytes they become
+    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms
+    // [| canonical scale rows]; ggml weights: A chunks | SFA atoms | B chunks |
+    // SFB atoms, so that the stage's 17-byte blocks land on the A and SFA bytes
+    // they become
     const uint32_t offB = GG ? kStageA + kChunks * 1024 : kStageA;
     const uint32_t offSA = GG ? kStageA : kStageA + kChunks * NB;
     const uint32_t offSB = GG ? offB + kChunks * NB : offSA + kChunks * 1024;
+    const uint32_t offRaw = offSB + kChunks * 1024;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.RS; ++s) {
@@ -331,6 +362,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         if (p.nmat > 1) prefetch_tmap(&tmA3);
+        if (CANON) {
+            prefetch_tmap(&tmS);
+            if (p.nmat > 1) prefetch_tmap(&tmS3);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -359,9 +394,14 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tma_load_2d(st, tm, bar, c.ks * (kGgRowBytes / 4), y);
         } else {
             for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
-            bulk_load(st + offSA,
-                      p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * (2 * p.KC) + 2 * c0) * 512,
-                      nch * 1024, bar);
+            if constexpr (CANON) {  // 16 scale bytes of each of the 128 rows (K is a multiple of 512)
+                tma_load_2d(st + offRaw, c.mat == 0 ? &tmS : &tmS3, bar, c.ks * 16, y);
+            } else {  // the stage's prepared atoms, consecutive within the tile
+                const int g0 = 2 * c0, ng = min(2 * kChunks, p.G - g0);
+                bulk_load(st + offSA,
+                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.G + g0) * 512,
+                          ng * 512, bar);
+            }
         }
     };
     auto issue_b = [&](const Cursor& c, uint8_t* st, uint64_t* bar) {
@@ -372,7 +412,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     };
     auto a_bytes = [&](const Cursor& c) {
         if (GG) return static_cast<uint32_t>(kGgStageBytes);
-        return static_cast<uint32_t>(min(kChunks, p.KC - c.ks * kChunks)) * (kChunkA + 1024);
+        const int c0 = c.ks * kChunks;
+        const int nch = min(kChunks, p.KC - c0);
+        const int sfb = CANON ? kRawSf : min(2 * kChunks, p.G - 2 * c0) * 512;
+        return static_cast<uint32_t>(nch * kChunkA + sfb);
     };
     // the barrier the stage's copies complete on
     auto ld_bar = [&](int s) { return GG ? &raw[s] : &full[s]; };
@@ -440,9 +483,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
     } else if (warp == 1 || warp == 6) {
-        if (lane == 0 && w0 < w1) {
+        if (w0 < w1) {
             // ------------------------------ MMA issuers ---------------------------
-            const int mt = warp == 1 ? 0 : 1;  // the stage's chunk this thread multiplies
+            // lane 0 waits and issues; with canonical scales the whole warp first
+            // re-lays its chunk's scale rows into atoms
+            const int mt = warp == 1 ? 0 : 1;  // the stage's chunk this warp multiplies
             int ks = Cursor(w0, p).ks;
             int s = 0, seg = 0, ps = 0;
             uint32_t ph = 0, pph = 0;
@@ -452,40 +497,50 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const bool seg_start = (w == w0) || ks == 0;
                 const bool seg_end = (w + 1 == w1) || ks == p.KS - 1;
                 const int a = seg & 1;
-                if (seg_start && !mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71))
-                    break;
-                if (!mbar_wait(&full[s], ph, abort_flag, p.hdr, 72)) break;
-                // the scale slots are reused: the previous stage's MMAs have finished
-                if (i > 0) {
-                    if (!mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73)) break;
-                    if (++ps == p.RS) {
-                        ps = 0;
-                        pph ^= 1;
-                    }
+                bool ok = true;
+                if (lane == 0) {
+                    ok = !seg_start || mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71);
+                    ok = ok && mbar_wait(&full[s], ph, abort_flag, p.hdr, 72);
+                    // the scale slots are reused: the previous stage's MMAs have finished
+                    ok = ok && (i == 0 || mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73));
+                }
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+                if (i > 0 && ++ps == p.RS) {
+                    ps = 0;
+                    pph ^= 1;
                 }
                 tc_fence_after();
-                const int nch = min(kChunks, p.KC - ks * kChunks);
-                if (mt < nch) {
-                    const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
-                    for (int h = 0; h < 2; ++h) {  // the chunk's two 128-wide scale groups
-                        tmem_cp_sf(slots + 64 * h, st + offSA + 512 * (2 * mt + h));
-                        tmem_cp_sf(slots + 64 * h + 32, st + offSB + 512 * (2 * mt + h));
+                const int kv = p.K - (ks * kChunks + mt) * 256;  // inputs of this chunk (<= 0: none)
+                if (kv > 0) {
+                    uint8_t* stage = smem + static_cast<size_t>(s) * p.stage_bytes;
+                    if constexpr (CANON) {
+                        relay_sf(stage + offRaw, stage + offSA + 1024 * mt, mt, lane);
+                        fence_proxy_async();  // tcgen05.cp reads the atoms through the async proxy
+                        __syncwarp();
                     }
-                    const uint32_t d_t = tmem + (2 * a + mt) * kMaxN;
-                    const uint64_t ad = sw128_desc(st + mt * kChunkA), bd = sw128_desc(st + offB + mt * NB);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {  // K = 64 each: group j / 2, scale id 2 (j % 2)
-                        const uint32_t sfa = slots + 64 * (j >> 1);
-                        const uint32_t id = static_cast<uint32_t>(2 * (j & 1));
-                        mma_f4(d_t, ad + 2 * j, bd + 2 * j, id0 | (id << 4) | (id << 29), sfa, sfa + 32,
-                               (seg_start && j == 0) ? 0u : 1u);
+                    if (lane == 0) {
+                        const uint32_t st = smem_u32(stage);
+                        for (int h = 0; h < 2; ++h) {  // the chunk's 128-wide scale groups
+                            if (128 * h >= kv) break;
+                            tmem_cp_sf(slots + 64 * h, st + offSA + 512 * (2 * mt + h));
+                            tmem_cp_sf(slots + 64 * h + 32, st + offSB + 512 * (2 * mt + h));
+                        }
+                        const uint32_t d_t = tmem + (2 * a + mt) * kMaxN;
+                        const uint64_t ad = sw128_desc(st + mt * kChunkA), bd = sw128_desc(st + offB + mt * NB);
+                        const int nmma = min(4, kv / 64);
+                        for (int j = 0; j < nmma; ++j) {  // K = 64 each: group j / 2, scale id 2 (j % 2)
+                            const uint32_t sfa = slots + 64 * (j >> 1);
+                            const uint32_t id = static_cast<uint32_t>(2 * (j & 1));
+                            mma_f4(d_t, ad + 2 * j, bd + 2 * j, id0 | (id << 4) | (id << 29), sfa, sfa + 32,
+                                   (seg_start && j == 0) ? 0u : 1u);
+                        }
                     }
                 }
-                mma_commit(&empty[s]);
-                if (seg_end) {
-                    mma_commit(&acc_full[a]);
-                    ++seg;
+                if (lane == 0) {
+                    mma_commit(&empty[s]);
+                    if (seg_end) mma_commit(&acc_full[a]);
                 }
+                if (seg_end) ++seg;
                 if (++s == p.RS) {
                     s = 0;
                     ph ^= 1;
@@ -552,18 +607,22 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (lane == 0) mbar_arrive(&acc_empty[a]);
             const int mat = c.mat, mats = p.nmat;
             const int row = c.tile * 128 + q * 32 + lane;
-            const size_t plane = static_cast<size_t>(p.umax) * p.T * p.rows_out;
-            float* dst = p.part + static_cast<size_t>((ks_begin == 0 ? 0 : 1) * mats + mat) * plane +
-                         static_cast<size_t>(c.u) * p.T * p.rows_out + row;
-            const int tokens = p.ucnt ? p.ucnt[c.u] : p.T;
+            // rows of the last tile past the expert's own rows belong to the next
+            // expert (or lie past the array): computed, never stored
+            if (row < p.rows) {
+                const size_t plane = static_cast<size_t>(p.umax) * p.T * p.rows_out;
+                float* dst = p.part + static_cast<size_t>((ks_begin == 0 ? 0 : 1) * mats + mat) * plane +
+                             static_cast<size_t>(c.u) * p.T * p.rows_out + row;
+                const int tokens = p.ucnt ? p.ucnt[c.u] : p.T;
 #pragma unroll
-            for (int t = 0; t < kMaxN / TERMS; ++t) {
-                if (t >= tokens) break;
-                float sum = 0.0f;
+                for (int t = 0; t < kMaxN / TERMS; ++t) {
+                    if (t >= tokens) break;
+                    float sum = 0.0f;
 #pragma unroll
-                for (int j = 0; j < TERMS; ++j) sum += v[TERMS * t + j];
-                dst[static_cast<size_t>(t) * p.rows_out] = sum;
-                if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
+                    for (int j = 0; j < TERMS; ++j) sum += v[TERMS * t + j];
+                    dst[static_cast<size_t>(t) * p.rows_out] = sum;
+                    if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
+                }
             }
             w += len;
             ++seg;
@@ -584,7 +643,8 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // chunk), grid-strided over the units: lane 4 kb + r takes elements 8 r ..
 // 8 r + 7 of 32-block kb (the grid is sized for the SMs, not for the largest
 // possible number of units).  Tokens a unit does not have are skipped: their
-// MMA columns are never read.
+// MMA columns are never read; so are the blocks of a last chunk past f (the
+// down projection issues no MMA there).
 template <int TERMS>
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
@@ -597,7 +657,7 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
-    const int KC = f / 256;
+    const int KC = (f + 255) / 256;
     const int items = *count * T * KC;
     const size_t plane = static_cast<size_t>(umax) * T * f;
     for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < items; i += gridDim.x * 8) {
@@ -605,21 +665,28 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
         const int rr = i - u * T * KC;
         const int t = rr / KC, c = rr - t * KC;
         if (ucnt && t >= ucnt[u]) continue;
-        const float* g0 = part + (static_cast<size_t>(u) * T + t) * f + 256 * c + 32 * kb + 8 * r;
-        float a[8], b[8], cc[8], dd[8];
-        *reinterpret_cast<float4*>(a) = *reinterpret_cast<const float4*>(g0);
-        *reinterpret_cast<float4*>(a + 4) = *reinterpret_cast<const float4*>(g0 + 4);
-        *reinterpret_cast<float4*>(b) = *reinterpret_cast<const float4*>(g0 + plane);
-        *reinterpret_cast<float4*>(b + 4) = *reinterpret_cast<const float4*>(g0 + plane + 4);
-        *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(g0 + 2 * plane);
-        *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(g0 + 2 * plane + 4);
-        *reinterpret_cast<float4*>(dd) = *reinterpret_cast<const float4*>(g0 + 3 * plane);
-        *reinterpret_cast<float4*>(dd + 4) = *reinterpret_cast<const float4*>(g0 + 3 * plane + 4);
+        const bool in = 256 * c + 32 * kb < f;  // this lane's block exists
         float v[8];
+        if (in) {
+            const float* g0 = part + (static_cast<size_t>(u) * T + t) * f + 256 * c + 32 * kb + 8 * r;
+            float a[8], b[8], cc[8], dd[8];
+            *reinterpret_cast<float4*>(a) = *reinterpret_cast<const float4*>(g0);
+            *reinterpret_cast<float4*>(a + 4) = *reinterpret_cast<const float4*>(g0 + 4);
+            *reinterpret_cast<float4*>(b) = *reinterpret_cast<const float4*>(g0 + plane);
+            *reinterpret_cast<float4*>(b + 4) = *reinterpret_cast<const float4*>(g0 + plane + 4);
+            *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(g0 + 2 * plane);
+            *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(g0 + 2 * plane + 4);
+            *reinterpret_cast<float4*>(dd) = *reinterpret_cast<const float4*>(g0 + 3 * plane);
+            *reinterpret_cast<float4*>(dd + 4) = *reinterpret_cast<const float4*>(g0 + 3 * plane + 4);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = silu_f32(a[q] + cc[q]) * (b[q] + dd[q]);
+            for (int q = 0; q < 8; ++q) v[q] = silu_f32(a[q] + cc[q]) * (b[q] + dd[q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+        }
         uint32_t w[TERMS], sb[TERMS];
-        quantize8_terms<TERMS>(v, w, sb);
+        quantize8_terms<TERMS>(v, w, sb);  // shuffles stay within the block's four lanes
+        if (!in) continue;
         uint8_t* codes = hq + (static_cast<size_t>(u) * KC + c) * N * 128;
         uint8_t* scales = hsf + (static_cast<size_t>(u) * KC + c) * 1024;
 #pragma unroll
@@ -788,15 +855,18 @@ mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
 // Token rows as kUnitTerms E2M1 terms, once per token (unswizzled): codes
 // [t][term][K / 2] (element 2i in the low nibble), E8M0 scales [t][term][K / 32].
 // One warp per (token, 256-wide chunk), lane 4 kb + r taking elements 8 r ..
-// 8 r + 7 of 32-block kb; grid-strided.
+// 8 r + 7 of 32-block kb (blocks past K, in a last partial chunk, idle);
+// grid-strided.
 __global__ void __launch_bounds__(256)
 mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __restrict__ tq,
                       uint8_t* __restrict__ tsf) {
     const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
-    const int KC = K / 256, nb = K / 32;
+    const int KC = (K + 255) / 256, nb = K / 32;
     for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < T * KC; i += gridDim.x * 8) {
         const int t = i / KC, c = i - t * KC;
-        const uint4 raw = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * K + 256 * c + 32 * kb + 8 * r);
+        const bool in = 256 * c + 32 * kb < K;
+        const uint4 raw = in ? *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * K + 256 * c + 32 * kb + 8 * r)
+                             : make_uint4(0, 0, 0, 0);
         const uint32_t wr[4] = {raw.x, raw.y, raw.z, raw.w};
         float v[8];
 #pragma unroll
@@ -806,6 +876,7 @@ mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __r
         }
         uint32_t w[kUnitTerms], sb[kUnitTerms];
         quantize8_terms<kUnitTerms>(v, w, sb);
+        if (!in) continue;
 #pragma unroll
         for (int j = 0; j < kUnitTerms; ++j) {
             const size_t row = static_cast<size_t>(t) * kUnitTerms + j;
@@ -824,7 +895,7 @@ mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__
                      const int32_t* __restrict__ perm, int k, int K, int N, const int32_t* __restrict__ nunits,
                      const int32_t* __restrict__ unit_row0, const int32_t* __restrict__ unit_cnt,
                      uint8_t* __restrict__ bq, uint8_t* __restrict__ bsf) {
-    const int nb = K / 32, KC = K / 256;
+    const int nb = K / 32, KC = (K + 255) / 256;
     const int per_unit = kUnitTokens * kUnitTerms * nb;
     const long long items = static_cast<long long>(*nunits) * per_unit;
     for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < items;
@@ -846,39 +917,55 @@ mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// Prepared scale-factor layout.  For a weight matrix with R rows (stacked over
-// the experts) and K inputs, the E8M0 bytes are grouped per tile of 128 rows
-// and 128-wide input chunk into 512-byte atoms, byte 16 (m % 32) + 4 (m / 32)
-// + b holding row m of the tile and block b of the chunk; the atom of (tile,
-// chunk) starts at (tile * K/128 + chunk) * 512.  One thread per 4-byte word
-// (the four blocks of one row and chunk).
+// Prepared scale-factor layout.  For a weight matrix of E experts with R rows
+// each (a multiple of 64) and K inputs (a multiple of 64), every expert's E8M0
+// bytes are grouped per tile of 128 rows (ceil(R / 128) tiles, the last padded
+// with zero rows) and 128-wide input group (ceil(K / 128) groups, the last
+// padded with zero blocks) into 512-byte atoms: byte 16 (m % 32) + 4 (m / 32)
+// + b holds row m of the tile and block b of the group.  The atom of (expert,
+// tile, group) starts at ((e * tiles + tile) * groups + group) * 512.  One
+// thread per 4-byte word of the atoms (the four blocks of one row and group);
+// the padding is written as zeros and skipped by the inverse.
 // ---------------------------------------------------------------------------
-__global__ void prepare_sf_kernel(uint8_t* __restrict__ canon, int64_t n_words, int K,
+__global__ void prepare_sf_kernel(uint8_t* __restrict__ canon, int64_t n_words, int R, int K,
                                   uint8_t* __restrict__ atoms, int inverse) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n_words) return;
-    const int KC = K / 128, nb = K / 32;
+    const int G = (K + 127) / 128, tiles = (R + 127) / 128, nb = K / 32;
     const int64_t atom = i / 128;            // 128 words per atom
     const int wi = static_cast<int>(i - atom * 128);
-    const int64_t tile = atom / KC;
-    const int chunk = static_cast<int>(atom - tile * KC);
+    const int g = static_cast<int>(atom % G);
+    const int64_t et = atom / G;             // e * tiles + tile
+    const int64_t e = et / tiles;
+    const int tile = static_cast<int>(et - e * tiles);
     const int r = wi >> 2, qd = wi & 3;      // word at byte 16 r + 4 qd: row m = 32 qd + r
-    const int64_t row = tile * 128 + 32 * qd + r;
-    uint32_t* cw = reinterpret_cast<uint32_t*>(canon + row * nb + 4 * chunk);
-    uint32_t* aw = reinterpret_cast<uint32_t*>(atoms + atom * 512 + 16 * r + 4 * qd);
-    if (inverse) *cw = *aw;
-    else *aw = *cw;
+    const int row = tile * 128 + 32 * qd + r;
+    uint8_t* aw = atoms + atom * 512 + 16 * r + 4 * qd;
+    uint8_t* cw = canon + (e * R + row) * nb + 4 * g;
+    const int nbv = row < R ? min(4, nb - 4 * g) : 0;  // blocks of this word inside the matrix
+    if (inverse) {
+        for (int b = 0; b < nbv; ++b) cw[b] = aw[b];
+    } else {
+        uint32_t w = 0;
+        for (int b = 0; b < nbv; ++b) w |= static_cast<uint32_t>(cw[b]) << (8 * b);
+        *reinterpret_cast<uint32_t*>(aw) = w;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t* atoms, int inverse,
+size_t prepared_sf_bytes(int64_t E, int R, int K) {
+    return static_cast<size_t>(E) * ((R + 127) / 128) * ((K + 127) / 128) * 512;
+}
+
+cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t E, int R, int K, uint8_t* atoms, int inverse,
                               cudaStream_t s) {
-    const int64_t n_words = rows * (K / 32) / 4;
+    const int64_t n_words = static_cast<int64_t>(prepared_sf_bytes(E, R, K) / 4);
     if (n_words <= 0) return cudaSuccess;
     const int64_t blocks = (n_words + 255) / 256;
-    prepare_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(const_cast<uint8_t*>(canon), n_words, K,
+    prepare_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(const_cast<uint8_t*>(canon), n_words, R, K,
                                                                     atoms, inverse);
+    trace_mark(inverse ? "unprepare_sf" : "prepare_sf", s);
     return cudaGetLastError();
 }
 
@@ -888,13 +975,17 @@ cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t rows, int K, uint8_t
 namespace {
 
 int mx_n(int T, int terms = kTerms) { return (terms * T + 15) / 16 * 16; }
+int kc256(int K) { return (K + 255) / 256; }
 
 struct MxScratch {
     uint8_t *xq, *xsf, *hq, *hsf;
     float *up, *y;
     int umax, N;
+    size_t bytes;
 };
 
+// the B operand takes one 256-wide chunk per 256 inputs (the last may be
+// partial): N rows x 128 bytes of codes and 1024 bytes of scale atoms each
 MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
     MxScratch m{};
     m.umax = std::min(E, T * k);
@@ -902,23 +993,26 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
     char* b = static_cast<char*>(scratch);
     size_t o = 0;
     auto take = [&](size_t bytes) {
-        char* r = b + o;
+        char* r = b ? b + o : nullptr;
         o += align_up(bytes);
         return r;
     };
-    m.xq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 256) * m.N * 128));
-    m.xsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(d / 128) * 512));
-    m.up = reinterpret_cast<float*>(take(4ull * m.umax * T * f * 4));
-    m.hq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 256) * m.N * 128));
-    m.hsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(m.umax) * (f / 128) * 512));
-    m.y = reinterpret_cast<float*>(take(2ull * m.umax * T * d * 4));
+    const size_t U = static_cast<size_t>(m.umax);
+    m.xq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(kc256(d)) * m.N * 128));
+    m.xsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(kc256(d)) * 1024));
+    m.up = reinterpret_cast<float*>(take(4 * U * T * f * 4));
+    m.hq = reinterpret_cast<uint8_t*>(take(U * kc256(f) * m.N * 128));
+    m.hsf = reinterpret_cast<uint8_t*>(take(U * kc256(f) * 1024));
+    m.y = reinterpret_cast<float*>(take(2 * U * T * d * 4));
+    m.bytes = o;
     return m;
 }
 
-template <int TERMS, bool GG>
-cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p, int grid, cudaStream_t s,
-                          const char* name) {
-    p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 2048), 1024));
+template <int TERMS, int WF>
+cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& sc,
+                          const CUtensorMap& sc3, MxArgs p, int grid, cudaStream_t s, const char* name) {
+    const size_t raw = WF == kWfCanon ? kRawSf : 0;
+    p.stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p.N * 128 + 2048) + raw, 1024));
     p.RS = std::min(kMaxStages, static_cast<int>((226 * 1024) / p.stage_bytes));
     if (p.RS < 2 || p.N > kMaxN) return cudaErrorNotSupported;
     const size_t smem = 1024 + static_cast<size_t>(p.RS) * p.stage_bytes;
@@ -930,57 +1024,106 @@ cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, MxArgs p,
     cudaGetDevice(&dev);
     std::atomic<int>& cur = set_bytes[dev & 63];
     if (cur.load() < static_cast<int>(smem)) {
-        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel<TERMS, GG>,
+        const cudaError_t e = cudaFuncSetAttribute(mx_stream_kernel<TERMS, WF>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cur.store(static_cast<int>(smem));
     }
-    const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS, GG>, dim3(grid),
-                                     dim3(GG ? kMxThreads + kGgThreads : kMxThreads), smem, s, a, a3, p);
+    const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS, WF>, dim3(grid),
+                                     dim3(WF == kWfGgml ? kMxThreads + kGgThreads : kMxThreads), smem, s, a, a3,
+                                     sc, sc3, p);
     trace_mark(name, s);
     return e;
 }
 
-// A operands of the three matrices over `nslots` expert slots.  Compressed-
+// Tensor maps of the three matrices over `nslots` expert slots.  Compressed-
 // tensors codes: [slots * rows, K / 2] bytes, boxes of 128 bytes (256 inputs)
-// x 128 rows, 128-byte swizzle.  ggml blocks: [slots * rows, K / 32 * 17]
-// bytes as 32-bit words, boxes of 68 words (one 512-input stage) x 128 rows,
-// no swizzle (the converting threads swizzle).
-bool make_weight_maps(const uint8_t* w1, const uint8_t* w3, const uint8_t* w2, int d, int f, uint64_t nslots,
-                      bool ggml, CUtensorMap* t1, CUtensorMap* t3, CUtensorMap* t2) {
-    if (ggml) {
-        const uint64_t rb_d = static_cast<uint64_t>(d) / 32 * 17, rb_f = static_cast<uint64_t>(f) / 32 * 17;
-        return make_tmap_rows(t1, w1, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_d, rb_d / 4, nslots * f, kGgRowBytes / 4,
-                              128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-               make_tmap_rows(t3, w3, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_d, rb_d / 4, nslots * f, kGgRowBytes / 4,
-                              128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-               make_tmap_rows(t2, w2, CU_TENSOR_MAP_DATA_TYPE_UINT32, rb_f, rb_f / 4, nslots * d, kGgRowBytes / 4,
-                              128, CU_TENSOR_MAP_SWIZZLE_NONE);
+// x 128 rows, 128-byte swizzle (a box past the end of a row, K % 256 != 0, or
+// past the last row is zero-filled).  Canonical E8M0 rows: [slots * rows,
+// K / 32] bytes, boxes of 16 bytes (one 512-input stage) x 128 rows, no
+// swizzle (rows must be whole 16-byte units: K % 512 == 0).  ggml blocks:
+// [slots * rows, K / 32 * 17] bytes as 32-bit words, boxes of 68 words (one
+// 512-input stage) x 128 rows, no swizzle (the converting threads swizzle).
+struct WeightMaps {
+    CUtensorMap q[3], sc[3];  // W1, W3, W2
+    int wf;
+};
+
+bool make_weight_maps(const uint8_t* const w_q[3], const uint8_t* const w_s[3], int sf_canon, int ggml, int d,
+                      int f, uint64_t nslots, WeightMaps* m) {
+    m->wf = ggml ? kWfGgml : (sf_canon ? kWfCanon : kWfAtoms);
+    for (int i = 0; i < 3; ++i) {
+        const uint64_t K = i < 2 ? d : f, rows = nslots * (i < 2 ? f : d);
+        bool ok;
+        if (ggml) {
+            const uint64_t rb = K / 32 * 17;
+            ok = make_tmap_rows(&m->q[i], w_q[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, rb, rb / 4, rows, kGgRowBytes / 4,
+                                128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        } else {
+            ok = make_tmap_rows(&m->q[i], w_q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, K / 2, rows, 128, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (!ok) return false;
+        if (m->wf == kWfCanon) {
+            if (K % 512) return false;
+            if (!make_tmap_rows(&m->sc[i], w_s[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 32, K / 32, rows, 16, 128,
+                                CU_TENSOR_MAP_SWIZZLE_NONE))
+                return false;
+        } else {
+            m->sc[i] = m->q[i];  // unused
+        }
     }
-    return make_tmap_rows(t1, w1, CU_TENSOR_MAP_DATA_TYPE_UINT8, d / 2, d / 2, nslots * f, 128, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tmap_rows(t3, w3, CU_TENSOR_MAP_DATA_TYPE_UINT8, d / 2, d / 2, nslots * f, 128, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tmap_rows(t2, w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, f / 2, f / 2, nslots * d, 128, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+    return true;
 }
 
 template <int TERMS>
-cudaError_t launch_stream_fmt(bool ggml, const CUtensorMap& a, const CUtensorMap& a3, const MxArgs& p, int grid,
-                              cudaStream_t s, const char* name) {
-    return ggml ? launch_stream<TERMS, true>(a, a3, p, grid, s, name)
-                : launch_stream<TERMS, false>(a, a3, p, grid, s, name);
+cudaError_t launch_stream_wf(const WeightMaps& wm, bool up, const MxArgs& p, int grid, cudaStream_t s,
+                             const char* name) {
+    const CUtensorMap& a = wm.q[up ? 0 : 2];
+    const CUtensorMap& a3 = wm.q[up ? 1 : 2];
+    const CUtensorMap& sc = wm.sc[up ? 0 : 2];
+    const CUtensorMap& sc3 = wm.sc[up ? 1 : 2];
+    switch (wm.wf) {
+        case kWfGgml: return launch_stream<TERMS, kWfGgml>(a, a3, sc, sc3, p, grid, s, name);
+        case kWfCanon: return launch_stream<TERMS, kWfCanon>(a, a3, sc, sc3, p, grid, s, name);
+        default: return launch_stream<TERMS, kWfAtoms>(a, a3, sc, sc3, p, grid, s, name);
+    }
+}
+
+// The fields of an up (W1, W3) and a down (W2) pass over units that share B
+// layouts of N rows: everything but the unit lists, B pointers and outputs.
+void pass_shapes(MxArgs* up, MxArgs* dn, const uint8_t* const w_s[3], int E, int d, int f, int N) {
+    up->sf[0] = w_s[0];
+    up->sf[1] = w_s[1];
+    up->nmat = 2;
+    up->E = E;
+    up->rows = f;
+    up->tiles = (f + 127) / 128;
+    up->K = d;
+    up->KC = kc256(d);
+    up->KS = (up->KC + kChunks - 1) / kChunks;
+    up->G = (d + 127) / 128;
+    up->N = N;
+    up->rows_out = f;
+    *dn = *up;
+    dn->sf[0] = w_s[2];
+    dn->sf[1] = w_s[2];
+    dn->nmat = 1;
+    dn->early_a = 1;
+    dn->rows = d;
+    dn->tiles = (d + 127) / 128;
+    dn->K = f;
+    dn->KC = kc256(f);
+    dn->KS = (dn->KC + kChunks - 1) / kChunks;
+    dn->G = (f + 127) / 128;
+    dn->rows_out = d;
 }
 
 }  // namespace
 
 size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f) {
-    const size_t umax = std::min(E, T * k);
-    const size_t N = mx_n(T);
-    return align_up(static_cast<size_t>(d / 256) * N * 128) + align_up(static_cast<size_t>(d / 128) * 512) +
-           align_up(4 * umax * T * f * 4) + align_up(umax * (f / 256) * N * 128) +
-           align_up(umax * (f / 128) * 512) + align_up(2 * umax * T * d * 4);
+    return mx_carve(nullptr, T, E, k, d, f).bytes;
 }
 
 void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_t** xq, uint8_t** xsf,
@@ -1003,63 +1146,48 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     }
     // A operands over a slot per expert, or over the cache's slots
     const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
-    CUtensorMap t1, t3, t2;
-    if (!make_weight_maps(a.w1_q, a.w3_q, a.w2_q, a.d, a.f, nslots, a.ggml != 0, &t1, &t3, &t2))
-        return cudaErrorNotSupported;
+    const uint8_t* const wq[3] = {a.w1_q, a.w3_q, a.w2_q};
+    const uint8_t* const ws[3] = {a.w1_sf, a.w3_sf, a.w2_sf};
+    WeightMaps wm;
+    if (!make_weight_maps(wq, ws, a.sf_canon, a.ggml, a.d, a.f, nslots, &wm)) return cudaErrorNotSupported;
 
-    MxArgs up{};
-    up.sf[0] = a.w1_sf;
-    up.sf[1] = a.w3_sf;
-    up.nmat = 2;
+    MxArgs up{}, dn{};
+    pass_shapes(&up, &dn, ws, a.E, a.d, a.f, m.N);
     up.bq = m.xq;
     up.bsf = m.xsf;
-    up.bq_ustride = 0;
-    up.bsf_ustride = 0;
     up.active = a.active;
     up.count = a.active + a.E;
-    up.ucnt = nullptr;
     up.slot_of = a.slot_of;
     up.nslots = static_cast<int>(nslots);
-    up.E = a.E;
-    up.rows = a.f;
-    up.tiles = a.f / 128;
-    up.KC = a.d / 256;
-    up.KS = (up.KC + kChunks - 1) / kChunks;
-    up.N = m.N;
     up.T = a.T;
     up.part = m.up;
     up.umax = m.umax;
-    up.rows_out = a.f;
     up.hdr = a.hdr;
     // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
+    if ((e = launch_stream_wf<kTerms>(wm, true, up, grid_up, s, "decode_up"))) return e;
 
-    if ((e = launch_stream_fmt<kTerms>(a.ggml != 0, t1, t3, up, grid_up, s, "decode_up"))) return e;
-
-    const int warps = m.umax * a.T * (a.f / 256);
+    const int warps = m.umax * a.T * kc256(a.f);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
     e = launch_pdl(mx_finish_kernel<kTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
                    m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf);
     trace_mark("decode_finish_up", s);
     if (e != cudaSuccess) return e;
 
-    MxArgs dn = up;
-    dn.sf[0] = a.w2_sf;
-    dn.sf[1] = a.w2_sf;
-    dn.nmat = 1;
-    dn.early_a = 1;
     dn.bq = m.hq;
     dn.bsf = m.hsf;
-    dn.bq_ustride = static_cast<size_t>(a.f / 256) * m.N * 128;
-    dn.bsf_ustride = static_cast<size_t>(a.f / 128) * 512;
-    dn.rows = a.d;
-    dn.tiles = a.d / 128;
-    dn.KC = a.f / 256;
-    dn.KS = (dn.KC + kChunks - 1) / kChunks;
+    dn.bq_ustride = static_cast<size_t>(kc256(a.f)) * m.N * 128;
+    dn.bsf_ustride = static_cast<size_t>(kc256(a.f)) * 1024;
+    dn.active = up.active;
+    dn.count = up.count;
+    dn.slot_of = up.slot_of;
+    dn.nslots = up.nslots;
+    dn.T = up.T;
     dn.part = m.y;
-    dn.rows_out = a.d;
+    dn.umax = m.umax;
+    dn.hdr = a.hdr;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream_fmt<kTerms>(a.ggml != 0, t2, t2, dn, grid_dn, s, "decode_down"))) return e;
+    if ((e = launch_stream_wf<kTerms>(wm, false, dn, grid_dn, s, "decode_down"))) return e;
 
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
@@ -1103,11 +1231,11 @@ MxUnitScratch mx_units_carve(void* scratch, int T, int E, int k, int d, int f) {
     m.rowmap = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P) * 4));
     m.tq = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kUnitTerms * (d / 2)));
     m.tsf = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * kUnitTerms * (d / 32)));
-    m.xq = reinterpret_cast<uint8_t*>(take(U * (d / 256) * m.N * 128));
-    m.xsf = reinterpret_cast<uint8_t*>(take(U * (d / 128) * 512));
+    m.xq = reinterpret_cast<uint8_t*>(take(U * kc256(d) * m.N * 128));
+    m.xsf = reinterpret_cast<uint8_t*>(take(U * kc256(d) * 1024));
     m.up = reinterpret_cast<float*>(take(4 * U * kUnitTokens * f * 4));
-    m.hq = reinterpret_cast<uint8_t*>(take(U * (f / 256) * m.N * 128));
-    m.hsf = reinterpret_cast<uint8_t*>(take(U * (f / 128) * 512));
+    m.hq = reinterpret_cast<uint8_t*>(take(U * kc256(f) * m.N * 128));
+    m.hsf = reinterpret_cast<uint8_t*>(take(U * kc256(f) * 1024));
     m.y = reinterpret_cast<float*>(take(2 * U * kUnitTokens * d * 4));
     m.bytes = o;
     return m;
@@ -1128,7 +1256,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     trace_mark("units", s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long twarps = static_cast<long long>(a.T) * (a.d / 256);
+    const long long twarps = static_cast<long long>(a.T) * kc256(a.d);
     mx_token_terms_kernel<<<static_cast<int>(std::min<long long>((twarps + 7) / 8, 8LL * a.num_sms)), 256, 0, s>>>(
         a.x, a.T, a.d, m.tq, m.tsf);
     trace_mark("token_terms", s);
@@ -1140,40 +1268,32 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const uint64_t nslots = a.slot_of ? static_cast<uint64_t>(a.nslots) : static_cast<uint64_t>(a.E);
-    CUtensorMap t1, t3, t2;
-    if (!make_weight_maps(a.w1_q, a.w3_q, a.w2_q, a.d, a.f, nslots, a.ggml != 0, &t1, &t3, &t2))
-        return cudaErrorNotSupported;
+    const uint8_t* const wq[3] = {a.w1_q, a.w3_q, a.w2_q};
+    const uint8_t* const ws[3] = {a.w1_sf, a.w3_sf, a.w2_sf};
+    WeightMaps wm;
+    if (!make_weight_maps(wq, ws, a.sf_canon, a.ggml, a.d, a.f, nslots, &wm)) return cudaErrorNotSupported;
 
-    MxArgs up{};
-    up.sf[0] = a.w1_sf;
-    up.sf[1] = a.w3_sf;
-    up.nmat = 2;
+    MxArgs up{}, dn{};
+    pass_shapes(&up, &dn, ws, a.E, a.d, a.f, m.N);
     up.bq = m.xq;
     up.bsf = m.xsf;
-    up.bq_ustride = static_cast<size_t>(a.d / 256) * m.N * 128;
-    up.bsf_ustride = static_cast<size_t>(a.d / 128) * 512;
+    up.bq_ustride = static_cast<size_t>(kc256(a.d)) * m.N * 128;
+    up.bsf_ustride = static_cast<size_t>(kc256(a.d)) * 1024;
     up.active = m.unit_exp;
     up.count = m.nunits;
     up.ucnt = m.unit_cnt;
     up.ubase = m.ubase;
     up.slot_of = a.slot_of;
     up.nslots = static_cast<int>(nslots);
-    up.E = a.E;
-    up.rows = a.f;
-    up.tiles = a.f / 128;
-    up.KC = a.d / 256;
-    up.KS = (up.KC + kChunks - 1) / kChunks;
-    up.N = m.N;
     up.T = kUnitTokens;
     up.part = m.up;
     up.umax = m.umax;
-    up.rows_out = a.f;
     up.hdr = a.hdr;
     // every CTA's range must be at least one tile long: there are at least k units
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
-    if ((e = launch_stream_fmt<kUnitTerms>(a.ggml != 0, t1, t3, up, grid_up, s, "units_up"))) return e;
+    if ((e = launch_stream_wf<kUnitTerms>(wm, true, up, grid_up, s, "units_up"))) return e;
 
-    const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * (a.f / 256);
+    const long long fwarps = static_cast<long long>(m.umax) * kUnitTokens * kc256(a.f);
     const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
     e = launch_pdl(mx_finish_kernel<kUnitTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
                    kUnitTokens, a.f, m.N, static_cast<const int32_t*>(m.nunits),
@@ -1181,23 +1301,22 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     trace_mark("units_finish_up", s);
     if (e != cudaSuccess) return e;
 
-    MxArgs dn = up;
-    dn.sf[0] = a.w2_sf;
-    dn.sf[1] = a.w2_sf;
-    dn.nmat = 1;
-    dn.early_a = 1;
     dn.bq = m.hq;
     dn.bsf = m.hsf;
-    dn.bq_ustride = static_cast<size_t>(a.f / 256) * m.N * 128;
-    dn.bsf_ustride = static_cast<size_t>(a.f / 128) * 512;
-    dn.rows = a.d;
-    dn.tiles = a.d / 128;
-    dn.KC = a.f / 256;
-    dn.KS = (dn.KC + kChunks - 1) / kChunks;
+    dn.bq_ustride = static_cast<size_t>(kc256(a.f)) * m.N * 128;
+    dn.bsf_ustride = static_cast<size_t>(kc256(a.f)) * 1024;
+    dn.active = up.active;
+    dn.count = up.count;
+    dn.ucnt = up.ucnt;
+    dn.ubase = up.ubase;
+    dn.slot_of = up.slot_of;
+    dn.nslots = up.nslots;
+    dn.T = up.T;
     dn.part = m.y;
-    dn.rows_out = a.d;
+    dn.umax = m.umax;
+    dn.hdr = a.hdr;
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
-    if ((e = launch_stream_fmt<kUnitTerms>(a.ggml != 0, t2, t2, dn, grid_dn, s, "units_down"))) return e;
+    if ((e = launch_stream_wf<kUnitTerms>(wm, false, dn, grid_dn, s, "units_down"))) return e;
 
     // the y slots are strided by units x kUnitTokens rows; the grid's y index is the token
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);

@@ -43,11 +43,13 @@ that branch alone.
 from .mxfp4 import (E2M1_MAGNITUDES, GGML_KVALUES, decode_ggml, decode_source, e8m0_scale,
                     ggml_e8m0_half, repack_ggml, source_codes, unpack_ggml)
 from .routing import bf16_to_f64, permute, router_logits, select_experts, sigmoid
-from .layer import (block_forward, expert_ffn, moe_forward, rmsnorm, round_bf16, silu)
+from .layer import (block_forward, block_head, block_tail, expert_ffn, moe_forward, rmsnorm,
+                    round_bf16, silu)
 
 __all__ = [
     "E2M1_MAGNITUDES", "GGML_KVALUES", "decode_ggml", "decode_source", "e8m0_scale",
     "ggml_e8m0_half", "repack_ggml", "source_codes", "unpack_ggml", "bf16_to_f64", "permute",
-    "router_logits", "select_experts", "sigmoid", "block_forward", "expert_ffn", "moe_forward",
+    "router_logits", "select_experts", "sigmoid", "block_forward", "block_head", "block_tail",
+    "expert_ffn", "moe_forward",
     "rmsnorm", "round_bf16", "silu",
 ]

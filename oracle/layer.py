@@ -53,7 +53,7 @@ def expert_ffn(x, w1, w3, w2, act: str = "silu_gated") -> np.ndarray:
 
 
 def moe_forward(x_router, router_w, router_b, k, x_expert, expert, idx=None,
-                act: str = "silu_gated"):
+                act: str = "silu_gated", experts=None):
     """The routed MoE layer on T token rows.
 
     x_router [T, d_r] float64   router input;
@@ -63,7 +63,10 @@ def moe_forward(x_router, router_w, router_b, k, x_expert, expert, idx=None,
     expert(m, e) -> (packed, scale) of matrix m (0 = w1, 1 = w3, 2 = w2) of
                                 expert e, in the compressed-tensors layout;
     idx [T, k] optional         a selection to use instead of the top-k (used
-                                only for tokens whose top-k is a near tie).
+                                only for tokens whose top-k is a near tie);
+    experts optional            only these experts' terms enter the sum (the
+                                layer output is the sum of such parts over a
+                                partition of the experts).
 
     Returns a dict: out [T, d] float64 plus the routing (idx, w, s, beta,
     margin, logits).
@@ -81,6 +84,8 @@ def moe_forward(x_router, router_w, router_b, k, x_expert, expert, idx=None,
     r["logits"] = logits
     out = np.zeros((T, x_expert.shape[1]), dtype=np.float64)
     used = np.unique(r["idx"])
+    if experts is not None:
+        used = np.intersect1d(used, np.asarray(experts, dtype=np.int64))
     for e in used:
         tok, slot = np.nonzero(r["idx"] == e)
         w1 = decode_source(*expert(0, int(e)))
@@ -116,6 +121,21 @@ def round_bf16(v) -> np.ndarray:
     return np.where(v == 0, v, r)
 
 
+def block_head(h, gamma, eps, w_down):
+    """The block's steps before the MoE: hn = bf16(RMSNorm(h) * gamma) (the
+    router input) and z = bf16(hn W_down^T) (the experts' latent input)."""
+    hn = round_bf16(rmsnorm(h, gamma, eps))
+    z = round_bf16(hn @ np.asarray(w_down, np.float64).T)
+    return hn, z
+
+
+def block_tail(moe_out, w_up):
+    """The block's step after the MoE: the combined latent row, rounded to bf16
+    where the block hands it on (m), through the up-projection."""
+    m = round_bf16(moe_out)
+    return m, m @ np.asarray(w_up, np.float64).T
+
+
 def block_forward(h, gamma, eps, w_down, w_up, router_w, router_b, k, expert, idx=None,
                   act: str = "silu_gated"):
     """Full latent block: RMSNorm -> router + down-projection -> MoE -> up-projection.
@@ -123,11 +143,10 @@ def block_forward(h, gamma, eps, w_down, w_up, router_w, router_b, k, expert, id
     h [T, D], gamma [D], w_down [d, D], w_up [D, d], router_w [E, D] float64.
     Returns a dict with out [T, D] and the intermediates (hn, z, m) and routing.
     """
-    hn = round_bf16(rmsnorm(h, gamma, eps))
-    z = round_bf16(hn @ np.asarray(w_down, np.float64).T)
+    hn, z = block_head(h, gamma, eps, w_down)
     r = moe_forward(hn, router_w, router_b, k, z, expert, idx=idx, act=act)
-    m = round_bf16(r["out"])
+    m, out = block_tail(r["out"], w_up)
     r["hn"], r["z"], r["m"] = hn, z, m
     r["moe_out"] = r["out"]
-    r["out"] = m @ np.asarray(w_up, np.float64).T
+    r["out"] = out
     return r

@@ -20,3 +20,15 @@ def golden(name):
     import json
     with open(os.path.join(GOLDEN, name)) as fh:
         return json.load(fh)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The parity margins the GPU tests recorded: worst err / row RMS of each
+    check beside its bound."""
+    mod = sys.modules.get("gpu_util")
+    margins = getattr(mod, "MARGINS", None) if mod else None
+    if not margins:
+        return
+    terminalreporter.write_sep("-", "parity margins: max over rows of err / row RMS (bound)")
+    for test, label, err, tol in margins:
+        terminalreporter.write_line(f"{err:10.3e}  (bound {tol:.0e})  {test}  {label}")

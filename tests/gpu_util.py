@@ -15,8 +15,13 @@ def to_dev(arr: np.ndarray, dev):
     return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
 
 
-def make_layer(cfg: synth.Config, dev="cuda", path=0, on_device_experts=None):
-    """(layer, dense host inputs, expert accessor for the oracle, device expert dict)."""
+def make_layer(cfg: synth.Config, dev="cuda", path=0, on_device_experts=None, prepared=False):
+    """(layer, dense host inputs, expert accessor for the oracle, device expert dict).
+
+    The layer gets the expert bytes exactly as generated: codes and canonical
+    E8M0 scales (the checkpoint's weight_packed / weight_scale layout); with
+    ``prepared`` it also carries the prepared scale atoms, which the kernels
+    then read instead."""
     import mxfp4_routed_expert_sigmoid_gb300 as k3
 
     dense = synth.dense_inputs(cfg)
@@ -30,7 +35,7 @@ def make_layer(cfg: synth.Config, dev="cuda", path=0, on_device_experts=None):
         names = synth.MATRIX_NAMES
         expert = lambda m, e: (ex[names[m] + "_q"][e], ex[names[m] + "_s"][e])
     kw = dict(router_w=to_dev(dense["router_w"], dev), router_b=to_dev(dense["router_b"], dev),
-              k=cfg.k, path=path, **ex_dev)
+              k=cfg.k, path=path, prepared=prepared, **ex_dev)
     if cfg.block:
         kw.update(norm_gamma=to_dev(dense["norm_gamma"], dev), w_down=to_dev(dense["w_down"], dev),
                   w_up=to_dev(dense["w_up"], dev), eps=dense["eps"])
@@ -69,3 +74,78 @@ def rel_err_rows(got: np.ndarray, ref: np.ndarray, out_bf16: bool = True) -> np.
 
 def bf16_tensor_to_np(t) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# margins: every parity check records its worst err / RMS against its bound,
+# and the session prints them (tests/conftest.py) so the headroom is visible
+# ---------------------------------------------------------------------------
+MARGINS = []
+
+
+def record_margin(label: str, err, tol: float):
+    import os
+
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append((test, label, float(np.max(err)), float(tol)))
+
+
+# ---------------------------------------------------------------------------
+# the oracle on many rows of a full-size workload, its expert sum split over
+# processes: the output is the sum of per-expert terms, so each worker sums a
+# subset of the used experts (oracle.moe_forward with `experts`) and the parts
+# are added; block mode wraps that in oracle.block_head / block_tail
+# ---------------------------------------------------------------------------
+def _moe_part(args):
+    cfg, x_router, router_w, bias, x_expert, idx, experts = args
+    expert = lambda m, e: synth.expert_matrix_np(cfg, m, e)  # noqa: E731
+    return oracle.moe_forward(x_router, router_w, bias, cfg.k, x_expert, expert, idx=idx,
+                              experts=experts)["out"]
+
+
+def oracle_rows_parallel(cfg, dense, tokens, idx=None, workers=None):
+    """oracle_forward(cfg, dense, expert, tokens, idx)["out"] with the expert
+    bytes regenerated per worker (synth.expert_matrix_np) and the used experts
+    split over a spawn pool.  Returns (out [n, width] float64, routing dict of
+    the oracle on these rows: idx, margin)."""
+    import multiprocessing as mp
+    import os
+
+    h = oracle.bf16_to_f64(dense["hidden"][tokens])
+    wr = oracle.bf16_to_f64(dense["router_w"])
+    if cfg.block:
+        x_r, x_e = oracle.block_head(h, oracle.bf16_to_f64(dense["norm_gamma"]), dense["eps"],
+                                     oracle.bf16_to_f64(dense["w_down"]))
+    else:
+        x_r = x_e = h
+    r = oracle.select_experts(oracle.router_logits(x_r, wr), dense["router_b"], cfg.k)
+    used = np.unique(r["idx"] if idx is None else idx)
+    n = workers or min(len(used), os.cpu_count() or 1)
+    parts = [used[i::n] for i in range(n)]
+    jobs = [(cfg, x_r, wr, dense["router_b"], x_e, idx, p) for p in parts]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n) as pool:
+        out = sum(pool.map(_moe_part, jobs))
+    if cfg.block:
+        out = oracle.block_tail(out, oracle.bf16_to_f64(dense["w_up"]))[1]
+    return out, {"idx": r["idx"], "margin": r["margin"]}
+
+
+def sample_rows(T: int, idx_gpu: np.ndarray, n: int, seed: int, per_expert: int = 6):
+    """n token rows of a large batch for a sampled parity check: the first and
+    last tokens routed to each of the 8 most-loaded experts (the heaviest
+    expert segments, their first and last tiles), the last tokens of the
+    highest-numbered expert that has tokens (the end of the tile list), and
+    seeded random rows for the rest."""
+    loads = np.bincount(idx_gpu.reshape(-1), minlength=int(idx_gpu.max()) + 1)
+    pick = []
+    for e in np.argsort(-loads, kind="stable")[:8]:
+        toks = np.nonzero((idx_gpu == e).any(axis=1))[0]
+        pick += toks[: per_expert // 2].tolist() + toks[-(per_expert // 2):].tolist()
+    last = int(np.nonzero(loads)[0][-1])
+    pick += np.nonzero((idx_gpu == last).any(axis=1))[0][-per_expert:].tolist()
+    chosen = list(dict.fromkeys(pick))[:n]
+    rest = np.setdiff1d(np.arange(T), chosen)
+    rng = np.random.default_rng(seed)
+    chosen += rng.choice(rest, n - len(chosen), replace=False).tolist()
+    return np.sort(np.asarray(chosen, dtype=np.int64))

@@ -35,7 +35,7 @@ def test_exports_match_header(k3):
     L = k3.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert k3.k3moe_abi_version() == 3
+    assert k3.k3moe_abi_version() == 4
 
 
 def test_status_strings(k3):
@@ -76,7 +76,7 @@ def desc(k3, **over):
     d = k3.LayerDesc()
     d.E, d.k, d.d, d.f, d.d_router = 896, 16, 3584, 3072, 3584
     d.act, d.path, d.D, d.eps, d.format = 0, 0, 0, 0.0, 0
-    for name in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf", "router_w", "router_b"):
+    for name in ("w1_q", "w3_q", "w2_q", "w1_s", "w3_s", "w2_s", "router_w", "router_b"):
         setattr(d, name, A16)
     for k_, v in over.items():
         setattr(d, k_, v)
@@ -95,13 +95,19 @@ def test_repack_validation(k3):
 
 def test_prepare_scales_validation(k3):
     L = k3.lib()
-    assert L.k3moe_prepare_scales(None, 128, 256, A16, None) == 1
-    assert L.k3moe_prepare_scales(A16, 0, 256, A16, None) == 1
-    assert L.k3moe_prepare_scales(A16, 192, 256, A16, None) == 2
-    assert L.k3moe_prepare_scales(A16, 128, 320, A16, None) == 2
-    assert L.k3moe_prepare_scales(A1, 128, 256, A16, None) == 3
-    assert L.k3moe_unprepare_scales(A16, 128, 64, A16, None) == 2
-    assert L.k3moe_unprepare_scales(A16, 128, 256, None, None) == 1
+    assert L.k3moe_prepare_scales(None, 1, 128, 256, A16, None) == 1
+    assert L.k3moe_prepare_scales(A16, 0, 128, 256, A16, None) == 1
+    assert L.k3moe_prepare_scales(A16, 1, 0, 256, A16, None) == 1
+    assert L.k3moe_prepare_scales(A16, 1, 96, 256, A16, None) == 2
+    assert L.k3moe_prepare_scales(A16, 1, 128, 352, A16, None) == 2
+    assert L.k3moe_prepare_scales(A1, 1, 128, 256, A16, None) == 3
+    assert L.k3moe_unprepare_scales(A16, 1, 128, 32, A16, None) == 2
+    assert L.k3moe_unprepare_scales(A16, 1, 128, 256, None, None) == 1
+    # per expert: ceil(rows / 128) tiles x ceil(cols / 128) groups x 512 bytes
+    assert L.k3moe_prepared_scales_size(896, 3072, 3584) == 896 * 3072 * 3584 // 32
+    assert L.k3moe_prepared_scales_size(8, 64, 64) == 8 * 512
+    assert L.k3moe_prepared_scales_size(3, 192, 320) == 3 * 2 * 3 * 512
+    assert L.k3moe_prepared_scales_size(0, 64, 64) == 0
 
 
 def test_route_validation(k3):
@@ -123,27 +129,33 @@ def test_route_validation(k3):
 
 
 def test_forward_validation(k3):
+    # every case fails validation before anything is launched (the pointers are fake)
     L = k3.lib()
     fwd = lambda dsc, **kw: L.k3moe_forward(ctypes.byref(dsc), kw.get("h", A16), kw.get("T", 1),
                                             A16, A16, kw.get("ws", 1 << 40), None)
-    assert fwd(desc(k3, d=96)) == 2
+    assert fwd(desc(k3, d=96, d_router=96)) == 2     # the MMAs take 64 inputs at a time
+    assert fwd(desc(k3, f=3072 + 32)) == 2
     assert fwd(desc(k3, k=40)) == 2
     assert fwd(desc(k3, k=17, E=16)) == 2
     assert fwd(desc(k3, E=2000)) == 2
     assert fwd(desc(k3, act=1)) == 8
     assert fwd(desc(k3, format=2)) == 1
     # ggml blocks: no separate scales; rows of whole 16-byte units; streaming path only
-    assert fwd(desc(k3, format=1, w2_sf=None, w3_sf=None, w1_sf=None, w1_q=A16 + 16), ws=16) == 4
-    assert fwd(desc(k3, format=1, d=3584 - 256, d_router=3584 - 256)) == 2
-    assert fwd(desc(k3, format=1, f=3072 + 256)) == 2
-    assert fwd(desc(k3, format=1, path=2)) == 8
-    assert fwd(desc(k3, format=1), T=1025) == 8
-    assert fwd(desc(k3, format=1, w2_q=A1)) == 3
+    gg = dict(format=1, w1_s=None, w3_s=None, w2_s=None)
+    assert fwd(desc(k3, w1_q=A16 + 16, **gg), ws=16) == 4
+    assert fwd(desc(k3, d=3584 - 256, d_router=3584 - 256, **gg)) == 2
+    assert fwd(desc(k3, f=3072 + 256, **gg)) == 2
+    assert fwd(desc(k3, path=2, **gg)) == 8
+    assert fwd(desc(k3, **gg), T=1025) == 8
+    assert fwd(desc(k3, w2_q=A1, **gg)) == 3
     assert fwd(desc(k3, path=7)) == 1
-    assert fwd(desc(k3, w2_sf=None)) == 1
-    assert fwd(desc(k3, d=192, d_router=192)) == 2  # the tensor-core K chunks are 256 wide
-    assert fwd(desc(k3, f=3072 + 64)) == 2
-    assert fwd(desc(k3, f=3072 + 128)) == 2
+    # scales: the canonical arrays, or all three prepared arrays
+    assert fwd(desc(k3, w2_s=None)) == 1
+    assert fwd(desc(k3, w1_s=None, w3_s=None, w2_s=None)) == 1
+    assert fwd(desc(k3, w1_sf=A16)) == 1                # one prepared array without the others
+    assert fwd(desc(k3, w1_sf=A16, w3_sf=A16, w2_sf=A1)) == 3
+    assert fwd(desc(k3, w1_sf=A16, w3_sf=A16, w2_sf=A16, w1_s=None, w3_s=None, w2_s=None), ws=16) == 4
+    assert fwd(desc(k3, w3_s=A1)) == 3
     assert fwd(desc(k3, w3_q=A1)) == 3
     assert fwd(desc(k3, w2_q=A16 + 16)) == 3  # E2M1 codes: 32-byte aligned for TMA
     assert fwd(desc(k3, d_router=7168)) == 2
@@ -151,12 +163,22 @@ def test_forward_validation(k3):
     assert fwd(desc(k3), h=A1) == 3
     assert fwd(desc(k3), ws=16) == 4
     assert fwd(desc(k3, path=1), T=1025) == 8  # the streaming kernels take at most 1024 tokens
+    # a workspace one byte short of the plan, for widths whose scales are
+    # prepared per call (d, f not multiples of 512) and for the K3 widths
+    for over in (dict(d=64, f=64, d_router=64, E=8, k=2), dict()):
+        dd = desc(k3, **over)
+        need = L.k3moe_workspace_size(ctypes.byref(dd), 4)
+        assert fwd(dd, T=4, ws=need - 1) == 4
+    small = desc(k3, d=64, f=64, d_router=64, E=8, k=2)
+    prep = desc(k3, d=64, f=64, d_router=64, E=8, k=2, w1_sf=A16, w3_sf=A16, w2_sf=A16)
+    # the per-call preparation takes workspace room that prepared scales do not
+    assert L.k3moe_workspace_size(ctypes.byref(small), 4) > L.k3moe_workspace_size(ctypes.byref(prep), 4)
 
 
 def cache_desc(k3, **over):
     c = k3.CacheDesc()
     c.slots, c.reserved = 64, 0
-    for name in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf", "state"):
+    for name in ("w1_q", "w3_q", "w2_q", "w1_s", "w3_s", "w2_s", "state"):
         setattr(c, name, A16)
     for k_, v in over.items():
         setattr(c, k_, v)
@@ -178,7 +200,9 @@ def test_cache_validation(k3):
     assert fwd(desc(k3), cache_desc(k3, slots=897)) == 2  # more slots than experts
     assert fwd(desc(k3), cache_desc(k3), T=8) == 2        # 8 tokens may use 128 experts
     assert fwd(desc(k3), cache_desc(k3, w2_q=A16 + 16)) == 3
-    assert fwd(desc(k3), cache_desc(k3, w3_sf=A1)) == 3
+    assert fwd(desc(k3), cache_desc(k3, w3_s=A1)) == 3
+    # canonical scales whose rows are not whole 512-input stages: no cache
+    assert fwd(desc(k3, d=768, d_router=768), cache_desc(k3)) == 8
     assert fwd(desc(k3), cache_desc(k3, w1_q=None)) == 1
     assert fwd(desc(k3, path=2), cache_desc(k3)) == 8     # the grouped path has no cache
     assert fwd(desc(k3), cache_desc(k3), T=2000) == 8

@@ -118,7 +118,8 @@ def test_hot_experts_stay_resident(k3):
     """Tokens that all favour the same 8 hot experts (bias +1, as in the
     draft-verification workload) hit the cache after the first call."""
     cfg = synth.custom("verify_t8", T=8, E=64, k=4, d=256, f=256)
-    layer, dense, expert, _ = make_layer(cfg, on_device_experts=False)
+    # d = f = 256 are not whole 512-input stages: the cache takes the prepared scales
+    layer, dense, expert, _ = make_layer(cfg, on_device_experts=False, prepared=True)
     import torch
 
     b = torch.zeros(cfg.E, dtype=torch.float32)
@@ -148,7 +149,7 @@ def test_cache_errors(k3, small):
     # state never initialised: the device flags it and nothing is fetched
     cache = k3.ExpertCache(hlayer, 8)
     cache.tensors["state"].zero_()
-    for t in ("w1_q", "w3_q", "w2_q", "w1_sf", "w3_sf", "w2_sf"):
+    for t in ("w1_q", "w3_q", "w2_q", "w1_s", "w3_s", "w2_s"):
         cache.tensors[t].zero_()
     k3.k3moe_forward_cached(hlayer, cache, x, ws=ws)
     assert k3.k3moe_get_status(ws) == 1

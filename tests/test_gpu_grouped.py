@@ -12,12 +12,13 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import bf16_tensor_to_np, make_layer, oracle_forward, rel_err_rows, to_dev
+from gpu_util import (bf16_tensor_to_np, make_layer, oracle_forward, oracle_rows_parallel,
+                      record_margin, rel_err_rows, sample_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
-TINY = dict(d=256, f=256)
+TINY = dict()  # the tiny workload at its stated shape (d = f = 64)
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +53,12 @@ def test_gemm_bf16(k3, T, N, K, fp32):
     assert np.all(np.abs(got - ref) <= tol + 1e-30), np.max(np.abs(got - ref) - tol)
 
 
-def compare_forward(k3, cfg, path, tokens=None, bundle=None, tol=TOL):
+def compare_forward(k3, cfg, path, tokens=None, bundle=None, tol=TOL, sample=0):
+    """The layer on the GPU against the oracle on `tokens` (all by default),
+    or, with `sample`, on that many rows chosen from the GPU's routing
+    (gpu_util.sample_rows: the heaviest experts' first and last tokens, the
+    end of the tile list, seeded random rows), the oracle's expert sum then
+    spread over host processes."""
     layer, dense, expert, _ = bundle or make_layer(cfg, path=path)
     x = to_dev(dense["hidden"], "cuda")
     ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T))
@@ -61,15 +67,26 @@ def compare_forward(k3, cfg, path, tokens=None, bundle=None, tol=TOL):
     assert k3.k3moe_get_status(ws) == 0
     got = bf16_tensor_to_np(out)
     idx_gpu = idx_gpu.cpu().numpy().astype(np.int64)
-    tokens = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
-    ref = oracle_forward(cfg, dense, expert, tokens=tokens)
+    if sample:
+        tokens = sample_rows(cfg.T, idx_gpu, sample, seed=cfg.seed)
+        run = lambda idx=None: oracle_rows_parallel(cfg, dense, tokens, idx=idx)  # noqa: E731
+        ref_out, ref = run()
+    else:
+        tokens = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+        ref = oracle_forward(cfg, dense, expert, tokens=tokens)
+        ref_out = ref["out"]
     thr = 1e-3 if cfg.block else 1e-5
     near = ref["margin"] < thr
     same = np.all(ref["idx"] == idx_gpu[tokens], axis=1)
     assert np.all(same | near), "selection differs outside near ties"
     if np.any(~same):
-        ref = oracle_forward(cfg, dense, expert, tokens=tokens, idx=idx_gpu[tokens])
-    err = rel_err_rows(got[tokens], ref["out"])
+        if sample:
+            ref_out, _ = run(idx=idx_gpu[tokens])
+        else:
+            ref_out = oracle_forward(cfg, dense, expert, tokens=tokens, idx=idx_gpu[tokens])["out"]
+    err = rel_err_rows(got[tokens], ref_out)
+    record_margin(f"{cfg.name} T={cfg.T} E={cfg.E} d={cfg.d} f={cfg.f} path={path} rows={len(tokens)}",
+                  err, tol)
     assert np.all(err <= tol), f"max err/rms {err.max():.3e} at token {tokens[np.argmax(err)]}"
     return out, ws, err
 
@@ -184,19 +201,18 @@ def test_block_small(k3, T, path):
 
 
 def test_chunk_t512_full_sampled(k3):
-    cfg = synth.CONFIGS["chunk_t512"]
-    rng = np.random.default_rng(5)
-    toks = np.sort(rng.choice(cfg.T, 4, replace=False))
-    compare_forward(k3, cfg, 0, tokens=toks)
+    """The T = 512 chunk at the K3 shape on the unit-grouped streaming path:
+    256 token rows checked (every expert's units, their first and last tokens
+    for the most loaded ones)."""
+    compare_forward(k3, synth.CONFIGS["chunk_t512"], 0, sample=256)
 
 
 def test_block_t8192_full_sampled(k3):
     """The full latent block at T = 8192, D = 7168 (Zipf-skewed routing): the
-    whole batch runs on the GPU, 4 seeded token rows are checked."""
-    cfg = synth.CONFIGS["block_t8192"]
-    rng = np.random.default_rng(6)
-    toks = np.sort(rng.choice(cfg.T, 4, replace=False))
-    compare_forward(k3, cfg, 0, tokens=toks)
+    whole batch runs on the GPU; 256 token rows are checked, among them the
+    first and last tokens of the 8 most-loaded experts (their first and last
+    tiles of the grouped GEMMs) and the last tile of the tile list."""
+    compare_forward(k3, synth.CONFIGS["block_t8192"], 0, sample=256)
 
 
 def test_verify_t8_grouped_path(k3):

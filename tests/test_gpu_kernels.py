@@ -57,18 +57,23 @@ def test_repack_unpack_bit_exact(k3, rows, cols):
 
 
 def prepared_atoms_np(s):
-    """The prepared scale layout written out with numpy: per tile of 128 rows
-    and 128-wide input chunk, a 512-byte atom with row m = 32 q + r, block b at
-    byte 16 r + 4 q + b."""
-    R, nb = s.shape
-    KC = nb // 4
-    return s.reshape(R // 128, 4, 32, KC, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+    """The prepared scale layout written out with numpy: per expert, rows
+    padded to whole tiles of 128 and blocks to whole groups of 4 with zeros;
+    per (tile, 128-wide input group) a 512-byte atom with row m = 32 q + r,
+    block b at byte 16 r + 4 q + b."""
+    E, R, nb = s.shape
+    tiles, G = -(-R // 128), -(-nb // 4)
+    pad = np.zeros((E, tiles * 128, G * 4), np.uint8)
+    pad[:, :R, :nb] = s
+    return pad.reshape(E, tiles, 4, 32, G, 4).transpose(0, 1, 4, 3, 2, 5).reshape(-1)
 
 
-@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 256), (5 * 1152, 768)])
-def test_prepare_scales_bit_exact(k3, rows, cols):
-    s = synth.random_bytes(rows * 3 + cols, rows * cols // 32).reshape(rows, cols // 32)
+@pytest.mark.parametrize("E,rows,cols", [(1, 128, 128), (3, 384, 256), (5, 1152, 768), (8, 64, 64),
+                                         (2, 192, 320), (3, 64, 448)])
+def test_prepare_scales_bit_exact(k3, E, rows, cols):
+    s = synth.random_bytes(E * rows * 3 + cols, E * rows * cols // 32).reshape(E, rows, cols // 32)
     sf = k3.k3moe_prepare_scales(to_dev(s, "cuda"))
+    assert sf.numel() == k3.k3moe_prepared_scales_size(E, rows, cols)
     assert np.array_equal(sf.cpu().numpy(), prepared_atoms_np(s))
     back = k3.k3moe_unprepare_scales(sf, s.shape)
     assert np.array_equal(back.cpu().numpy(), s)

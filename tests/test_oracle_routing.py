@@ -116,3 +116,28 @@ def test_permute_invariants_random():
         rows = p["perm"][p["offsets"][e]:p["offsets"][e + 1]]
         assert np.all(flat[rows] == e)
         assert np.all(np.diff(rows // k) > 0)  # ascending tokens
+
+
+def test_bf16_to_f64_hand_bit_patterns():
+    """bf16 is the top half of an IEEE binary32: sign bit 15, 8 exponent bits
+    (bias 127), 7 mantissa bits.  Values worked out by hand from that
+    definition; a shift or mask error in the widening fails one of them."""
+    cases = {
+        0x3F80: 1.0,                     # exponent 127, mantissa 0
+        0xC000: -2.0,                    # sign, exponent 128
+        0x4049: 3.140625,                # 2 * (1 + 73/128)
+        0x3F81: 1.0 + 2.0 ** -7,         # lowest mantissa bit
+        0x0080: 2.0 ** -126,             # smallest normal
+        0x0001: 2.0 ** -133,             # smallest subnormal: 2^-126 * 2^-7
+        0x007F: 127 * 2.0 ** -133,       # largest subnormal
+        0x7F7F: (2.0 - 2.0 ** -7) * 2.0 ** 127,  # largest finite
+        0x0000: 0.0,
+    }
+    bits = np.array(list(cases), dtype=np.uint16)
+    got = oracle.bf16_to_f64(bits)
+    assert got.tolist() == list(cases.values())
+    neg0 = oracle.bf16_to_f64(np.array([0x8000], np.uint16))[0]
+    assert neg0 == 0.0 and math.copysign(1.0, neg0) == -1.0
+    inf = oracle.bf16_to_f64(np.array([0x7F80, 0xFF80], np.uint16))
+    assert inf.tolist() == [math.inf, -math.inf]
+    assert math.isnan(oracle.bf16_to_f64(np.array([0x7FC0], np.uint16))[0])
