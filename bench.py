@@ -38,14 +38,9 @@ EXPERT_MATRIX_BYTES = None  # filled per config
 
 
 # DRAM bytes (read + write) per launch of a kernel from an ncu capture of the
-# current kernel version, by (workload, kernel); absent: not captured.  The
-# decode capture (profiles/mx_stream_kernel_decode_e128.md) ran a 128-expert
-# copy of the layer: one token touches 16 experts either way, so a launch moves
-# the same bytes as in the 896-expert layer.
-TRAFFIC = {
-    ("decode_t1", "decode_up"): 187_269_376 + 3_475_968,
-    ("decode_t1", "decode_down"): 94_227_200 + 2_305_024,
-}
+# current kernel version, by (workload, weight format, scales, kernel); absent:
+# not captured since the kernel last changed.
+TRAFFIC = {}
 
 
 def parse():
@@ -66,9 +61,13 @@ def parse():
     ap.add_argument("--format", choices=["split", "ggml"], default="split",
                     help="expert weight format: compressed-tensors codes + scales, or llama.cpp "
                          "17-byte MXFP4 blocks read directly by the streaming kernels")
-    ap.add_argument("--prepared", action="store_true",
-                    help="hand the kernels the scales in the prepared atom layout instead of the "
-                         "checkpoint's canonical E8M0 rows")
+    ap.add_argument("--scales", choices=["prepared", "canonical"], default="prepared",
+                    help="hand the kernels the E8M0 scales in the prepared atom layout (written once "
+                         "at load by k3moe_prepare_scales) or as the checkpoint's canonical rows")
+    ap.add_argument("--all-configs", type=int, default=1,
+                    help="the default decode_t1 run also measures verify_t8, chunk_t512 and "
+                         "block_t8192 (key 'configs'); 0 = the headline workload only")
+    ap.add_argument("--oracle-timing", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cache-slots", type=int, default=0,
                     help="host-resident experts behind a device cache of this many experts "
                          "(k3moe_forward_cached); 0 = experts resident in HBM")
@@ -275,6 +274,223 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def dev_tensor(a, dev):
+    import torch
+
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def build_layer(k3, cfg, args, dev):
+    """The config's layer on the device: seeded expert bytes generated in place
+    (15.7 GB at the K3 shape), the scales canonical or also prepared."""
+    dense = synth.dense_inputs(cfg)
+    kw = dict(router_w=dev_tensor(dense["router_w"], dev), router_b=dev_tensor(dense["router_b"], dev),
+              k=cfg.k, path=args.path, prepared=args.scales == "prepared", **synth.experts_torch(cfg, dev))
+    if cfg.block:
+        kw.update(norm_gamma=dev_tensor(dense["norm_gamma"], dev), w_down=dev_tensor(dense["w_down"], dev),
+                  w_up=dev_tensor(dense["w_up"], dev), eps=dense["eps"])
+    layer = k3.MoELayer(**kw)
+    if args.format == "ggml":
+        import torch
+
+        layer = k3.ggml_layer(layer)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return layer, dense
+
+
+def pool_size(cfg, requested):
+    # token batches rotated over the steps: enough distinct batches for the
+    # small-T workloads (every step routes to fresh experts); the large ones
+    # are far larger than L2 each
+    return requested if cfg.T <= 8 else max(4, min(requested, 8))
+
+
+def stamp_pass(k3, layer, pool, out, ws, order, flush, stream):
+    """Device stamps of the forward replayed from graphs captured with stamps
+    on (k3moe_trace mode 2): per kernel the mean of (last CTA end - first CTA
+    start after its dependency wait), and the mean span of the whole forward."""
+    import torch
+
+    k3.k3moe_trace(2)
+    graphs = {i: k3.ForwardGraph(layer, pool[i], out, ws) for i in sorted(set(order))}
+    k3.k3moe_trace(0)
+    per, spans, names = {}, [], None
+    for i in order:
+        flush.zero_()
+        graphs[i].launch(stream)
+        st = k3.k3moe_trace_read_stamps()
+        if names is None:
+            names = [n for n, _, _ in st]
+        seen = {}
+        for n, a, b in st:
+            if a < 0:
+                continue
+            c = seen.get(n, 0)
+            seen[n] = c + 1
+            key = n if c == 0 else f"{n}#{c}"
+            per.setdefault(key, []).append((b - a) * 1e-3)
+        spans.append(max(b for _, _, b in st) * 1e-3)
+    torch.cuda.synchronize()
+    del graphs
+    mean = {n: sum(v) / len(v) for n, v in per.items()}
+    return mean, sum(spans) / len(spans)
+
+
+def algorithmic_work(cfg, u_mean, mb):
+    """Per launch: bytes of the streaming kernels (every distinct selected
+    expert's matrices once; the router's weights), flops of the tensor-core
+    GEMMs (2 m n k)."""
+    T, k, d, f = cfg.T, cfg.k, cfg.d, cfg.f
+    bytes_ = {
+        "decode_up": u_mean * 2 * mb, "decode_down": u_mean * mb,
+        "units_up": u_mean * 2 * mb, "units_down": u_mean * mb,
+        "route_small": cfg.E * cfg.d_router * 2 + T * cfg.d_router * 2 + T * cfg.E * 4,
+    }
+    flops = {
+        "expert_up": T * k * 2 * 2.0 * f * d, "expert_down": T * k * 2.0 * f * d,
+        "latent_down": 2.0 * T * cfg.D * d, "latent_up": 2.0 * T * d * cfg.D,
+        "router_logits": 2.0 * T * cfg.E * cfg.d_router,
+    }
+    return bytes_, flops
+
+
+def roofline_of(name, ms, bytes_, flops, peaks, traffic):
+    """The roofline entry of one kernel from its stamp duration."""
+    if name in bytes_:
+        peak = peaks.get("hbm_gbs", 6800.0)
+        achieved = bytes_[name] / (ms * 1e-3) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes_per_launch": bytes_[name], "avg_launch_ms": ms,
+                "duration_source": "device stamps inside the graph replay (first CTA past its "
+                                   "dependency wait to last CTA end)"}
+    if name in flops:
+        # f16 / bf16 operands, inside a step of several ms: the sustained bf16 figure
+        peak = peaks.get("bf16_tflops_sustained", 1700.0)
+        achieved = flops[name] / (ms * 1e-3) / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "peak_source": "measured bf16, sustained" if "bf16_tflops_sustained" in peaks else "fallback",
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_flops_per_launch": flops[name], "avg_launch_ms": ms,
+                "duration_source": "device stamps inside the graph replay"}
+    return None
+
+
+def measure(k3, cfg, args, dev, world, steps, warmup, peaks):
+    """One workload: its layer, a pool of token batches, one CUDA graph of
+    k3moe_forward per batch; K timed replays (events around each on the
+    launching stream, L2 flushed between steps outside the events), a second
+    pass with device stamps for the per-kernel times, and the end-to-end
+    figure through k3moe_forward_host (pinned host input and output, copies
+    inside the call).  Returns the measurement and the per-rank total ms."""
+    import torch
+    import torch.distributed as dist
+
+    layer, dense = build_layer(k3, cfg, args, dev)
+    npool = pool_size(cfg, args.pool)
+    pool_np = token_pool(cfg, npool)
+    pool = [dev_tensor(pool_np[i], dev) for i in range(npool)]
+    stage = k3.k3moe_host_staging_size(layer, cfg.T)
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T) + stage, dev)
+    ws_f = ws[: ws.numel() - stage]
+    out = torch.empty_like(pool[0])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # routing of every pool entry: experts touched per step (algorithmic bytes)
+    uniq = []
+    for i in range(npool):
+        k3.k3moe_forward(layer, pool[i], out=out, ws=ws_f)
+        idx, _, _ = k3.k3moe_forward_routing(layer, ws_f, cfg.T, with_logits=False)
+        uniq.append(len(torch.unique(idx)))
+    check_status(k3, ws_f)
+
+    graphs = [k3.ForwardGraph(layer, pool[i], out, ws_f) for i in range(npool)]
+    for i in range(max(warmup, 3)):
+        flush.zero_()
+        graphs[i % npool].launch(stream)
+    torch.cuda.synchronize()
+    order = [(warmup + i) % npool for i in range(steps)]
+
+    # ---- timed region: K steps, per-step events on the launching stream ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(dev.index or 0) as clk:
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            graphs[order[i]].launch(stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    check_status(k3, ws_f)
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    del graphs
+
+    kern, span = stamp_pass(k3, layer, pool, out, ws_f, order, flush, stream)
+
+    # ---- end to end through the host-buffer entry point ----
+    width = layer.width
+    io = cfg.T * width * 2
+    pool_host = [torch.from_numpy(pool_np[i].view(np.int16)).view(torch.bfloat16).pin_memory()
+                 for i in range(npool)]
+    out_host = torch.empty_like(pool_host[0]).pin_memory()
+    for i in range(max(warmup, 1)):
+        k3.k3moe_forward_host(layer, pool_host[i % npool], out_host=out_host, ws=ws)
+    torch.cuda.synchronize()
+    e2e_s = 0.0
+    for i in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        k3.k3moe_forward_host(layer, pool_host[order[i]], out_host=out_host, ws=ws)
+        e2e_s += time.perf_counter() - t0
+    check_status(k3, ws)
+
+    mb = matrix_bytes(cfg)
+    u_mean = sum(uniq) / len(uniq)
+    bytes_, flops = algorithmic_work(cfg, u_mean, mb)
+    dom = max(kern, key=kern.get)
+    fmt = "split" if args.format == "split" else "ggml"
+    roof = roofline_of(dom, kern[dom], bytes_, flops, peaks,
+                       TRAFFIC.get((cfg.name, fmt, args.scales, dom)))
+    mean_ms = total_ms / steps
+    res = {
+        "value": cfg.T * steps / (total_ms / 1e3), "unit": "tokens/s", "ms_per_step": mean_ms,
+        "dtype": dtype_of(cfg.T, args.path),
+        "config": dict(workload_config(cfg, npool),
+                       weight_format=("ggml 17-byte MXFP4 blocks" if args.format == "ggml" else
+                                      "codes + E8M0 scales as " +
+                                      ("prepared atoms" if args.scales == "prepared" else
+                                       "the checkpoint's canonical rows"))),
+        "experts_touched_per_step": u_mean,
+        "hbm_gbs_step": (u_mean * 3 * mb + bytes_["route_small"]) / (mean_ms * 1e-3) / 1e9,
+        "kernels_ms": kern,
+        "kernels_ms_source": "device stamps inside graph replays of the same steps",
+        "forward_span_ms": span,
+        "roofline": roof,
+        "e2e": {"value": cfg.T * steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": io,
+                "d2h_bytes_per_step": io},
+        "gpu_launches": len(kern) * steps,
+        "clocks": clk.summary(),
+    }
+    if cfg.T >= 512:
+        fl = sum(v for n, v in flops.items() if n.startswith("expert_") or cfg.block)
+        res["tflops_step"] = fl / (mean_ms * 1e-3) / 1e12
+    del layer, pool, ws, ws_f, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res, total_ms
+
+
 def ours_arm(args):
     import torch
     import torch.distributed as dist
@@ -290,207 +506,76 @@ def ours_arm(args):
     __graft_entry__.build()
     import mxfp4_routed_expert_sigmoid_gb300 as k3
 
-    cfg = bench_config(args)
-    dense = synth.dense_inputs(cfg)
-    ex = synth.experts_torch(cfg, dev)
-
-    def dv(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    kw = dict(router_w=dv(dense["router_w"]), router_b=dv(dense["router_b"]), k=cfg.k,
-              path=args.path, prepared=args.prepared, **ex)
-    if cfg.block:
-        kw.update(norm_gamma=dv(dense["norm_gamma"]), w_down=dv(dense["w_down"]),
-                  w_up=dv(dense["w_up"]), eps=dense["eps"])
-    layer = k3.MoELayer(**kw)
-    del kw, ex
-    if args.format == "ggml":
-        layer = k3.ggml_layer(layer)
-        torch.cuda.synchronize()
-        torch.cuda.empty_cache()
-    pool_np = token_pool(cfg, args.pool)
-    pool = [dv(pool_np[i]) for i in range(args.pool)]
-    ws = k3.workspace(k3.k3moe_workspace_size(layer, cfg.T) + k3.k3moe_host_staging_size(layer, cfg.T), dev)
-    ws_fwd = ws.numel() - k3.k3moe_host_staging_size(layer, cfg.T)
-    out = torch.empty_like(pool[0])
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    ws_f = ws[:ws_fwd]
-
-    def step(i):
-        k3.k3moe_forward(layer, pool[i % args.pool], out=out, ws=ws_f)
-
-    # routing of every pool entry: experts touched per step (algorithmic bytes)
-    uniq = []
-    for i in range(args.pool):
-        step(i)
-        idx, _, _ = k3.k3moe_forward_routing(layer, ws, cfg.T, with_logits=False)
-        uniq.append(len(torch.unique(idx)))
-    check_status(k3, ws)
-
-    # one CUDA graph per token batch: the forward's launches replay back to
-    # back on the device, without host launch overhead between them
-    def capture(traced):
-        # one library-made CUDA graph of k3moe_forward per token batch
-        k3.k3moe_trace(traced)
-        graphs = [k3.ForwardGraph(layer, pool[i], out, ws_f) for i in range(args.pool)]
-        torch.cuda.synchronize()
-        k3.k3moe_trace(False)
-        return graphs
-
-    graphs = capture(False)
-    for i in range(max(args.warmup, 3)):
-        graphs[i % args.pool].launch(stream)
-    torch.cuda.synchronize()
-
-    # ---- timed region: K steps, per-step events on the launching stream ----
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            evs[i][0].record(stream)
-            graphs[(args.warmup + i) % args.pool].launch(stream)
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    value = job_tokens_per_s(cfg.T, args.steps, world, total_ms)
-
-    # ---- per-kernel durations (traced pass over the same steps) ----
-    tgraphs = capture(True)
-    per_kernel = {}
-    launches_per_step = 0
-    trace_source = "graph replay"
-    for i in range(args.steps):
-        flush.zero_()
-        tgraphs[(args.warmup + i) % args.pool].launch(stream)
-        tr = k3.k3moe_trace_read()
-        launches_per_step = max(launches_per_step, len(tr))
-        for name, ms in tr:
-            per_kernel.setdefault(name, []).append(ms)
-    if not per_kernel:  # events of the graph not readable: trace direct launches
-        trace_source = "direct launches (host launch gaps included)"
-        k3.k3moe_trace(True)
-        for i in range(args.steps):
-            flush.zero_()
-            step(args.warmup + i)
-            tr = k3.k3moe_trace_read()
-            launches_per_step = max(launches_per_step, len(tr))
-            for name, ms in tr:
-                per_kernel.setdefault(name, []).append(ms)
-        k3.k3moe_trace(False)
-    torch.cuda.synchronize()
-    kern_mean = {n: sum(v) / len(v) for n, v in per_kernel.items()}
-    del graphs, tgraphs
-
-    # ---- end to end through the host-buffer entry point ----
-    width = layer.width
-    h2d = cfg.T * width * 2
-    pool_host = [torch.from_numpy(pool_np[i].view(np.int16)).view(torch.bfloat16).pin_memory()
-                 for i in range(args.pool)]
-    out_host = torch.empty_like(pool_host[0]).pin_memory()
-    for i in range(args.warmup):
-        k3.k3moe_forward_host(layer, pool_host[i % args.pool], out_host=out_host, ws=ws)
-    torch.cuda.synchronize()
-    e2e_s = 0.0
-    for i in range(args.steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        k3.k3moe_forward_host(layer, pool_host[(args.warmup + i) % args.pool], out_host=out_host,
-                              ws=ws)
-        e2e_s += time.perf_counter() - t0
-    e2e_value = cfg.T * args.steps / e2e_s
-
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
-
-    # ---- roofline of the dominant kernel ----
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
             peaks = json.load(fh)
     except OSError:
         pass
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    mb = matrix_bytes(cfg)
-    u_mean = sum(uniq) / len(uniq)
-    # algorithmic bytes per launch of the streaming kernels: every distinct
-    # selected expert's matrices once (units of the same expert re-read them)
-    algo = {
-        "decode_up": u_mean * 2 * mb,
-        "decode_down": u_mean * mb,
-        "units_up": u_mean * 2 * mb,
-        "units_down": u_mean * mb,
-        "route_small": cfg.E * cfg.d_router * 2 + cfg.T * cfg.d_router * 2 + cfg.T * cfg.E * 4,
-    }
-    # algorithmic flops of the grouped GEMMs: 2 f d per (token, expert) and matrix
-    flops = {
-        "expert_up": cfg.T * cfg.k * 2 * 2.0 * cfg.f * cfg.d,
-        "expert_down": cfg.T * cfg.k * 2.0 * cfg.f * cfg.d,
-    }
-    dom = max(kern_mean, key=kern_mean.get)
-    roof = None
-    if dom in algo:
-        achieved = algo[dom] / (kern_mean[dom] * 1e-3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": TRAFFIC.get((cfg.name, dom)) if args.format == "split" else None,
-                "algorithmic_bytes_per_launch": algo[dom],
-                "avg_launch_ms": kern_mean[dom]}
-    elif dom in flops:
-        # f16 operands: the measured bf16 rate (same tensor-core rate); the kernel
-        # runs inside a step of several ms, so the sustained figure
-        tf_peak = peaks.get("bf16_tflops_sustained", 1700.0)
-        achieved = flops[dom] / (kern_mean[dom] * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tf_peak,
-                "peak_source": ("measured bf16, sustained" if "bf16_tflops_sustained" in peaks else "fallback"),
-                "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": TRAFFIC.get((cfg.name, dom)),
-                "algorithmic_flops_per_launch": flops[dom], "avg_launch_ms": kern_mean[dom]}
-    step_bytes = u_mean * 3 * mb + algo["route_small"]
-    mean_ms = total_ms / args.steps
+
+    cfg = bench_config(args)
+    res, total_ms = measure(k3, cfg, args, dev, world, args.steps, args.warmup, peaks)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    value = job_tokens_per_s(cfg.T, args.steps, world, total_ms)
+
+    # the other workloads of the layer, measured in the same run (headline run only)
+    others = {}
+    if args.all_configs and not (args.E or args.T or args.config != "decode_t1"):
+        for name in ("verify_t8", "chunk_t512", "block_t8192"):
+            o, o_ms = measure(k3, synth.CONFIGS[name], args, dev, world, args.steps, args.warmup, peaks)
+            o_ms = max_over_ranks(o_ms, world, dev)
+            o["value"] = job_tokens_per_s(synth.CONFIGS[name].T, args.steps, world, o_ms)
+            others[name] = o
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": dtype_of(cfg.T, args.path),
+        "dtype": res["dtype"],
         "data": "synthetic (seeded; random-init weights of the K3 layer shapes)",
-        "config": dict(workload_config(cfg, args.pool),
-                       weight_format=("ggml 17-byte MXFP4 blocks" if args.format == "ggml" else
-                                      "codes + E8M0 scales, " +
-                                      ("prepared atoms" if args.prepared else "canonical rows"))),
-        "hbm_gbs_step": step_bytes / (mean_ms * 1e-3) / 1e9,
-        "experts_touched_per_step": u_mean,
-        "kernels_ms": kern_mean,
-        "kernels_ms_source": trace_source,
-        "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": h2d},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
     }
+    line.update({k: v for k, v in res.items() if k not in ("value", "ms_per_step", "unit", "dtype")})
+    line["gpu_launches"] = res["gpu_launches"]
+    if others:
+        line["configs"] = others
     if not args.no_cpu_baseline and world == 1:
         k_steps = 2 if cfg.name != "tiny" else 5
-        nt, times = time_oracle(cfg, pool_np, k_steps, 0, dense)
+        dense = synth.dense_inputs(cfg)
+        nt, times = time_oracle(cfg, token_pool(cfg, k_steps), k_steps, 0, dense)
+        one = oracle_one_thread(cfg.name, k_steps)
         line["cpu_baseline"] = {"value": nt * len(times) / sum(times), "unit": "tokens/s",
                                 "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{k_steps} steps of {nt} token(s) of the workload "
-                                          "(NumPy fp64 oracle, expert bytes prefetched)"}
+                                          "(NumPy fp64 oracle, expert bytes prefetched; BLAS "
+                                          "threads = cores)",
+                                "one_thread": one}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def oracle_one_thread(config: str, steps: int):
+    """The same oracle timing in a child process whose BLAS and OpenMP pools
+    have one thread (value in tokens/s), or None if the child fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-timing", "--config", config,
+                            "--steps", str(steps)], env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])["value"]
+    except Exception:
+        return None
+
+
+def oracle_timing_only(args):
+    cfg = bench_config(args)
+    dense = synth.dense_inputs(cfg)
+    nt, times = time_oracle(cfg, token_pool(cfg, args.steps), args.steps, 0, dense)
+    print(json.dumps({"value": nt * len(times) / sum(times), "unit": "tokens/s"}), flush=True)
 
 
 def cached_arm(args):
@@ -516,7 +601,7 @@ def cached_arm(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     layer = k3.MoELayer(router_w=dv(dense["router_w"]), router_b=dv(dense["router_b"]), k=cfg.k,
-                        path=args.path, prepared=args.prepared, **synth.experts_torch(cfg, dev))
+                        path=args.path, prepared=args.scales == "prepared", **synth.experts_torch(cfg, dev))
     hlayer = k3.host_resident(layer)
     del layer
     torch.cuda.empty_cache()
@@ -655,7 +740,9 @@ def dtype_of(T: int, path: int) -> str:
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.oracle_timing:
+        oracle_timing_only(args)
+    elif args.impl == "reference":
         reference_arm(args)
     elif args.cache_slots > 0:
         cached_arm(args)

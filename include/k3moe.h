@@ -58,7 +58,7 @@ typedef enum k3moe_status {
     K3MOE_ERR_ALIGN = 3,        /* a base pointer is not 16-byte aligned */
     K3MOE_ERR_WORKSPACE = 4,    /* workspace smaller than required */
     K3MOE_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, copy, ...) */
-    K3MOE_ERR_NONFINITE = 6,    /* device: a router logit was NaN or inf */
+    K3MOE_ERR_NONFINITE = 6,    /* device: a router logit was NaN or inf, or a bias was NaN */
     K3MOE_ERR_TIMEOUT = 7,      /* device: a bounded wait inside a kernel expired */
     K3MOE_ERR_UNSUPPORTED = 8   /* activation or path not available for the shape */
 } k3moe_status;
@@ -175,6 +175,21 @@ typedef struct k3moe_layer_desc {
 
 /* Library ABI version (K3MOE_ABI_VERSION of the build). */
 int k3moe_abi_version(void);
+
+/* Testing aid for the device-side failure path; the paper has no
+ * counterpart.  k3moe_inject_fault(K3MOE_FAULT_DROP_SIGNAL) arms a fault for
+ * the next k3moe_forward (eager, or the set-up forward of a graph creation)
+ * issued by the calling host thread on the BLOCK_SCALED path: in the W1/W3
+ * streaming kernel, the first CTA's producer never signals its first pipeline
+ * stage, and every bounded wait of that launch gives up after 1 ms instead of
+ * 2 s.  The MMA issuer waiting for that stage records K3MOE_ERR_TIMEOUT in the
+ * workspace status word; the CTA's roles stop, its copies in flight land, its
+ * tensor memory is released and the kernel returns; the rest of the forward
+ * runs to its end and its output is unspecified.  No wait is left unbounded
+ * and nothing faults.  0 disarms.  Returns the previously armed code.  The
+ * next forward consumes the armed code whatever its path. */
+#define K3MOE_FAULT_DROP_SIGNAL 1
+int k3moe_inject_fault(int code);
 
 /* Static description of a status code (never NULL). */
 const char* k3moe_status_string(int status);
@@ -446,16 +461,30 @@ k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws,
  * Returns CUDA if the stream reported an error. */
 k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status);
 
-/* Kernel tracing.  While enabled (enable != 0), k3moe_forward records a CUDA
- * event on its stream after each kernel it launches (a forward captured into
- * a CUDA graph captures the event records too, and each replay re-records
- * them).  k3moe_trace_read waits for the last event and fills up to `max`
- * entries with the kernel names (static strings) and the milliseconds between
- * consecutive events of the most recently traced forward; it returns the
- * number of entries, or 0 if the events cannot be read.  Tracing is process-wide and meant for one host thread;
- * it is off by default.  k3moe_trace returns the previous setting. */
-int k3moe_trace(int enable);
+/* Kernel tracing, off by default, process-wide and meant for one host thread.
+ * k3moe_trace(mode) returns the previous mode; mode is a bit set:
+ *   bit 0 (1): k3moe_forward records a CUDA event on its stream after each
+ *     kernel it launches (a forward captured into a CUDA graph captures the
+ *     records as external-event nodes, and each replay re-records them).
+ *     k3moe_trace_read waits for the last event and fills up to `max` entries
+ *     with the kernel names (static strings) and the milliseconds between
+ *     consecutive events of the most recently traced forward, and returns the
+ *     number of entries (0 if the events cannot be read).  The records sit
+ *     between the kernels, so they also stop the next kernel from starting
+ *     early (programmatic launch) and each interval carries launch latency.
+ *   bit 1 (2): device stamps.  Each kernel of the forward records, in a
+ *     1.5 KB area of the caller's workspace, the global timer when its first
+ *     CTA passes its dependency wait and when its last CTA finishes (the
+ *     area is reset at the start of every forward, graph replays included).
+ *     Nothing is inserted between the kernels, so the timeline is that of the
+ *     untraced forward.  k3moe_trace_read_stamps synchronises the device,
+ *     reads the stamps of the most recently stamped forward (its workspace
+ *     must still exist) and fills up to `max` entries with the kernel names
+ *     and the start and end in microseconds after the earliest start (-1 for
+ *     a kernel that did not run); it returns the number of entries. */
+int k3moe_trace(int mode);
 int k3moe_trace_read(int max, const char** names, float* ms);
+int k3moe_trace_read_stamps(int max, const char** names, double* start_us, double* end_us);
 
 #ifdef __cplusplus
 }

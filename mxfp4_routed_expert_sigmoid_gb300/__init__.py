@@ -35,13 +35,15 @@ STATUS = {
 
 #: every symbol the C header declares (checked by the CPU test suite)
 EXPORTS = (
-    "k3moe_abi_version", "k3moe_status_string", "k3moe_repack_mxfp4", "k3moe_unpack_mxfp4",
+    "k3moe_abi_version", "k3moe_inject_fault", "k3moe_status_string", "k3moe_repack_mxfp4",
+    "k3moe_unpack_mxfp4",
     "k3moe_route_workspace_size", "k3moe_route", "k3moe_route_noalloc", "k3moe_permute",
     "k3moe_rmsnorm",
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
-    "k3moe_trace_read", "k3moe_prepared_scales_size", "k3moe_prepare_scales",
+    "k3moe_trace_read", "k3moe_trace_read_stamps", "k3moe_prepared_scales_size",
+    "k3moe_prepare_scales",
     "k3moe_unprepare_scales",
     "k3moe_cache_state_size", "k3moe_cache_init", "k3moe_forward_cached",
     "k3moe_cache_read_stats", "k3moe_graph_create_cached",
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
     f32 = ctypes.c_float
     sigs = {
         "k3moe_abi_version": ([], ctypes.c_int),
+        "k3moe_inject_fault": ([ctypes.c_int], ctypes.c_int),
         "k3moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "k3moe_repack_mxfp4": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "k3moe_unpack_mxfp4": ([vp, i64, i64, vp, vp, vp], ctypes.c_int),
@@ -126,6 +129,9 @@ def lib() -> ctypes.CDLL:
         "k3moe_graph_destroy": ([vp], ctypes.c_int),
         "k3moe_trace_read": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                               ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+        "k3moe_trace_read_stamps": ([ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+                                    ctypes.c_int),
         "k3moe_prepared_scales_size": ([i64, i64, i64], sz),
         "k3moe_prepare_scales": ([vp, i64, i64, i64, vp, vp], ctypes.c_int),
         "k3moe_cache_state_size": ([i32, i32], sz),
@@ -190,6 +196,16 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
 # ---------------------------------------------------------------------------
 def k3moe_abi_version() -> int:
     return lib().k3moe_abi_version()
+
+
+FAULT_DROP_SIGNAL = 1
+
+
+def k3moe_inject_fault(code: int) -> int:
+    """Testing aid: arm a device-side fault for the next k3moe_forward of this
+    thread (FAULT_DROP_SIGNAL: a pipeline stage is never signalled and the
+    bounded wait for it runs out after 1 ms); 0 disarms."""
+    return int(lib().k3moe_inject_fault(int(code)))
 
 
 def k3moe_repack_mxfp4(packed: torch.Tensor, scale: torch.Tensor, out=None, stream=None):
@@ -407,17 +423,29 @@ def k3moe_get_status(ws, stream=None) -> int:
     return st.value
 
 
-def k3moe_trace(enable: bool) -> bool:
-    """Turn per-kernel event tracing of k3moe_forward on or off; returns the old setting."""
-    return bool(lib().k3moe_trace(1 if enable else 0))
+def k3moe_trace(mode) -> int:
+    """Set kernel tracing of k3moe_forward: 0 off, 1 events between launches,
+    2 device stamps (start / end of each kernel inside the forward), 3 both.
+    True / False are 1 / 0.  Returns the previous mode."""
+    return int(lib().k3moe_trace(int(mode)))
 
 
 def k3moe_trace_read(max_entries: int = 32):
-    """[(kernel name, ms)] of the most recent traced forward (waits for its events)."""
+    """[(kernel name, ms)] of the most recent event-traced forward (waits for its events)."""
     names = (ctypes.c_char_p * max_entries)()
     ms = (ctypes.c_float * max_entries)()
     n = lib().k3moe_trace_read(max_entries, names, ms)
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+def k3moe_trace_read_stamps(max_entries: int = 48):
+    """[(kernel name, start us, end us)] of the most recent stamped forward
+    (device times after the earliest start; synchronises the device)."""
+    names = (ctypes.c_char_p * max_entries)()
+    st = (ctypes.c_double * max_entries)()
+    en = (ctypes.c_double * max_entries)()
+    n = lib().k3moe_trace_read_stamps(max_entries, names, st, en)
+    return [(names[i].decode(), float(st[i]), float(en[i])) for i in range(n)]
 
 
 def expert_arrays(layer: MoELayer):

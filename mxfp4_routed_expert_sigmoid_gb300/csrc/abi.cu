@@ -51,6 +51,9 @@ k3moe_status cuda_status(cudaError_t e) {
     return K3MOE_ERR_CUDA;
 }
 
+// fault armed by k3moe_inject_fault for the next forward of this host thread
+thread_local int g_inject = 0;
+
 // PDL is on unless K3MOE_NO_PDL is set in the environment (read once)
 bool pdl_on() {
     static const bool on = [] {
@@ -97,6 +100,7 @@ ScaleSource scale_source(const k3moe_layer_desc* d) {
 }
 
 struct FwdPlan {
+    size_t stamps;                                  // device timeline (k3moe_trace mode 2)
     size_t sf1, sf3, sf2;                           // atoms written per call (SCALES_CANON_PREP)
     size_t logits, idx, wts, counts, offsets, active, perm, inv, chunk;
     size_t dec, y;                                  // decode scratch, shared y (fp32)
@@ -111,6 +115,7 @@ FwdPlan fwd_plan(const k3moe_layer_desc* d, int T) {
     Carve c;
     FwdPlan p{};
     const size_t P = static_cast<size_t>(T) * d->k;
+    p.stamps = c.take(2 * kStampSlots * sizeof(uint64_t));
     if (d->format == K3MOE_FORMAT_SPLIT && scale_source(d) == SCALES_CANON_PREP) {
         p.sf1 = c.take(prepared_sf_bytes(d->E, d->f, d->d));
         p.sf3 = c.take(prepared_sf_bytes(d->E, d->f, d->d));
@@ -192,17 +197,24 @@ k3moe_status check_desc(const k3moe_layer_desc* d) {
 }
 
 // ---------------------------------------------------------------------------
-// tracing: events between the kernel launches of one forward
+// tracing: events between the kernel launches of one forward (mode bit 0),
+// device stamps of each launch's first CTA start and last CTA end (bit 1)
 // ---------------------------------------------------------------------------
 struct Trace {
     std::mutex mu;
-    bool on = false;
+    int mode = 0;
     int n = 0;
     cudaEvent_t ev[33] = {};
     const char* names[32] = {};
     int n_last = 0;
     float ms_last[32] = {};
     const char* names_last[32] = {};
+    uint64_t* stamp_base = nullptr;        // stamp area of the forward being issued
+    int ns = 0;
+    const char* snames[kStampSlots] = {};
+    const uint64_t* stamp_last = nullptr;  // stamp area of the last stamped forward
+    int ns_last = 0;
+    const char* snames_last[kStampSlots] = {};
 };
 Trace g_trace;
 
@@ -217,20 +229,37 @@ void trace_record(cudaEvent_t ev, cudaStream_t s) {
         cudaEventRecord(ev, s);
 }
 
-void trace_begin(cudaStream_t s) {
-    if (!g_trace.on) return;
-    g_trace.n = 0;
-    if (!g_trace.ev[0])
-        for (auto& e : g_trace.ev) cudaEventCreate(&e);
-    trace_record(g_trace.ev[0], s);
+void trace_begin(cudaStream_t s, uint64_t* stamps) {
+    g_trace.stamp_base = nullptr;
+    if (g_trace.mode & 1) {
+        g_trace.n = 0;
+        if (!g_trace.ev[0])
+            for (auto& e : g_trace.ev) cudaEventCreate(&e);
+        trace_record(g_trace.ev[0], s);
+    }
+    if ((g_trace.mode & 2) && stamps) {
+        // starts at the largest value (atomicMin), ends at 0 (atomicMax); in a
+        // captured forward these are memset nodes, so every replay starts clean
+        cudaMemsetAsync(stamps, 0xFF, kStampSlots * sizeof(uint64_t), s);
+        cudaMemsetAsync(stamps + kStampSlots, 0, kStampSlots * sizeof(uint64_t), s);
+        g_trace.stamp_base = stamps;
+        g_trace.ns = 0;
+    }
 }
 
 void trace_end() {
-    if (!g_trace.on) return;
     // the events are read in k3moe_trace_read (they may also be replayed by a
     // CUDA graph that captured this forward); remember the names now
-    for (int i = 0; i < g_trace.n; ++i) g_trace.names_last[i] = g_trace.names[i];
-    g_trace.n_last = g_trace.n;
+    if (g_trace.mode & 1) {
+        for (int i = 0; i < g_trace.n; ++i) g_trace.names_last[i] = g_trace.names[i];
+        g_trace.n_last = g_trace.n;
+    }
+    if (g_trace.stamp_base) {
+        for (int i = 0; i < g_trace.ns; ++i) g_trace.snames_last[i] = g_trace.snames[i];
+        g_trace.ns_last = g_trace.ns;
+        g_trace.stamp_last = g_trace.stamp_base;
+        g_trace.stamp_base = nullptr;
+    }
 }
 
 }  // namespace
@@ -239,10 +268,16 @@ namespace k3 {
 bool pdl_enabled() { return pdl_on(); }
 
 void trace_mark(const char* name, cudaStream_t s) {
-    if (!g_trace.on || g_trace.n >= 32) return;
+    if (!(g_trace.mode & 1) || g_trace.n >= 32) return;
     g_trace.names[g_trace.n] = name;
     trace_record(g_trace.ev[g_trace.n + 1], s);
     ++g_trace.n;
+}
+
+uint64_t* trace_stamp(const char* name) {
+    if (!g_trace.stamp_base || g_trace.ns >= kStampSlots) return nullptr;
+    g_trace.snames[g_trace.ns] = name;
+    return g_trace.stamp_base + g_trace.ns++;
 }
 }  // namespace k3
 
@@ -250,8 +285,8 @@ extern "C" {
 
 int k3moe_trace(int enable) {
     std::lock_guard<std::mutex> lock(g_trace.mu);
-    const int prev = g_trace.on ? 1 : 0;
-    g_trace.on = enable != 0;
+    const int prev = g_trace.mode;
+    g_trace.mode = enable & 3;
     return prev;
 }
 
@@ -280,7 +315,34 @@ int k3moe_trace_read(int max, const char** names, float* ms) {
     return n;
 }
 
+int k3moe_trace_read_stamps(int max, const char** names, double* start_us, double* end_us) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    const int n = g_trace.ns_last < max ? g_trace.ns_last : max;
+    if (n <= 0 || !g_trace.stamp_last) return 0;
+    uint64_t st[2 * kStampSlots];
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(st, g_trace.stamp_last, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    uint64_t t0 = ~0ull;
+    for (int i = 0; i < n; ++i) t0 = st[i] < t0 ? st[i] : t0;
+    for (int i = 0; i < n; ++i) {
+        const bool ran = st[i] != ~0ull && st[kStampSlots + i] >= st[i];
+        if (names) names[i] = g_trace.snames_last[i];
+        if (start_us) start_us[i] = ran ? (st[i] - t0) * 1e-3 : -1.0;
+        if (end_us) end_us[i] = ran ? (st[kStampSlots + i] - t0) * 1e-3 : -1.0;
+    }
+    return n;
+}
+
 int k3moe_abi_version(void) { return K3MOE_ABI_VERSION; }
+
+int k3moe_inject_fault(int code) {
+    const int prev = g_inject;
+    g_inject = code == K3MOE_FAULT_DROP_SIGNAL ? code : 0;
+    return prev;
+}
 
 const char* k3moe_status_string(int status) {
     switch (status) {
@@ -373,7 +435,7 @@ k3moe_status k3moe_route(const uint16_t* x, int32_t T, int32_t d_r, const uint16
     if (T <= kDecodeMaxT) return cuda_status(launch_route_small(a, s));
     cudaError_t e = cudaSuccess;
     if (T >= 64 && E % 128 == 0) {
-        e = launch_gemm_bf16(x, router_w, T, E, d_r, a.logits, 1, a.hdr, device_sms(), s);
+        e = launch_gemm_bf16(x, router_w, T, E, d_r, a.logits, 1, a.hdr, device_sms(), s, "router_logits");
         if (e == cudaErrorNotSupported) e = launch_logits_simt(a, s);
     } else {
         e = launch_logits_simt(a, s);
@@ -529,10 +591,12 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     WsHeader* hdr = reinterpret_cast<WsHeader*>(base);
     const int sms = device_sms();
     std::lock_guard<std::mutex> trace_lock(g_trace.mu);
-    trace_begin(s);
+    trace_begin(s, reinterpret_cast<uint64_t*>(base + p.stamps));
     struct TraceEnd { ~TraceEnd() { trace_end(); } } trace_end_guard;
     auto at = [&](size_t off) { return static_cast<void*>(base + off); };
     cudaError_t e = cudaSuccess;
+    const int inject = g_inject;  // armed for this forward only
+    g_inject = 0;
     const ScaleSource ss = desc->format == K3MOE_FORMAT_GGML ? SCALES_PREPARED : scale_source(desc);
     if (ss == SCALES_CANON_PREP) {
         // widths that are not whole 512-input stages: the canonical rows are
@@ -550,7 +614,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         uint16_t* hn = static_cast<uint16_t*>(at(p.hn));
         uint16_t* z = static_cast<uint16_t*>(at(p.z));
         if ((e = launch_rmsnorm(hidden, T, desc->D, desc->norm_gamma, desc->eps, hn, s))) return K3MOE_ERR_CUDA;
-        e = launch_gemm_bf16(hn, desc->w_down, T, desc->d, desc->D, z, 0, hdr, sms, s);
+        e = launch_gemm_bf16(hn, desc->w_down, T, desc->d, desc->D, z, 0, hdr, sms, s, "latent_down");
         if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
         if (e) return K3MOE_ERR_CUDA;
         x_router = hn;
@@ -584,7 +648,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     } else {
         if (T >= 64 && desc->E % 128 == 0) {
             e = launch_gemm_bf16(x_router, desc->router_w, T, desc->E, desc->d_router, r.logits, 1,
-                                 hdr, sms, s);
+                                 hdr, sms, s, "router_logits");
             if (e == cudaErrorNotSupported) e = launch_logits_simt(r, s);
         } else {
             e = launch_logits_simt(r, s);
@@ -629,7 +693,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         a.x = x_expert; a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.counts = counts; a.offsets = offsets; a.perm = perm; a.inv = inv; a.idx = r.idx; a.wts = r.wts;
         a.scratch = at(p.units);
-        a.out = latent_out; a.hdr = hdr; a.num_sms = sms;
+        a.out = latent_out; a.hdr = hdr; a.num_sms = sms; a.inject = inject;
         e = launch_mx_units(a, s);
         if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
         if (e) return cuda_status(e);
@@ -643,7 +707,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         a.T = T; a.E = desc->E; a.k = desc->k; a.d = desc->d; a.f = desc->f;
         a.active = active; a.idx = r.idx; a.wts = r.wts;
         a.scratch = at(p.dec);
-        a.out = latent_out; a.hdr = hdr; a.num_sms = sms;
+        a.out = latent_out; a.hdr = hdr; a.num_sms = sms; a.inject = inject;
         e = launch_mx_decode(a, s);
         if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
         if (e) return cuda_status(e);
@@ -669,7 +733,7 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     }
 
     if (desc->D > 0) {
-        e = launch_gemm_bf16(latent_out, desc->w_up, T, desc->D, desc->d, out, 0, hdr, sms, s);
+        e = launch_gemm_bf16(latent_out, desc->w_up, T, desc->D, desc->d, out, 0, hdr, sms, s, "latent_up");
         if (e == cudaErrorNotSupported) return K3MOE_ERR_UNSUPPORTED;
         if (e) return K3MOE_ERR_CUDA;
     }

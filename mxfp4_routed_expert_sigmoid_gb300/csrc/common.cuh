@@ -42,6 +42,24 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded waits give up after this long and record K3MOE_ERR_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Device-side kernel timeline (k3moe_trace mode 2).  A stamp area in the
+// forward's workspace holds kStampSlots start words then kStampSlots end words;
+// the launch that owns slot i records the earliest globaltimer over its CTAs
+// at start[i] and the latest at end[i].  A null slot pointer turns it off.
+constexpr int kStampSlots = 48;
+__device__ __forceinline__ void stamp_start(uint64_t* st) {
+    if (st && threadIdx.x == 0) atomicMin(reinterpret_cast<unsigned long long*>(st), global_ns());
+}
+__device__ __forceinline__ void stamp_end(uint64_t* st) {
+    if (st && threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned long long*>(st + kStampSlots), global_ns());
+}
+// start on construction, end when the scope (and so the CTA's thread 0) exits
+struct StampScope {
+    uint64_t* st;
+    __device__ explicit StampScope(uint64_t* s) : st(s) { stamp_start(st); }
+    __device__ ~StampScope() { stamp_end(st); }
+};
+
 // ---------------------------------------------------------------------------
 // small numeric helpers
 // ---------------------------------------------------------------------------
@@ -293,8 +311,11 @@ __device__ __forceinline__ void store_terms(const uint32_t (&q)[kTerms], const u
 // ---------------------------------------------------------------------------
 namespace k3 {
 
-// Tracing hook: records an event after a launch when tracing is on (abi.cu).
+// Tracing hooks (abi.cu): trace_mark records an event after a launch when
+// event tracing is on; trace_stamp, called before a launch, returns the
+// launch's stamp slot when device stamps are on inside a forward (else null).
 void trace_mark(const char* name, cudaStream_t s);
+uint64_t* trace_stamp(const char* name);
 
 // Kernel launch with programmatic stream serialisation (see pdl_wait).
 bool pdl_enabled();
@@ -333,6 +354,8 @@ struct RouteArgs {
     uint8_t* xq;
     uint8_t* xsf;
     int xq_n;          // MMA N: rows per stage (>= kTerms * T)
+    uint64_t* st_a;    // stamp slots: logits kernel, top-k kernel (null: off)
+    uint64_t* st_b;
 };
 
 cudaError_t launch_repack(const uint8_t* packed, const uint8_t* scale, int64_t nblocks,
@@ -383,6 +406,7 @@ struct MxDecodeArgs {
     uint16_t* out;            // [T, d] bf16
     WsHeader* hdr;
     int num_sms;
+    int inject;               // test aid (k3moe_inject_fault) for the up pass
 };
 size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f);
 // where the decode scratch keeps the quantised token rows (router output)
@@ -411,6 +435,7 @@ struct MxUnitsArgs {
     uint16_t* out;            // [T, d] bf16
     WsHeader* hdr;
     int num_sms;
+    int inject;               // test aid (k3moe_inject_fault) for the up pass
 };
 size_t mx_units_scratch_bytes(int T, int E, int k, int d, int f);
 cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s);
@@ -490,6 +515,7 @@ cudaError_t launch_grouped(const GroupedArgs& a, cudaStream_t s);
 
 // dense bf16 GEMM (tcgen05): out[t, n] = sum_c x[t, c] w[n, c]
 cudaError_t launch_gemm_bf16(const uint16_t* x, const uint16_t* w, int T, int N, int K, void* out,
-                             int out_fp32, WsHeader* hdr, int num_sms, cudaStream_t s);
+                             int out_fp32, WsHeader* hdr, int num_sms, cudaStream_t s,
+                             const char* name = "gemm_bf16");
 
 }  // namespace k3

@@ -73,6 +73,7 @@ struct DenseParams {
     int out_fp32;
     int n_out;
     WsHeader* hdr;
+    uint64_t* st;  // stamp slot (null: off)
 };
 
 constexpr int kDenseBN = 256, kDenseStages = 4, kDenseThreads = 256, kDenseTmemCols = 512;
@@ -137,6 +138,7 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = p.n_tiles * p.m_tiles;
+    stamp_start(p.st);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -253,6 +255,7 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     tc_fence_before();
     __syncthreads();
+    stamp_end(p.st);
     if (warp == 2) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -306,6 +309,7 @@ struct ExpParams {
     uint32_t* h_amax;     // UP: max |h| per row (fp32 bits)
     float* y;             // DOWN: [P, d]
     WsHeader* hdr;
+    uint64_t* st;         // stamp slot (null: off)
 };
 
 template <int NA>
@@ -353,6 +357,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = p.tiles[0].x;
     const int k_stages = p.K / BK;
+    stamp_start(p.st);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -657,6 +662,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     tc_fence_before();
     __syncthreads();
+    stamp_end(p.st);
     if (warp == 2) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -672,7 +678,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int P, int k,
                    int d, uint16_t* __restrict__ xp, int32_t* __restrict__ xexp,
-                   uint32_t* __restrict__ h_amax) {
+                   uint32_t* __restrict__ h_amax, uint64_t* st) {
+    StampScope stamp(st);
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= P) return;
@@ -711,7 +718,8 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ p
 // hp[r] = f16(hf[r] * 2^-ex), ex = floor(log2(h_amax[r])); one warp per row
 __global__ void __launch_bounds__(256)
 convert_h_kernel(const float* __restrict__ hf, const uint32_t* __restrict__ h_amax, int P, int f,
-                 uint16_t* __restrict__ hp, int32_t* __restrict__ hexp) {
+                 uint16_t* __restrict__ hp, int32_t* __restrict__ hexp, uint64_t* st) {
+    StampScope stamp(st);
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= P) return;
@@ -740,7 +748,8 @@ convert_h_kernel(const float* __restrict__ hf, const uint32_t* __restrict__ h_am
 // (expert, first row, rows, m tile).
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
-                   int bn_up, int bn_dn, int m_up, int m_dn, int4* up, int4* dn, int cap) {
+                   int bn_up, int bn_dn, int m_up, int m_dn, int4* up, int4* dn, int cap, uint64_t* st) {
+    StampScope stamp(st);
     __shared__ int base[1024 + 1];
     for (int pass = 0; pass < 2; ++pass) {
         const int bn = pass == 0 ? bn_up : bn_dn;
@@ -782,7 +791,7 @@ build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
 // host side
 // ---------------------------------------------------------------------------
 cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const DenseParams& p,
-                         int grid, cudaStream_t s) {
+                         int grid, cudaStream_t s, const char* name) {
     constexpr size_t smem = dense_smem_bytes();
     static_assert(smem <= 232448, "shared memory budget");
     // the attribute is per device; set it once per device (not inside graph captures)
@@ -796,8 +805,10 @@ cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const Dense
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
-    tc_dense_kernel<<<grid, kDenseThreads, smem, s>>>(a, b, p);
-    trace_mark("gemm_bf16", s);
+    DenseParams q = p;
+    q.st = trace_stamp(name);
+    tc_dense_kernel<<<grid, kDenseThreads, smem, s>>>(a, b, q);
+    trace_mark(name, s);
     return cudaGetLastError();
 }
 
@@ -821,7 +832,9 @@ cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
-    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, p);
+    ExpParams q = p;
+    q.st = trace_stamp(name);
+    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, q);
     trace_mark(name, s);
     return cudaGetLastError();
 }
@@ -842,7 +855,7 @@ size_t grouped_tile_cap(int T, int E, int k, int d, int f) {
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t* x, const uint16_t* w, int T, int N, int K, void* out,
-                             int out_fp32, WsHeader* hdr, int num_sms, cudaStream_t s) {
+                             int out_fp32, WsHeader* hdr, int num_sms, cudaStream_t s, const char* name) {
     if (N % BM || K % BK || T < 1) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, BK, BM,
@@ -862,7 +875,7 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const uint16_t* w, int T, int N,
     p.hdr = hdr;
     const int tiles = p.n_tiles * p.m_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    return launch_dense(ta, tb, p, grid, s);
+    return launch_dense(ta, tb, p, grid, s, name);
 }
 
 cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
@@ -871,10 +884,11 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     int4* tiles_up = reinterpret_cast<int4*>(g.tiles);
     int4* tiles_dn = tiles_up + (cap + 1);
     cudaError_t e;
-    gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.x, g.perm, P, g.k, g.d, g.xp, g.xp_exp, g.h_amax);
+    gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.x, g.perm, P, g.k, g.d, g.xp, g.xp_exp, g.h_amax,
+                                                   trace_stamp("gather_rows"));
     trace_mark("gather_rows", s);
     build_tiles_kernel<<<1, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUpRows, kDownRows, (g.f + BM - 1) / BM,
-                                          (g.d + BM - 1) / BM, tiles_up, tiles_dn, cap);
+                                          (g.d + BM - 1) / BM, tiles_up, tiles_dn, cap, trace_stamp("build_tiles"));
     trace_mark("build_tiles", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -904,7 +918,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     p.hdr = g.hdr;
     if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
-    convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp);
+    convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp, trace_stamp("convert_h"));
     trace_mark("convert_h", s);
 
     // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16 in 16-row boxes

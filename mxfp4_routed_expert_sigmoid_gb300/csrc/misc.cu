@@ -18,7 +18,8 @@ constexpr int kNormThreads = 256;
 
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(const uint16_t* __restrict__ h, int D, const uint16_t* __restrict__ gamma,
-               float eps, uint16_t* __restrict__ out) {
+               float eps, uint16_t* __restrict__ out, uint64_t* st) {
+    StampScope stamp(st);
     __shared__ float part[kNormThreads / 32];
     __shared__ float inv_rms_s;
     const size_t row = blockIdx.x;
@@ -70,11 +71,12 @@ constexpr int kCombineThreads = 128;
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ y, int nslots, size_t slot_stride,
                const float* __restrict__ wts, const int32_t* __restrict__ inv, int k, int d,
-               uint16_t* __restrict__ out) {
+               uint16_t* __restrict__ out, uint64_t* st) {
     __shared__ int rows[32];
     __shared__ float wk[32];
     pdl_wait();
     pdl_trigger();
+    StampScope stamp(st);
     const int t = blockIdx.y;
     if (threadIdx.x < k) {
         rows[threadIdx.x] = inv[t * k + threadIdx.x];
@@ -109,7 +111,7 @@ combine_kernel(const float* __restrict__ y, int nslots, size_t slot_stride,
 cudaError_t launch_rmsnorm(const uint16_t* h, int T, int D, const uint16_t* gamma, float eps,
                            uint16_t* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<T, kNormThreads, 0, s>>>(h, D, gamma, eps, out);
+    rmsnorm_kernel<<<T, kNormThreads, 0, s>>>(h, D, gamma, eps, out, trace_stamp("rmsnorm"));
     trace_mark("rmsnorm", s);
     return cudaGetLastError();
 }
@@ -120,7 +122,7 @@ cudaError_t launch_combine(const float* y, int nslots, const float* wts, const i
     dim3 grid((d + 4 * kCombineThreads - 1) / (4 * kCombineThreads), T);
     const size_t slot_stride = static_cast<size_t>(T) * k * d;
     const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, nslots, slot_stride,
-                                     wts, inv, k, d, out);
+                                     wts, inv, k, d, out, trace_stamp("combine"));
     trace_mark("combine", s);
     return e;
 }

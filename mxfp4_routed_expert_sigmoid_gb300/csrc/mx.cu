@@ -140,6 +140,8 @@ struct MxArgs {
     int umax;
     int rows_out;           // f (up) or d (down)
     WsHeader* hdr;
+    uint64_t* st;           // stamp slot (null: off)
+    int inject;             // test aid: CTA 0 drops its first stage's signal; waits give up after 1 ms
 };
 
 // Position in the sequence of stages.  Decode: (unit, matrix, row tile,
@@ -335,6 +337,8 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     volatile int* abort_flag = &abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t NB = static_cast<uint32_t>(p.N) * 128;  // B bytes per chunk
+    const uint64_t lim = p.inject ? 1000000ull : kWaitLimitNs;
+    const bool drop_first = p.inject && blockIdx.x == 0;
     // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms
     // [| canonical scale rows]; ggml weights: A chunks | SFA atoms | B chunks |
     // SFB atoms, so that the stage's 17-byte blocks land on the A and SFA bytes
@@ -445,6 +449,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     pdl_wait();
     if (!p.early_a) pdl_trigger();
     if (!p.early_a) split();
+    stamp_start(p.st);
 
     if (warp == 0) {
         if (lane == 0 && w0 < w1) {
@@ -459,8 +464,11 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (issued < early) {
                     mbar_expect_tx(ld_bar(s), b_bytes(c));  // the arrival of the stage
                     issue_b(c, st, ld_bar(s));
+                } else if (drop_first && w == w0) {
+                    // test aid: this stage is never signalled, so its consumer's
+                    // bounded wait runs out
                 } else {
-                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70)) break;
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.hdr, 70, lim)) break;
                     mbar_expect_tx(ld_bar(s), a_bytes(c) + b_bytes(c));
                     issue_a(c, e, st, ld_bar(s));
                     issue_b(c, st, ld_bar(s));
@@ -476,6 +484,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             // copies still in flight (after an abort) finish before the CTA exits
             for (int j = issued > p.RS ? issued - p.RS : 0; j < issued; ++j) {
+                if (drop_first && j == 0) continue;  // nothing was issued for it
                 const uint64_t t0 = global_ns();
                 while (!mbar_try_wait(ld_bar(j % p.RS), (j / p.RS) & 1) &&
                        global_ns() - t0 < kWaitLimitNs) {
@@ -499,10 +508,10 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int a = seg & 1;
                 bool ok = true;
                 if (lane == 0) {
-                    ok = !seg_start || mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71);
-                    ok = ok && mbar_wait(&full[s], ph, abort_flag, p.hdr, 72);
+                    ok = !seg_start || mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, p.hdr, 71, lim);
+                    ok = ok && mbar_wait(&full[s], ph, abort_flag, p.hdr, 72, lim);
                     // the scale slots are reused: the previous stage's MMAs have finished
-                    ok = ok && (i == 0 || mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73));
+                    ok = ok && (i == 0 || mbar_wait(&empty[ps], pph, abort_flag, p.hdr, 73, lim));
                 }
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
                 if (i > 0 && ++ps == p.RS) {
@@ -556,7 +565,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         int s = 0;
         uint32_t ph = 0;
         for (int w = w0; w < w1; ++w) {
-            const bool ok = mbar_wait(&raw[s], ph, abort_flag, p.hdr, 76);
+            const bool ok = mbar_wait(&raw[s], ph, abort_flag, p.hdr, 76, lim);
             if (!named_bar_and(kGgBar, kGgThreads, ok)) break;
             gg_convert_row(smem + static_cast<size_t>(s) * p.stage_bytes, r, offSA);
             fence_proxy_async();  // the MMA and tcgen05.cp read these bytes through the async proxy
@@ -577,7 +586,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int len = min(p.KS - c.ks, w1 - w);
             const bool whole = ks_begin == 0 && len == p.KS;
             const int a = seg & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, p.hdr, 74)))
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, p.hdr, 74, lim)))
                 break;
             tc_fence_after();
             // the second issuer's accumulator holds data unless the segment is only
@@ -632,6 +641,7 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     tc_fence_before();
     __syncthreads();
+    stamp_end(p.st);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -649,13 +659,14 @@ template <int TERMS>
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
                  const int32_t* __restrict__ count, const int32_t* __restrict__ ucnt, uint8_t* __restrict__ hq,
-                 uint8_t* __restrict__ hsf) {
+                 uint8_t* __restrict__ hsf, uint64_t* st) {
     // the down projection may launch now: its CTAs start on the SMs the up
     // projection frees and issue their first weight loads during this kernel
     // (this grid was launched after every up CTA passed its wait, so the active
     // list they read is final)
     pdl_trigger();
     pdl_wait();
+    StampScope stamp(st);
     const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
     const int KC = (f + 255) / 256;
     const int items = *count * T * KC;
@@ -702,9 +713,10 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
 // router did not write them).  One warp per (token, 32-block).
 __global__ void __launch_bounds__(256)
 mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int T, int K, int N, uint8_t* __restrict__ xq,
-                        uint8_t* __restrict__ xsf) {
+                        uint8_t* __restrict__ xsf, uint64_t* st) {
     pdl_wait();
     pdl_trigger();
+    StampScope stamp(st);
     const int lane = threadIdx.x & 31;
     const int nb = K / 32;
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -729,13 +741,14 @@ constexpr int kCombineMaxUnits = 256;  // decode: T * k <= 8 * 32
 __global__ void __launch_bounds__(kCombineThreads)
 mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const float* __restrict__ wts,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ active, int E, int k,
-                  const int32_t* __restrict__ rowmap, uint16_t* __restrict__ out) {
+                  const int32_t* __restrict__ rowmap, uint16_t* __restrict__ out, uint64_t* st) {
     __shared__ int rows[32];
     __shared__ float wk[32];
     __shared__ int act[kCombineMaxUnits];
     __shared__ __align__(16) float part[32][kCombineCols];
     pdl_wait();
     pdl_trigger();
+    StampScope stamp(st);
     const int t = blockIdx.y;
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     if (rowmap) {
@@ -803,7 +816,9 @@ __global__ void __launch_bounds__(1024)
 mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ idx, const int32_t* __restrict__ inv, int E, int P,
                 int32_t* __restrict__ unit_exp, int32_t* __restrict__ unit_row0, int32_t* __restrict__ unit_cnt,
-                int32_t* __restrict__ nunits, int32_t* __restrict__ rowmap, int32_t* __restrict__ ubase_out) {
+                int32_t* __restrict__ nunits, int32_t* __restrict__ rowmap, int32_t* __restrict__ ubase_out,
+                uint64_t* st) {
+    StampScope stamp(st);
     __shared__ int ubase[1024 + 1];
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -859,7 +874,8 @@ mx_units_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
 // grid-strided.
 __global__ void __launch_bounds__(256)
 mx_token_terms_kernel(const uint16_t* __restrict__ x, int T, int K, uint8_t* __restrict__ tq,
-                      uint8_t* __restrict__ tsf) {
+                      uint8_t* __restrict__ tsf, uint64_t* st) {
+    StampScope stamp(st);
     const int lane = threadIdx.x & 31, kb = lane >> 2, r = lane & 3;
     const int KC = (K + 255) / 256, nb = K / 32;
     for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < T * KC; i += gridDim.x * 8) {
@@ -894,7 +910,8 @@ __global__ void __launch_bounds__(256)
 mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__ tsf,
                      const int32_t* __restrict__ perm, int k, int K, int N, const int32_t* __restrict__ nunits,
                      const int32_t* __restrict__ unit_row0, const int32_t* __restrict__ unit_cnt,
-                     uint8_t* __restrict__ bq, uint8_t* __restrict__ bsf) {
+                     uint8_t* __restrict__ bq, uint8_t* __restrict__ bsf, uint64_t* st) {
+    StampScope stamp(st);
     const int nb = K / 32, KC = (K + 255) / 256;
     const int per_unit = kUnitTokens * kUnitTerms * nb;
     const long long items = static_cast<long long>(*nunits) * per_unit;
@@ -928,7 +945,8 @@ mx_unit_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__
 // the padding is written as zeros and skipped by the inverse.
 // ---------------------------------------------------------------------------
 __global__ void prepare_sf_kernel(uint8_t* __restrict__ canon, int64_t n_words, int R, int K,
-                                  uint8_t* __restrict__ atoms, int inverse) {
+                                  uint8_t* __restrict__ atoms, int inverse, uint64_t* st) {
+    StampScope stamp(st);
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n_words) return;
     const int G = (K + 127) / 128, tiles = (R + 127) / 128, nb = K / 32;
@@ -963,8 +981,8 @@ cudaError_t launch_prepare_sf(const uint8_t* canon, int64_t E, int R, int K, uin
     const int64_t n_words = static_cast<int64_t>(prepared_sf_bytes(E, R, K) / 4);
     if (n_words <= 0) return cudaSuccess;
     const int64_t blocks = (n_words + 255) / 256;
-    prepare_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(const_cast<uint8_t*>(canon), n_words, R, K,
-                                                                    atoms, inverse);
+    prepare_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        const_cast<uint8_t*>(canon), n_words, R, K, atoms, inverse, trace_stamp(inverse ? "unprepare_sf" : "prepare_sf"));
     trace_mark(inverse ? "unprepare_sf" : "prepare_sf", s);
     return cudaGetLastError();
 }
@@ -1030,6 +1048,7 @@ cudaError_t launch_stream(const CUtensorMap& a, const CUtensorMap& a3, const CUt
         if (e != cudaSuccess) return e;
         cur.store(static_cast<int>(smem));
     }
+    p.st = trace_stamp(name);
     const cudaError_t e = launch_pdl(mx_stream_kernel<TERMS, WF>, dim3(grid),
                                      dim3(WF == kWfGgml ? kMxThreads + kGgThreads : kMxThreads), smem, s, a, a3,
                                      sc, sc3, p);
@@ -1140,7 +1159,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     if (!a.xq_ready) {
         const int warps = a.T * (a.d / 32);
         e = launch_pdl(mx_quantize_rows_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, a.x, a.T, a.d, m.N,
-                       m.xq, m.xsf);
+                       m.xq, m.xsf, trace_stamp("quantize_x"));
         trace_mark("quantize_x", s);
         if (e != cudaSuccess) return e;
     }
@@ -1163,6 +1182,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     up.part = m.up;
     up.umax = m.umax;
     up.hdr = a.hdr;
+    up.inject = a.inject;
     // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
     if ((e = launch_stream_wf<kTerms>(wm, true, up, grid_up, s, "decode_up"))) return e;
@@ -1170,7 +1190,8 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     const int warps = m.umax * a.T * kc256(a.f);
     const int fgrid = std::min((warps + 7) / 8, 8 * a.num_sms);
     e = launch_pdl(mx_finish_kernel<kTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up),
-                   m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf);
+                   m.umax, a.T, a.f, m.N, a.active + a.E, static_cast<const int32_t*>(nullptr), m.hq, m.hsf,
+                   trace_stamp("decode_finish_up"));
     trace_mark("decode_finish_up", s);
     if (e != cudaSuccess) return e;
 
@@ -1191,7 +1212,8 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
 
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
-                   m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, static_cast<const int32_t*>(nullptr), a.out);
+                   m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, static_cast<const int32_t*>(nullptr), a.out,
+                   trace_stamp("combine"));
     trace_mark("combine", s);
     return e;
 }
@@ -1252,18 +1274,19 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     if (a.E > 1024) return cudaErrorNotSupported;
     const int P = a.T * a.k;
     mx_units_kernel<<<1, 1024, 0, s>>>(a.counts, a.offsets, a.idx, a.inv, a.E, P, m.unit_exp, m.unit_row0,
-                                       m.unit_cnt, m.nunits, m.rowmap, m.ubase);
+                                       m.unit_cnt, m.nunits, m.rowmap, m.ubase, trace_stamp("units"));
     trace_mark("units", s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long twarps = static_cast<long long>(a.T) * kc256(a.d);
     mx_token_terms_kernel<<<static_cast<int>(std::min<long long>((twarps + 7) / 8, 8LL * a.num_sms)), 256, 0, s>>>(
-        a.x, a.T, a.d, m.tq, m.tsf);
+        a.x, a.T, a.d, m.tq, m.tsf, trace_stamp("token_terms"));
     trace_mark("token_terms", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long citems = static_cast<long long>(m.umax) * kUnitTokens * kUnitTerms * (a.d / 32);
     mx_unit_terms_kernel<<<static_cast<int>(std::min<long long>((citems + 255) / 256, 8LL * a.num_sms)), 256, 0,
-                           s>>>(m.tq, m.tsf, a.perm, a.k, a.d, m.N, m.nunits, m.unit_row0, m.unit_cnt, m.xq, m.xsf);
+                           s>>>(m.tq, m.tsf, a.perm, a.k, a.d, m.N, m.nunits, m.unit_row0, m.unit_cnt, m.xq, m.xsf,
+                                trace_stamp("unit_terms"));
     trace_mark("unit_terms", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -1289,6 +1312,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     up.part = m.up;
     up.umax = m.umax;
     up.hdr = a.hdr;
+    up.inject = a.inject;
     // every CTA's range must be at least one tile long: there are at least k units
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
     if ((e = launch_stream_wf<kUnitTerms>(wm, true, up, grid_up, s, "units_up"))) return e;
@@ -1297,7 +1321,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     const int fgrid = static_cast<int>(std::min<long long>((fwarps + 7) / 8, 8LL * a.num_sms));
     e = launch_pdl(mx_finish_kernel<kUnitTerms>, dim3(fgrid), dim3(256), 0, s, static_cast<const float*>(m.up), m.umax,
                    kUnitTokens, a.f, m.N, static_cast<const int32_t*>(m.nunits),
-                   static_cast<const int32_t*>(m.unit_cnt), m.hq, m.hsf);
+                   static_cast<const int32_t*>(m.unit_cnt), m.hq, m.hsf, trace_stamp("units_finish_up"));
     trace_mark("units_finish_up", s);
     if (e != cudaSuccess) return e;
 
@@ -1322,7 +1346,7 @@ cudaError_t launch_mx_units(const MxUnitsArgs& a, cudaStream_t s) {
     dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y), m.umax,
                    kUnitTokens, a.d, a.wts, a.idx, static_cast<const int32_t*>(nullptr), a.E, a.k,
-                   static_cast<const int32_t*>(m.rowmap), a.out);
+                   static_cast<const int32_t*>(m.rowmap), a.out, trace_stamp("combine"));
     trace_mark("combine", s);
     return e;
 }

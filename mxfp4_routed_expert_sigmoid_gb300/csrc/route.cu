@@ -180,8 +180,11 @@ route_topk_kernel(RouteArgs a) {
     select_topk(valid ? expert_key(0.0f, b, e) : 0, 0.5f, a.k, nullptr, nullptr, true);
     pdl_wait();
     pdl_trigger();
+    StampScope stamp(a.st_b);
     const float l = valid ? a.logits[static_cast<size_t>(t) * a.E + e] : 0.0f;
-    if (__syncthreads_or(valid && !isfinite(l)) && e == 0) set_error(a.hdr, K3MOE_ERR_NONFINITE, 1);
+    // a logit that is not finite, or a NaN bias (a bias of +-inf orders like
+    // any other key), leaves the selection undefined: flagged
+    if (__syncthreads_or(valid && (!isfinite(l) || isnan(b))) && e == 0) set_error(a.hdr, K3MOE_ERR_NONFINITE, 1);
     const bool chosen = select_topk(valid ? expert_key(l, b, e) : 0, sigmoid_f32(l), a.k,
                                     a.idx + static_cast<size_t>(t) * a.k,
                                     a.wts + static_cast<size_t>(t) * a.k, false);
@@ -285,6 +288,7 @@ route_small_kernel(RouteArgs a) {
     // the top-k kernel may start launching now: it waits for this grid's
     // completion (griddepcontrol.wait) before reading the logits
     pdl_trigger();
+    StampScope stamp(a.st_a);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int gemv_ctas = (a.E + 7) / 8;
     if (static_cast<int>(blockIdx.x) >= gemv_ctas) {
@@ -357,6 +361,7 @@ route_small_kernel(RouteArgs a) {
 // Plain tiled SIMT logits for moderate T: 64 tokens x 64 experts per CTA.
 __global__ void __launch_bounds__(256)
 logits_simt_kernel(RouteArgs a) {
+    StampScope stamp(a.st_a);
     __shared__ float xs[64][33];
     __shared__ float ws[64][33];
     const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
@@ -399,7 +404,8 @@ constexpr int kChunk = 64;  // tokens per chunk
 
 __global__ void __launch_bounds__(256)
 perm_count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* chunk_cnt,
-                  WsHeader* hdr) {
+                  WsHeader* hdr, uint64_t* st) {
+    StampScope stamp(st);
     extern __shared__ int hist[];
     const int c = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -421,7 +427,8 @@ perm_count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t*
 // active list
 __global__ void __launch_bounds__(256)
 perm_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int P, int32_t* counts,
-                 int32_t* offsets, int32_t* active) {
+                 int32_t* offsets, int32_t* active, uint64_t* st) {
+    StampScope stamp(st);
     extern __shared__ int sm[];  // [2 * E]
     int* tot = sm;
     int* flag = sm + E;
@@ -462,7 +469,8 @@ perm_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int P, int32_t* counts,
 __global__ void __launch_bounds__(32)
 perm_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
                     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
-                    int32_t* perm, int32_t* inv) {
+                    int32_t* perm, int32_t* inv, uint64_t* st) {
+    StampScope stamp(st);
     extern __shared__ int running[];
     const int c = blockIdx.x, lane = threadIdx.x;
     for (int e = lane; e < E; e += 32)
@@ -486,13 +494,17 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
 
 }  // namespace
 
-cudaError_t launch_route_topk(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_route_topk(const RouteArgs& a_in, cudaStream_t s) {
+    RouteArgs a = a_in;
+    a.st_b = trace_stamp("route_topk");
     const cudaError_t e = launch_pdl(route_topk_kernel, dim3(a.T), dim3(kMaxE), 0, s, a);
     trace_mark("route_topk", s);
     return e;
 }
 
-cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_route_small(const RouteArgs& a_in, cudaStream_t s) {
+    RouteArgs a = a_in;
+    a.st_a = trace_stamp("route_small");
     const int gemv_ctas = (a.E + 7) / 8;
     const int xq_ctas = a.xq ? std::min(128, (a.T * (a.d_r / 32) + 7) / 8) : 0;
     const size_t smem = static_cast<size_t>(a.T) * a.d_r * 2;
@@ -564,7 +576,9 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s) {
     return launch_route_topk(b, s);
 }
 
-cudaError_t launch_logits_simt(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_logits_simt(const RouteArgs& a_in, cudaStream_t s) {
+    RouteArgs a = a_in;
+    a.st_a = trace_stamp("logits_simt");
     dim3 grid((a.E + 63) / 64, (a.T + 63) / 64);
     logits_simt_kernel<<<grid, 256, 0, s>>>(a);
     trace_mark("logits_simt", s);
@@ -591,11 +605,13 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
     if (2 * smem > 48 * 1024)
         cudaFuncSetAttribute(perm_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(2 * smem));
-    perm_count_kernel<<<nchunks, 256, smem, s>>>(idx, T, k, E, chunk, hdr);
+    perm_count_kernel<<<nchunks, 256, smem, s>>>(idx, T, k, E, chunk, hdr, trace_stamp("perm_count"));
     trace_mark("perm_count", s);
-    perm_scan_kernel<<<1, 256, 2 * smem, s>>>(chunk, nchunks, E, T * k, counts, offsets, active);
+    perm_scan_kernel<<<1, 256, 2 * smem, s>>>(chunk, nchunks, E, T * k, counts, offsets, active,
+                                              trace_stamp("perm_scan"));
     trace_mark("perm_scan", s);
-    perm_scatter_kernel<<<nchunks, 32, smem, s>>>(idx, T, k, E, chunk, offsets, perm, inv);
+    perm_scatter_kernel<<<nchunks, 32, smem, s>>>(idx, T, k, E, chunk, offsets, perm, inv,
+                                                  trace_stamp("perm_scatter"));
     trace_mark("perm_scatter", s);
     return cudaGetLastError();
 }

@@ -53,7 +53,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait: false if the CTA is aborting or the limit expired.
 __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
-                          int where) {
+                                 int where, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
@@ -61,7 +61,7 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* a
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             if (hdr) set_error(hdr, K3MOE_ERR_TIMEOUT, where);
             return false;
