@@ -456,6 +456,16 @@ k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws,
                                    int32_t* idx_out, float* w_out, float* logits_out,
                                    void* stream);
 
+/* Block mode: copy the intermediates of the last k3moe_forward that used
+ * `ws` (device to device, on `stream`; any output may be NULL): hn_out [T, D]
+ * bf16, the normalised hidden (the router's input); z_out [T, d] bf16, the
+ * latent input of the experts (hn W_down^T); m_out [T, d] bf16, the combined
+ * latent rows before the up-projection.  Errors: INVALID_ARG, UNSUPPORTED
+ * (latent mode), CUDA. */
+k3moe_status k3moe_forward_intermediates(const k3moe_layer_desc* desc, const void* ws, int32_t T,
+                                         uint16_t* hn_out, uint16_t* z_out, uint16_t* m_out,
+                                         void* stream);
+
 /* Read and clear the device status word of a workspace.  Synchronises
  * `stream`; *device_status receives K3MOE_OK or the first device error code.
  * Returns CUDA if the stream reported an error. */

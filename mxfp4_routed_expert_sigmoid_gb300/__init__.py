@@ -40,7 +40,8 @@ EXPORTS = (
     "k3moe_route_workspace_size", "k3moe_route", "k3moe_route_noalloc", "k3moe_permute",
     "k3moe_rmsnorm",
     "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
-    "k3moe_forward_host", "k3moe_forward_routing", "k3moe_get_status", "k3moe_trace",
+    "k3moe_forward_host", "k3moe_forward_routing", "k3moe_forward_intermediates",
+    "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
     "k3moe_trace_read", "k3moe_trace_read_stamps", "k3moe_prepared_scales_size",
     "k3moe_prepare_scales",
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
         "k3moe_forward_host": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz, vp], ctypes.c_int),
         "k3moe_forward_routing": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, vp],
                                   ctypes.c_int),
+        "k3moe_forward_intermediates": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, vp],
+                                        ctypes.c_int),
         "k3moe_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "k3moe_trace": ([ctypes.c_int], ctypes.c_int),
         "k3moe_graph_create": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz,
@@ -414,6 +417,17 @@ def k3moe_forward_routing(layer: MoELayer, ws, T: int, with_logits: bool = True,
     _check(lib().k3moe_forward_routing(ctypes.byref(layer.desc), _p(ws), T, _p(idx), _p(w),
                                        _p(logits), _stream(stream)))
     return idx, w, logits
+
+
+def k3moe_forward_intermediates(layer: MoELayer, ws, T: int, stream=None):
+    """Block mode: (hn [T, D], z [T, d], m [T, d]) bf16 of the last forward on ``ws``."""
+    dev = ws.device
+    hn = torch.empty((T, layer.D), dtype=torch.bfloat16, device=dev)
+    z = torch.empty((T, layer.d), dtype=torch.bfloat16, device=dev)
+    m = torch.empty((T, layer.d), dtype=torch.bfloat16, device=dev)
+    _check(lib().k3moe_forward_intermediates(ctypes.byref(layer.desc), _p(ws), T, _p(hn), _p(z), _p(m),
+                                             _stream(stream)))
+    return hn, z, m
 
 
 def k3moe_get_status(ws, stream=None) -> int:

@@ -897,6 +897,20 @@ k3moe_status k3moe_forward_routing(const k3moe_layer_desc* desc, const void* ws,
     return K3MOE_OK;
 }
 
+k3moe_status k3moe_forward_intermediates(const k3moe_layer_desc* desc, const void* ws, int32_t T,
+                                         uint16_t* hn_out, uint16_t* z_out, uint16_t* m_out, void* stream) {
+    if (!desc || !ws || T < 1 || desc->E < 1 || desc->k < 1) return K3MOE_ERR_INVALID_ARG;
+    if (desc->D <= 0) return K3MOE_ERR_UNSUPPORTED;  // latent mode keeps no intermediates
+    const FwdPlan p = fwd_plan(desc, T);
+    const char* base = static_cast<const char*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nD = static_cast<size_t>(T) * desc->D * 2, nd = static_cast<size_t>(T) * desc->d * 2;
+    if (hn_out && cudaMemcpyAsync(hn_out, base + p.hn, nD, cudaMemcpyDeviceToDevice, s)) return K3MOE_ERR_CUDA;
+    if (z_out && cudaMemcpyAsync(z_out, base + p.z, nd, cudaMemcpyDeviceToDevice, s)) return K3MOE_ERR_CUDA;
+    if (m_out && cudaMemcpyAsync(m_out, base + p.m, nd, cudaMemcpyDeviceToDevice, s)) return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
 k3moe_status k3moe_get_status(void* ws, void* stream, int32_t* device_status) {
     if (!ws || !device_status) return K3MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -271,26 +271,36 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
 // token producer (TMA of the tile's token rows in 16-row boxes, only as many
 // as the tile has, into a BS-deep ring), 4..7 epilogue, 8..15
-// dequantisation (raw ring -> f16 A stages of an AS-deep ring).  Three rings
-// with their own full/empty barriers: the raw weights and the token rows are
-// fetched several stages ahead (HBM and L2 latency), while the f16 stages
-// only have to cover the dequantise -> MMA hand-off.
+// dequantisation (raw ring -> f16 A stages of an AS-deep ring in TMEM).
+// The f16 weights never touch shared memory: each dequantising thread writes
+// its row's 32 values of a stage straight into tensor memory (tcgen05.st,
+// lane = weight row), and the MMAs read A from there (the A-in-TMEM form of
+// tcgen05.mma), so shared memory carries only the raw codes and the token
+// rows.  Three rings with their own full/empty barriers: the raw weights and
+// the token rows are fetched several stages ahead (HBM and L2 latency), while
+// the f16 stages only have to cover the dequantise -> MMA hand-off.
 // ---------------------------------------------------------------------------
 template <int NA>
 struct ExpCfg;
-// RS: raw-weight stages, AS: dequantised A stages, BS: token (B) stages,
-// NBUF: accumulator buffers in TMEM.  The down projection takes 256 token rows
-// per tile (each MMA, M = 128, N = 256, K = 16, then outlasts its issue cost);
-// the up projection keeps 128 so that its two accumulators (W1, W3) stay
-// double-buffered (with 256 and one buffer it measured 35 % slower).
+// RS: raw-weight stages, AS: dequantised A stages (in TMEM), BS: token (B)
+// stages, NBUF: accumulator buffers in TMEM.  TMEM (512 columns of 128
+// lanes) holds NBUF x NA accumulators of BN fp32 columns, then AS x NA A
+// stages of 32 columns (64 f16 inputs per row): the up projection takes 96
+// token rows per tile (2 x 2 x 96 + 2 x 2 x 32 = 512), the down projection
+// 192 (2 x 192 + 4 x 32 = 512); both keep their accumulators double-buffered
+// so the epilogue of a tile runs under the next tile's MMAs.
 template <>
 struct ExpCfg<2> {
-    static constexpr int BN = 128, RS = 8, AS = 2, BS = 4, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 96, RS = 10, AS = 2, BS = 6, NBUF = 2, TMEM_COLS = 512;
 };
 template <>
 struct ExpCfg<1> {
-    static constexpr int BN = 256, RS = 8, AS = 4, BS = 3, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 192, RS = 12, AS = 4, BS = 5, NBUF = 2, TMEM_COLS = 512;
 };
+template <int NA>
+constexpr int exp_acol() { return ExpCfg<NA>::NBUF * NA * ExpCfg<NA>::BN; }  // first A column
+static_assert(exp_acol<2>() + ExpCfg<2>::AS * 2 * 32 <= 512, "up: TMEM budget");
+static_assert(exp_acol<1>() + ExpCfg<1>::AS * 1 * 32 <= 512, "down: TMEM budget");
 constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
 constexpr int kBoxRows = 16;    // token rows per TMA box
 constexpr int kExpThreads = 512;
@@ -316,7 +326,6 @@ template <int NA>
 constexpr size_t exp_smem_bytes() {
     using C = ExpCfg<NA>;
     size_t b = 1024;
-    b += static_cast<size_t>(C::AS) * NA * kTileA;
     b += static_cast<size_t>(C::BS) * C::BN * BK * 2;
     b += static_cast<size_t>(C::RS) * NA * (kTileRaw + 512);
     b += static_cast<size_t>(kES) * NA * BM * 4;
@@ -336,8 +345,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     constexpr int BN = C::BN, RS = C::RS, AS = C::AS, BS = C::BS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;                                // [AS][NA][16 KB]
-    uint8_t* sB = sA + AS * NA * kTileA;               // [BS][BN * 128]
+    uint8_t* sB = smem;                                // [BS][BN * 128]
     uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RS][NA][4 KB]
     uint8_t* sRawSf = sRaw + RS * NA * kTileRaw;       // [RS][NA][512]: the stage's scale atom
     int* sE = reinterpret_cast<int*>(sRawSf + RS * NA * 512);  // [kES][NA][128]
@@ -472,11 +480,12 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t b_addr = smem_u32(sB + b * BN * BK * 2);
 #pragma unroll
                     for (int m = 0; m < NA; ++m) {
-                        const uint32_t a_addr = smem_u32(sA + (a * NA + m) * kTileA);
+                        // A stage (a, m): TMEM columns, 8 per 16-wide K slice
+                        const uint32_t a_tm = tmem_base + static_cast<uint32_t>(exp_acol<NA>() + (a * NA + m) * 32);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_f16(d0 + m * BN, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                                    idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16_ts(d0 + m * BN, a_tm + 8 * kk, sw128_desc(b_addr + kk * 32), idesc,
+                                       (ks > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&a_empty[a]);
                     mma_commit(&b_empty[b]);
@@ -575,8 +584,12 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp >= 8) {
         // ---------------------------- dequantisation -------------------------
-        const int dt = threadIdx.x - 256;  // 0..255
-        const int row = dt >> 1, half = dt & 1;
+        // warp 8 + 4 half + q: TMEM lane quadrant q, one weight row per lane,
+        // inputs 32 half .. 32 half + 31 of each 64-wide stage
+        const int q = warp & 3, half = (warp - 8) >> 2;
+        const int row = 32 * q + lane;
+        const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                static_cast<uint32_t>(exp_acol<NA>() + 16 * half);
         int r = 0, a = 0;
         uint32_t rph = 0, aph = 0;
         int it = 0;
@@ -617,6 +630,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     ok = false;
                     break;
                 }
+                tc_fence_after();  // the MMAs that read this A stage have completed
                 int e1, e3;
                 if (SFC) {
                     e1 = vec_byte(v1, blk & 15);
@@ -638,15 +652,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     e2m1x8_to_f16x8(raw.w, w[12], w[13], w[14], w[15]);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[i] = hmul2(w[i], sc2);
-                    uint8_t* dst = sA + (a * NA + mm) * kTileA + row * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int chunk = (half * 4 + c) ^ (row & 7);
-                        *reinterpret_cast<uint4*>(dst + chunk * 16) =
-                            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                    }
+                    tmem_st16(a_lane + static_cast<uint32_t>((a * NA + mm) * 32), w);
                 }
-                fence_proxy_async();
+                tmem_wait_st();
+                tc_fence_before();
+                fence_proxy_async();  // the raw codes were read here; the producer's TMA rewrites them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&a_full[a]);

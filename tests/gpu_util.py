@@ -103,21 +103,25 @@ def _moe_part(args):
                               experts=experts)["out"]
 
 
-def oracle_rows_parallel(cfg, dense, tokens, idx=None, workers=None):
+def oracle_rows_parallel(cfg, dense, tokens, idx=None, workers=None, moe_inputs=None):
     """oracle_forward(cfg, dense, expert, tokens, idx)["out"] with the expert
     bytes regenerated per worker (synth.expert_matrix_np) and the used experts
     split over a spawn pool.  Returns (out [n, width] float64, routing dict of
-    the oracle on these rows: idx, margin)."""
+    the oracle on these rows: idx, margin).  With ``moe_inputs`` = (router
+    input rows, expert input rows) the MoE layer alone is evaluated on them
+    (block mode: its unrounded output, before the bf16 hand-off and W_up)."""
     import multiprocessing as mp
     import os
 
-    h = oracle.bf16_to_f64(dense["hidden"][tokens])
     wr = oracle.bf16_to_f64(dense["router_w"])
-    if cfg.block:
+    if moe_inputs is not None:
+        x_r, x_e = moe_inputs
+    elif cfg.block:
+        h = oracle.bf16_to_f64(dense["hidden"][tokens])
         x_r, x_e = oracle.block_head(h, oracle.bf16_to_f64(dense["norm_gamma"]), dense["eps"],
                                      oracle.bf16_to_f64(dense["w_down"]))
     else:
-        x_r = x_e = h
+        x_r = x_e = oracle.bf16_to_f64(dense["hidden"][tokens])
     r = oracle.select_experts(oracle.router_logits(x_r, wr), dense["router_b"], cfg.k)
     used = np.unique(r["idx"] if idx is None else idx)
     n = workers or min(len(used), os.cpu_count() or 1)
@@ -126,7 +130,7 @@ def oracle_rows_parallel(cfg, dense, tokens, idx=None, workers=None):
     ctx = mp.get_context("spawn")
     with ctx.Pool(n) as pool:
         out = sum(pool.map(_moe_part, jobs))
-    if cfg.block:
+    if cfg.block and moe_inputs is None:
         out = oracle.block_tail(out, oracle.bf16_to_f64(dense["w_up"]))[1]
     return out, {"idx": r["idx"], "margin": r["margin"]}
 

@@ -193,11 +193,70 @@ def test_grouped_deterministic_and_power_of_two(k3):
     assert torch.equal(out3.float(), 2 * out1.float())
 
 
+def staged_block_check(k3, cfg, layer, ws, out, idx_gpu, dense, expert, tokens):
+    """The block step by step, each step against the oracle's definition
+    applied to the GPU's own previous step (so a bf16 hand-off that rounds a
+    value the other way than the oracle does is not carried into the next
+    step's comparison):
+      hn = bf16(RMSNorm(h) gamma)         within half a bf16 ulp of the exact value;
+      z  = bf16(hn W_down^T)              within half an ulp plus fp32 accumulation;
+      m  = bf16(MoE layer(hn -> router, z -> experts))
+                                          the layer's bound (1e-2 x row RMS + half an ulp);
+      out = bf16(m W_up^T)                within half an ulp plus fp32 accumulation.
+    Returns the layer step's err / RMS per row."""
+    T = cfg.T
+    hn, z, m = (bf16_tensor_to_np(t)[tokens] for t in k3.k3moe_forward_intermediates(layer, ws, T))
+    got = bf16_tensor_to_np(out)[tokens]
+    q = 2.0 ** -8
+    h = oracle.bf16_to_f64(dense["hidden"][tokens])
+    gamma = oracle.bf16_to_f64(dense["norm_gamma"])
+    hn_ref = oracle.rmsnorm(h, gamma, dense["eps"])
+    assert np.all(np.abs(hn - hn_ref) <= q * np.abs(hn_ref) + 1e-6 * np.abs(hn_ref) + 1e-30)
+    w_down = oracle.bf16_to_f64(dense["w_down"])
+    z_ref = hn @ w_down.T
+    acc = np.abs(hn) @ np.abs(w_down).T
+    assert np.all(np.abs(z - z_ref) <= q * np.abs(z_ref) + 1e-5 * acc + 1e-30)
+    idx_gpu = idx_gpu[tokens]
+    if len(tokens) > 32:
+        moe_ref, r = oracle_rows_parallel(cfg, dense, tokens, moe_inputs=(hn, z))
+    else:
+        r = oracle.moe_forward(hn, oracle.bf16_to_f64(dense["router_w"]), dense["router_b"], cfg.k, z, expert)
+        moe_ref = r["out"]
+    same = np.all(r["idx"] == idx_gpu, axis=1)
+    assert np.all(same | (r["margin"] < 1e-5)), "selection differs outside near ties"
+    if not np.all(same):
+        if len(tokens) > 32:
+            moe_ref, _ = oracle_rows_parallel(cfg, dense, tokens, idx=idx_gpu, moe_inputs=(hn, z))
+        else:
+            moe_ref = oracle.moe_forward(hn, oracle.bf16_to_f64(dense["router_w"]), dense["router_b"], cfg.k,
+                                         z, expert, idx=idx_gpu)["out"]
+    err = rel_err_rows(m, moe_ref)
+    record_margin(f"{cfg.name} T={T} block step: MoE layer on the GPU's hn, z (rows={len(tokens)})", err, TOL)
+    assert np.all(err <= TOL), f"MoE step max err/rms {err.max():.3e}"
+    w_up = oracle.bf16_to_f64(dense["w_up"])
+    o_ref = m @ w_up.T
+    acc = np.abs(m) @ np.abs(w_up).T
+    assert np.all(np.abs(got - o_ref) <= q * np.abs(o_ref) + 1e-5 * acc + 1e-30)
+    return err
+
+
+def run_block(k3, cfg, path, sample=0, tokens=None):
+    """The end-to-end check (compare_forward), then the step-by-step check on
+    the same forward's intermediates."""
+    bundle = make_layer(cfg, path=path)
+    out, ws, _ = compare_forward(k3, cfg, path, bundle=bundle, sample=sample, tokens=tokens)
+    layer, dense, expert, _ = bundle
+    idx_gpu = k3.k3moe_forward_routing(layer, ws, cfg.T)[0].cpu().numpy().astype(np.int64)
+    rows = (sample_rows(cfg.T, idx_gpu, sample, seed=cfg.seed) if sample else
+            np.arange(cfg.T) if tokens is None else np.asarray(tokens))
+    staged_block_check(k3, cfg, layer, ws, out, idx_gpu, dense, expert, rows)
+
+
 @pytest.mark.parametrize("T,path", [(4, 1), (4, 2), (300, 1), (300, 2)])
 def test_block_small(k3, T, path):
     """Full latent block (RMSNorm, projections, router at the model width)."""
     cfg = synth.custom("block_t8192", T=T, E=32, k=4, d=256, f=512, D=512, seed_index=24)
-    compare_forward(k3, cfg, path)
+    run_block(k3, cfg, path)
 
 
 def test_chunk_t512_full_sampled(k3):
@@ -212,7 +271,17 @@ def test_block_t8192_full_sampled(k3):
     whole batch runs on the GPU; 256 token rows are checked, among them the
     first and last tokens of the 8 most-loaded experts (their first and last
     tiles of the grouped GEMMs) and the last tile of the tile list."""
-    compare_forward(k3, synth.CONFIGS["block_t8192"], 0, sample=256)
+    run_block(k3, synth.CONFIGS["block_t8192"], 0, sample=256)
+
+
+@pytest.mark.parametrize("T", [95, 97, 200, 385])
+def test_grouped_tile_edges(k3, T):
+    """Token counts around the grouped GEMMs' tile sizes (96 token rows per
+    up-projection tile, 192 per down-projection tile): experts with one
+    partial tile, several full tiles and a ragged last one (k = E, so every
+    expert takes every token)."""
+    cfg = synth.custom("decode_t1", T=T, E=4, k=4, d=512, f=768, seed_index=61)
+    compare_forward(k3, cfg, 2)
 
 
 def test_verify_t8_grouped_path(k3):
