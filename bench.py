@@ -345,6 +345,7 @@ def algorithmic_work(cfg, u_mean, mb):
     GEMMs (2 m n k)."""
     T, k, d, f = cfg.T, cfg.k, cfg.d, cfg.f
     bytes_ = {
+        "decode_experts": u_mean * 3 * mb,
         "decode_up": u_mean * 2 * mb, "decode_down": u_mean * mb,
         "units_up": u_mean * 2 * mb, "units_down": u_mean * mb,
         "route_small": cfg.E * cfg.d_router * 2 + T * cfg.d_router * 2 + T * cfg.E * 4,

@@ -338,7 +338,17 @@ k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden,
  * `stream`, runs the layer, copies out back to host memory and waits for the
  * stream.  Pinned host memory gives asynchronous copies; pageable memory
  * works too.  The workspace must hold k3moe_workspace_size(desc, T) plus
- * k3moe_host_staging_size(desc, T) bytes. */
+ * k3moe_host_staging_size(desc, T) bytes; the copies go through staging
+ * buffers at fixed offsets of it.  The first call with a given descriptor
+ * (its contents), workspace, size, T, stream and device runs the forward
+ * directly and records it into a CUDA graph (host and driver objects, no
+ * device memory); a later call with the same arguments replays that graph.
+ * The library keeps the 8 most recently used such graphs for the life of the
+ * process.  A graph reads the buffers the descriptor points to, so weights
+ * rewritten in place are seen; point the descriptor at new buffers (a new
+ * key) rather than freeing and reallocating under an unchanged descriptor
+ * with other shapes.  While tracing is on, or when `stream` is being
+ * captured, every call runs directly. */
 size_t k3moe_host_staging_size(const k3moe_layer_desc* desc, int32_t T);
 k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hidden_host,
                                 int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,

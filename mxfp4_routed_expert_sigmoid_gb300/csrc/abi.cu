@@ -641,6 +641,8 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         r.active = path == K3MOE_PATH_BLOCK_SCALED ? active : nullptr;
         if (fuse_prep)
             mx_decode_xq_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.xq, &r.xsf, &r.xq_n);
+        if (path == K3MOE_PATH_BLOCK_SCALED)
+            mx_decode_sync_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.clear0, &r.clear1);
         if ((e = launch_route_small(r, s))) return cuda_status(e);
         if (path != K3MOE_PATH_BLOCK_SCALED &&
             (e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s)))
@@ -781,6 +783,86 @@ k3moe_status k3moe_cache_read_stats(const void* state, void* stream, k3moe_cache
     return K3MOE_OK;
 }
 
+namespace {
+// k3moe_forward_host replays a cached CUDA graph of the forward when a call
+// repeats the last ones' arguments: its staging buffers sit at fixed offsets
+// of the workspace, so the same descriptor contents, workspace, token count,
+// stream and device mean the same kernels on the same addresses.  A graph
+// references the buffers, not their contents, so new weights written in
+// place are read by the next replay.  At most kHostGraphs entries, the least
+// recently used one replaced.
+struct HostGraph {
+    k3moe_layer_desc desc;
+    const void* ws;
+    size_t ws_bytes;
+    int32_t T;
+    cudaStream_t s;
+    int dev;
+    cudaGraphExec_t exec;
+    uint64_t used;
+};
+constexpr int kHostGraphs = 8;
+std::mutex g_host_mu;
+HostGraph g_host[kHostGraphs] = {};
+uint64_t g_host_clock = 0;
+
+bool same_key(const HostGraph& h, const k3moe_layer_desc* d, const void* ws, size_t ws_bytes, int32_t T,
+              cudaStream_t s, int dev) {
+    return h.exec && h.ws == ws && h.ws_bytes == ws_bytes && h.T == T && h.s == s && h.dev == dev &&
+           std::memcmp(&h.desc, d, sizeof(k3moe_layer_desc)) == 0;
+}
+
+// the cached graph for these arguments, or null
+cudaGraphExec_t host_graph_find(const k3moe_layer_desc* d, const void* ws, size_t ws_bytes, int32_t T,
+                                cudaStream_t s, int dev) {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    for (auto& h : g_host)
+        if (same_key(h, d, ws, ws_bytes, T, s, dev)) {
+            h.used = ++g_host_clock;
+            return h.exec;
+        }
+    return nullptr;
+}
+
+// capture the forward (nothing runs) on a private stream and keep the graph
+void host_graph_add(const k3moe_layer_desc* d, const uint16_t* in_dev, int32_t T, uint16_t* out_dev, void* ws,
+                    size_t need, size_t ws_bytes, cudaStream_t s, int dev) {
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+    if (ok) {
+        ok = k3moe_forward(d, in_dev, T, out_dev, ws, need, cs) == K3MOE_OK;
+        ok = cudaStreamEndCapture(cs, &g) == cudaSuccess && ok;
+    }
+    ok = ok && cudaGraphInstantiate(&exec, g, 0) == cudaSuccess;
+    if (g) cudaGraphDestroy(g);
+    cudaStreamDestroy(cs);
+    if (!ok) {
+        if (exec) cudaGraphExecDestroy(exec);
+        cudaGetLastError();
+        return;
+    }
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostGraph* slot = &g_host[0];
+    for (auto& h : g_host)
+        if (!h.exec || h.used < slot->used) slot = &h;
+    if (slot->exec) cudaGraphExecDestroy(slot->exec);
+    slot->desc = *d;
+    slot->ws = ws;
+    slot->ws_bytes = ws_bytes;
+    slot->T = T;
+    slot->s = s;
+    slot->dev = dev;
+    slot->exec = exec;
+    slot->used = ++g_host_clock;
+}
+}  // namespace
+
 k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hidden_host,
                                 int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes,
                                 void* stream) {
@@ -796,9 +878,22 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
     uint16_t* in_dev = reinterpret_cast<uint16_t*>(base + need);
     uint16_t* out_dev = reinterpret_cast<uint16_t*>(base + need + stage / 2);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return K3MOE_ERR_CUDA;
+    // a graph only when nothing else would record this forward: no tracing and
+    // no capture of the caller's stream
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool plain = g_trace.mode == 0 && g_inject == 0 && cudaStreamIsCapturing(s, &cap) == cudaSuccess &&
+                       cap == cudaStreamCaptureStatusNone;
     if (cudaMemcpyAsync(in_dev, hidden_host, bytes, cudaMemcpyHostToDevice, s)) return K3MOE_ERR_CUDA;
-    st = k3moe_forward(desc, in_dev, T, out_dev, ws, need, stream);
-    if (st != K3MOE_OK) return st;
+    cudaGraphExec_t exec = plain ? host_graph_find(desc, ws, ws_bytes, T, s, dev) : nullptr;
+    if (exec) {
+        if (cudaGraphLaunch(exec, s) != cudaSuccess) return K3MOE_ERR_CUDA;
+    } else {
+        st = k3moe_forward(desc, in_dev, T, out_dev, ws, need, stream);
+        if (st != K3MOE_OK) return st;
+        if (plain) host_graph_add(desc, in_dev, T, out_dev, ws, need, ws_bytes, s, dev);
+    }
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s)) return K3MOE_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
 }

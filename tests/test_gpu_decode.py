@@ -114,6 +114,35 @@ def test_forward_host_buffers(k3):
     assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
 
 
+def test_forward_host_repeated_calls(k3):
+    """k3moe_forward_host replays a cached graph when its arguments repeat:
+    new inputs copied in each call, weights rewritten in place (W2 scales + 1
+    doubles the output bit-exactly), and a second workspace (a new key) all
+    give what k3moe_forward gives."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=3, E=32, k=4, d=512, f=512, seed_index=36)
+    layer, dense, expert, ex = make_layer(cfg, path=1)
+    big = synth.custom(cfg.name, T=3 * 4, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, seed_index=37)
+    xs = synth.hidden(big).reshape(4, 3, -1)
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, 3) + k3.k3moe_host_staging_size(layer, 3))
+    ws2 = k3.workspace(k3.k3moe_workspace_size(layer, 3) + k3.k3moe_host_staging_size(layer, 3))
+    out_host = torch.empty((3, cfg.d), dtype=torch.bfloat16).pin_memory()
+    for i, x in enumerate(xs):
+        x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        want = k3.k3moe_forward(layer, x_host.cuda()).cpu()
+        for w in (ws, ws, ws2):
+            k3.k3moe_forward_host(layer, x_host, out_host=out_host, ws=w)
+            assert torch.equal(out_host.view(torch.int16), want.view(torch.int16)), i
+        if i == 1:
+            ex["w2_s"].add_(1)  # in place: the cached graphs read the new scales
+            want2 = k3.k3moe_forward(layer, x_host.cuda()).cpu()
+            assert torch.equal(want2.float(), 2 * want.float())
+            k3.k3moe_forward_host(layer, x_host, out_host=out_host, ws=ws)
+            assert torch.equal(out_host.view(torch.int16), want2.view(torch.int16))
+            ex["w2_s"].sub_(1)
+
+
 def test_graph_replay_matches_forward(k3):
     """k3moe_graph_create / k3moe_graph_launch reproduce k3moe_forward bit for bit."""
     import torch
