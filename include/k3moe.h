@@ -334,6 +334,21 @@ size_t k3moe_workspace_size(const k3moe_layer_desc* desc, int32_t T_max);
 k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
                            uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* The experts and the combine of the layer on a selection the caller made
+ * (latent mode): no router runs; out[t] = sum_j wts[t,j] * expert_{idx[t,j]}(
+ * hidden[t]), summed in slot order, the expert path as k3moe_forward picks
+ * it.  For expert parallelism ([PR26185]: the pages place expert stacks
+ * across devices): a rank that holds experts [r E_l, (r + 1) E_l) runs this
+ * with a descriptor of its E_l experts, k = 1 and the rows other ranks sent
+ * it, each with the local index of its expert and its combine weight.
+ *   hidden [T, d] bf16, idx [T, k] int32 in [0, E), wts [T, k] fp32 (device),
+ *   out [T, d] bf16; ws as for k3moe_forward (k3moe_workspace_size).
+ * Errors: those of k3moe_forward; UNSUPPORTED in block mode; device:
+ * INVALID_ARG if an index is outside [0, E) (the output is then undefined). */
+k3moe_status k3moe_forward_routed(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                                  const int32_t* idx, const float* wts, uint16_t* out, void* ws,
+                                  size_t ws_bytes, void* stream);
+
 /* k3moe_forward on HOST buffers: copies hidden (host) to the device on
  * `stream`, runs the layer, copies out back to host memory and waits for the
  * stream.  Pinned host memory gives asynchronous copies; pageable memory

@@ -39,7 +39,8 @@ EXPORTS = (
     "k3moe_unpack_mxfp4",
     "k3moe_route_workspace_size", "k3moe_route", "k3moe_route_noalloc", "k3moe_permute",
     "k3moe_rmsnorm",
-    "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_host_staging_size",
+    "k3moe_gemm_bf16", "k3moe_workspace_size", "k3moe_forward", "k3moe_forward_routed",
+    "k3moe_host_staging_size",
     "k3moe_forward_host", "k3moe_forward_routing", "k3moe_forward_intermediates",
     "k3moe_get_status", "k3moe_trace",
     "k3moe_graph_create", "k3moe_graph_launch", "k3moe_graph_destroy",
@@ -118,6 +119,7 @@ def lib() -> ctypes.CDLL:
         "k3moe_gemm_bf16": ([vp, vp, i32, i32, i32, vp, i32, vp], ctypes.c_int),
         "k3moe_workspace_size": ([ctypes.POINTER(LayerDesc), i32], sz),
         "k3moe_forward": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz, vp], ctypes.c_int),
+        "k3moe_forward_routed": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "k3moe_host_staging_size": ([ctypes.POINTER(LayerDesc), i32], sz),
         "k3moe_forward_host": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, sz, vp], ctypes.c_int),
         "k3moe_forward_routing": ([ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, vp],
@@ -389,6 +391,23 @@ def k3moe_forward(layer: MoELayer, hidden, out=None, ws=None, stream=None):
         ws = workspace(k3moe_workspace_size(layer, T), hidden.device)
     _check(lib().k3moe_forward(ctypes.byref(layer.desc), _p(hidden), T, _p(out), _p(ws),
                                ws.numel(), _stream(stream)))
+    return out
+
+
+def k3moe_forward_routed(layer: MoELayer, hidden, idx, wts, out=None, ws=None, stream=None):
+    """The layer's experts and combine on the caller's selection: hidden [T, d]
+    bf16, idx [T, k] int32, wts [T, k] fp32 (device) -> out [T, d] bf16."""
+    hidden = _bf16(hidden, "hidden")
+    _dev(idx, "idx"), _dev(wts, "wts")
+    if idx.dtype != torch.int32 or wts.dtype != torch.float32:
+        raise TypeError("idx must be int32 and wts float32")
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = workspace(k3moe_workspace_size(layer, T), hidden.device)
+    _check(lib().k3moe_forward_routed(ctypes.byref(layer.desc), _p(hidden), T, _p(idx), _p(wts), _p(out),
+                                      _p(ws), ws.numel(), _stream(stream)))
     return out
 
 

@@ -565,13 +565,21 @@ k3moe_status check_cache(const k3moe_layer_desc* d, const k3moe_expert_cache* c,
     return K3MOE_OK;
 }
 
+// The forward; with idx_in / wts_in (device [T, k]) the caller's selection
+// replaces the router (latent mode only).
 k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache* cache,
                           const uint16_t* hidden, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
-                          void* stream) {
+                          void* stream, const int32_t* idx_in = nullptr, const float* wts_in = nullptr) {
     k3moe_status st = check_desc(desc);
     if (st != K3MOE_OK) return st;
     if (!hidden || !out || !ws || T < 1) return K3MOE_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(out) || !aligned16(ws)) return K3MOE_ERR_ALIGN;
+    const bool routed = idx_in != nullptr;
+    if (routed) {
+        if (!wts_in) return K3MOE_ERR_INVALID_ARG;
+        if (desc->D > 0) return K3MOE_ERR_UNSUPPORTED;
+        if (!aligned16(idx_in) || !aligned16(wts_in)) return K3MOE_ERR_ALIGN;
+    }
     const FwdPlan p = fwd_plan(desc, T);
     if (ws_bytes < p.total) return K3MOE_ERR_WORKSPACE;
     int path = desc->path;
@@ -634,8 +642,26 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     int32_t* perm = static_cast<int32_t*>(at(p.perm));
     int32_t* inv = static_cast<int32_t*>(at(p.inv));
     int32_t* active = static_cast<int32_t*>(at(p.active));
-    const bool fuse_prep = T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED && desc->D == 0;
-    if (T <= kDecodeMaxT) {
+    const bool fuse_prep = !routed && T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED && desc->D == 0;
+    if (routed) {
+        // the caller's selection: checked on the device by the histogram kernel
+        // (an expert outside [0, E) records INVALID_ARG), permuted, and for the
+        // fused decode kernel its per-unit words cleared
+        const size_t P = static_cast<size_t>(T) * desc->k;
+        if (cudaMemcpyAsync(r.idx, idx_in, P * 4, cudaMemcpyDeviceToDevice, s) ||
+            cudaMemcpyAsync(r.wts, wts_in, P * 4, cudaMemcpyDeviceToDevice, s))
+            return K3MOE_ERR_CUDA;
+        if ((e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s,
+                                1)))
+            return K3MOE_ERR_CUDA;
+        if (T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED) {
+            int32_t *done = nullptr, *ready = nullptr;
+            mx_decode_sync_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &done, &ready);
+            const size_t umax = static_cast<size_t>(std::min(desc->E, T * desc->k));
+            if (cudaMemsetAsync(done, 0, umax * 4, s) || cudaMemsetAsync(ready, 0, umax * 4, s))
+                return K3MOE_ERR_CUDA;
+        }
+    } else if (T <= kDecodeMaxT) {
         // decode needs only the active experts (listed by the top-k kernel); the
         // grouped path takes the full permutation
         r.active = path == K3MOE_PATH_BLOCK_SCALED ? active : nullptr;
@@ -747,6 +773,13 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
 k3moe_status k3moe_forward(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
                            uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
     return forward_impl(desc, nullptr, hidden, T, out, ws, ws_bytes, stream);
+}
+
+k3moe_status k3moe_forward_routed(const k3moe_layer_desc* desc, const uint16_t* hidden, int32_t T,
+                                  const int32_t* idx, const float* wts, uint16_t* out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+    if (!idx || !wts) return K3MOE_ERR_INVALID_ARG;
+    return forward_impl(desc, nullptr, hidden, T, out, ws, ws_bytes, stream, idx, wts);
 }
 
 size_t k3moe_cache_state_size(int32_t E, int32_t slots) {

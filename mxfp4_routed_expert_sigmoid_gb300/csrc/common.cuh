@@ -381,9 +381,11 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_logits_simt(const RouteArgs& a, cudaStream_t s);
 // permutation of any T (chunked, deterministic); scratch >= permute_scratch_bytes
 size_t permute_scratch_bytes(int T, int E);
+// clamp = 1: idx is library-owned scratch; an entry outside [0, E) is recorded
+// and rewritten to 0 (else it is recorded and left out of the permutation)
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
-                           void* scratch, WsHeader* hdr, cudaStream_t s);
+                           void* scratch, WsHeader* hdr, cudaStream_t s, int clamp = 0);
 
 cudaError_t launch_rmsnorm(const uint16_t* h, int T, int D, const uint16_t* gamma, float eps,
                            uint16_t* out, cudaStream_t s);

@@ -413,8 +413,8 @@ logits_simt_kernel(RouteArgs a) {
 constexpr int kChunk = 64;  // tokens per chunk
 
 __global__ void __launch_bounds__(256)
-perm_count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* chunk_cnt,
-                  WsHeader* hdr, uint64_t* st) {
+perm_count_kernel(int32_t* __restrict__ idx, int T, int k, int E, int32_t* chunk_cnt, WsHeader* hdr,
+                  int clamp, uint64_t* st) {
     StampScope stamp(st);
     extern __shared__ int hist[];
     const int c = blockIdx.x;
@@ -422,11 +422,16 @@ perm_count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t*
     __syncthreads();
     const int t0 = c * kChunk, t1 = min(T, t0 + kChunk);
     for (int p = t0 * k + threadIdx.x; p < t1 * k; p += blockDim.x) {
-        const int e = idx[p];
-        if (e >= 0 && e < E)
-            atomicAdd(&hist[e], 1);
-        else
+        int e = idx[p];
+        if (e < 0 || e >= E) {
+            // an expert outside [0, E): recorded; with clamp (a selection copied into
+            // the workspace) the entry becomes expert 0, so every later index stays in range
             set_error(hdr, K3MOE_ERR_INVALID_ARG, 2);
+            if (!clamp) continue;
+            e = 0;
+            idx[p] = 0;
+        }
+        atomicAdd(&hist[e], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -602,7 +607,7 @@ size_t permute_scratch_bytes(int T, int E) {
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
-                           void* scratch, WsHeader* hdr, cudaStream_t s) {
+                           void* scratch, WsHeader* hdr, cudaStream_t s, int clamp) {
     const int nchunks = (T + kChunk - 1) / kChunk;
     int32_t* chunk = static_cast<int32_t*>(scratch);
     const size_t smem = static_cast<size_t>(E) * sizeof(int);
@@ -615,7 +620,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
     if (2 * smem > 48 * 1024)
         cudaFuncSetAttribute(perm_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(2 * smem));
-    perm_count_kernel<<<nchunks, 256, smem, s>>>(idx, T, k, E, chunk, hdr, trace_stamp("perm_count"));
+    perm_count_kernel<<<nchunks, 256, smem, s>>>(const_cast<int32_t*>(idx), T, k, E, chunk, hdr, clamp,
+                                                 trace_stamp("perm_count"));
     trace_mark("perm_count", s);
     perm_scan_kernel<<<1, 256, 2 * smem, s>>>(chunk, nchunks, E, T * k, counts, offsets, active,
                                               trace_stamp("perm_scan"));

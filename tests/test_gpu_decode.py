@@ -179,7 +179,7 @@ def test_trace_of_graph_replay(k3):
     tr = k3.k3moe_trace_read()
     torch.cuda.synchronize()
     names = [n for n, _ in tr]
-    assert "route_small" in names and "decode_up" in names and "combine" in names
+    assert "route_small" in names and "decode_experts" in names and "combine" in names
     assert all(ms > 0 for _, ms in tr)
     graph.close()
 
@@ -302,3 +302,50 @@ def test_lowest_binade_activation_block(k3, path):
     dense["hidden"] = synth.f32_to_bf16_bits(h)
     out, _, _ = run_and_compare(k3, cfg, path, layer_bundle=(layer, dense, expert, ex))
     assert np.all(np.isfinite(bf16_tensor_to_np(out)))
+
+
+@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (40, 1), (40, 2)])
+def test_forward_routed_matches_forward(k3, T, path):
+    """k3moe_forward_routed on the selection a k3moe_forward made reproduces
+    that forward bit for bit (the same expert kernels on the same inputs)."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=T, E=32, k=4, d=512, f=512, seed_index=38)
+    layer, dense, expert, _ = make_layer(cfg, path=path)
+    x = to_dev(dense["hidden"], "cuda")
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, T))
+    ref = k3.k3moe_forward(layer, x, ws=ws).clone()
+    idx, w, _ = k3.k3moe_forward_routing(layer, ws, T)
+    idx, w = idx.clone(), w.clone()
+    out = k3.k3moe_forward_routed(layer, x, idx, w, ws=ws)
+    assert k3.k3moe_get_status(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("R", [3, 50])
+def test_forward_routed_one_expert_per_row(k3, R):
+    """The expert-parallel receive side: rows that each carry one local expert
+    and its weight (k = 1), checked against the oracle's expert FFN."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=R, E=16, k=1, d=512, f=512, seed_index=39)
+    layer, dense, expert, _ = make_layer(cfg, path=0)
+    rng = np.random.default_rng(R)
+    idx = rng.integers(0, cfg.E, size=(R, 1)).astype(np.int32)
+    wts = rng.uniform(0.05, 0.6, size=(R, 1)).astype(np.float32)
+    x = to_dev(dense["hidden"], "cuda")
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, R))
+    out = k3.k3moe_forward_routed(layer, x, torch.from_numpy(idx).cuda(), torch.from_numpy(wts).cuda(), ws=ws)
+    assert k3.k3moe_get_status(ws) == 0
+    xr = oracle.bf16_to_f64(dense["hidden"])
+    ref = np.zeros_like(xr)
+    for e in np.unique(idx):
+        rows = np.nonzero(idx[:, 0] == e)[0]
+        W = [oracle.decode_source(*expert(m, int(e))) for m in range(3)]
+        ref[rows] = wts[rows, :1].astype(np.float64) * oracle.expert_ffn(xr[rows], *W)
+    err = rel_err_rows(bf16_tensor_to_np(out), ref)
+    record_margin(f"routed k=1 R={R}", err, TOL)
+    assert np.all(err <= TOL)
+    bad = torch.from_numpy(np.full((R, 1), cfg.E, np.int32)).cuda()  # outside [0, E)
+    k3.k3moe_forward_routed(layer, x, bad, torch.from_numpy(wts).cuda(), ws=ws)
+    assert k3.k3moe_get_status(ws) == 1
