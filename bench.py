@@ -317,13 +317,11 @@ def stamp_pass(k3, layer, pool, out, ws, order, flush, stream):
     k3.k3moe_trace(2)
     graphs = {i: k3.ForwardGraph(layer, pool[i], out, ws) for i in sorted(set(order))}
     k3.k3moe_trace(0)
-    per, spans, names = {}, [], None
+    per, spans, marks = {}, [], {}
     for i in order:
         flush.zero_()
         graphs[i].launch(stream)
         st = k3.k3moe_trace_read_stamps()
-        if names is None:
-            names = [n for n, _, _ in st]
         seen = {}
         for n, a, b in st:
             if a < 0:
@@ -332,11 +330,15 @@ def stamp_pass(k3, layer, pool, out, ws, order, flush, stream):
             seen[n] = c + 1
             key = n if c == 0 else f"{n}#{c}"
             per.setdefault(key, []).append((b - a) * 1e-3)
+            marks.setdefault(key, []).append((a, b))
         spans.append(max(b for _, _, b in st) * 1e-3)
     torch.cuda.synchronize()
     del graphs
     mean = {n: sum(v) / len(v) for n, v in per.items()}
-    return mean, sum(spans) / len(spans)
+    # mean start / end (us after the forward's first kernel start) per kernel
+    timeline = {n: [round(sum(a for a, _ in v) / len(v), 2), round(sum(b for _, b in v) / len(v), 2)]
+                for n, v in marks.items()}
+    return mean, sum(spans) / len(spans), timeline
 
 
 def algorithmic_work(cfg, u_mean, mb):
@@ -345,7 +347,6 @@ def algorithmic_work(cfg, u_mean, mb):
     GEMMs (2 m n k)."""
     T, k, d, f = cfg.T, cfg.k, cfg.d, cfg.f
     bytes_ = {
-        "decode_experts": u_mean * 3 * mb,
         "decode_up": u_mean * 2 * mb, "decode_down": u_mean * mb,
         "units_up": u_mean * 2 * mb, "units_down": u_mean * mb,
         "route_small": cfg.E * cfg.d_router * 2 + T * cfg.d_router * 2 + T * cfg.E * 4,
@@ -436,7 +437,7 @@ def measure(k3, cfg, args, dev, world, steps, warmup, peaks):
     total_ms = sum(a.elapsed_time(b) for a, b in evs)
     del graphs
 
-    kern, span = stamp_pass(k3, layer, pool, out, ws_f, order, flush, stream)
+    kern, span, timeline = stamp_pass(k3, layer, pool, out, ws_f, order, flush, stream)
 
     # ---- end to end through the host-buffer entry point ----
     width = layer.width
@@ -477,6 +478,7 @@ def measure(k3, cfg, args, dev, world, steps, warmup, peaks):
         "kernels_ms": kern,
         "kernels_ms_source": "device stamps inside graph replays of the same steps",
         "forward_span_ms": span,
+        "timeline_us": timeline,
         "roofline": roof,
         "e2e": {"value": cfg.T * steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": io,
                 "d2h_bytes_per_step": io},

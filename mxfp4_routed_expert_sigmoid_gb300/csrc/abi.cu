@@ -645,8 +645,8 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
     const bool fuse_prep = !routed && T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED && desc->D == 0;
     if (routed) {
         // the caller's selection: checked on the device by the histogram kernel
-        // (an expert outside [0, E) records INVALID_ARG), permuted, and for the
-        // fused decode kernel its per-unit words cleared
+        // (an expert outside [0, E) records INVALID_ARG and becomes expert 0)
+        // and permuted (the permutation also lists the active experts)
         const size_t P = static_cast<size_t>(T) * desc->k;
         if (cudaMemcpyAsync(r.idx, idx_in, P * 4, cudaMemcpyDeviceToDevice, s) ||
             cudaMemcpyAsync(r.wts, wts_in, P * 4, cudaMemcpyDeviceToDevice, s))
@@ -654,21 +654,12 @@ k3moe_status forward_impl(const k3moe_layer_desc* desc, const k3moe_expert_cache
         if ((e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s,
                                 1)))
             return K3MOE_ERR_CUDA;
-        if (T <= kDecodeMaxT && path == K3MOE_PATH_BLOCK_SCALED) {
-            int32_t *done = nullptr, *ready = nullptr;
-            mx_decode_sync_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &done, &ready);
-            const size_t umax = static_cast<size_t>(std::min(desc->E, T * desc->k));
-            if (cudaMemsetAsync(done, 0, umax * 4, s) || cudaMemsetAsync(ready, 0, umax * 4, s))
-                return K3MOE_ERR_CUDA;
-        }
     } else if (T <= kDecodeMaxT) {
         // decode needs only the active experts (listed by the top-k kernel); the
         // grouped path takes the full permutation
         r.active = path == K3MOE_PATH_BLOCK_SCALED ? active : nullptr;
         if (fuse_prep)
             mx_decode_xq_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.xq, &r.xsf, &r.xq_n);
-        if (path == K3MOE_PATH_BLOCK_SCALED)
-            mx_decode_sync_slots(at(p.dec), T, desc->E, desc->k, desc->d, desc->f, &r.clear0, &r.clear1);
         if ((e = launch_route_small(r, s))) return cuda_status(e);
         if (path != K3MOE_PATH_BLOCK_SCALED &&
             (e = launch_permute(r.idx, T, desc->k, desc->E, counts, offsets, perm, inv, active, at(p.chunk), hdr, s)))

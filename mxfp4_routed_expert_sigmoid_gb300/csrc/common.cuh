@@ -348,11 +348,6 @@ struct RouteArgs {
     // decode: the ascending experts that received any token, count at [E]
     // (written by the small-T top-k kernel; null = not wanted)
     int32_t* active;   // [E + 1]
-    // decode: per-unit words of the fused expert kernel (progress counters and
-    // readiness flags), zeroed for the units of this call when the active list
-    // is written (null: none)
-    int32_t* clear0;
-    int32_t* clear1;
     // optional (decode, latent mode): the router input quantised for the
     // block-scaled expert kernels (codes [d_r / 256][xq_n][128], scale atoms
     // [d_r / 128][512]); the CTAs share the work
@@ -419,9 +414,6 @@ size_t mx_decode_scratch_bytes(int T, int E, int k, int d, int f);
 // where the decode scratch keeps the quantised token rows (router output)
 void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_t** xq, uint8_t** xsf,
                         int* N);
-// where the decode scratch keeps the fused kernel's per-unit words (the top-k
-// kernel zeroes them for the call's units)
-void mx_decode_sync_slots(void* scratch, int T, int E, int k, int d, int f, int32_t** done, int32_t** ready);
 cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s);
 // unit-grouped streaming forward (more tokens, few per expert): the experts'
 // sorted token lists (from the permutation) are cut into units of at most 16

@@ -692,10 +692,10 @@ __device__ __forceinline__ void finish_item(const float* __restrict__ part, size
     }
 }
 
-// The finish step as a kernel (unit-grouped path, ggml weights): one warp per
-// (unit, token, 256-wide chunk), grid-strided over the units (the grid is
-// sized for the SMs, not for the largest possible number of units).  Tokens a
-// unit does not have are skipped: their MMA columns are never read.
+// The finish step: one warp per (unit, token, 256-wide chunk), grid-strided
+// over the units (the grid is sized for the SMs, not for the largest possible
+// number of units).  Tokens a unit does not have are skipped: their MMA
+// columns are never read.
 template <int TERMS>
 __global__ void __launch_bounds__(256)
 mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
@@ -718,404 +718,6 @@ mx_finish_kernel(const float* __restrict__ part, int umax, int T, int f, int N,
         const int t = rr / KC, c = rr - t * KC;
         if (ucnt && t >= ucnt[u]) continue;
         finish_item<TERMS>(part, plane, T, f, N, u, t, c, hq, hsf, lane);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Fused decode stream (T <= 8): the W1/W3 pass and the W2 pass of the active
-// experts in one launch, one ring, one ramp and one tail.
-//
-// Each CTA takes a stream-K range of the up pass (active expert, matrix, row
-// tile, stage) and then a range of the down pass, and pushes both through
-// its ring in that order.  The producer runs two cursors: the weight side
-// (codes and scales) of a stage is issued as soon as its ring slot is free,
-// whatever the pass, because the weights depend on nothing; the activation
-// side (token terms in the up pass, h terms in the down pass) of a down stage
-// waits until that expert's h is ready.  h of expert u is formed by the four
-// finish warps of CTA u % grid: the epilogue adds the stages of every up
-// segment it writes to done[u] (after its partial sums are visible), and
-// when all of the expert's up stages are in, the finish warps compute
-// h = silu(g) * u from both partial slots, quantise it to E2M1 terms and set
-// ready[u].  The top-k kernel zeroes done[] and ready[] of the call's experts.
-// The result is that of the separate up, finish and down kernels, bit for
-// bit.  Every wait is bounded; on expiry the CTA records K3MOE_ERR_TIMEOUT,
-// gives each stage whose activation side was never issued its missing
-// arrival, waits for its copies in flight and releases TMEM, and a finish
-// group that gives up still sets ready[] so that no other CTA waits longer.
-// ---------------------------------------------------------------------------
-constexpr int kFuseThreads = kMxThreads + 128;  // + four finish warps (7 .. 10)
-constexpr int kFinishBar = 2;                   // their named barrier
-
-struct FuseArgs {
-    MxArgs pass[2];  // 0: W1 and W3 (up), 1: W2 (down); same N and stage layout
-    int32_t* done;   // [umax] up stages written per unit, counted by each of the 4 epilogue warps
-    int32_t* ready;  // [umax] 1 once the unit's h terms are written
-    int f;           // expert hidden width (the h rows)
-};
-
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(int32_t* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// later async-proxy reads (bulk copies) see the global writes this thread has observed
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-template <int TERMS, int WF>
-__global__ void __launch_bounds__(kFuseThreads, 1)
-mx_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
-                const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmS3,
-                const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmS2, FuseArgs fa) {
-    constexpr bool CANON = WF == kWfCanon;
-    static_assert(WF != kWfGgml, "ggml blocks use the separate kernels");
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
-    __shared__ uint32_t tmem_holder;
-    __shared__ int abort_s;
-    volatile int* abort_flag = &abort_s;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const MxArgs& P0 = fa.pass[0];
-    const MxArgs& P1 = fa.pass[1];
-    auto P = [&](int pass) -> const MxArgs& { return pass == 0 ? P0 : P1; };
-    const uint32_t NB = static_cast<uint32_t>(P0.N) * 128;  // B bytes per chunk
-    // stage layout: A chunks | B chunks | SFA atoms (2 per chunk) | SFB atoms [| canonical scale rows]
-    const uint32_t offB = kStageA, offSA = kStageA + kChunks * NB, offSB = offSA + kChunks * 1024;
-    const uint32_t offRaw = offSB + kChunks * 1024;
-    const uint32_t stage_bytes = P0.stage_bytes;
-    const int RS = P0.RS;
-    const uint64_t lim = P0.inject ? 1000000ull : kWaitLimitNs;
-    WsHeader* hdr = P0.hdr;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < RS; ++s) {
-            mbar_init(&full[s], 2);   // weight side and activation side, each with its bytes
-            mbar_init(&empty[s], 2);  // one commit per MMA issuer
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], 2);
-            mbar_init(&acc_empty[a], 4);
-        }
-        abort_s = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        fence_proxy_async();
-    }
-    if (warp == 1) tmem_alloc(&tmem_holder, kTmemCols);
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmA3);
-        prefetch_tmap(&tmA2);
-        if (CANON) {
-            prefetch_tmap(&tmS);
-            prefetch_tmap(&tmS3);
-            prefetch_tmap(&tmS2);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_holder;
-
-    // the top-k kernel wrote the active list and cleared done[] / ready[]
-    pdl_wait();
-    pdl_trigger();
-    stamp_start(P0.st);
-    const int U = *P0.count;
-    const long long W0 = static_cast<long long>(U) * P0.nmat * P0.tiles * P0.KS;
-    const long long W1 = static_cast<long long>(U) * P1.nmat * P1.tiles * P1.KS;
-    const int u0 = static_cast<int>(W0 * blockIdx.x / gridDim.x), u1 = static_cast<int>(W0 * (blockIdx.x + 1) / gridDim.x);
-    const int d0 = static_cast<int>(W1 * blockIdx.x / gridDim.x), d1 = static_cast<int>(W1 * (blockIdx.x + 1) / gridDim.x);
-    const int n0 = u1 - u0, n = n0 + (d1 - d0);
-    const bool drop_first = P0.inject && blockIdx.x == 0 && n0 > 0;  // test aid
-
-    auto issue_a = [&](int pass, const Cursor& c, int e, uint8_t* st, uint64_t* bar) {
-        const MxArgs& p = P(pass);
-        const int c0 = c.ks * kChunks;
-        const int nch = min(kChunks, p.KC - c0);
-        const CUtensorMap* tm = pass == 1 ? &tmA2 : (c.mat == 0 ? &tmA : &tmA3);
-        const int y = e * p.rows + c.tile * 128;
-        for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
-        if constexpr (CANON) {
-            tma_load_2d(st + offRaw, pass == 1 ? &tmS2 : (c.mat == 0 ? &tmS : &tmS3), bar, c.ks * 16, y);
-        } else {
-            const int g0 = 2 * c0, ng = min(2 * kChunks, p.G - g0);
-            bulk_load(st + offSA, p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.G + g0) * 512,
-                      ng * 512, bar);
-        }
-    };
-    auto a_bytes = [&](int pass, const Cursor& c) {
-        const MxArgs& p = P(pass);
-        const int c0 = c.ks * kChunks;
-        const int nch = min(kChunks, p.KC - c0);
-        const int sfb = CANON ? kRawSf : min(2 * kChunks, p.G - 2 * c0) * 512;
-        return static_cast<uint32_t>(nch * kChunkA + sfb);
-    };
-    auto issue_b = [&](int pass, const Cursor& c, uint8_t* st, uint64_t* bar) {
-        const MxArgs& p = P(pass);
-        const int c0 = c.ks * kChunks;
-        const int nch = min(kChunks, p.KC - c0);
-        mbar_expect_tx(bar, static_cast<uint32_t>(nch) * (NB + 1024));
-        bulk_load(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, bar);
-        bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024, bar);
-    };
-
-    if (warp == 0) {
-        if (lane == 0 && n > 0) {
-            // ------------------------------ producer ------------------------------
-            int ja = 0, jb = 0, sa = 0, sb = 0;
-            uint32_t pha = 0;
-            int pa = n0 > 0 ? 0 : 1, pb = pa;
-            Cursor ca(pa == 0 ? u0 : d0, P(pa)), cb = ca;
-            int ea = weight_slot(P(pa), P(pa).active[ca.u]);
-            int seen = -1;  // the last down-pass unit whose h was seen ready
-            uint64_t t_prog = global_ns();
-            while (jb < n) {
-                bool prog = false;
-                if (ja < n && mbar_try_wait(&empty[sa], pha ^ 1)) {
-                    uint8_t* st = smem + static_cast<size_t>(sa) * stage_bytes;
-                    if (!(drop_first && ja == 0)) {
-                        mbar_expect_tx(&full[sa], a_bytes(pa, ca));
-                        issue_a(pa, ca, ea, st, &full[sa]);
-                    }
-                    if (++sa == RS) {
-                        sa = 0;
-                        pha ^= 1;
-                    }
-                    if (++ja == n0) {
-                        pa = 1;
-                        ca = Cursor(d0, P1);
-                        if (ja < n) ea = weight_slot(P1, P1.active[ca.u]);
-                    } else if (ja < n) {
-                        const int up = ca.u;
-                        ca.next(P(pa));
-                        if (ca.u != up) ea = weight_slot(P(pa), P(pa).active[ca.u]);
-                    }
-                    prog = true;
-                }
-                if (jb < ja) {
-                    bool ok = true;
-                    if (pb == 1 && cb.u != seen) {
-                        ok = ld_acquire(fa.ready + cb.u) != 0;
-                        if (ok) {
-                            fence_proxy_async_global();  // the bulk copies read h written by another SM
-                            seen = cb.u;
-                        }
-                    }
-                    if (ok) {
-                        if (!(drop_first && jb == 0))
-                            issue_b(pb, cb, smem + static_cast<size_t>(sb) * stage_bytes, &full[sb]);
-                        if (++sb == RS) sb = 0;
-                        if (++jb == n0) {
-                            pb = 1;
-                            cb = Cursor(d0, P1);
-                        } else if (jb < n) {
-                            cb.next(P(pb));
-                        }
-                        prog = true;
-                    }
-                }
-                if (prog) {
-                    t_prog = global_ns();
-                } else {
-                    if (*abort_flag) break;
-                    if (global_ns() - t_prog > lim) {
-                        *abort_flag = 1;
-                        set_error(hdr, K3MOE_ERR_TIMEOUT, 80);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            // after an abort: stages whose activation side was never issued get the
-            // missing arrival, then every issued copy lands before the CTA exits
-            for (int j = jb; j < ja; ++j)
-                if (!(drop_first && j == 0)) mbar_arrive(&full[j % RS]);
-            for (int j = ja > RS ? ja - RS : 0; j < ja; ++j) {
-                if (drop_first && j == 0) continue;  // nothing was issued for it
-                const uint64_t t0 = global_ns();
-                while (!mbar_try_wait(&full[j % RS], (j / RS) & 1) && global_ns() - t0 < kWaitLimitNs) {
-                }
-            }
-        }
-    } else if (warp == 1 || warp == 6) {
-        if (n > 0) {
-            // ------------------------------ MMA issuers ---------------------------
-            const int mt = warp == 1 ? 0 : 1;  // the stage's chunk this warp multiplies
-            int ks = Cursor(n0 > 0 ? u0 : d0, P(n0 > 0 ? 0 : 1)).ks;
-            int s = 0, seg = 0, ps = 0;
-            uint32_t ph = 0, pph = 0;
-            const uint32_t id0 = idesc_f4(128, P0.N, 0, 0);
-            const uint32_t slots = tmem + kSfBase + 128 * mt;
-            for (int i = 0, j = 0; j < n; ++i, ++j) {
-                const int pass = j < n0 ? 0 : 1;
-                const MxArgs& p = P(pass);
-                if (j == n0 && j > 0) ks = Cursor(d0, P1).ks;
-                const bool seg_start = j == 0 || j == n0 || ks == 0;
-                const bool seg_end = j + 1 == n0 || j + 1 == n || ks == p.KS - 1;
-                const int a = seg & 1;
-                bool ok = true;
-                if (lane == 0) {
-                    ok = !seg_start || mbar_wait(&acc_empty[a], ((seg >> 1) & 1) ^ 1, abort_flag, hdr, 81, lim);
-                    ok = ok && mbar_wait(&full[s], ph, abort_flag, hdr, 82, lim);
-                    ok = ok && (i == 0 || mbar_wait(&empty[ps], pph, abort_flag, hdr, 83, lim));
-                }
-                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-                if (i > 0 && ++ps == RS) {
-                    ps = 0;
-                    pph ^= 1;
-                }
-                tc_fence_after();
-                const int kv = p.K - (ks * kChunks + mt) * 256;  // inputs of this chunk (<= 0: none)
-                if (kv > 0) {
-                    uint8_t* stage = smem + static_cast<size_t>(s) * stage_bytes;
-                    if constexpr (CANON) {
-                        relay_sf(stage + offRaw, stage + offSA + 1024 * mt, mt, lane);
-                        fence_proxy_async();
-                        __syncwarp();
-                    }
-                    if (lane == 0) {
-                        const uint32_t st = smem_u32(stage);
-                        for (int h = 0; h < 2; ++h) {
-                            if (128 * h >= kv) break;
-                            tmem_cp_sf(slots + 64 * h, st + offSA + 512 * (2 * mt + h));
-                            tmem_cp_sf(slots + 64 * h + 32, st + offSB + 512 * (2 * mt + h));
-                        }
-                        const uint32_t d_t = tmem + (2 * a + mt) * kMaxN;
-                        const uint64_t ad = sw128_desc(st + mt * kChunkA), bd = sw128_desc(st + offB + mt * NB);
-                        const int nmma = min(4, kv / 64);
-                        for (int jj = 0; jj < nmma; ++jj) {
-                            const uint32_t sfa = slots + 64 * (jj >> 1);
-                            const uint32_t id = static_cast<uint32_t>(2 * (jj & 1));
-                            mma_f4(d_t, ad + 2 * jj, bd + 2 * jj, id0 | (id << 4) | (id << 29), sfa, sfa + 32,
-                                   (seg_start && jj == 0) ? 0u : 1u);
-                        }
-                    }
-                }
-                if (lane == 0) {
-                    mma_commit(&empty[s]);
-                    if (seg_end) mma_commit(&acc_full[a]);
-                }
-                if (seg_end) ++seg;
-                if (++s == RS) {
-                    s = 0;
-                    ph ^= 1;
-                }
-                if (++ks == p.KS) ks = 0;
-            }
-        }
-    } else if (warp >= kMxThreads / 32) {
-        // ------------------------------ finish ------------------------------------
-        const int fw = warp - kMxThreads / 32;
-        const int target = 4 * P0.nmat * P0.tiles * P0.KS;
-        const int KCf = (fa.f + 255) / 256;
-        const size_t plane = static_cast<size_t>(P0.umax) * P0.T * fa.f;
-        for (int u = blockIdx.x; u < U; u += gridDim.x) {
-            if (fw == 0 && lane == 0) {
-                const uint64_t t0 = global_ns();
-                while (ld_acquire(fa.done + u) < target) {
-                    if (global_ns() - t0 > lim) {
-                        set_error(hdr, K3MOE_ERR_TIMEOUT, 84);
-                        break;
-                    }
-                    __nanosleep(256);
-                }
-            }
-            named_bar_sync(kFinishBar, 128);
-            __threadfence();
-            for (int it = fw; it < P0.T * KCf; it += 4) {
-                const int t = it / KCf, c = it - t * KCf;
-                finish_item<TERMS>(P0.part, plane, P0.T, fa.f, P0.N, u, t, c, const_cast<uint8_t*>(P1.bq),
-                                   const_cast<uint8_t*>(P1.bsf), lane);
-            }
-            __threadfence();
-            named_bar_sync(kFinishBar, 128);
-            if (fw == 0 && lane == 0) st_release(fa.ready + u, 1);
-        }
-    } else if (n > 0) {
-        // ------------------------------ epilogue ---------------------------------
-        const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
-        int seg = 0;
-        for (int pass = 0; pass < 2; ++pass) {
-            const MxArgs& p = P(pass);
-            const int w0 = pass == 0 ? u0 : d0, w1 = pass == 0 ? u1 : d1;
-            if (w0 >= w1) continue;
-            Cursor c(w0, p);
-            bool aborted = false;
-            for (int w = w0; w < w1;) {
-                const int ks_begin = c.ks;
-                const int len = min(p.KS - c.ks, w1 - w);
-                const bool whole = ks_begin == 0 && len == p.KS;
-                const int a = seg & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (seg >> 1) & 1, abort_flag, hdr, 85, lim))) {
-                    aborted = true;
-                    break;
-                }
-                tc_fence_after();
-                const bool has_d1 = (p.KC % kChunks) == 0 || ks_begin < p.KS - 1;
-                float v[kMaxN];
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * a * kMaxN;
-#pragma unroll
-                for (int c16 = 0; c16 < kMaxN / 16; ++c16) {
-                    if (c16 * 16 < p.N) {
-                        float v16[16];
-                        tmem_ld16(taddr + c16 * 16, v16);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = v16[i];
-                        if (has_d1) {
-                            tmem_ld16(taddr + kMaxN + c16 * 16, v16);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[c16 * 16 + i] += v16[i];
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[c16 * 16 + i] = 0.0f;
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[a]);
-                const int mat = c.mat, mats = p.nmat;
-                const int row = c.tile * 128 + q * 32 + lane;
-                if (row < p.rows) {
-                    const size_t plane = static_cast<size_t>(p.umax) * p.T * p.rows_out;
-                    float* dst = p.part + static_cast<size_t>((ks_begin == 0 ? 0 : 1) * mats + mat) * plane +
-                                 static_cast<size_t>(c.u) * p.T * p.rows_out + row;
-#pragma unroll
-                    for (int t = 0; t < kMaxN / TERMS; ++t) {
-                        if (t >= p.T) break;
-                        float sum = 0.0f;
-#pragma unroll
-                        for (int j = 0; j < TERMS; ++j) sum += v[TERMS * t + j];
-                        dst[static_cast<size_t>(t) * p.rows_out] = sum;
-                        if (whole) dst[static_cast<size_t>(mats) * plane + static_cast<size_t>(t) * p.rows_out] = 0.0f;
-                    }
-                }
-                if (pass == 0) {
-                    // this warp's rows of the segment are written: count its stages
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) atomicAdd(fa.done + c.u, len);
-                }
-                w += len;
-                ++seg;
-                c.next_segment(p);
-            }
-            if (aborted) break;
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    stamp_end(P0.st);
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -1408,7 +1010,6 @@ int kc256(int K) { return (K + 255) / 256; }
 struct MxScratch {
     uint8_t *xq, *xsf, *hq, *hsf;
     float *up, *y;
-    int32_t *done, *ready;  // fused kernel: per-unit progress and h readiness
     int umax, N;
     size_t bytes;
 };
@@ -1433,8 +1034,6 @@ MxScratch mx_carve(void* scratch, int T, int E, int k, int d, int f) {
     m.hq = reinterpret_cast<uint8_t*>(take(U * kc256(f) * m.N * 128));
     m.hsf = reinterpret_cast<uint8_t*>(take(U * kc256(f) * 1024));
     m.y = reinterpret_cast<float*>(take(2 * U * T * d * 4));
-    m.done = reinterpret_cast<int32_t*>(take(U * 4));
-    m.ready = reinterpret_cast<int32_t*>(take(U * 4));
     m.bytes = o;
     return m;
 }
@@ -1444,31 +1043,6 @@ void ring_shape(MxArgs* p, int wf) {
     const size_t raw = wf == kWfCanon ? kRawSf : 0;
     p->stage_bytes = static_cast<uint32_t>(align_up(kStageA + kChunks * (p->N * 128 + 2048) + raw, 1024));
     p->RS = std::min(kMaxStages, static_cast<int>((226 * 1024) / p->stage_bytes));
-}
-
-template <int TERMS, int WF>
-cudaError_t launch_fused(const CUtensorMap (&q)[3], const CUtensorMap (&sc)[3], FuseArgs fa, int grid,
-                         cudaStream_t s) {
-    ring_shape(&fa.pass[0], WF);
-    fa.pass[1].stage_bytes = fa.pass[0].stage_bytes;
-    fa.pass[1].RS = fa.pass[0].RS;
-    if (fa.pass[0].RS < 2 || fa.pass[0].N > kMaxN) return cudaErrorNotSupported;
-    const size_t smem = 1024 + static_cast<size_t>(fa.pass[0].RS) * fa.pass[0].stage_bytes;
-    static std::atomic<int> set_bytes[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::atomic<int>& cur = set_bytes[dev & 63];
-    if (cur.load() < static_cast<int>(smem)) {
-        const cudaError_t e = cudaFuncSetAttribute(mx_fused_kernel<TERMS, WF>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        cur.store(static_cast<int>(smem));
-    }
-    fa.pass[0].st = trace_stamp("decode_experts");
-    const cudaError_t e = launch_pdl(mx_fused_kernel<TERMS, WF>, dim3(grid), dim3(kFuseThreads), smem, s, q[0], q[1],
-                                     sc[0], sc[1], q[2], sc[2], fa);
-    trace_mark("decode_experts", s);
-    return e;
 }
 
 template <int TERMS, int WF>
@@ -1596,11 +1170,6 @@ void mx_decode_xq_slots(void* scratch, int T, int E, int k, int d, int f, uint8_
     *N = m.N;
 }
 
-void mx_decode_sync_slots(void* scratch, int T, int E, int k, int d, int f, int32_t** done, int32_t** ready) {
-    const MxScratch m = mx_carve(scratch, T, E, k, d, f);
-    *done = m.done;
-    *ready = m.ready;
-}
 
 cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     const MxScratch m = mx_carve(a.scratch, a.T, a.E, a.k, a.d, a.f);
@@ -1645,28 +1214,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     dn.umax = m.umax;
     dn.hdr = a.hdr;
 
-    dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
-    if (!a.ggml) {
-        // one launch for both passes (the finish step inside); every CTA's ranges
-        // must be at least one tile long: at least k experts are active
-        FuseArgs fa{};
-        fa.pass[0] = up;
-        fa.pass[1] = dn;
-        fa.done = m.done;
-        fa.ready = m.ready;
-        fa.f = a.f;
-        const int grid = std::min(a.num_sms, a.k * std::min(up.nmat * up.tiles, dn.tiles));
-        e = wm.wf == kWfCanon ? launch_fused<kTerms, kWfCanon>(wm.q, wm.sc, fa, grid, s)
-                              : launch_fused<kTerms, kWfAtoms>(wm.q, wm.sc, fa, grid, s);
-        if (e) return e;
-        e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
-                       m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, static_cast<const int32_t*>(nullptr),
-                       a.out, trace_stamp("combine"));
-        trace_mark("combine", s);
-        return e;
-    }
-
-    // ggml blocks: up pass, finish kernel, down pass
+    // every CTA's range must be at least one tile long: at least k experts are active
     const int grid_up = std::min(a.num_sms, a.k * up.nmat * up.tiles);
     if ((e = launch_stream_wf<kTerms>(wm, true, up, grid_up, s, "decode_up"))) return e;
 
@@ -1681,6 +1229,7 @@ cudaError_t launch_mx_decode(const MxDecodeArgs& a, cudaStream_t s) {
     const int grid_dn = std::min(a.num_sms, a.k * dn.tiles);
     if ((e = launch_stream_wf<kTerms>(wm, false, dn, grid_dn, s, "decode_down"))) return e;
 
+    dim3 cgrid((a.d + kCombineCols - 1) / kCombineCols, a.T);
     e = launch_pdl(mx_combine_kernel, cgrid, dim3(kCombineThreads), 0, s, static_cast<const float*>(m.y),
                    m.umax, a.T, a.d, a.wts, a.idx, a.active, a.E, a.k, static_cast<const int32_t*>(nullptr), a.out,
                    trace_stamp("combine"));

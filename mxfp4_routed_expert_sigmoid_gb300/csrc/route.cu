@@ -199,10 +199,6 @@ route_topk_kernel(RouteArgs a) {
             int pos = __popc(bal & ((1u << lane) - 1u));
             for (int w = 0; w < (e >> 5); ++w) pos += wcount[w];
             a.active[pos] = e;
-            if (a.clear0) {
-                a.clear0[pos] = 0;
-                a.clear1[pos] = 0;
-            }
         }
         if (e == 0) {
             int total = 0;
@@ -228,13 +224,7 @@ route_topk_kernel(RouteArgs a) {
         if (lane >= o) incl += v;
     }
     int pos = incl - c;
-    for (uint32_t w = word; w != 0; w &= w - 1) {
-        if (a.clear0) {
-            a.clear0[pos] = 0;
-            a.clear1[pos] = 0;
-        }
-        a.active[pos++] = 32 * lane + (__ffs(w) - 1);
-    }
+    for (uint32_t w = word; w != 0; w &= w - 1) a.active[pos++] = 32 * lane + (__ffs(w) - 1);
     if (lane == 31) a.active[a.E] = incl;
     bitmap[lane] = 0;
     if (lane == 0) a.hdr->counters[CTR_ROUTE] = 0;
