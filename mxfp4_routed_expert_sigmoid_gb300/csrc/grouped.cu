@@ -54,7 +54,6 @@ using namespace tc;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kTileA = BM * BK * 2;   // 16 KB of f16/bf16
-constexpr int kTileRaw = BM * BK / 2; // 4 KB of packed E2M1
 
 // ---------------------------------------------------------------------------
 // Dense bf16 GEMM: out[t, n] = sum_c x[t, c] * w[n, c]
@@ -266,12 +265,19 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // ---------------------------------------------------------------------------
 // Expert GEMM kernel (UP: NA = 2 matrices w1/w3, DOWN: NA = 1 matrix w2)
 //
-// Warps: 0 raw-weight producer (TMA into an RS-deep ring of packed E2M1
-// tiles), 1 MMA issuer, 2 TMEM owner and exponent helper (computes each
-// tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
-// token producer (TMA of the tile's token rows in 16-row boxes, only as many
-// as the tile has, into a BS-deep ring), 4..7 epilogue, 8..15
+// Warps: 0 raw-weight producer (TMA into an RE-deep ring of packed E2M1
+// entries, each 128 rows x 256 inputs: four 64-input stages, one 128-byte
+// box row per weight row), 1 and 16 MMA issuers, 2 TMEM owner and exponent helper (computes
+// each tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
+// token producer (TMA of the tile's token rows in 64- and 16-row boxes, only
+// as many as the tile has, into a BS-deep ring), 4..7 epilogue, 8..15
 // dequantisation (raw ring -> f16 A stages of an AS-deep ring in TMEM).
+// One thread issues a tcgen05.mma about every 60 ns whatever its N up to 192,
+// so a single issuer caps these N <= 192 tiles near half the tensor pipe; two
+// issuers share each stage: in the up projection issuer i takes matrix i
+// (w1 or w3, its own accumulator), in the down projection issuer i takes
+// token columns [96 i, 96 i + 96) of the 192-wide accumulator, so the
+// epilogue reads the same layout either way.
 // The f16 weights never touch shared memory: each dequantising thread writes
 // its row's 32 values of a stage straight into tensor memory (tcgen05.st,
 // lane = weight row), and the MMAs read A from there (the A-in-TMEM form of
@@ -282,8 +288,8 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // ---------------------------------------------------------------------------
 template <int NA>
 struct ExpCfg;
-// RS: raw-weight stages, AS: dequantised A stages (in TMEM), BS: token (B)
-// stages, NBUF: accumulator buffers in TMEM.  TMEM (512 columns of 128
+// RE: raw-weight entries (four stages each), AS: dequantised A stages (in
+// TMEM), BS: token (B) stages, NBUF: accumulator buffers in TMEM.  TMEM (512 columns of 128
 // lanes) holds NBUF x NA accumulators of BN fp32 columns, then AS x NA A
 // stages of 32 columns (64 f16 inputs per row): the up projection takes 96
 // token rows per tile (2 x 2 x 96 + 2 x 2 x 32 = 512), the down projection
@@ -291,19 +297,25 @@ struct ExpCfg;
 // so the epilogue of a tile runs under the next tile's MMAs.
 template <>
 struct ExpCfg<2> {
-    static constexpr int BN = 96, RS = 10, AS = 2, BS = 6, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 96, RE = 4, AS = 2, BS = 6, NBUF = 2, TMEM_COLS = 512;
 };
 template <>
 struct ExpCfg<1> {
-    static constexpr int BN = 192, RS = 12, AS = 4, BS = 5, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 192, RE = 5, AS = 4, BS = 5, NBUF = 2, TMEM_COLS = 512;
 };
 template <int NA>
 constexpr int exp_acol() { return ExpCfg<NA>::NBUF * NA * ExpCfg<NA>::BN; }  // first A column
 static_assert(exp_acol<2>() + ExpCfg<2>::AS * 2 * 32 <= 512, "up: TMEM budget");
 static_assert(exp_acol<1>() + ExpCfg<1>::AS * 1 * 32 <= 512, "down: TMEM budget");
 constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
-constexpr int kBoxRows = 16;    // token rows per TMA box
-constexpr int kExpThreads = 512;
+constexpr int kBoxRows = 16;    // token rows per small TMA box (the tile's row granule)
+constexpr int kBigBoxRows = 64; // token rows per large TMA box
+constexpr int kSub = 4;         // 64-input stages per raw-weight entry
+constexpr int kRawEntry = BM * kSub * BK / 2;  // 16 KB of packed E2M1: 128 rows x 128 bytes
+constexpr int kSfEntry = kSub / 2 * 512;       // the entry's two prepared scale atoms
+constexpr int kExpThreads = 544;  // 17 warps: 16 is the second MMA issuer
+constexpr int kDownHalf = 96;     // token columns per issuer in the down projection
+static_assert(ExpCfg<1>::BN == 2 * kDownHalf, "down: two issuers split the tile's token columns");
 
 struct ExpParams {
     int K;                // reduction length (multiple of 64)
@@ -327,31 +339,32 @@ constexpr size_t exp_smem_bytes() {
     using C = ExpCfg<NA>;
     size_t b = 1024;
     b += static_cast<size_t>(C::BS) * C::BN * BK * 2;
-    b += static_cast<size_t>(C::RS) * NA * (kTileRaw + 512);
+    b += static_cast<size_t>(C::RE) * NA * (kRawEntry + kSfEntry);
     b += static_cast<size_t>(kES) * NA * BM * 4;
     b += 512;
     return b;
 }
 
-// SFC = 0: the scales are prepared atoms, one 512-byte atom per stage copied
+// SFC = 0: the scales are prepared atoms, two 512-byte atoms per entry copied
 // with the raw codes; SFC = 1: canonical E8M0 rows (K a multiple of 512), read
 // by each dequantising thread straight from global memory, 16 blocks (eight
 // stages) per 16-byte load, the next load issued eight stages ahead.
 template <int NA, int SFC>
 __global__ void __launch_bounds__(kExpThreads, 1)
 tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
-                 const __grid_constant__ CUtensorMap tmB, ExpParams p) {
+                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB64,
+                 ExpParams p) {
     using C = ExpCfg<NA>;
-    constexpr int BN = C::BN, RS = C::RS, AS = C::AS, BS = C::BS;
+    constexpr int BN = C::BN, RE = C::RE, AS = C::AS, BS = C::BS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = smem;                                // [BS][BN * 128]
-    uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RS][NA][4 KB]
-    uint8_t* sRawSf = sRaw + RS * NA * kTileRaw;       // [RS][NA][512]: the stage's scale atom
-    int* sE = reinterpret_cast<int*>(sRawSf + RS * NA * 512);  // [kES][NA][128]
+    uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RE][NA][16 KB], 128-byte swizzle
+    uint8_t* sRawSf = sRaw + RE * NA * kRawEntry;      // [RE][NA][1 KB]: the entry's scale atoms
+    int* sE = reinterpret_cast<int*>(sRawSf + RE * NA * kSfEntry);  // [kES][NA][128]
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(sE + kES * NA * BM);
-    uint64_t* raw_empty = raw_full + RS;
-    uint64_t* b_full = raw_empty + RS;
+    uint64_t* raw_empty = raw_full + RE;
+    uint64_t* b_full = raw_empty + RE;
     uint64_t* b_empty = b_full + BS;
     uint64_t* a_full = b_empty + BS;
     uint64_t* a_empty = a_full + AS;
@@ -365,23 +378,24 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = p.tiles[0].x;
     const int k_stages = p.K / BK;
+    const int k_entries = (k_stages + kSub - 1) / kSub;
     stamp_start(p.st);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < RS; ++i) {
+        for (int i = 0; i < RE; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 8);
         }
         for (int i = 0; i < BS; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
+            mbar_init(&b_empty[i], 2);  // both issuers
         }
         for (int i = 0; i < AS; ++i) {
             mbar_init(&a_full[i], 8);
-            mbar_init(&a_empty[i], 1);
+            mbar_init(&a_empty[i], 2);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_full[i], 2);
             mbar_init(&acc_empty[i], 4);
         }
         for (int i = 0; i < kES; ++i) {
@@ -401,6 +415,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmB64);
         if (NA == 2) prefetch_tmap(&tmA3);
     }
     tc_fence_before();
@@ -419,17 +434,21 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 // the tile's prepared scale atoms, one per 128 inputs (two stages)
                 const size_t atoms = static_cast<size_t>(tl.x * p.tiles_e + tl.w) * p.G * 512;
                 bool ok = true;
-                for (int ks = 0; ks < k_stages; ++ks) {
+                for (int en = 0; en < k_entries; ++en) {
                     if (!mbar_wait(&raw_empty[r], ph ^ 1, abort_flag, p.hdr, 50)) { ok = false; break; }
-                    mbar_expect_tx(&raw_full[r], NA * (kTileRaw + (SFC ? 0 : 512)));
-                    const size_t atom = atoms + static_cast<size_t>(ks >> 1) * 512;
-                    tma_load_2d(sRaw + (r * NA) * kTileRaw, &tmA, &raw_full[r], ks * BK / 2, arow);
-                    if (!SFC) bulk_load(sRawSf + (r * NA) * 512, p.s1 + atom, 512, &raw_full[r]);
+                    // a last entry of fewer stages: the box past the row end is
+                    // zero-filled (and counted); only its own atoms are copied
+                    const int nst = min(kSub, k_stages - en * kSub);
+                    const int sfb = SFC ? 0 : (nst + 1) / 2 * 512;
+                    mbar_expect_tx(&raw_full[r], NA * (kRawEntry + sfb));
+                    const size_t atom = atoms + static_cast<size_t>(en * kSub / 2) * 512;
+                    tma_load_2d(sRaw + (r * NA) * kRawEntry, &tmA, &raw_full[r], en * kSub * BK / 2, arow);
+                    if (!SFC) bulk_load(sRawSf + (r * NA) * kSfEntry, p.s1 + atom, sfb, &raw_full[r]);
                     if (NA == 2) {
-                        tma_load_2d(sRaw + (r * NA + 1) * kTileRaw, &tmA3, &raw_full[r], ks * BK / 2, arow);
-                        if (!SFC) bulk_load(sRawSf + (r * NA + 1) * 512, p.s3 + atom, 512, &raw_full[r]);
+                        tma_load_2d(sRaw + (r * NA + 1) * kRawEntry, &tmA3, &raw_full[r], en * kSub * BK / 2, arow);
+                        if (!SFC) bulk_load(sRawSf + (r * NA + 1) * kSfEntry, p.s3 + atom, sfb, &raw_full[r]);
                     }
-                    if (++r == RS) { r = 0; ph ^= 1; }
+                    if (++r == RE) { r = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
@@ -441,22 +460,28 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t ph = 0;
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 const int4 tl = p.tiles[1 + tile];
-                const int nbox = (tl.z + kBoxRows - 1) / kBoxRows;
+                const int n_rows = (tl.z + kBoxRows - 1) / kBoxRows * kBoxRows;
+                const int n_big = n_rows / kBigBoxRows, n_small = (n_rows % kBigBoxRows) / kBoxRows;
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&b_empty[b], ph ^ 1, abort_flag, p.hdr, 51)) { ok = false; break; }
-                    mbar_expect_tx(&b_full[b], nbox * kBoxRows * BK * 2);
-                    for (int i = 0; i < nbox; ++i)
-                        tma_load_2d(sB + b * BN * BK * 2 + i * kBoxRows * BK * 2, &tmB, &b_full[b], ks * BK,
-                                    tl.y + i * kBoxRows);
+                    mbar_expect_tx(&b_full[b], n_rows * BK * 2);
+                    uint8_t* dst = sB + b * BN * BK * 2;
+                    for (int i = 0; i < n_big; ++i)
+                        tma_load_2d(dst + i * kBigBoxRows * BK * 2, &tmB64, &b_full[b], ks * BK,
+                                    tl.y + i * kBigBoxRows);
+                    for (int i = 0; i < n_small; ++i)
+                        tma_load_2d(dst + (n_big * kBigBoxRows + i * kBoxRows) * BK * 2, &tmB, &b_full[b], ks * BK,
+                                    tl.y + n_big * kBigBoxRows + i * kBoxRows);
                     if (++b == BS) { b = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------- MMA issuer -----------------------------
+    } else if (warp == 1 || warp == 16) {
+        // ---------------------------- MMA issuers ----------------------------
         if (lane == 0) {
+            const int me = warp == 16;
             int a = 0, b = 0;
             uint32_t aph = 0, bph = 0;
             int it = 0;
@@ -465,10 +490,15 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int acc = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t acc_ph = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 const int n_mma = ((tl.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
-                const uint32_t idesc = idesc_f16(0, BM, n_mma);
+                // up: matrix `me`, all token columns; down: token columns
+                // [96 me, 96 me + n_me), possibly none
+                const int m_me = NA == 2 ? me : 0;
+                const int c_me = NA == 2 ? me * BN : me * kDownHalf;
+                const int n_me = NA == 2 ? n_mma : (me ? max(0, n_mma - kDownHalf) : min(n_mma, kDownHalf));
+                const uint32_t idesc = idesc_f16(0, BM, n_me > 0 ? n_me : 16);
                 if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort_flag, p.hdr, 52)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * NA * BN);
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * NA * BN + c_me);
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&b_full[b], bph, abort_flag, p.hdr, 53) ||
@@ -477,23 +507,29 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_addr = smem_u32(sB + b * BN * BK * 2);
-#pragma unroll
-                    for (int m = 0; m < NA; ++m) {
-                        // A stage (a, m): TMEM columns, 8 per 16-wide K slice
-                        const uint32_t a_tm = tmem_base + static_cast<uint32_t>(exp_acol<NA>() + (a * NA + m) * 32);
+                    if (n_me > 0) {
+                        const uint32_t b_addr = smem_u32(sB + b * BN * BK * 2 + (NA == 2 ? 0 : c_me) * BK * 2);
+                        // A stage (a, m_me): TMEM columns, 8 per 16-wide K slice
+                        const uint32_t a_tm =
+                            tmem_base + static_cast<uint32_t>(exp_acol<NA>() + (a * NA + m_me) * 32);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_f16_ts(d0 + m * BN, a_tm + 8 * kk, sw128_desc(b_addr + kk * 32), idesc,
+                            mma_f16_ts(d0, a_tm + 8 * kk, sw128_desc(b_addr + kk * 32), idesc,
                                        (ks > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&a_empty[a]);
+                        mma_commit(&b_empty[b]);
+                    } else {
+                        mbar_arrive(&a_empty[a]);
+                        mbar_arrive(&b_empty[b]);
                     }
-                    mma_commit(&a_empty[a]);
-                    mma_commit(&b_empty[b]);
                     if (++a == AS) { a = 0; aph ^= 1; }
                     if (++b == BS) { b = 0; bph ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[acc]);
+                if (n_me > 0)
+                    mma_commit(&acc_full[acc]);
+                else
+                    mbar_arrive(&acc_full[acc]);
             }
         }
     } else if (warp == 2) {
@@ -582,7 +618,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 mbar_arrive(&eref_empty[slot]);
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && warp < 16) {
         // ---------------------------- dequantisation -------------------------
         // warp 8 + 4 half + q: TMEM lane quadrant q, one weight row per lane,
         // inputs 32 half .. 32 half + 31 of each 64-wide stage
@@ -593,6 +629,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         int r = 0, a = 0;
         uint32_t rph = 0, aph = 0;
         int it = 0;
+        const int swz = row & 7;  // 128-byte swizzle of the raw entries: 16-byte chunk j sits at j ^ (row % 8)
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
             const int4 tl = p.tiles[1 + tile];
             const int slot = it % kES;
@@ -601,6 +638,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int eref1 = sE[(slot * NA + 0) * BM + row];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + row] : 0;
             // this thread's byte of a scale atom: row `row`, block 2 ks + half
+            // (an entry holds two atoms: stages 0-1 and 2-3)
             const int sfo = 16 * (row & 31) + 4 * (row >> 5);
             // canonical scales: the row's 16-byte vectors, current and next (a
             // row past the expert reads zeros: its products are never stored)
@@ -625,7 +663,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         if (NA == 2) n3 = ldg_nc_v4(c3 + 16 * ((ks >> 3) + 1));
                     }
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59) &&
+                const int sub = ks % kSub;  // stage within the raw entry
+                if (!__all_sync(0xffffffffu, (sub != 0 || mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59)) &&
                                                  mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
                     break;
@@ -636,13 +675,14 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     e1 = vec_byte(v1, blk & 15);
                     e3 = NA == 2 ? vec_byte(v3, blk & 15) : 0;
                 } else {
-                    e1 = sRawSf[(r * NA) * 512 + sfo + (blk & 3)];
-                    e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * 512 + sfo + (blk & 3)] : 0;
+                    const int sfb = (sub >> 1) * 512 + sfo + (blk & 3);
+                    e1 = sRawSf[(r * NA) * kSfEntry + sfb];
+                    e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * kSfEntry + sfb] : 0;
                 }
 #pragma unroll
                 for (int mm = 0; mm < NA; ++mm) {
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4*>(sRaw + (r * NA + mm) * kTileRaw + row * 32 + half * 16);
+                    const uint4 raw = *reinterpret_cast<const uint4*>(sRaw + (r * NA + mm) * kRawEntry + row * 128 +
+                                                                      (((2 * sub + half) ^ swz) << 4));
                     const uint16_t sh = f16_pow2(mm == 0 ? e1 - eref1 : e3 - eref3);
                     const uint32_t sc2 = static_cast<uint32_t>(sh) | (static_cast<uint32_t>(sh) << 16);
                     uint32_t w[16];
@@ -656,13 +696,14 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                fence_proxy_async();  // the raw codes were read here; the producer's TMA rewrites them
+                const bool last = sub == kSub - 1 || ks == k_stages - 1;  // the entry's last stage
+                if (last) fence_proxy_async();  // the raw codes were read here; the producer's TMA rewrites them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&a_full[a]);
-                    mbar_arrive(&raw_empty[r]);
+                    if (last) mbar_arrive(&raw_empty[r]);
                 }
-                if (++r == RS) { r = 0; rph ^= 1; }
+                if (last && ++r == RE) { r = 0; rph ^= 1; }
                 if (++a == AS) { a = 0; aph ^= 1; }
             }
             if (!ok) break;
@@ -828,7 +869,8 @@ constexpr int kUnitRows = kUpRows < kDownRows ? kUpRows : kDownRows;  // bounds 
 
 template <int NA, int SFC>
 cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                              const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+                              const CUtensorMap& b64, const ExpParams& p, int grid, cudaStream_t s,
+                              const char* name) {
     constexpr size_t smem = exp_smem_bytes<NA>();
     static_assert(smem <= 232448, "shared memory budget");
     static std::atomic<uint64_t> done{0};
@@ -844,16 +886,16 @@ cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const
     }
     ExpParams q = p;
     q.st = trace_stamp(name);
-    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, q);
+    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, b64, q);
     trace_mark(name, s);
     return cudaGetLastError();
 }
 
 template <int NA>
 cudaError_t launch_expert(int sf_canon, const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                          const ExpParams& p, int grid, cudaStream_t s, const char* name) {
-    return sf_canon ? launch_expert_sfc<NA, 1>(a, a3, b, p, grid, s, name)
-                    : launch_expert_sfc<NA, 0>(a, a3, b, p, grid, s, name);
+                          const CUtensorMap& b64, const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+    return sf_canon ? launch_expert_sfc<NA, 1>(a, a3, b, b64, p, grid, s, name)
+                    : launch_expert_sfc<NA, 0>(a, a3, b, b64, p, grid, s, name);
 }
 
 }  // namespace
@@ -902,14 +944,18 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     trace_mark("build_tiles", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    // UP: A = w1 / w3 raw bytes [E*f, d/2], B = xp [P, d] f16 in 16-row boxes
-    CUtensorMap t1, t3, tb;
+    // UP: A = w1 / w3 raw bytes [E*f, d/2] in 128-byte x 128-row boxes (a box
+    // past the end of a row, d % 256 != 0, is zero-filled), B = xp [P, d] f16
+    // in 64- and 16-row boxes
+    CUtensorMap t1, t3, tb, tb64;
     const uint64_t rows_up = static_cast<uint64_t>(g.E) * g.f;
-    if (!make_tmap(&t1, g.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, BK / 2, BM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap(&t3, g.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, BK / 2, BM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!make_tmap(&t1, g.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, kSub * BK / 2, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&t3, g.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, kSub * BK / 2, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&tb64, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBigBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
     if (g.sf_canon && (g.d % 512 || g.f % 512)) return cudaErrorNotSupported;
@@ -926,17 +972,19 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     p.hf = g.hf;
     p.h_amax = g.h_amax;
     p.hdr = g.hdr;
-    if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
+    if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, tb64, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
     convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp, trace_stamp("convert_h"));
     trace_mark("convert_h", s);
 
-    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16 in 16-row boxes
-    CUtensorMap t2, th;
+    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16, boxes as above
+    CUtensorMap t2, th, th64;
     const uint64_t rows_dn = static_cast<uint64_t>(g.E) * g.d;
-    if (!make_tmap(&t2, g.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.f / 2, rows_dn, BK / 2, BM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!make_tmap(&t2, g.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.f / 2, rows_dn, kSub * BK / 2, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap(&th, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&th64, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kBigBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
     ExpParams q{};
@@ -950,7 +998,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     q.n_out = g.d;
     q.y = g.y;
     q.hdr = g.hdr;
-    if ((e = launch_expert<1>(g.sf_canon, t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
+    if ((e = launch_expert<1>(g.sf_canon, t2, t2, th, th64, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
 
     return launch_combine(g.y, 1, g.wts, g.inv, g.T, g.k, g.d, g.out, s);
 }

@@ -284,6 +284,17 @@ def test_grouped_tile_edges(k3, T):
     compare_forward(k3, cfg, 2)
 
 
+@pytest.mark.parametrize("path", [1, 2])
+def test_reduction_tails(k3, path):
+    """Reduction lengths that are multiples of 64 but not of 256 (d = 320,
+    f = 448): the grouped GEMMs read their weights 256 inputs at a time, so
+    the last read of each row is partial (one and three 64-input stages) and
+    the last prepared scale atom of a row is half used.  Token counts span a
+    64-row box plus 16-row boxes (k = E, T = 150)."""
+    cfg = synth.custom("decode_t1", T=150, E=4, k=4, d=320, f=448, seed_index=62)
+    compare_forward(k3, cfg, path)
+
+
 def test_verify_t8_grouped_path(k3):
     """The full-size K3 layer through the tcgen05 path at T = 8 (hot experts)."""
     compare_forward(k3, synth.CONFIGS["verify_t8"], 2)
