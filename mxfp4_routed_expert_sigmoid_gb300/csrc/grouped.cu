@@ -81,7 +81,28 @@ constexpr size_t dense_smem_bytes() {
     return 1024 + static_cast<size_t>(kDenseStages) * (kTileA + kDenseBN * BK * 2) + 256;
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Per-token maxima over a warp: a[i] holds lane l's value for token i (16
+// tokens).  Each step trades half of the values with the partner lane
+// (offsets 16, 8, 4, 2), keeping the maxima of the half whose tokens this
+// lane keeps, then a last exchange with lane ^ 1; 16 shuffles in all instead
+// of 5 per token.  Returns the token whose warp maximum a[0] now holds (lanes
+// l and l ^ 1 hold the same token).
+__device__ __forceinline__ int token_max16(float (&a)[16], int lane) {
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool hi = (lane & (2 * w)) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float send = hi ? a[j] : a[j + w];
+            const float keep = hi ? a[j + w] : a[j];
+            a[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2 * w));
+        }
+    }
+    a[0] = fmaxf(a[0], __shfl_xor_sync(0xffffffffu, a[0], 1));
+    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
 
 // Prepared scale atoms (per expert ceil(rows / 128) tiles of G = ceil(K / 128)
 // atoms, zero-padded): row r of expert e is row m = r % 128 of atom tile
@@ -269,8 +290,10 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // entries, each 128 rows x 256 inputs: four 64-input stages, one 128-byte
 // box row per weight row), 1 and 16 MMA issuers, 2 TMEM owner and exponent helper (computes
 // each tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
-// token producer (TMA of the tile's token rows in 64- and 16-row boxes, only
-// as many as the tile has, into a BS-deep ring), 4..7 epilogue, 8..15
+// token producer (one TMA box of BN token rows per stage into a BS-deep ring;
+// in a tile of fewer rows the rest of the box is rows of the next expert or
+// zero fill, which the MMAs never read: one copy per stage costs less than
+// several smaller ones), 4..7 epilogue, 8..15
 // dequantisation (raw ring -> f16 A stages of an AS-deep ring in TMEM).
 // One thread issues a tcgen05.mma about every 60 ns whatever its N up to 192,
 // so a single issuer caps these N <= 192 tiles near half the tensor pipe; two
@@ -308,8 +331,7 @@ constexpr int exp_acol() { return ExpCfg<NA>::NBUF * NA * ExpCfg<NA>::BN; }  // 
 static_assert(exp_acol<2>() + ExpCfg<2>::AS * 2 * 32 <= 512, "up: TMEM budget");
 static_assert(exp_acol<1>() + ExpCfg<1>::AS * 1 * 32 <= 512, "down: TMEM budget");
 constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
-constexpr int kBoxRows = 16;    // token rows per small TMA box (the tile's row granule)
-constexpr int kBigBoxRows = 64; // token rows per large TMA box
+constexpr int kBoxRows = 16;    // token-row granule of the MMAs' N
 constexpr int kSub = 4;         // 64-input stages per raw-weight entry
 constexpr int kRawEntry = BM * kSub * BK / 2;  // 16 KB of packed E2M1: 128 rows x 128 bytes
 constexpr int kSfEntry = kSub / 2 * 512;       // the entry's two prepared scale atoms
@@ -352,8 +374,7 @@ constexpr size_t exp_smem_bytes() {
 template <int NA, int SFC>
 __global__ void __launch_bounds__(kExpThreads, 1)
 tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
-                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB64,
-                 ExpParams p) {
+                 const __grid_constant__ CUtensorMap tmB, ExpParams p) {
     using C = ExpCfg<NA>;
     constexpr int BN = C::BN, RE = C::RE, AS = C::AS, BS = C::BS;
     extern __shared__ uint8_t smem_raw[];
@@ -415,7 +436,6 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        prefetch_tmap(&tmB64);
         if (NA == 2) prefetch_tmap(&tmA3);
     }
     tc_fence_before();
@@ -460,19 +480,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t ph = 0;
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 const int4 tl = p.tiles[1 + tile];
-                const int n_rows = (tl.z + kBoxRows - 1) / kBoxRows * kBoxRows;
-                const int n_big = n_rows / kBigBoxRows, n_small = (n_rows % kBigBoxRows) / kBoxRows;
                 bool ok = true;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&b_empty[b], ph ^ 1, abort_flag, p.hdr, 51)) { ok = false; break; }
-                    mbar_expect_tx(&b_full[b], n_rows * BK * 2);
-                    uint8_t* dst = sB + b * BN * BK * 2;
-                    for (int i = 0; i < n_big; ++i)
-                        tma_load_2d(dst + i * kBigBoxRows * BK * 2, &tmB64, &b_full[b], ks * BK,
-                                    tl.y + i * kBigBoxRows);
-                    for (int i = 0; i < n_small; ++i)
-                        tma_load_2d(dst + (n_big * kBigBoxRows + i * kBoxRows) * BK * 2, &tmB, &b_full[b], ks * BK,
-                                    tl.y + n_big * kBigBoxRows + i * kBoxRows);
+                    mbar_expect_tx(&b_full[b], BN * BK * 2);
+                    tma_load_2d(sB + b * BN * BK * 2, &tmB, &b_full[b], ks * BK, tl.y);
                     if (++b == BS) { b = 0; ph ^= 1; }
                 }
                 if (!ok) break;
@@ -584,30 +596,32 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int eref1 = sE[(slot * NA + 0) * BM + m];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + m] : 0;
             for (int n0 = 0; n0 < n_used; n0 += 16) {
-                float v1[16];
-                tmem_ld16(tbase + n0, v1);
+                // tokens n0 .. n0 + cnt - 1 of the tile are real; lane i < cnt
+                // fetches token i's exponent for the whole warp
+                const int cnt = min(16, nrows - n0);
+                const int xe_l = lane < cnt ? p.bexp[row0 + n0 + lane] : 0;
                 if (NA == 2) {
-                    float v3[16];
-                    tmem_ld16(tbase + BN + n0, v3);
+                    float v1[16], v3[16], a[16];
+                    tmem_ld16x2(tbase + n0, tbase + BN + n0, v1, v3);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        if (n0 + i >= nrows) break;
-                        const int pr = row0 + n0 + i;
-                        const int xe = p.bexp[pr];
+                        const int xe = __shfl_sync(0xffffffffu, xe_l, i);
                         const float gg = v1[i] * exp2i(eref1 - 127 + xe);
                         const float u = v3[i] * exp2i(eref3 - 127 + xe);
                         const float h = silu_f32(gg) * u;
-                        if (valid) p.hf[static_cast<size_t>(pr) * p.n_out + r] = h;
-                        const float amx = warp_max(valid ? fabsf(h) : 0.0f);
-                        if (lane == 0) atomicMax(p.h_amax + pr, __float_as_uint(amx));
+                        if (valid && i < cnt) p.hf[static_cast<size_t>(row0 + n0 + i) * p.n_out + r] = h;
+                        a[i] = valid ? fabsf(h) : 0.0f;
                     }
+                    const int t = token_max16(a, lane);
+                    if ((lane & 1) == 0 && t < cnt) atomicMax(p.h_amax + row0 + n0 + t, __float_as_uint(a[0]));
                 } else {
+                    float v1[16];
+                    tmem_ld16(tbase + n0, v1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        if (n0 + i >= nrows) break;
-                        const int pr = row0 + n0 + i;
-                        const float yv = v1[i] * exp2i(eref1 - 127 + p.bexp[pr]);
-                        if (valid) p.y[static_cast<size_t>(pr) * p.n_out + r] = yv;
+                        const int xe = __shfl_sync(0xffffffffu, xe_l, i);
+                        const float yv = v1[i] * exp2i(eref1 - 127 + xe);
+                        if (valid && i < cnt) p.y[static_cast<size_t>(row0 + n0 + i) * p.n_out + r] = yv;
                     }
                 }
             }
@@ -869,8 +883,7 @@ constexpr int kUnitRows = kUpRows < kDownRows ? kUpRows : kDownRows;  // bounds 
 
 template <int NA, int SFC>
 cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                              const CUtensorMap& b64, const ExpParams& p, int grid, cudaStream_t s,
-                              const char* name) {
+                              const ExpParams& p, int grid, cudaStream_t s, const char* name) {
     constexpr size_t smem = exp_smem_bytes<NA>();
     static_assert(smem <= 232448, "shared memory budget");
     static std::atomic<uint64_t> done{0};
@@ -886,16 +899,16 @@ cudaError_t launch_expert_sfc(const CUtensorMap& a, const CUtensorMap& a3, const
     }
     ExpParams q = p;
     q.st = trace_stamp(name);
-    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, b64, q);
+    tc_expert_kernel<NA, SFC><<<grid, kExpThreads, smem, s>>>(a, a3, b, q);
     trace_mark(name, s);
     return cudaGetLastError();
 }
 
 template <int NA>
 cudaError_t launch_expert(int sf_canon, const CUtensorMap& a, const CUtensorMap& a3, const CUtensorMap& b,
-                          const CUtensorMap& b64, const ExpParams& p, int grid, cudaStream_t s, const char* name) {
-    return sf_canon ? launch_expert_sfc<NA, 1>(a, a3, b, b64, p, grid, s, name)
-                    : launch_expert_sfc<NA, 0>(a, a3, b, b64, p, grid, s, name);
+                          const ExpParams& p, int grid, cudaStream_t s, const char* name) {
+    return sf_canon ? launch_expert_sfc<NA, 1>(a, a3, b, p, grid, s, name)
+                    : launch_expert_sfc<NA, 0>(a, a3, b, p, grid, s, name);
 }
 
 }  // namespace
@@ -946,16 +959,14 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
 
     // UP: A = w1 / w3 raw bytes [E*f, d/2] in 128-byte x 128-row boxes (a box
     // past the end of a row, d % 256 != 0, is zero-filled), B = xp [P, d] f16
-    // in 64- and 16-row boxes
-    CUtensorMap t1, t3, tb, tb64;
+    // in boxes of 96 rows
+    CUtensorMap t1, t3, tb;
     const uint64_t rows_up = static_cast<uint64_t>(g.E) * g.f;
     if (!make_tmap(&t1, g.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, kSub * BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap(&t3, g.w3_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, kSub * BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&tb64, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kBigBoxRows,
+        !make_tmap(&tb, g.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.d, P, BK, kUpRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
     if (g.sf_canon && (g.d % 512 || g.f % 512)) return cudaErrorNotSupported;
@@ -972,19 +983,17 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     p.hf = g.hf;
     p.h_amax = g.h_amax;
     p.hdr = g.hdr;
-    if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, tb64, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
+    if ((e = launch_expert<2>(g.sf_canon, t1, t3, tb, p, g.num_sms, s, "expert_up")) != cudaSuccess) return e;
 
     convert_h_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.hf, g.h_amax, P, g.f, g.hp, g.hp_exp, trace_stamp("convert_h"));
     trace_mark("convert_h", s);
 
-    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16, boxes as above
-    CUtensorMap t2, th, th64;
+    // DOWN: A = w2 raw bytes [E*d, f/2], B = hp [P, f] f16 in boxes of 192 rows
+    CUtensorMap t2, th;
     const uint64_t rows_dn = static_cast<uint64_t>(g.E) * g.d;
     if (!make_tmap(&t2, g.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.f / 2, rows_dn, kSub * BK / 2, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&th, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&th64, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kBigBoxRows,
+        !make_tmap(&th, g.hp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.f, P, BK, kDownRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
     ExpParams q{};
@@ -998,7 +1007,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     q.n_out = g.d;
     q.y = g.y;
     q.hdr = g.hdr;
-    if ((e = launch_expert<1>(g.sf_canon, t2, t2, th, th64, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
+    if ((e = launch_expert<1>(g.sf_canon, t2, t2, th, q, g.num_sms, s, "expert_down")) != cudaSuccess) return e;
 
     return launch_combine(g.y, 1, g.wts, g.inv, g.T, g.k, g.d, g.out, s);
 }
