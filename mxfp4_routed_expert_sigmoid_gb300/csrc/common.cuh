@@ -133,6 +133,17 @@ __device__ __forceinline__ int ilog2f(float x) {
     return e - 1;
 }
 
+// v * 2^n without a branch, for use inside unrolled loops: n is clamped to
+// [-252, 254] and applied as two power-of-two factors 2^hi * 2^lo, both
+// normal floats (hi in [-126, 127]); exact except that a result below the
+// normal range may round twice.
+__device__ __forceinline__ float mul_pow2(float v, int n) {
+    n = max(min(n, 254), -252);
+    const int lo = n < -126 ? n + 126 : (n > 127 ? n - 127 : 0);
+    const int hi = n - lo;
+    return v * __int_as_float((hi + 127) << 23) * __int_as_float((lo + 127) << 23);
+}
+
 // f16 bit pattern of 2^n for n in [-24, 15]; 0 below (flush), inf above.
 __device__ __forceinline__ uint16_t f16_pow2(int n) {
     if (n < -24) return 0;

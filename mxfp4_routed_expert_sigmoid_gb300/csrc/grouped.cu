@@ -320,7 +320,7 @@ struct ExpCfg;
 // so the epilogue of a tile runs under the next tile's MMAs.
 template <>
 struct ExpCfg<2> {
-    static constexpr int BN = 96, RE = 4, AS = 2, BS = 6, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 192, RE = 3, AS = 2, BS = 4, NBUF = 1, TMEM_COLS = 512;
 };
 template <>
 struct ExpCfg<1> {
@@ -335,7 +335,7 @@ constexpr int kBoxRows = 16;    // token-row granule of the MMAs' N
 constexpr int kSub = 4;         // 64-input stages per raw-weight entry
 constexpr int kRawEntry = BM * kSub * BK / 2;  // 16 KB of packed E2M1: 128 rows x 128 bytes
 constexpr int kSfEntry = kSub / 2 * 512;       // the entry's two prepared scale atoms
-constexpr int kExpThreads = 544;  // 17 warps: 16 is the second MMA issuer
+constexpr int kExpThreads = 672;  // 21 warps: 16 is the second MMA issuer, 17..20 a second epilogue set
 constexpr int kDownHalf = 96;     // token columns per issuer in the down projection
 static_assert(ExpCfg<1>::BN == 2 * kDownHalf, "down: two issuers split the tile's token columns");
 
@@ -417,11 +417,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 2);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&acc_empty[i], 8);  // both epilogue sets
         }
         for (int i = 0; i < kES; ++i) {
             mbar_init(&eref_full[i], 1);
-            mbar_init(&eref_empty[i], 12);
+            mbar_init(&eref_empty[i], 16);  // 8 epilogue + 8 dequantising warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -572,9 +572,12 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&eref_full[slot]);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || warp >= 17) {
         // ---------------------------- epilogue -------------------------------
+        // two sets of four warps (4..7 and 17..20), one warp per TMEM lane
+        // quadrant in each; set h takes the 16-token chunks 2 j + h
         const int wr = warp & 3;
+        const int eset = warp >= 17 ? 1 : 0;
         const int m = wr * 32 + lane;
         int it = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
@@ -595,7 +598,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const bool valid = r < p.rows_per_expert;
             const int eref1 = sE[(slot * NA + 0) * BM + m];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + m] : 0;
-            for (int n0 = 0; n0 < n_used; n0 += 16) {
+            for (int n0 = 16 * eset; n0 < n_used; n0 += 32) {
                 // tokens n0 .. n0 + cnt - 1 of the tile are real; lane i < cnt
                 // fetches token i's exponent for the whole warp
                 const int cnt = min(16, nrows - n0);
@@ -606,8 +609,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int xe = __shfl_sync(0xffffffffu, xe_l, i);
-                        const float gg = v1[i] * exp2i(eref1 - 127 + xe);
-                        const float u = v3[i] * exp2i(eref3 - 127 + xe);
+                        const float gg = mul_pow2(v1[i], eref1 - 127 + xe);
+                        const float u = mul_pow2(v3[i], eref3 - 127 + xe);
                         const float h = silu_f32(gg) * u;
                         if (valid && i < cnt) p.hf[static_cast<size_t>(row0 + n0 + i) * p.n_out + r] = h;
                         a[i] = valid ? fabsf(h) : 0.0f;
@@ -620,7 +623,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int xe = __shfl_sync(0xffffffffu, xe_l, i);
-                        const float yv = v1[i] * exp2i(eref1 - 127 + xe);
+                        const float yv = mul_pow2(v1[i], eref1 - 127 + xe);
                         if (valid && i < cnt) p.y[static_cast<size_t>(row0 + n0 + i) * p.n_out + r] = yv;
                     }
                 }
