@@ -288,19 +288,23 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 //
 // Warps: 0 raw-weight producer (TMA into an RE-deep ring of packed E2M1
 // entries, each 128 rows x 256 inputs: four 64-input stages, one 128-byte
-// box row per weight row), 1 and 16 MMA issuers, 2 TMEM owner and exponent helper (computes
-// each tile's per-row E8M0 maximum e_ref ahead of time into a small ring), 3
-// token producer (one TMA box of BN token rows per stage into a BS-deep ring;
-// in a tile of fewer rows the rest of the box is rows of the next expert or
-// zero fill, which the MMAs never read: one copy per stage costs less than
-// several smaller ones), 4..7 epilogue, 8..15
-// dequantisation (raw ring -> f16 A stages of an AS-deep ring in TMEM).
-// One thread issues a tcgen05.mma about every 60 ns whatever its N up to 192,
-// so a single issuer caps these N <= 192 tiles near half the tensor pipe; two
-// issuers share each stage: in the up projection issuer i takes matrix i
-// (w1 or w3, its own accumulator), in the down projection issuer i takes
-// token columns [96 i, 96 i + 96) of the 192-wide accumulator, so the
-// epilogue reads the same layout either way.
+// box row per weight row), 1 and 16 MMA issuers, 2 TMEM owner and exponent
+// helper (computes each tile's per-row E8M0 maximum e_ref ahead of time into
+// a small ring), 3 token producer (one TMA box of BN token rows per stage
+// into a BS-deep ring; in a tile of fewer rows the rest of the box is rows
+// of the next expert or zero fill, which the MMAs never read: one copy per
+// stage costs less than several smaller ones), 4..7 and 17..20 epilogue (two
+// sets, one warp per TMEM lane quadrant in each, alternating 16-token
+// chunks), 8..15 dequantisation (raw ring -> f16 A stages of an AS-deep ring
+// in TMEM).
+//
+// What bounds it, measured on this part: a thread needs about 60 ns (100 ns
+// when its SM sub-partition is also running dequantising warps) to issue one
+// tcgen05.mma, whatever its N, so the tiles take as many tokens per MMA as
+// the tensor memory allows, and two issuers share each stage: in the up
+// projection issuer i takes matrix i (w1 or w3, its own accumulator), in the
+// down projection issuer i takes token columns [96 i, 96 i + 96) of the
+// 192-wide accumulator, so the epilogue reads the same layout either way.
 // The f16 weights never touch shared memory: each dequantising thread writes
 // its row's 32 values of a stage straight into tensor memory (tcgen05.st,
 // lane = weight row), and the MMAs read A from there (the A-in-TMEM form of
@@ -312,12 +316,14 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 template <int NA>
 struct ExpCfg;
 // RE: raw-weight entries (four stages each), AS: dequantised A stages (in
-// TMEM), BS: token (B) stages, NBUF: accumulator buffers in TMEM.  TMEM (512 columns of 128
-// lanes) holds NBUF x NA accumulators of BN fp32 columns, then AS x NA A
-// stages of 32 columns (64 f16 inputs per row): the up projection takes 96
-// token rows per tile (2 x 2 x 96 + 2 x 2 x 32 = 512), the down projection
-// 192 (2 x 192 + 4 x 32 = 512); both keep their accumulators double-buffered
-// so the epilogue of a tile runs under the next tile's MMAs.
+// TMEM), BS: token (B) stages, NBUF: accumulator buffers in TMEM.  TMEM (512
+// columns of 128 lanes) holds NBUF x NA accumulators of BN fp32 columns, then
+// AS x NA A stages of 32 columns (64 f16 inputs per row).  The up projection
+// takes 192 token rows per tile with one accumulator buffer (2 x 192 + 2 x 2
+// x 32 = 512): its epilogue does not overlap the next tile's MMAs, which
+// costs less than issuing twice as many 96-wide MMAs would.  The down
+// projection takes 192 rows with two buffers (2 x 192 + 4 x 32 = 512), so its
+// epilogue runs under the next tile's MMAs.
 template <>
 struct ExpCfg<2> {
     static constexpr int BN = 192, RE = 3, AS = 2, BS = 4, NBUF = 1, TMEM_COLS = 512;
@@ -962,7 +968,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
 
     // UP: A = w1 / w3 raw bytes [E*f, d/2] in 128-byte x 128-row boxes (a box
     // past the end of a row, d % 256 != 0, is zero-filled), B = xp [P, d] f16
-    // in boxes of 96 rows
+    // in boxes of 192 rows
     CUtensorMap t1, t3, tb;
     const uint64_t rows_up = static_cast<uint64_t>(g.E) * g.f;
     if (!make_tmap(&t1, g.w1_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.d / 2, rows_up, kSub * BK / 2, BM,

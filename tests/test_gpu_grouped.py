@@ -276,10 +276,10 @@ def test_block_t8192_full_sampled(k3):
 
 @pytest.mark.parametrize("T", [95, 97, 200, 385])
 def test_grouped_tile_edges(k3, T):
-    """Token counts around the grouped GEMMs' tile sizes (96 token rows per
-    up-projection tile, 192 per down-projection tile): experts with one
-    partial tile, several full tiles and a ragged last one (k = E, so every
-    expert takes every token)."""
+    """Token counts around the grouped GEMMs' tile size (192 token rows per
+    tile, split 96 / 96 between the two issuers of the down projection):
+    experts with one partial tile, several full tiles and a ragged last one
+    (k = E, so every expert takes every token)."""
     cfg = synth.custom("decode_t1", T=T, E=4, k=4, d=512, f=768, seed_index=61)
     compare_forward(k3, cfg, 2)
 
