@@ -104,33 +104,47 @@ __device__ __forceinline__ int token_max16(float (&a)[16], int lane) {
     return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
-// Prepared scale atoms (per expert ceil(rows / 128) tiles of G = ceil(K / 128)
-// atoms, zero-padded): row r of expert e is row m = r % 128 of atom tile
-// e * tiles_e + r / 128; its block b sits at + (b / 4) * 512 + b % 4 from the
-// returned pointer.
-__device__ __forceinline__ const uint8_t* sf_row(const uint8_t* sf, int e, int r, int tiles_e, int G) {
-    const int tile = e * tiles_e + r / 128;
-    const int m = r % 128;
-    return sf + static_cast<size_t>(tile) * G * 512 + 16 * (m & 31) + 4 * (m >> 5);
-}
+// Prepared scale atoms: per expert ceil(rows / 128) tiles of G = ceil(K / 128)
+// atoms (zero-padded); row r of expert e is row m = r % 128 of atom tile
+// e * tiles_e + r / 128, its block b at byte (b / 4) * 512 + 16 (m % 32) +
+// 4 (m / 32) + b % 4 of the tile's atoms.
 
-// largest exponent of a row from its prepared atoms (four blocks per word)
-__device__ __forceinline__ int row_emax_sf(const uint8_t* srow, int G) {
-    int m = 0;
-    for (int s = 0; s < G; ++s) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(srow + static_cast<size_t>(s) * 512);
+// Largest E8M0 exponent of the four rows m0 + 32 k (k = 0..3) of a 128-row
+// tile from its prepared atoms: in every 512-byte atom, bytes 16 m0 .. 16 m0
+// + 15 are those rows' four blocks (word k = row m0 + 32 k), so one 16-byte
+// load per atom serves all four; the loads go out eight atoms at a time.
+__device__ __forceinline__ void rows_emax_sf(const uint8_t* atoms, int G, int m0, int (&em)[4]) {
+    uint32_t mx[4] = {0u, 0u, 0u, 0u};
+    const uint8_t* base = atoms + 16 * m0;
+    for (int s0 = 0; s0 < G; s0 += 8) {
+        uint4 v[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) m = max(m, static_cast<int>((w >> (8 * b)) & 0xFF));
+        for (int i = 0; i < 8; ++i)
+            v[i] = s0 + i < G ? ldg_nc_v4(base + static_cast<size_t>(s0 + i) * 512) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            mx[0] = __vmaxu4(mx[0], v[i].x);
+            mx[1] = __vmaxu4(mx[1], v[i].y);
+            mx[2] = __vmaxu4(mx[2], v[i].z);
+            mx[3] = __vmaxu4(mx[3], v[i].w);
+        }
     }
-    return m;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        em[k] = static_cast<int>(max(max(mx[k] & 0xFF, (mx[k] >> 8) & 0xFF), max((mx[k] >> 16) & 0xFF, mx[k] >> 24)));
 }
 
-// largest exponent of a canonical E8M0 row (nv 16-byte vectors)
+// largest exponent of a canonical E8M0 row (nv 16-byte vectors), the loads
+// issued four at a time
 __device__ __forceinline__ int row_emax_canon(const uint8_t* row, int nv) {
     uint32_t m = 0;
-    for (int i = 0; i < nv; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * i);
-        m = __vmaxu4(m, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+    for (int i0 = 0; i0 < nv; i0 += 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = i0 + i < nv ? ldg_nc_v4(row + 16 * (i0 + i)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = __vmaxu4(m, __vmaxu4(__vmaxu4(v[i].x, v[i].y), __vmaxu4(v[i].z, v[i].w)));
     }
     return static_cast<int>(max(max(m & 0xFF, (m >> 8) & 0xFF), max((m >> 16) & 0xFF, m >> 24)));
 }
@@ -323,24 +337,30 @@ struct ExpCfg;
 // x 32 = 512): its epilogue does not overlap the next tile's MMAs, which
 // costs less than issuing twice as many 96-wide MMAs would.  The down
 // projection takes 192 rows with two buffers (2 x 192 + 4 x 32 = 512), so its
-// epilogue runs under the next tile's MMAs.
+// epilogue runs under the next tile's MMAs.  SUB: 64-input stages handed over
+// together (one set of barrier waits, arrivals and commits per SUB stages;
+// AS and BS count such groups).  Every hand-off costs the dequantising warps
+// and the issuers a fixed time, so the down projection, whose TMEM has room
+// for two-stage A groups, takes them in pairs; the up projection's A ring
+// (two single stages) cannot grow without losing the dequantise / MMA overlap.
 template <>
 struct ExpCfg<2> {
-    static constexpr int BN = 192, RE = 3, AS = 2, BS = 4, NBUF = 1, TMEM_COLS = 512;
+    static constexpr int BN = 192, RE = 3, AS = 2, BS = 4, NBUF = 1, SUB = 1, TMEM_COLS = 512;
 };
 template <>
 struct ExpCfg<1> {
-    static constexpr int BN = 192, RE = 5, AS = 4, BS = 5, NBUF = 2, TMEM_COLS = 512;
+    static constexpr int BN = 192, RE = 4, AS = 2, BS = 3, NBUF = 2, SUB = 2, TMEM_COLS = 512;
 };
 template <int NA>
 constexpr int exp_acol() { return ExpCfg<NA>::NBUF * NA * ExpCfg<NA>::BN; }  // first A column
-static_assert(exp_acol<2>() + ExpCfg<2>::AS * 2 * 32 <= 512, "up: TMEM budget");
-static_assert(exp_acol<1>() + ExpCfg<1>::AS * 1 * 32 <= 512, "down: TMEM budget");
+static_assert(exp_acol<2>() + ExpCfg<2>::AS * 2 * ExpCfg<2>::SUB * 32 <= 512, "up: TMEM budget");
+static_assert(exp_acol<1>() + ExpCfg<1>::AS * 1 * ExpCfg<1>::SUB * 32 <= 512, "down: TMEM budget");
 constexpr int kES = 4;          // exponent-reference slots (tiles ahead)
 constexpr int kBoxRows = 16;    // token-row granule of the MMAs' N
 constexpr int kSub = 4;         // 64-input stages per raw-weight entry
 constexpr int kRawEntry = BM * kSub * BK / 2;  // 16 KB of packed E2M1: 128 rows x 128 bytes
 constexpr int kSfEntry = kSub / 2 * 512;       // the entry's two prepared scale atoms
+static_assert(kSub % ExpCfg<1>::SUB == 0 && kSub % ExpCfg<2>::SUB == 0, "a hand-off group ends at most one entry");
 constexpr int kExpThreads = 672;  // 21 warps: 16 is the second MMA issuer, 17..20 a second epilogue set
 constexpr int kDownHalf = 96;     // token columns per issuer in the down projection
 static_assert(ExpCfg<1>::BN == 2 * kDownHalf, "down: two issuers split the tile's token columns");
@@ -366,7 +386,7 @@ template <int NA>
 constexpr size_t exp_smem_bytes() {
     using C = ExpCfg<NA>;
     size_t b = 1024;
-    b += static_cast<size_t>(C::BS) * C::BN * BK * 2;
+    b += static_cast<size_t>(C::BS) * C::SUB * C::BN * BK * 2;
     b += static_cast<size_t>(C::RE) * NA * (kRawEntry + kSfEntry);
     b += static_cast<size_t>(kES) * NA * BM * 4;
     b += 512;
@@ -382,11 +402,12 @@ __global__ void __launch_bounds__(kExpThreads, 1)
 tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                  const __grid_constant__ CUtensorMap tmB, ExpParams p) {
     using C = ExpCfg<NA>;
-    constexpr int BN = C::BN, RE = C::RE, AS = C::AS, BS = C::BS;
+    constexpr int BN = C::BN, RE = C::RE, AS = C::AS, BS = C::BS, SUB = C::SUB;
+    constexpr int kBStage = BN * BK * 2;  // one 64-input stage of token rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = smem;                                // [BS][BN * 128]
-    uint8_t* sRaw = sB + BS * BN * BK * 2;             // [RE][NA][16 KB], 128-byte swizzle
+    uint8_t* sRaw = sB + BS * SUB * kBStage;           // [RE][NA][16 KB], 128-byte swizzle
     uint8_t* sRawSf = sRaw + RE * NA * kRawEntry;      // [RE][NA][1 KB]: the entry's scale atoms
     int* sE = reinterpret_cast<int*>(sRawSf + RE * NA * kSfEntry);  // [kES][NA][128]
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(sE + kES * NA * BM);
@@ -406,6 +427,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int n_tiles = p.tiles[0].x;
     const int k_stages = p.K / BK;
     const int k_entries = (k_stages + kSub - 1) / kSub;
+    const int k_groups = (k_stages + SUB - 1) / SUB;  // hand-off groups per tile
     stamp_start(p.st);
 
     if (threadIdx.x == 0) {
@@ -487,10 +509,12 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 const int4 tl = p.tiles[1 + tile];
                 bool ok = true;
-                for (int ks = 0; ks < k_stages; ++ks) {
+                for (int gs = 0; gs < k_groups; ++gs) {
                     if (!mbar_wait(&b_empty[b], ph ^ 1, abort_flag, p.hdr, 51)) { ok = false; break; }
-                    mbar_expect_tx(&b_full[b], BN * BK * 2);
-                    tma_load_2d(sB + b * BN * BK * 2, &tmB, &b_full[b], ks * BK, tl.y);
+                    const int nsub = min(SUB, k_stages - gs * SUB);
+                    mbar_expect_tx(&b_full[b], nsub * kBStage);
+                    for (int j = 0; j < nsub; ++j)
+                        tma_load_2d(sB + (b * SUB + j) * kBStage, &tmB, &b_full[b], (gs * SUB + j) * BK, tl.y);
                     if (++b == BS) { b = 0; ph ^= 1; }
                 }
                 if (!ok) break;
@@ -518,7 +542,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * NA * BN + c_me);
                 bool ok = true;
-                for (int ks = 0; ks < k_stages; ++ks) {
+                for (int gs = 0; gs < k_groups; ++gs) {
                     if (!mbar_wait(&b_full[b], bph, abort_flag, p.hdr, 53) ||
                         !mbar_wait(&a_full[a], aph, abort_flag, p.hdr, 54)) {
                         ok = false;
@@ -526,14 +550,18 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                     tc_fence_after();
                     if (n_me > 0) {
-                        const uint32_t b_addr = smem_u32(sB + b * BN * BK * 2 + (NA == 2 ? 0 : c_me) * BK * 2);
-                        // A stage (a, m_me): TMEM columns, 8 per 16-wide K slice
-                        const uint32_t a_tm =
-                            tmem_base + static_cast<uint32_t>(exp_acol<NA>() + (a * NA + m_me) * 32);
+                        const int nsub = min(SUB, k_stages - gs * SUB);
+                        for (int j = 0; j < nsub; ++j) {
+                            const uint32_t b_addr =
+                                smem_u32(sB + (b * SUB + j) * kBStage + (NA == 2 ? 0 : c_me) * BK * 2);
+                            // A stage (a, m_me, j): TMEM columns, 8 per 16-wide K slice
+                            const uint32_t a_tm = tmem_base + static_cast<uint32_t>(
+                                                                  exp_acol<NA>() + ((a * NA + m_me) * SUB + j) * 32);
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_f16_ts(d0, a_tm + 8 * kk, sw128_desc(b_addr + kk * 32), idesc,
-                                       (ks > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                mma_f16_ts(d0, a_tm + 8 * kk, sw128_desc(b_addr + kk * 32), idesc,
+                                           (gs > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                        }
                         mma_commit(&a_empty[a]);
                         mma_commit(&b_empty[b]);
                     } else {
@@ -562,18 +590,24 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
             for (int m = 0; m < NA; ++m) {
                 const uint8_t* sm_ = m == 0 ? p.s1 : p.s3;
-                for (int i = lane; i < BM; i += 32) {
-                    const int r = tl.w * BM + i;
-                    int em = 0;
-                    if (r < p.rows_per_expert) {
-                        if (SFC)
-                            em = row_emax_canon(sm_ + (static_cast<size_t>(tl.x) * p.rows_per_expert + r) * (p.K / 32),
-                                                p.K / 512);
-                        else
-                            em = row_emax_sf(sf_row(sm_, tl.x, r, p.tiles_e, p.G), p.G);
+                int em[4];
+                if (SFC) {
+                    // rows lane + 32 k of the tile; a row past the expert gets 0
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = tl.w * BM + lane + 32 * k;
+                        em[k] = r < p.rows_per_expert
+                                    ? row_emax_canon(sm_ + (static_cast<size_t>(tl.x) * p.rows_per_expert + r) *
+                                                               (p.K / 32),
+                                                     p.K / 512)
+                                    : 0;
                     }
-                    sE[(slot * NA + m) * BM + i] = em;
+                } else {
+                    // a partial last tile's atoms are zero-padded: its missing rows read 0
+                    rows_emax_sf(sm_ + static_cast<size_t>(tl.x * p.tiles_e + tl.w) * p.G * 512, p.G, lane, em);
                 }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sE[(slot * NA + m) * BM + lane + 32 * k] = em[k];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&eref_full[slot]);
@@ -676,57 +710,69 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (NA == 2) n3 = ldg_nc_v4(c3);
             }
             bool ok = true;
-            for (int ks = 0; ks < k_stages; ++ks) {
-                const int blk = 2 * ks + half;
-                if (SFC && (ks & 7) == 0) {
-                    v1 = n1;
-                    v3 = n3;
-                    if (rvalid && (ks >> 3) + 1 < nvec) {
-                        n1 = ldg_nc_v4(c1 + 16 * ((ks >> 3) + 1));
-                        if (NA == 2) n3 = ldg_nc_v4(c3 + 16 * ((ks >> 3) + 1));
-                    }
-                }
-                const int sub = ks % kSub;  // stage within the raw entry
-                if (!__all_sync(0xffffffffu, (sub != 0 || mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59)) &&
-                                                 mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
+            for (int gs = 0; gs < k_groups; ++gs) {
+                const int nsub = min(SUB, k_stages - gs * SUB);
+                if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[a], aph ^ 1, abort_flag, p.hdr, 60))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();  // the MMAs that read this A stage have completed
-                int e1, e3;
-                if (SFC) {
-                    e1 = vec_byte(v1, blk & 15);
-                    e3 = NA == 2 ? vec_byte(v3, blk & 15) : 0;
-                } else {
-                    const int sfb = (sub >> 1) * 512 + sfo + (blk & 3);
-                    e1 = sRawSf[(r * NA) * kSfEntry + sfb];
-                    e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * kSfEntry + sfb] : 0;
-                }
+                tc_fence_after();  // the MMAs that read this A group have completed
+                int ended = -1;    // the raw entry whose last stage is in this group
+                for (int j = 0; j < nsub; ++j) {
+                    const int ks = gs * SUB + j;
+                    const int blk = 2 * ks + half;
+                    if (SFC && (ks & 7) == 0) {
+                        v1 = n1;
+                        v3 = n3;
+                        if (rvalid && (ks >> 3) + 1 < nvec) {
+                            n1 = ldg_nc_v4(c1 + 16 * ((ks >> 3) + 1));
+                            if (NA == 2) n3 = ldg_nc_v4(c3 + 16 * ((ks >> 3) + 1));
+                        }
+                    }
+                    const int sub = ks % kSub;  // stage within the raw entry
+                    if (sub == 0 &&
+                        !__all_sync(0xffffffffu, mbar_wait(&raw_full[r], rph, abort_flag, p.hdr, 59))) {
+                        ok = false;
+                        break;
+                    }
+                    int e1, e3;
+                    if (SFC) {
+                        e1 = vec_byte(v1, blk & 15);
+                        e3 = NA == 2 ? vec_byte(v3, blk & 15) : 0;
+                    } else {
+                        const int sfb = (sub >> 1) * 512 + sfo + (blk & 3);
+                        e1 = sRawSf[(r * NA) * kSfEntry + sfb];
+                        e3 = NA == 2 ? sRawSf[(r * NA + (NA - 1)) * kSfEntry + sfb] : 0;
+                    }
 #pragma unroll
-                for (int mm = 0; mm < NA; ++mm) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(sRaw + (r * NA + mm) * kRawEntry + row * 128 +
-                                                                      (((2 * sub + half) ^ swz) << 4));
-                    const uint16_t sh = f16_pow2(mm == 0 ? e1 - eref1 : e3 - eref3);
-                    const uint32_t sc2 = static_cast<uint32_t>(sh) | (static_cast<uint32_t>(sh) << 16);
-                    uint32_t w[16];
-                    e2m1x8_to_f16x8(raw.x, w[0], w[1], w[2], w[3]);
-                    e2m1x8_to_f16x8(raw.y, w[4], w[5], w[6], w[7]);
-                    e2m1x8_to_f16x8(raw.z, w[8], w[9], w[10], w[11]);
-                    e2m1x8_to_f16x8(raw.w, w[12], w[13], w[14], w[15]);
+                    for (int mm = 0; mm < NA; ++mm) {
+                        const uint4 raw = *reinterpret_cast<const uint4*>(
+                            sRaw + (r * NA + mm) * kRawEntry + row * 128 + (((2 * sub + half) ^ swz) << 4));
+                        const uint16_t sh = f16_pow2(mm == 0 ? e1 - eref1 : e3 - eref3);
+                        const uint32_t sc2 = static_cast<uint32_t>(sh) | (static_cast<uint32_t>(sh) << 16);
+                        uint32_t w[16];
+                        e2m1x8_to_f16x8(raw.x, w[0], w[1], w[2], w[3]);
+                        e2m1x8_to_f16x8(raw.y, w[4], w[5], w[6], w[7]);
+                        e2m1x8_to_f16x8(raw.z, w[8], w[9], w[10], w[11]);
+                        e2m1x8_to_f16x8(raw.w, w[12], w[13], w[14], w[15]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = hmul2(w[i], sc2);
-                    tmem_st16(a_lane + static_cast<uint32_t>((a * NA + mm) * 32), w);
+                        for (int i = 0; i < 16; ++i) w[i] = hmul2(w[i], sc2);
+                        tmem_st16(a_lane + static_cast<uint32_t>(((a * NA + mm) * SUB + j) * 32), w);
+                    }
+                    if (sub == kSub - 1 || ks == k_stages - 1) {  // the entry's last stage
+                        ended = r;
+                        if (++r == RE) { r = 0; rph ^= 1; }
+                    }
                 }
                 tmem_wait_st();
+                if (!ok) break;
                 tc_fence_before();
-                const bool last = sub == kSub - 1 || ks == k_stages - 1;  // the entry's last stage
-                if (last) fence_proxy_async();  // the raw codes were read here; the producer's TMA rewrites them
+                if (ended >= 0) fence_proxy_async();  // the raw codes were read here; the producer's TMA rewrites them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&a_full[a]);
-                    if (last) mbar_arrive(&raw_empty[r]);
+                    if (ended >= 0) mbar_arrive(&raw_empty[ended]);
                 }
-                if (last && ++r == RE) { r = 0; rph ^= 1; }
                 if (++a == AS) { a = 0; aph ^= 1; }
             }
             if (!ok) break;
