@@ -307,10 +307,10 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // a small ring), 3 token producer (one TMA box of BN token rows per stage
 // into a BS-deep ring; in a tile of fewer rows the rest of the box is rows
 // of the next expert or zero fill, which the MMAs never read: one copy per
-// stage costs less than several smaller ones), 4..7 and 17..20 epilogue (two
-// sets, one warp per TMEM lane quadrant in each, alternating 16-token
-// chunks), 8..15 dequantisation (raw ring -> f16 A stages of an AS-deep ring
-// in TMEM).
+// stage costs less than several smaller ones), 4..7 and 17..24 epilogue
+// (three sets, one warp per TMEM lane quadrant in each, taking 16-token
+// chunks in turn), 8..15 dequantisation (raw ring -> f16 A stages of an
+// AS-deep ring in TMEM).
 //
 // What bounds it, measured on this part: a thread needs about 60 ns (100 ns
 // when its SM sub-partition is also running dequantising warps) to issue one
@@ -361,7 +361,8 @@ constexpr int kSub = 4;         // 64-input stages per raw-weight entry
 constexpr int kRawEntry = BM * kSub * BK / 2;  // 16 KB of packed E2M1: 128 rows x 128 bytes
 constexpr int kSfEntry = kSub / 2 * 512;       // the entry's two prepared scale atoms
 static_assert(kSub % ExpCfg<1>::SUB == 0 && kSub % ExpCfg<2>::SUB == 0, "a hand-off group ends at most one entry");
-constexpr int kExpThreads = 672;  // 21 warps: 16 is the second MMA issuer, 17..20 a second epilogue set
+constexpr int kEpiSets = 3;       // epilogue warp sets (4 warps each: 4..7, then 17.. in fours)
+constexpr int kExpThreads = 32 * (17 + 4 * (kEpiSets - 1));  // 16 is the second MMA issuer
 constexpr int kDownHalf = 96;     // token columns per issuer in the down projection
 static_assert(ExpCfg<1>::BN == 2 * kDownHalf, "down: two issuers split the tile's token columns");
 
@@ -445,11 +446,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 2);
-            mbar_init(&acc_empty[i], 8);  // both epilogue sets
+            mbar_init(&acc_empty[i], 4 * kEpiSets);  // every epilogue warp
         }
         for (int i = 0; i < kES; ++i) {
             mbar_init(&eref_full[i], 1);
-            mbar_init(&eref_empty[i], 16);  // 8 epilogue + 8 dequantising warps
+            mbar_init(&eref_empty[i], 4 * kEpiSets + 8);  // epilogue + dequantising warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -614,10 +615,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 17) {
         // ---------------------------- epilogue -------------------------------
-        // two sets of four warps (4..7 and 17..20), one warp per TMEM lane
-        // quadrant in each; set h takes the 16-token chunks 2 j + h
+        // kEpiSets sets of four warps (4..7, then 17.. in fours), one warp per
+        // TMEM lane quadrant in each; set h takes the 16-token chunks
+        // kEpiSets j + h
         const int wr = warp & 3;
-        const int eset = warp >= 17 ? 1 : 0;
+        const int eset = warp >= 17 ? 1 + (warp - 17) / 4 : 0;
         const int m = wr * 32 + lane;
         int it = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
@@ -638,7 +640,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const bool valid = r < p.rows_per_expert;
             const int eref1 = sE[(slot * NA + 0) * BM + m];
             const int eref3 = NA == 2 ? sE[(slot * NA + (NA - 1)) * BM + m] : 0;
-            for (int n0 = 16 * eset; n0 < n_used; n0 += 32) {
+            for (int n0 = 16 * eset; n0 < n_used; n0 += 16 * kEpiSets) {
                 // tokens n0 .. n0 + cnt - 1 of the tile are real; lane i < cnt
                 // fetches token i's exponent for the whole warp
                 const int cnt = min(16, nrows - n0);
