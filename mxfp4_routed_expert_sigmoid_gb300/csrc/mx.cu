@@ -397,7 +397,14 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if constexpr (GG) {  // one box of 32-bit words: 128 rows x 272 bytes (K is a multiple of 512)
             tma_load_2d(st, tm, bar, c.ks * (kGgRowBytes / 4), y);
         } else {
-            for (int cc = 0; cc < nch; ++cc) tma_load_2d(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y);
+            // weight codes pass through L2 once (the last unit of an expert
+            // reads them for the last time), so they are let go first; with
+            // several units per expert the earlier reads ask L2 to keep them
+            const uint64_t pol = c.grp + 1 < c.ngrp ? l2_policy_evict_last() : l2_policy_evict_first();
+            for (int cc = 0; cc < nch; ++cc)
+                tma_load_2d_hint(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y, pol);
+        }
+        if constexpr (!GG) {
             if constexpr (CANON) {  // 16 scale bytes of each of the 128 rows (K is a multiple of 512)
                 tma_load_2d(st + offRaw, c.mat == 0 ? &tmS : &tmS3, bar, c.ks * 16, y);
             } else {  // the stage's prepared atoms, consecutive within the tile
@@ -408,11 +415,16 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
     };
+    // the activation side of a unit is read again for every row tile of both
+    // matrices (48 times at the K3 widths), spread over the unit's whole
+    // stream: L2 is asked to keep it while the weights stream past
     auto issue_b = [&](const Cursor& c, uint8_t* st, uint64_t* bar) {
         const int c0 = c.ks * kChunks;
         const int nch = min(kChunks, p.KC - c0);
-        bulk_load(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, bar);
-        bulk_load(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024, bar);
+        const uint64_t pol = l2_policy_evict_last();
+        bulk_load_hint(st + offB, p.bq + c.u * p.bq_ustride + static_cast<size_t>(c0) * NB, nch * NB, bar, pol);
+        bulk_load_hint(st + offSB, p.bsf + c.u * p.bsf_ustride + static_cast<size_t>(2 * c0) * 512, nch * 1024, bar,
+                       pol);
     };
     auto a_bytes = [&](const Cursor& c) {
         if (GG) return static_cast<uint32_t>(kGgStageBytes);
