@@ -394,24 +394,22 @@ mx_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int nch = min(kChunks, p.KC - c0);
         const CUtensorMap* tm = c.mat == 0 ? &tmA : &tmA3;
         const int y = e * p.rows + c.tile * 128;
+        // weights pass through L2 once (the last unit of an expert reads them
+        // for the last time), so they are let go first; with several units
+        // per expert the earlier reads ask L2 to keep them
+        const uint64_t pol = c.grp + 1 < c.ngrp ? l2_policy_evict_last() : l2_policy_evict_first();
         if constexpr (GG) {  // one box of 32-bit words: 128 rows x 272 bytes (K is a multiple of 512)
-            tma_load_2d(st, tm, bar, c.ks * (kGgRowBytes / 4), y);
+            tma_load_2d_hint(st, tm, bar, c.ks * (kGgRowBytes / 4), y, pol);
         } else {
-            // weight codes pass through L2 once (the last unit of an expert
-            // reads them for the last time), so they are let go first; with
-            // several units per expert the earlier reads ask L2 to keep them
-            const uint64_t pol = c.grp + 1 < c.ngrp ? l2_policy_evict_last() : l2_policy_evict_first();
             for (int cc = 0; cc < nch; ++cc)
                 tma_load_2d_hint(st + cc * kChunkA, tm, bar, (c0 + cc) * 128, y, pol);
-        }
-        if constexpr (!GG) {
             if constexpr (CANON) {  // 16 scale bytes of each of the 128 rows (K is a multiple of 512)
-                tma_load_2d(st + offRaw, c.mat == 0 ? &tmS : &tmS3, bar, c.ks * 16, y);
+                tma_load_2d_hint(st + offRaw, c.mat == 0 ? &tmS : &tmS3, bar, c.ks * 16, y, pol);
             } else {  // the stage's prepared atoms, consecutive within the tile
                 const int g0 = 2 * c0, ng = min(2 * kChunks, p.G - g0);
-                bulk_load(st + offSA,
-                          p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.G + g0) * 512,
-                          ng * 512, bar);
+                bulk_load_hint(st + offSA,
+                               p.sf[c.mat] + (static_cast<size_t>(e * p.tiles + c.tile) * p.G + g0) * 512,
+                               ng * 512, bar, pol);
             }
         }
     };
