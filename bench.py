@@ -43,7 +43,12 @@ EXPERT_MATRIX_BYTES = None  # filled per config
 # these four workloads at full size (dram__bytes_read.sum +
 # dram__bytes_write.sum, one pass, mean over the captured launches of the
 # kernel; profiles/launches_<workload>.md give the command).
-TRAFFIC = {}
+TRAFFIC = {
+    ("decode_t1", "split", "prepared", "decode_up"): 187.6e6,
+    ("verify_t8", "split", "prepared", "decode_up"): 379.1e6,
+    ("chunk_t512", "split", "prepared", "units_up"): 9117.2e6,
+    ("block_t8192", "split", "prepared", "expert_up"): 8460.2e6,
+}
 
 
 def parse():
