@@ -329,20 +329,21 @@ tc_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // ---------------------------------------------------------------------------
 template <int NA>
 struct ExpCfg;
-// RE: raw-weight entries (four stages each), AS: dequantised A stages (in
-// TMEM), BS: token (B) stages, NBUF: accumulator buffers in TMEM.  TMEM (512
-// columns of 128 lanes) holds NBUF x NA accumulators of BN fp32 columns, then
-// AS x NA A stages of 32 columns (64 f16 inputs per row).  The up projection
-// takes 192 token rows per tile with one accumulator buffer (2 x 192 + 2 x 2
-// x 32 = 512): its epilogue does not overlap the next tile's MMAs, which
-// costs less than issuing twice as many 96-wide MMAs would.  The down
-// projection takes 192 rows with two buffers (2 x 192 + 4 x 32 = 512), so its
-// epilogue runs under the next tile's MMAs.  SUB: 64-input stages handed over
-// together (one set of barrier waits, arrivals and commits per SUB stages;
-// AS and BS count such groups).  Every hand-off costs the dequantising warps
+// RE: raw-weight entries (four stages each), AS: dequantised A groups (in
+// TMEM), BS: token (B) groups, NBUF: accumulator buffers in TMEM, SUB:
+// 64-input stages per group, handed over together (one set of barrier waits,
+// arrivals and commits per group).  TMEM (512 columns of 128 lanes) holds NBUF
+// x NA accumulators of BN fp32 columns, then AS x NA x SUB A stages of 32
+// columns (64 f16 inputs per row).  The up projection takes 192 token rows
+// per tile with one accumulator buffer (2 x 192 + 2 x 2 x 32 = 512): its
+// epilogue does not overlap the next tile's MMAs, which costs less than
+// issuing twice as many 96-wide MMAs would.  The down projection takes 192
+// rows with two buffers (2 x 192 + 2 x 2 x 32 = 512), so its epilogue runs
+// under the next tile's MMAs.  Every hand-off costs the dequantising warps
 // and the issuers a fixed time, so the down projection, whose TMEM has room
-// for two-stage A groups, takes them in pairs; the up projection's A ring
-// (two single stages) cannot grow without losing the dequantise / MMA overlap.
+// for two-stage A groups, takes its stages in pairs; the up projection's A
+// ring (two single stages) cannot grow without losing the dequantise / MMA
+// overlap.
 template <>
 struct ExpCfg<2> {
     static constexpr int BN = 192, RE = 3, AS = 2, BS = 4, NBUF = 1, SUB = 1, TMEM_COLS = 512;
