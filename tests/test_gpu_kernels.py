@@ -119,9 +119,27 @@ def _route_case(k3, cfg, T=None):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode_t1", None), ("verify_t8", None),
-                                    ("decode_t1", 3), ("chunk_t512", 40), ("chunk_t512", 100)])
+                                    ("decode_t1", 3), ("chunk_t512", 40), ("chunk_t512", 100),
+                                    ("chunk_t512", 3000)])
 def test_route_matches_oracle(k3, name, T):
+    """T = 3000 goes through the warp-per-token top-k (from 2048 tokens on)."""
     _route_case(k3, synth.CONFIGS[name], T)
+
+
+def test_route_warp_topk_equals_block_topk(k3):
+    """The two top-k kernels give bitwise the same slots and weights: the first
+    2048 tokens of a 3000-token batch (one block per token) against the same
+    rows inside the whole batch (one warp per token)."""
+    import torch
+    cfg = synth.custom("chunk_t512", T=3000)
+    dense = synth.dense_inputs(cfg)
+    x = to_dev(dense["hidden"], "cuda")
+    args = (to_dev(dense["router_w"], "cuda"), to_dev(dense["router_b"], "cuda"), cfg.k)
+    i_all, w_all, _ = k3.k3moe_route(x, *args)
+    i_blk, w_blk, _ = k3.k3moe_route(x[:2048].contiguous(), *args)
+    torch.cuda.synchronize()
+    assert torch.equal(i_all[:2048], i_blk)
+    assert torch.equal(w_all[:2048], w_blk)
 
 
 def test_route_hot_experts(k3):
