@@ -873,26 +873,43 @@ __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
                    int bn_up, int bn_dn, int m_up, int m_dn, int4* up, int4* dn, int cap, uint64_t* st) {
     StampScope stamp(st);
+    // every CTA scans the per-expert chunk counts (E <= 1024, one per thread)
+    // and writes its share of the list entries
     __shared__ int base[1024 + 1];
+    __shared__ int wsum[32];
+    __shared__ int total_s;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     for (int pass = 0; pass < 2; ++pass) {
         const int bn = pass == 0 ? bn_up : bn_dn;
-        for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = (counts[e] + bn - 1) / bn;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int run = 0;
-            for (int e = 0; e < E; ++e) {
-                const int c = base[e];
-                base[e] = run;
-                run += c;
-            }
-            base[E] = run;
+        const int v = tid < E ? (counts[tid] + bn - 1) / bn : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
+        if (lane == 31) wsum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            const int w = lane < static_cast<int>(blockDim.x >> 5) ? wsum[lane] : 0;
+            int wi = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += t;
+            }
+            wsum[lane] = wi - w;  // exclusive offsets of the warps
+            if (lane == 31) total_s = wi;
+        }
+        __syncthreads();
+        if (tid < E) base[tid] = wsum[wid] + incl - v;
+        if (tid == 0) base[E] = total_s;
         __syncthreads();
         const int mt_n = pass == 0 ? m_up : m_dn;
         const int n = min(base[E] * mt_n, cap);
         int4* list = pass == 0 ? up : dn;
-        if (threadIdx.x == 0) list[0] = make_int4(n, 0, 0, 0);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        if (blockIdx.x == 0 && tid == 0) list[0] = make_int4(n, 0, 0, 0);
+        for (int i = blockIdx.x * blockDim.x + tid; i < n; i += gridDim.x * blockDim.x) {
             // expert of entry i: largest e with base[e] * mt_n <= i
             int lo = 0, hi = E - 1;
             while (lo < hi) {
@@ -906,7 +923,7 @@ build_tiles_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
             const int cnt = counts[e];
             list[1 + i] = make_int4(e, offsets[e] + c * bn, min(bn, cnt - c * bn), mt);
         }
-        __syncthreads();  // base[] is rebuilt for the next pass
+        __syncthreads();  // base[] and wsum[] are rebuilt for the next pass
     }
 }
 
@@ -1010,7 +1027,7 @@ cudaError_t launch_grouped(const GroupedArgs& g, cudaStream_t s) {
     gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(g.x, g.perm, P, g.k, g.d, g.xp, g.xp_exp, g.h_amax,
                                                    trace_stamp("gather_rows"));
     trace_mark("gather_rows", s);
-    build_tiles_kernel<<<1, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUpRows, kDownRows, (g.f + BM - 1) / BM,
+    build_tiles_kernel<<<g.num_sms, 1024, 0, s>>>(g.counts, g.offsets, g.E, kUpRows, kDownRows, (g.f + BM - 1) / BM,
                                           (g.d + BM - 1) / BM, tiles_up, tiles_dn, cap, trace_stamp("build_tiles"));
     trace_mark("build_tiles", s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -501,17 +501,39 @@ perm_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int P, int32_t* counts,
     extern __shared__ int sm[];  // [2 * E]
     int* tot = sm;
     int* flag = sm + E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            int* p = chunk_cnt + static_cast<size_t>(c) * E + e;
-            const int v = *p;
-            *p = run;  // exclusive within the expert
-            run += v;
+    // each thread scans the chunk counts of its (at most four) experts, the
+    // loads of 16 chunks x 4 experts issued together
+    constexpr int kBatch = 16;
+    int run[4] = {0, 0, 0, 0};
+    for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+        int v[4][kBatch];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * blockDim.x;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                v[q][i] = (e < E && c0 + i < nchunks) ? chunk_cnt[static_cast<size_t>(c0 + i) * E + e] : 0;
         }
-        tot[e] = run;
-        counts[e] = run;
-        flag[e] = run > 0 ? 1 : 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * blockDim.x;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (e < E && c0 + i < nchunks) {
+                    chunk_cnt[static_cast<size_t>(c0 + i) * E + e] = run[q];  // exclusive within the expert
+                    run[q] += v[q][i];
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int e = threadIdx.x + q * blockDim.x;
+        if (e < E) {
+            tot[e] = run[q];
+            counts[e] = run[q];
+            flag[e] = run[q] > 0 ? 1 : 0;
+        }
     }
     __syncthreads();
     // scan in chunks of 1024 (block_exclusive_scan handles up to 1024 entries)
