@@ -231,22 +231,29 @@ route_topk_kernel(RouteArgs a) {
 }
 
 // Top-k of many tokens (the permutation path, no active list), one warp per
-// token (used from kTopkWarpMinT tokens on): lane l holds the keys of experts
-// l, l + 32, ... (up to 32 each) in registers.  Each of the k rounds takes the warp's largest remaining key (a
-// butterfly maximum over the lanes' own maxima); the lane that holds it drops
-// it and recomputes its maximum.  Keys are unique, so the slots come out in
+// token: lane l holds the keys of experts l, l + 32, ... (up to 32 each) in
+// registers.  The k-th largest of the 32 lane maxima, M, bounds the selection
+// from below (the k lanes whose maxima are >= M hold k keys >= M), so the
+// chosen keys are among those >= M; when at most kCandW of them qualify they
+// are gathered in shared memory and ranked by counting.  Otherwise k rounds
+// each take the warp's largest remaining key (a butterfly maximum over the
+// lanes' own maxima).  Keys are unique, so either way the slots come out in
 // key order exactly as in the one-CTA-per-token kernel, and the weights are
 // formed the same way (w = s / sum(s), the sum in slot order): the result is
-// bitwise that kernel's, without a 1024-thread block per token.
-constexpr int kTopkWarpTokens = 8;  // tokens (warps) per CTA
-constexpr int kTopkWarpMinT = 2048; // below: one block per token
+// bitwise that kernel's.
+constexpr int kTopkWarpTokens = 8;   // tokens (warps) per CTA
+constexpr int kTopkWarpMinT = 2048;  // up to this many tokens: one block per token
+constexpr int kCandW = 64;           // candidates ranked by counting
 __global__ void __launch_bounds__(32 * kTopkWarpTokens)
 route_topk_warp_kernel(RouteArgs a) {
+    __shared__ uint64_t cand_s[kTopkWarpTokens][kCandW];
+    __shared__ int slot_s[kTopkWarpTokens][32];
     pdl_wait();
     pdl_trigger();
     StampScope stamp(a.st_b);
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarpTokens + (threadIdx.x >> 5);
+    constexpr uint32_t kFull = 0xffffffffu;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int t = blockIdx.x * kTopkWarpTokens + wid;
     if (t >= a.T) return;
     const float* lrow = a.logits + static_cast<size_t>(t) * a.E;
     uint64_t key[kMaxE / 32];
@@ -262,32 +269,62 @@ route_topk_warp_kernel(RouteArgs a) {
         }
     }
     // a logit that is not finite, or a NaN bias, leaves the selection undefined: flagged
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(a.hdr, K3MOE_ERR_NONFINITE, 1);
+    if (__any_sync(kFull, bad) && lane == 0) set_error(a.hdr, K3MOE_ERR_NONFINITE, 1);
     uint64_t mine = 0;
 #pragma unroll
     for (int j = 0; j < kMaxE / 32; ++j) mine = key[j] > mine ? key[j] : mine;
-    int slot_e = 0;  // lane r < k: the expert of slot r
-    for (int r = 0; r < a.k; ++r) {
-        uint64_t m = mine;
+    // rank of this lane's maximum among the lane maxima; M = the one ranked k - 1
+    int rk = 0;
+    for (int o = 1; o < 32; ++o) rk += __shfl_sync(kFull, mine, (lane + o) & 31) > mine ? 1 : 0;
+    const uint32_t at = __ballot_sync(kFull, rk == a.k - 1 && mine != 0);
+    const uint64_t M = at ? __shfl_sync(kFull, mine, __ffs(at) - 1) : 0;
+    int cnt = 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t v = __shfl_xor_sync(0xffffffffu, m, o);
-            m = v > m ? v : m;
-        }
-        if (mine == m) {  // this lane holds the round's key: drop it
-            uint64_t nm = 0;
+    for (int j = 0; j < kMaxE / 32; ++j) cnt += (M != 0 && key[j] >= M) ? 1 : 0;
+    int incl = cnt;
 #pragma unroll
-            for (int j = 0; j < kMaxE / 32; ++j) {
-                if (key[j] == m) key[j] = 0;
-                nm = key[j] > nm ? key[j] : nm;
-            }
-            mine = nm;
-        }
-        if (lane == r) slot_e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(m));
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
     }
+    const int n = __shfl_sync(kFull, incl, 31);
+    if (M != 0 && n <= kCandW) {
+        int pos = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < kMaxE / 32; ++j)
+            if (key[j] >= M) cand_s[wid][pos++] = key[j];
+        __syncwarp();
+        for (int c = lane; c < n; c += 32) {
+            const uint64_t kc = cand_s[wid][c];
+            int r = 0;
+            for (int q = 0; q < n; ++q) r += cand_s[wid][q] > kc ? 1 : 0;
+            if (r < a.k) slot_s[wid][r] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kc));
+        }
+    } else {
+        for (int r = 0; r < a.k; ++r) {
+            uint64_t m = mine;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t v = __shfl_xor_sync(kFull, m, o);
+                m = v > m ? v : m;
+            }
+            if (mine == m) {  // this lane holds the round's key: drop it
+                uint64_t nm = 0;
+#pragma unroll
+                for (int j = 0; j < kMaxE / 32; ++j) {
+                    if (key[j] == m) key[j] = 0;
+                    nm = key[j] > nm ? key[j] : nm;
+                }
+                mine = nm;
+            }
+            if (lane == 0) slot_s[wid][r] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(m));
+        }
+    }
+    __syncwarp();
+    const int slot_e = lane < a.k ? slot_s[wid][lane] : 0;  // lane r < k: the expert of slot r
     const float sj = lane < a.k ? sigmoid_f32(lrow[slot_e]) : 0.0f;
     float sum = 0.0f;
-    for (int j = 0; j < a.k; ++j) sum += __shfl_sync(0xffffffffu, sj, j);
+    for (int j = 0; j < a.k; ++j) sum += __shfl_sync(kFull, sj, j);
     if (lane < a.k) {
         a.idx[static_cast<size_t>(t) * a.k + lane] = slot_e;
         a.wts[static_cast<size_t>(t) * a.k + lane] = sj / sum;
@@ -664,10 +701,9 @@ cudaError_t launch_route_noalloc(RouteArgs a, cudaStream_t s) {
 cudaError_t launch_topk(const RouteArgs& a_in, cudaStream_t s) {
     RouteArgs a = a_in;
     a.active = nullptr;  // the permutation kernels list the active experts
-    // a warp takes about 20 us per token against about 3 us for a 1024-thread
-    // block, but 1,216 warps run at once against 304 blocks: the warp kernel
-    // wins from a few thousand tokens on (block workload, 8192 tokens: 104
-    // against 150 us; 512 tokens: 23 against 9 us)
+    // a block per token finishes a token sooner (9 us for 512 tokens against
+    // 15 us with warps), warps cover more tokens at once (58 us for 8192
+    // tokens against 150 us with blocks)
     if (a.T <= kTopkWarpMinT) return launch_route_topk(a, s);
     a.st_b = trace_stamp("route_topk");
     const cudaError_t e = launch_pdl(route_topk_warp_kernel, dim3((a.T + kTopkWarpTokens - 1) / kTopkWarpTokens),

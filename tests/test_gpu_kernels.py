@@ -122,14 +122,14 @@ def _route_case(k3, cfg, T=None):
                                     ("decode_t1", 3), ("chunk_t512", 40), ("chunk_t512", 100),
                                     ("chunk_t512", 3000)])
 def test_route_matches_oracle(k3, name, T):
-    """T = 3000 goes through the warp-per-token top-k (from 2048 tokens on)."""
+    """T = 3000 goes through the warp-per-token top-k (beyond 2048 tokens)."""
     _route_case(k3, synth.CONFIGS[name], T)
 
 
 def test_route_warp_topk_equals_block_topk(k3):
     """The two top-k kernels give bitwise the same slots and weights: the first
-    2048 tokens of a 3000-token batch (one block per token) against the same
-    rows inside the whole batch (one warp per token)."""
+    2048 tokens of a 3000-token batch on their own (one block per token)
+    against the same rows inside the whole batch (one warp per token)."""
     import torch
     cfg = synth.custom("chunk_t512", T=3000)
     dense = synth.dense_inputs(cfg)
@@ -162,15 +162,18 @@ def test_route_ties_lower_index(k3):
     assert np.allclose(wts.cpu().numpy(), 1.0 / k)
 
 
+@pytest.mark.parametrize("T", [2, 2100])
 @pytest.mark.parametrize("case", ["all_equal", "one_tied_per_warp"])
-def test_route_ties_wide(k3, case):
-    """Equal scores at the decode width (896 experts, top-16), both ways the
-    selection can run: all scores equal puts hundreds of keys above the
-    warp-maximum bound (bisection), one tied expert per warp puts exactly k
-    there (ranked directly).  Ties go to the lower index in both."""
+def test_route_ties_wide(k3, case, T):
+    """Equal scores at the decode width (896 experts, top-16), both ways each
+    top-k kernel can run: all scores equal puts hundreds of keys above the
+    maximum bound (bisection in the block kernel, k extraction rounds in the
+    warp kernel), one tied expert per warp puts exactly k there (ranked
+    directly).  Ties go to the lower index in all four.  T = 2 runs the
+    block-per-token kernel, T = 2100 the warp-per-token one."""
     import torch
 
-    E, k, T, d = 896, 16, 2, 64
+    E, k, d = 896, 16, 64
     x = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((E, d), dtype=torch.bfloat16, device="cuda")
     b = torch.zeros(E, dtype=torch.float32, device="cuda")
@@ -184,10 +187,11 @@ def test_route_ties_wide(k3, case):
     assert r["idx"].tolist() == [want] * T
 
 
-def test_route_nonfinite_flag(k3):
+@pytest.mark.parametrize("T", [None, 2100])
+def test_route_nonfinite_flag(k3, T):
     import torch
 
-    cfg = synth.CONFIGS["tiny"]
+    cfg = synth.CONFIGS["tiny"] if T is None else synth.custom("tiny", T=T)
     dense = synth.dense_inputs(cfg)
     x = to_dev(dense["hidden"], "cuda").clone()
     x[1, 3] = float("nan")
