@@ -358,6 +358,10 @@ k3moe_status k3moe_forward_routed(const k3moe_layer_desc* desc, const uint16_t* 
  * (its contents), workspace, size, T, stream and device runs the forward
  * directly and records it into a CUDA graph (host and driver objects, no
  * device memory); a later call with the same arguments replays that graph.
+ * When the batch is at most 1 MiB (T * width * 2 bytes) the graph also holds
+ * the two copies, from and to two page-locked host buffers of that size that
+ * the library allocates with it: a replay then copies hidden into one with
+ * memcpy, launches the graph, waits and copies the other into out_host.
  * The library keeps the 8 most recently used such graphs for the life of the
  * process.  A graph reads the buffers the descriptor points to, so weights
  * rewritten in place are seen; point the descriptor at new buffers (a new

@@ -814,7 +814,13 @@ namespace {
 // stream and device mean the same kernels on the same addresses.  A graph
 // references the buffers, not their contents, so new weights written in
 // place are read by the next replay.  At most kHostGraphs entries, the least
-// recently used one replaced.
+// recently used one replaced.  For small batches (kHostStageMax bytes of
+// tokens or less) the entry also owns two page-locked host buffers and the
+// graph copies the tokens in from one and the output out to the other, so a
+// call is two host memcpys, one graph launch and one wait instead of three
+// stream operations; larger batches copy straight from and to the caller's
+// buffers around the graph.
+constexpr size_t kHostStageMax = 1 << 20;
 struct HostGraph {
     k3moe_layer_desc desc;
     const void* ws;
@@ -823,7 +829,14 @@ struct HostGraph {
     cudaStream_t s;
     int dev;
     cudaGraphExec_t exec;
+    void* pin_in;  // page-locked staging of a small batch, or null
+    void* pin_out;
     uint64_t used;
+};
+struct HostGraphHit {
+    cudaGraphExec_t exec;
+    void* pin_in;
+    void* pin_out;
 };
 constexpr int kHostGraphs = 8;
 std::mutex g_host_mu;
@@ -836,31 +849,80 @@ bool same_key(const HostGraph& h, const k3moe_layer_desc* d, const void* ws, siz
            std::memcmp(&h.desc, d, sizeof(k3moe_layer_desc)) == 0;
 }
 
-// the cached graph for these arguments, or null
-cudaGraphExec_t host_graph_find(const k3moe_layer_desc* d, const void* ws, size_t ws_bytes, int32_t T,
-                                cudaStream_t s, int dev) {
+// the cached graph for these arguments (exec null when there is none)
+HostGraphHit host_graph_find(const k3moe_layer_desc* d, const void* ws, size_t ws_bytes, int32_t T,
+                             cudaStream_t s, int dev) {
     std::lock_guard<std::mutex> lock(g_host_mu);
     for (auto& h : g_host)
         if (same_key(h, d, ws, ws_bytes, T, s, dev)) {
             h.used = ++g_host_clock;
-            return h.exec;
+            return {h.exec, h.pin_in, h.pin_out};
         }
-    return nullptr;
+    return {nullptr, nullptr, nullptr};
 }
 
-// capture the forward (nothing runs) on a private stream and keep the graph
-void host_graph_add(const k3moe_layer_desc* d, const uint16_t* in_dev, int32_t T, uint16_t* out_dev, void* ws,
-                    size_t need, size_t ws_bytes, cudaStream_t s, int dev) {
+// Copies n 16-bit words between device memory and mapped page-locked host
+// memory: for a batch of a few KiB the loads and stores of one small grid
+// reach the host over the chip-to-chip link sooner than a copy-engine
+// transfer is set up.  16-byte words when both ends allow, else 2-byte ones.
+__global__ void stage_copy_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0) {
+        const size_t n16 = n / 8;
+        const uint4* s16 = reinterpret_cast<const uint4*>(src);
+        uint4* d16 = reinterpret_cast<uint4*>(dst);
+        for (size_t i = tid; i < n16; i += stride) d16[i] = s16[i];
+        for (size_t i = n16 * 8 + tid; i < n; i += stride) dst[i] = src[i];
+    } else {
+        for (size_t i = tid; i < n; i += stride) dst[i] = src[i];
+    }
+}
+
+cudaError_t stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+    const size_t n = bytes / 2;
+    const int threads = 256;
+    const size_t want = (n / 8 + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > 256 ? 256 : want));
+    stage_copy_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), n);
+    return cudaGetLastError();
+}
+
+void free_pinned(void* a, void* b) {
+    if (a) cudaFreeHost(a);
+    if (b) cudaFreeHost(b);
+}
+
+// capture the forward (nothing runs) on a private stream and keep the graph;
+// with staging buffers the copies from and to them are part of the graph
+void host_graph_add(const k3moe_layer_desc* d, uint16_t* in_dev, int32_t T, uint16_t* out_dev, void* ws,
+                    size_t need, size_t ws_bytes, size_t bytes, cudaStream_t s, int dev) {
+    void* pin_in = nullptr;
+    void* pin_out = nullptr;
+    void* map_in = nullptr;  // their device addresses
+    void* map_out = nullptr;
+    if (bytes <= kHostStageMax && (cudaHostAlloc(&pin_in, bytes, cudaHostAllocMapped) != cudaSuccess ||
+                                   cudaHostAlloc(&pin_out, bytes, cudaHostAllocMapped) != cudaSuccess ||
+                                   cudaHostGetDevicePointer(&map_in, pin_in, 0) != cudaSuccess ||
+                                   cudaHostGetDevicePointer(&map_out, pin_out, 0) != cudaSuccess)) {
+        // no staging: the graph holds the forward alone
+        free_pinned(pin_in, pin_out);
+        pin_in = pin_out = nullptr;
+        cudaGetLastError();
+    }
     cudaStream_t cs = nullptr;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
         cudaGetLastError();
+        free_pinned(pin_in, pin_out);
         return;
     }
     cudaGraph_t g = nullptr;
     cudaGraphExec_t exec = nullptr;
     bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
     if (ok) {
-        ok = k3moe_forward(d, in_dev, T, out_dev, ws, need, cs) == K3MOE_OK;
+        if (pin_in) ok = stage_copy(map_in, in_dev, bytes, cs) == cudaSuccess;
+        ok = ok && k3moe_forward(d, in_dev, T, out_dev, ws, need, cs) == K3MOE_OK;
+        if (pin_out) ok = ok && stage_copy(out_dev, map_out, bytes, cs) == cudaSuccess;
         ok = cudaStreamEndCapture(cs, &g) == cudaSuccess && ok;
     }
     ok = ok && cudaGraphInstantiate(&exec, g, 0) == cudaSuccess;
@@ -868,6 +930,7 @@ void host_graph_add(const k3moe_layer_desc* d, const uint16_t* in_dev, int32_t T
     cudaStreamDestroy(cs);
     if (!ok) {
         if (exec) cudaGraphExecDestroy(exec);
+        free_pinned(pin_in, pin_out);
         cudaGetLastError();
         return;
     }
@@ -876,6 +939,7 @@ void host_graph_add(const k3moe_layer_desc* d, const uint16_t* in_dev, int32_t T
     for (auto& h : g_host)
         if (!h.exec || h.used < slot->used) slot = &h;
     if (slot->exec) cudaGraphExecDestroy(slot->exec);
+    free_pinned(slot->pin_in, slot->pin_out);
     slot->desc = *d;
     slot->ws = ws;
     slot->ws_bytes = ws_bytes;
@@ -883,6 +947,8 @@ void host_graph_add(const k3moe_layer_desc* d, const uint16_t* in_dev, int32_t T
     slot->s = s;
     slot->dev = dev;
     slot->exec = exec;
+    slot->pin_in = pin_in;
+    slot->pin_out = pin_out;
     slot->used = ++g_host_clock;
 }
 }  // namespace
@@ -909,14 +975,22 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     const bool plain = g_trace.mode == 0 && g_inject == 0 && cudaStreamIsCapturing(s, &cap) == cudaSuccess &&
                        cap == cudaStreamCaptureStatusNone;
+    const HostGraphHit hit = plain ? host_graph_find(desc, ws, ws_bytes, T, s, dev) : HostGraphHit{};
+    if (hit.exec && hit.pin_in) {
+        // the graph copies in from and out to its own page-locked buffers
+        std::memcpy(hit.pin_in, hidden_host, bytes);
+        if (cudaGraphLaunch(hit.exec, s) != cudaSuccess) return K3MOE_ERR_CUDA;
+        const k3moe_status done = cuda_status(cudaStreamSynchronize(s));
+        if (done == K3MOE_OK) std::memcpy(out_host, hit.pin_out, bytes);
+        return done;
+    }
     if (cudaMemcpyAsync(in_dev, hidden_host, bytes, cudaMemcpyHostToDevice, s)) return K3MOE_ERR_CUDA;
-    cudaGraphExec_t exec = plain ? host_graph_find(desc, ws, ws_bytes, T, s, dev) : nullptr;
-    if (exec) {
-        if (cudaGraphLaunch(exec, s) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (hit.exec) {
+        if (cudaGraphLaunch(hit.exec, s) != cudaSuccess) return K3MOE_ERR_CUDA;
     } else {
         st = k3moe_forward(desc, in_dev, T, out_dev, ws, need, stream);
         if (st != K3MOE_OK) return st;
-        if (plain) host_graph_add(desc, in_dev, T, out_dev, ws, need, ws_bytes, s, dev);
+        if (plain) host_graph_add(desc, in_dev, T, out_dev, ws, need, ws_bytes, bytes, s, dev);
     }
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s)) return K3MOE_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));

@@ -143,6 +143,30 @@ def test_forward_host_repeated_calls(k3):
             ex["w2_s"].sub_(1)
 
 
+@pytest.mark.parametrize("T", [3, 600])
+def test_forward_host_staging_sizes(k3, T):
+    """Repeated host-buffer calls below and above the 1 MiB staging limit
+    (T * d * 2 bytes: 3 KiB and 1.2 MiB): the replayed graph copies through
+    its own page-locked buffers or around them and gives k3moe_forward's
+    output each time, also from pageable host memory."""
+    import torch
+
+    cfg = synth.custom("decode_t1", T=T, E=32, k=4, d=1024, f=512, seed_index=38)
+    layer, dense, expert, ex = make_layer(cfg, path=1)
+    big = synth.custom(cfg.name, T=T * 3, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, seed_index=39)
+    xs = synth.hidden(big).reshape(3, T, -1)
+    ws = k3.workspace(k3.k3moe_workspace_size(layer, T) + k3.k3moe_host_staging_size(layer, T))
+    for i, x in enumerate(xs):
+        x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        if i != 1:
+            x_host = x_host.pin_memory()
+        want = k3.k3moe_forward(layer, x_host.cuda()).cpu()
+        for _ in range(2):
+            out_host = torch.empty((T, cfg.d), dtype=torch.bfloat16)
+            k3.k3moe_forward_host(layer, x_host, out_host=out_host, ws=ws)
+            assert torch.equal(out_host.view(torch.int16), want.view(torch.int16)), i
+
+
 def test_graph_replay_matches_forward(k3):
     """k3moe_graph_create / k3moe_graph_launch reproduce k3moe_forward bit for bit."""
     import torch
