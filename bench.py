@@ -46,8 +46,8 @@ EXPERT_MATRIX_BYTES = None  # filled per config
 TRAFFIC = {
     ("decode_t1", "split", "prepared", "decode_up"): 187.6e6,
     ("verify_t8", "split", "prepared", "decode_up"): 379.1e6,
-    ("chunk_t512", "split", "prepared", "units_up"): 9117.2e6,
-    ("block_t8192", "split", "prepared", "expert_up"): 8460.2e6,
+    ("chunk_t512", "split", "prepared", "units_up"): 9122.0e6,
+    ("block_t8192", "split", "prepared", "expert_up"): 8467.6e6,
 }
 
 
