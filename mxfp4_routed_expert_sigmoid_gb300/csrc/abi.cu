@@ -819,7 +819,9 @@ namespace {
 // graph copies the tokens in from one and the output out to the other, so a
 // call is two host memcpys, one graph launch and one wait instead of three
 // stream operations; larger batches copy straight from and to the caller's
-// buffers around the graph.
+// buffers around the graph.  An entry in use by a call (it may run in another
+// host thread) is never replaced: a new graph that finds every entry in use
+// is not kept.
 constexpr size_t kHostStageMax = 1 << 20;
 struct HostGraph {
     k3moe_layer_desc desc;
@@ -832,11 +834,13 @@ struct HostGraph {
     void* pin_in;  // page-locked staging of a small batch, or null
     void* pin_out;
     uint64_t used;
+    int busy;      // calls using the entry now
 };
 struct HostGraphHit {
     cudaGraphExec_t exec;
     void* pin_in;
     void* pin_out;
+    int index;     // the entry, held until host_graph_release (-1: none)
 };
 constexpr int kHostGraphs = 8;
 std::mutex g_host_mu;
@@ -849,17 +853,33 @@ bool same_key(const HostGraph& h, const k3moe_layer_desc* d, const void* ws, siz
            std::memcmp(&h.desc, d, sizeof(k3moe_layer_desc)) == 0;
 }
 
-// the cached graph for these arguments (exec null when there is none)
+// the cached graph for these arguments (exec null when there is none), held
+// for the caller until host_graph_release
 HostGraphHit host_graph_find(const k3moe_layer_desc* d, const void* ws, size_t ws_bytes, int32_t T,
                              cudaStream_t s, int dev) {
     std::lock_guard<std::mutex> lock(g_host_mu);
-    for (auto& h : g_host)
+    for (int i = 0; i < kHostGraphs; ++i) {
+        HostGraph& h = g_host[i];
         if (same_key(h, d, ws, ws_bytes, T, s, dev)) {
             h.used = ++g_host_clock;
-            return {h.exec, h.pin_in, h.pin_out};
+            ++h.busy;
+            return {h.exec, h.pin_in, h.pin_out, i};
         }
-    return {nullptr, nullptr, nullptr};
+    }
+    return {nullptr, nullptr, nullptr, -1};
 }
+
+void host_graph_release(int index) {
+    if (index < 0) return;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    --g_host[index].busy;
+}
+
+// releases a found entry when the call returns
+struct HostGraphHold {
+    int index;
+    ~HostGraphHold() { host_graph_release(index); }
+};
 
 // Copies n 16-bit words between device memory and mapped page-locked host
 // memory: for a batch of a few KiB the loads and stores of one small grid
@@ -935,9 +955,16 @@ void host_graph_add(const k3moe_layer_desc* d, uint16_t* in_dev, int32_t T, uint
         return;
     }
     std::lock_guard<std::mutex> lock(g_host_mu);
-    HostGraph* slot = &g_host[0];
-    for (auto& h : g_host)
-        if (!h.exec || h.used < slot->used) slot = &h;
+    HostGraph* slot = nullptr;  // an empty entry, else the least recently used one not in use
+    for (auto& h : g_host) {
+        if (h.busy > 0) continue;
+        if (!slot || !h.exec || (slot->exec && h.used < slot->used)) slot = &h;
+    }
+    if (!slot) {
+        cudaGraphExecDestroy(exec);
+        free_pinned(pin_in, pin_out);
+        return;
+    }
     if (slot->exec) cudaGraphExecDestroy(slot->exec);
     free_pinned(slot->pin_in, slot->pin_out);
     slot->desc = *d;
@@ -950,6 +977,7 @@ void host_graph_add(const k3moe_layer_desc* d, uint16_t* in_dev, int32_t T, uint
     slot->pin_in = pin_in;
     slot->pin_out = pin_out;
     slot->used = ++g_host_clock;
+    slot->busy = 0;
 }
 }  // namespace
 
@@ -975,7 +1003,9 @@ k3moe_status k3moe_forward_host(const k3moe_layer_desc* desc, const uint16_t* hi
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     const bool plain = g_trace.mode == 0 && g_inject == 0 && cudaStreamIsCapturing(s, &cap) == cudaSuccess &&
                        cap == cudaStreamCaptureStatusNone;
-    const HostGraphHit hit = plain ? host_graph_find(desc, ws, ws_bytes, T, s, dev) : HostGraphHit{};
+    const HostGraphHit hit =
+        plain ? host_graph_find(desc, ws, ws_bytes, T, s, dev) : HostGraphHit{nullptr, nullptr, nullptr, -1};
+    const HostGraphHold hold{hit.index};
     if (hit.exec && hit.pin_in) {
         // the graph copies in from and out to its own page-locked buffers
         std::memcpy(hit.pin_in, hidden_host, bytes);

@@ -167,6 +167,52 @@ def test_forward_host_staging_sizes(k3, T):
             assert torch.equal(out_host.view(torch.int16), want.view(torch.int16)), i
 
 
+def test_forward_host_threads_evicting(k3):
+    """Four host threads, each on its own stream, cycle through ten distinct
+    (workspace, T) keys of the host-buffer entry point, more than the eight
+    cached graphs: entries are replaced while other threads use theirs, and
+    every call still returns k3moe_forward's output."""
+    import threading
+
+    import torch
+
+    cfg = synth.custom("decode_t1", T=4, E=32, k=4, d=512, f=512, seed_index=40)
+    layer, dense, expert, ex = make_layer(cfg, path=1)
+    xs = synth.hidden(synth.custom(cfg.name, T=4, E=cfg.E, k=cfg.k, d=cfg.d, f=cfg.f, seed_index=41))
+    cases = []
+    for i in range(10):
+        T = 1 + i % 4
+        x_host = torch.from_numpy(xs[:T].view(np.int16)).view(torch.bfloat16).pin_memory()
+        want = k3.k3moe_forward(layer, x_host.cuda()).cpu()
+        ws = k3.workspace(k3.k3moe_workspace_size(layer, T) + k3.k3moe_host_staging_size(layer, T))
+        cases.append((x_host, want, ws))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(tid):
+        stream = torch.cuda.Stream()
+        # a thread's workspaces are its own: a workspace serves one stream at a time
+        mine = [c for i, c in enumerate(cases) if i % 4 == tid]
+        others = [c for i, c in enumerate(cases) if i % 4 != tid][:3]
+        extra = [(x, want, k3.workspace(ws.numel())) for x, want, ws in others]
+        try:
+            for rep in range(6):
+                for x_host, want, ws in mine + extra:
+                    out_host = torch.empty_like(x_host).pin_memory()
+                    k3.k3moe_forward_host(layer, x_host, out_host=out_host, ws=ws, stream=stream)
+                    if not torch.equal(out_host.view(torch.int16), want.view(torch.int16)):
+                        errors.append((tid, rep))
+        except Exception as e:  # reported below
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:4]
+
+
 def test_graph_replay_matches_forward(k3):
     """k3moe_graph_create / k3moe_graph_launch reproduce k3moe_forward bit for bit."""
     import torch
