@@ -412,9 +412,23 @@ route_small_kernel(RouteArgs a) {
         const int c = i * 256 + lane * 8;
         wv[i] = (e < a.E && c < a.d_r) ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
     }
+    // the token rows into shared memory, eight loads per thread in flight
+    // before their stores (T = 8 rows of 3584 are 14 loads per thread)
     const int nvec = a.T * a.d_r / 8;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x)
-        xs[v] = reinterpret_cast<const uint4*>(a.x)[v];
+    constexpr int kStageLoads = 8;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kStageLoads * blockDim.x) {
+        uint4 xv[kStageLoads];
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j) {
+            const int v = v0 + j * blockDim.x;
+            if (v < nvec) xv[j] = reinterpret_cast<const uint4*>(a.x)[v];
+        }
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j) {
+            const int v = v0 + j * blockDim.x;
+            if (v < nvec) xs[v] = xv[j];
+        }
+    }
     __syncthreads();
 
     if (e < a.E) {
