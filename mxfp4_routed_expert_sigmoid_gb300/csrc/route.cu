@@ -383,6 +383,72 @@ __device__ int block_exclusive_scan(int* data, int n) {
 // kernels, one warp per 32-element block.
 constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
 
+// One warp's logits of expert e: lane l holds the weight elements 256 i +
+// 8 l .. 256 i + 8 l + 7 (wv, loaded by the caller; rows longer than 256
+// kRouteChunks are fetched here in further rounds) and multiplies them with
+// the token rows staged in xs; a token's products add in the order chunk,
+// q = 0..3, low half before high half.  gemv_row_tokens takes up to eight
+// tokens, one token's chunk after the other; gemv_row_one is the same for a
+// single token without the per-token guards (it measured 3.7 against 4.2 us
+// for the whole router at T = 1).
+template <typename Body>
+__device__ __forceinline__ void gemv_chunks(const RouteArgs& a, int lane, const uint16_t* wrow,
+                                            uint4 (&wv)[kRouteChunks], Body body) {
+    for (int base = 0; base < a.d_r; base += 256 * kRouteChunks) {
+        if (base > 0) {
+#pragma unroll
+            for (int i = 0; i < kRouteChunks; ++i) {
+                const int c = base + i * 256 + lane * 8;
+                wv[i] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRouteChunks; ++i) {
+            const int c = base + i * 256 + lane * 8;
+            if (c >= a.d_r) break;
+            body(wv[i], c);
+        }
+    }
+}
+
+__device__ __forceinline__ float dot8_bf16(const uint4& w, const uint4& x, float acc) {
+    const uint32_t wq[4] = {w.x, w.y, w.z, w.w}, xq[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc = fmaf(__uint_as_float(wq[q] << 16), __uint_as_float(xq[q] << 16), acc);
+        acc = fmaf(__uint_as_float(wq[q] & 0xFFFF0000u), __uint_as_float(xq[q] & 0xFFFF0000u), acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void gemv_row_one(const RouteArgs& a, int e, int lane, const uint16_t* wrow,
+                                             uint4 (&wv)[kRouteChunks], const uint4* xs) {
+    float acc = 0.0f;
+    gemv_chunks(a, lane, wrow, wv, [&](const uint4& w, int c) { acc = dot8_bf16(w, xs[c / 8], acc); });
+    const float v = warp_sum(acc);
+    if (lane == 0) a.logits[e] = v;
+}
+
+__device__ __forceinline__ void gemv_row_tokens(const RouteArgs& a, int e, int lane, const uint16_t* wrow,
+                                                uint4 (&wv)[kRouteChunks], const uint4* xs) {
+    float acc[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
+    gemv_chunks(a, lane, wrow, wv, [&](const uint4& w, int c) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t >= a.T) break;
+            acc[t] = dot8_bf16(w, xs[(t * a.d_r + c) / 8], acc[t]);
+        }
+    });
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        if (t >= a.T) break;
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) a.logits[static_cast<size_t>(t) * a.E + e] = v;
+    }
+}
+
 __global__ void __launch_bounds__(256)
 route_small_kernel(RouteArgs a) {
     extern __shared__ __align__(16) uint4 xs[];  // [T * d_r / 8]
@@ -432,44 +498,8 @@ route_small_kernel(RouteArgs a) {
     __syncthreads();
 
     if (e < a.E) {
-        float acc[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
-        for (int base = 0; base < a.d_r; base += 256 * kRouteChunks) {
-            if (base > 0) {
-#pragma unroll
-                for (int i = 0; i < kRouteChunks; ++i) {
-                    const int c = base + i * 256 + lane * 8;
-                    wv[i] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kRouteChunks; ++i) {
-                const int c = base + i * 256 + lane * 8;
-                if (c >= a.d_r) break;
-                const uint32_t wq[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (t >= a.T) break;
-                    const uint4 xv = xs[(t * a.d_r + c) / 8];
-                    const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
-                    float sacc = acc[t];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        sacc = fmaf(__uint_as_float(wq[q] << 16), __uint_as_float(xq[q] << 16), sacc);
-                        sacc = fmaf(__uint_as_float(wq[q] & 0xFFFF0000u),
-                                    __uint_as_float(xq[q] & 0xFFFF0000u), sacc);
-                    }
-                    acc[t] = sacc;
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (t >= a.T) break;
-            const float v = warp_sum(acc[t]);
-            if (lane == 0) a.logits[static_cast<size_t>(t) * a.E + e] = v;
-        }
+        if (a.T == 1) gemv_row_one(a, e, lane, wrow, wv, xs);
+        else gemv_row_tokens(a, e, lane, wrow, wv, xs);
     }
 }
 
