@@ -768,9 +768,11 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
     __shared__ float wk[32];
     __shared__ int act[kCombineMaxUnits];
     __shared__ __align__(16) float part[32][kCombineCols];
-    pdl_wait();
-    pdl_trigger();
-    StampScope stamp(st);
+    // The selection, its weights and the unit lists were final before this
+    // grid could launch: every kernel of the forward waits for its
+    // predecessor before it completes, and this one launches only once the
+    // down pass has started, so the top-k (or unit listing) kernel had
+    // completed.  The rows are looked up before the wait for the down pass.
     const int t = blockIdx.y;
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     if (rowmap) {
@@ -796,6 +798,9 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
         }
     }
     __syncthreads();
+    pdl_wait();  // y is the down pass's output
+    pdl_trigger();
+    StampScope stamp(st);
     const int c0 = blockIdx.x * kCombineCols;
     const size_t slot = static_cast<size_t>(umax) * T * d;
     if (c0 + lane * 4 < d) {

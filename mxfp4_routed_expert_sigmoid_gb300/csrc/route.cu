@@ -190,21 +190,27 @@ route_topk_kernel(RouteArgs a) {
                                     a.wts + static_cast<size_t>(t) * a.k, false);
     if (!a.active) return;
     if (gridDim.x == 1) {
-        // one token: its selection, in ascending expert order, is the active list
-        __shared__ int wcount[kMaxE / 32];
+        // one token: its selection, in ascending expert order, is the active
+        // list (warp w's chosen experts start at the prefix of the warp counts)
+        __shared__ int wbase[kMaxE / 32 + 1];
         const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
-        if (lane == 0) wcount[e >> 5] = __popc(bal);
+        if (lane == 0) wbase[e >> 5] = __popc(bal);
         __syncthreads();
-        if (chosen) {
-            int pos = __popc(bal & ((1u << lane) - 1u));
-            for (int w = 0; w < (e >> 5); ++w) pos += wcount[w];
-            a.active[pos] = e;
+        if (e < 32) {
+            const int c = wbase[lane];
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            __syncwarp();
+            wbase[lane] = incl - c;
+            if (lane == 31) wbase[32] = incl;
         }
-        if (e == 0) {
-            int total = 0;
-            for (int w = 0; w < kMaxE / 32; ++w) total += wcount[w];
-            a.active[a.E] = total;
-        }
+        __syncthreads();
+        if (chosen) a.active[wbase[e >> 5] + __popc(bal & ((1u << lane) - 1u))] = e;
+        if (e == 0) a.active[a.E] = wbase[32];
         return;
     }
     if (chosen) atomicOr(&a.hdr->pad[e >> 5], 1u << (e & 31));
