@@ -769,10 +769,11 @@ mx_combine_kernel(const float* __restrict__ y, int umax, int T, int d, const flo
     __shared__ int act[kCombineMaxUnits];
     __shared__ __align__(16) float part[32][kCombineCols];
     // The selection, its weights and the unit lists were final before this
-    // grid could launch: every kernel of the forward waits for its
-    // predecessor before it completes, and this one launches only once the
-    // down pass has started, so the top-k (or unit listing) kernel had
-    // completed.  The rows are looked up before the wait for the down pass.
+    // grid could launch: it launches only after the down pass has started,
+    // the down pass only after the finish kernel has started, and the finish
+    // kernel only after the up pass has passed its own wait, which returns
+    // once the top-k (or unit listing) kernel has completed.  The rows are
+    // looked up before the wait for the down pass.
     const int t = blockIdx.y;
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     if (rowmap) {
