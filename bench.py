@@ -99,11 +99,14 @@ def matrix_bytes(cfg):
     return rows * cols // 2 + rows * cols // 32
 
 
-def workload_config(cfg, pool):
+def workload_config(cfg):
+    """The workload and its L2 handling; how many distinct token batches a run
+    rotates through is reported beside it (``token_batches``), so that both
+    arms name the same workload with the same dictionary."""
     c = {"workload": cfg.name, "tokens_per_step": cfg.T, "experts": cfg.E, "top_k": cfg.k,
          "latent_d": cfg.d, "expert_hidden_f": cfg.f,
          "expert_bytes_resident": 3 * cfg.E * matrix_bytes(cfg),
-         "l2": f"{pool} rotating token batches (fresh experts per step) + 256 MB L2 flush "
+         "l2": "rotating token batches (fresh experts per step) + 256 MB L2 flush "
                "between steps, outside the timed kernels",
          "parallelism": "replicas only"}
     if cfg.block:
@@ -272,7 +275,9 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(cfg, args.steps + args.warmup),
+        "config": workload_config(cfg),
+        "token_batches": args.steps + args.warmup,
+        "weight_format": "codes + E8M0 scales as the checkpoint's canonical rows",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{nt} token(s) of the workload per step, expert bytes "
                                    "prefetched outside the timed region"},
@@ -476,11 +481,12 @@ def measure(k3, cfg, args, dev, world, steps, warmup, peaks):
     res = {
         "value": cfg.T * steps / (total_ms / 1e3), "unit": "tokens/s", "ms_per_step": mean_ms,
         "dtype": dtype_of(cfg.T, args.path),
-        "config": dict(workload_config(cfg, npool),
-                       weight_format=("ggml 17-byte MXFP4 blocks" if args.format == "ggml" else
-                                      "codes + E8M0 scales as " +
-                                      ("prepared atoms" if args.scales == "prepared" else
-                                       "the checkpoint's canonical rows"))),
+        "config": workload_config(cfg),
+        "token_batches": npool,
+        "weight_format": ("ggml 17-byte MXFP4 blocks" if args.format == "ggml" else
+                          "codes + E8M0 scales as " +
+                          ("prepared atoms" if args.scales == "prepared" else
+                           "the checkpoint's canonical rows")),
         "experts_touched_per_step": u_mean,
         "hbm_gbs_step": (u_mean * 3 * mb + bytes_["route_small"]) / (mean_ms * 1e-3) / 1e9,
         "kernels_ms": kern,
@@ -708,7 +714,8 @@ def cached_arm(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg.T, args.path),
         "data": "synthetic (seeded; random-init weights of the K3 layer shapes)",
-        "config": dict(workload_config(cfg, args.pool), workload=cfg.name + "_host_experts",
+        "token_batches": args.pool,
+        "config": dict(workload_config(cfg), workload=cfg.name + "_host_experts",
                        expert_bytes_resident=0, expert_bytes_host=3 * cfg.E * mb,
                        cache_slots=S, cache_bytes=3 * S * mb),
         "cache": {"hit_rate": hits / max(hits + misses, 1), "hits_per_step": hits / max(calls, 1),
