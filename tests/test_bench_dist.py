@@ -74,3 +74,9 @@ def test_reference_arm_json_contract():
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny"
+    # config names the workload only: the same dictionary the GPU arm prints
+    # (run details such as the number of token batches sit beside it)
+    import bench
+
+    assert d["config"] == bench.workload_config(bench.synth.CONFIGS["tiny"])
+    assert d["token_batches"] == 3
