@@ -382,36 +382,37 @@ __device__ int block_exclusive_scan(int* data, int n) {
     return total_s;
 }
 
-// Logits by GEMV (one warp per expert, all T tokens).  Each warp issues all
-// loads of its weight row before it needs them; the T token rows are staged
-// once per CTA in shared memory.  With xq requested, CTAs past the ceil(E / 8)
-// that compute logits write the token rows as E2M1 terms for the expert
-// kernels, one warp per 32-element block.
+// Logits by GEMV (one warp per expert at T = 1, two per expert for more
+// tokens, all T tokens).  Each warp issues all loads of its part of the
+// weight row before it needs them; the T token rows are staged once per CTA
+// in shared memory.  With xq requested, CTAs past those that compute logits
+// write the token rows as E2M1 terms for the expert kernels, one warp per
+// 32-element block.
 constexpr int kRouteChunks = 16;  // 16-byte weight loads per lane in flight
 
 // One warp's logits of expert e: lane l holds the weight elements 256 i +
 // 8 l .. 256 i + 8 l + 7 (wv, loaded by the caller; rows longer than 256
 // kRouteChunks are fetched here in further rounds) and multiplies them with
 // the token rows staged in xs; a token's products add in the order chunk,
-// q = 0..3, low half before high half.  gemv_row_tokens takes up to eight
-// tokens, one token's chunk after the other; gemv_row_one is the same for a
-// single token without the per-token guards (it measured 3.7 against 4.2 us
-// for the whole router at T = 1).
+// q = 0..3, low half before high half.  gemv_part_tokens takes up to eight
+// tokens over part of a row, one token's chunk after the other; gemv_row_one
+// is the whole row for a single token without the per-token guards (it
+// measured 3.7 against 4.2 us for the whole router at T = 1).
 template <typename Body>
-__device__ __forceinline__ void gemv_chunks(const RouteArgs& a, int lane, const uint16_t* wrow,
+__device__ __forceinline__ void gemv_chunks(int k0, int k1, int lane, const uint16_t* wrow,
                                             uint4 (&wv)[kRouteChunks], Body body) {
-    for (int base = 0; base < a.d_r; base += 256 * kRouteChunks) {
-        if (base > 0) {
+    for (int base = k0; base < k1; base += 256 * kRouteChunks) {
+        if (base > k0) {
 #pragma unroll
             for (int i = 0; i < kRouteChunks; ++i) {
                 const int c = base + i * 256 + lane * 8;
-                wv[i] = c < a.d_r ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+                wv[i] = c < k1 ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
         for (int i = 0; i < kRouteChunks; ++i) {
             const int c = base + i * 256 + lane * 8;
-            if (c >= a.d_r) break;
+            if (c >= k1) break;
             body(wv[i], c);
         }
     }
@@ -430,17 +431,20 @@ __device__ __forceinline__ float dot8_bf16(const uint4& w, const uint4& x, float
 __device__ __forceinline__ void gemv_row_one(const RouteArgs& a, int e, int lane, const uint16_t* wrow,
                                              uint4 (&wv)[kRouteChunks], const uint4* xs) {
     float acc = 0.0f;
-    gemv_chunks(a, lane, wrow, wv, [&](const uint4& w, int c) { acc = dot8_bf16(w, xs[c / 8], acc); });
+    gemv_chunks(0, a.d_r, lane, wrow, wv, [&](const uint4& w, int c) { acc = dot8_bf16(w, xs[c / 8], acc); });
     const float v = warp_sum(acc);
     if (lane == 0) a.logits[e] = v;
 }
 
-__device__ __forceinline__ void gemv_row_tokens(const RouteArgs& a, int e, int lane, const uint16_t* wrow,
-                                                uint4 (&wv)[kRouteChunks], const uint4* xs) {
+// Up to eight tokens over inputs [k0, k1) of a row, one token's chunk after
+// the other: the warp's per-token sums go to part[0 .. T) (lane 0 writes).
+__device__ __forceinline__ void gemv_part_tokens(const RouteArgs& a, int k0, int k1, int lane,
+                                                 const uint16_t* wrow, uint4 (&wv)[kRouteChunks],
+                                                 const uint4* xs, float* part) {
     float acc[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
-    gemv_chunks(a, lane, wrow, wv, [&](const uint4& w, int c) {
+    gemv_chunks(k0, k1, lane, wrow, wv, [&](const uint4& w, int c) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             if (t >= a.T) break;
@@ -451,9 +455,15 @@ __device__ __forceinline__ void gemv_row_tokens(const RouteArgs& a, int e, int l
     for (int t = 0; t < 8; ++t) {
         if (t >= a.T) break;
         const float v = warp_sum(acc[t]);
-        if (lane == 0) a.logits[static_cast<size_t>(t) * a.E + e] = v;
+        if (lane == 0) part[t] = v;
     }
 }
+
+// Rows per logits CTA: one warp per row for one token; for more tokens two
+// warps per row, each multiplying half of the row's 256-wide chunks, so that
+// a warp's chains are half as long (the two halves' sums are then added,
+// half 0 first).
+__host__ __device__ inline int route_rows_per_cta(int T) { return T == 1 ? 8 : 4; }
 
 __global__ void __launch_bounds__(256)
 route_small_kernel(RouteArgs a) {
@@ -463,7 +473,8 @@ route_small_kernel(RouteArgs a) {
     pdl_trigger();
     StampScope stamp(a.st_a);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int gemv_ctas = (a.E + 7) / 8;
+    const int rpc = route_rows_per_cta(a.T);
+    const int gemv_ctas = (a.E + rpc - 1) / rpc;
     if (static_cast<int>(blockIdx.x) >= gemv_ctas) {
         const int nb = a.d_r / 32;
         const int xq_ctas = gridDim.x - gemv_ctas;
@@ -476,13 +487,17 @@ route_small_kernel(RouteArgs a) {
         }
         return;
     }
-    const int e = blockIdx.x * 8 + wid;
+    // this warp's row and inputs [k0, k1) of it
+    const int half = rpc == 8 ? 0 : (wid & 1);
+    const int e = blockIdx.x * rpc + (rpc == 8 ? wid : wid >> 1);
+    const int nch = (a.d_r + 255) / 256, hch = rpc == 8 ? nch : (nch + 1) / 2;
+    const int k0 = half * hch * 256, k1 = min(a.d_r, (half + 1) * hch * 256);
     const uint16_t* wrow = a.w + static_cast<size_t>(e < a.E ? e : 0) * a.d_r;
     uint4 wv[kRouteChunks];
 #pragma unroll
     for (int i = 0; i < kRouteChunks; ++i) {
-        const int c = i * 256 + lane * 8;
-        wv[i] = (e < a.E && c < a.d_r) ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+        const int c = k0 + i * 256 + lane * 8;
+        wv[i] = (e < a.E && c < k1) ? ldg_nc_v4(wrow + c) : make_uint4(0, 0, 0, 0);
     }
     // the token rows into shared memory, eight loads per thread in flight
     // before their stores (T = 8 rows of 3584 are 14 loads per thread)
@@ -503,10 +518,15 @@ route_small_kernel(RouteArgs a) {
     }
     __syncthreads();
 
-    if (e < a.E) {
-        if (a.T == 1) gemv_row_one(a, e, lane, wrow, wv, xs);
-        else gemv_row_tokens(a, e, lane, wrow, wv, xs);
+    if (a.T == 1) {
+        if (e < a.E) gemv_row_one(a, e, lane, wrow, wv, xs);
+        return;
     }
+    __shared__ float part_s[8][8];  // [warp][token]
+    if (e < a.E) gemv_part_tokens(a, k0, k1, lane, wrow, wv, xs, part_s[wid]);
+    __syncthreads();
+    if (half == 0 && e < a.E && lane < a.T)
+        a.logits[static_cast<size_t>(lane) * a.E + e] = part_s[wid][lane] + part_s[wid + 1][lane];
 }
 
 // Plain tiled SIMT logits for moderate T: 64 tokens x 64 experts per CTA.
@@ -683,7 +703,8 @@ cudaError_t launch_route_topk(const RouteArgs& a_in, cudaStream_t s) {
 cudaError_t launch_route_small(const RouteArgs& a_in, cudaStream_t s) {
     RouteArgs a = a_in;
     a.st_a = trace_stamp("route_small");
-    const int gemv_ctas = (a.E + 7) / 8;
+    const int rpc = route_rows_per_cta(a.T);
+    const int gemv_ctas = (a.E + rpc - 1) / rpc;
     const int xq_ctas = a.xq ? std::min(128, (a.T * (a.d_r / 32) + 7) / 8) : 0;
     const size_t smem = static_cast<size_t>(a.T) * a.d_r * 2;
     if (smem > 48 * 1024) {
